@@ -1,0 +1,261 @@
+/*
+ * sparsekv.h -- C interface of the GB300 sparse paged-KV decode attention library.
+ *
+ * One decode step of attention over a paged KV cache, with query-aware page selection:
+ *
+ *   kv_build_page_stats    per-page, per-KV-head element-wise min/max of the keys
+ *   kv_score_pages         an upper bound of q.k over each page, summed over a GQA group
+ *   kv_select_topk         top-k pages per (sequence, KV head) under a keep ratio/budget
+ *   kv_sparse_decode_attn  split-K softmax attention over the selected pages -> partials
+ *   kv_merge_splits        log-sum-exp merge of the (m, l, acc) partials -> output, lse
+ *   kv_dropped_mass        diagnostic: dense attention mass of the pages not selected
+ *   kv_decode_step         the four per-step calls above in one call, on a workspace
+ *
+ * Sources, by page title and section:
+ *   [ENTMAX]  "EntmaxKV: Support-Aware Decoding for Entmax Attention", abstract: pages are
+ *             scored against the query from cheap per-page statistics before any page is
+ *             read; the output error is governed by the dropped mass delta.
+ *   [SPARDA]  "SparDA: Sparse Decoupled Attention for Efficient Long-Context LLM
+ *             Inference", section 3.1 (per-head relevance summed inside a GQA group into
+ *             one shared score), appendix A (the top-k operator over block scores),
+ *             appendix C (a fixed block budget).
+ *   [BYTEX]   "Where Activation Sparsity and KV-Cache Sparsity Cross in LLM Decoding",
+ *             abstract and Table 11 (dense and sparse decoding read the cache through the
+ *             same split-K attention kernel; dense is that kernel with every page kept),
+ *             Tables 16-17 (keep ratios r_KV).
+ *   [PRHS]    "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference",
+ *             abstract (top-k KV selection; delta = attention mass of discarded entries).
+ *
+ * Conventions for every call
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless the comment
+ *     says "host". The library allocates no device memory and keeps no per-call state:
+ *     the caller provides every output and workspace buffer.
+ *   - Every call is asynchronous on the given stream (0 = the legacy default stream).
+ *   - Host-detectable argument errors return KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED or
+ *     KV_ERR_MISALIGNED and launch nothing. A failed launch returns KV_ERR_CUDA.
+ *   - Device-detected faults in the DATA (a page-table entry outside [0, num_phys_pages),
+ *     a sequence longer than its page-table row, a selected index outside the sequence,
+ *     a keep count above k_max, an asynchronous copy that did not land in time) never
+ *     trap: the kernel skips the bad access, records a flag in a per-device error word
+ *     and finishes. kv_check_device_errors() reports and clears that word.
+ *   - Supported shapes: head_dim 64 or 128; page_size 16, 32 or 64; group size
+ *     G = num_q_heads / num_kv_heads in {1, 2, 4, 8}; dtype bf16 or fp32. Anything else
+ *     returns KV_ERR_UNSUPPORTED.
+ *
+ * Layouts (row-major, innermost last)
+ *   k_pool, v_pool  [num_phys_pages][num_kv_heads][page_size][head_dim]   dtype
+ *   page_table      [batch][page_table_stride] int32; entry p of row b is the physical
+ *                   page of logical page p of sequence b; only p < ceil(len_b/page_size)
+ *                   are read.
+ *   seq_lens        [batch] int32 tokens, the current decode token included.
+ *   q               [batch][num_q_heads][head_dim] dtype; query head h reads KV head
+ *                   h / G (consecutive query heads share a KV head).
+ *   stats           [num_phys_pages][num_kv_heads][2][head_dim] dtype; [..][0][:] = min,
+ *                   [..][1][:] = max over the page's valid tokens.
+ *   scores          [batch][num_kv_heads][scores_stride] float32.
+ *   sel_idx         [batch][num_kv_heads][sel_stride] int32 logical page indices,
+ *                   ascending; sel_cnt [batch][num_kv_heads] int32 entries used.
+ *   part_acc        [batch][num_q_heads][num_splits][head_dim] float32
+ *   part_ml         [batch][num_q_heads][num_splits][2] float32 = (m, l)
+ *   out             [batch][num_q_heads][head_dim] float32; lse [batch][num_q_heads].
+ *
+ * Alignment: k_pool, v_pool, stats and q must be 16-byte aligned (pages are moved with
+ * bulk asynchronous copies); otherwise KV_ERR_MISALIGNED.
+ */
+#ifndef SPARSEKV_H_
+#define SPARSEKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kv_status {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = -1,   /* a null pointer, a non-positive size, inconsistent sizes */
+  KV_ERR_UNSUPPORTED = -2,   /* a shape or dtype outside the supported set */
+  KV_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+  KV_ERR_WORKSPACE = -4,     /* workspace null or smaller than the *_workspace_size */
+  KV_ERR_BAD_INDEX = -5,     /* device-detected: bad page, length, index or keep count */
+  KV_ERR_TIMEOUT = -6,       /* device-detected: a bounded wait ran out */
+  KV_ERR_MISALIGNED = -7     /* a buffer is not 16-byte aligned */
+} kv_status;
+
+typedef enum kv_dtype { KV_BF16 = 0, KV_FP32 = 1 } kv_dtype;
+
+/* Device-side error flags (bit mask) behind kv_check_device_errors(). */
+enum {
+  KV_DEVERR_BAD_PAGE = 1,    /* page-table entry outside [0, num_phys_pages) */
+  KV_DEVERR_BAD_LEN = 2,     /* seq_len < 0 or above page_table_stride * page_size */
+  KV_DEVERR_BAD_SEL = 4,     /* selected index outside [0, n_pages) or sel_cnt > stride */
+  KV_DEVERR_KEEP = 8,        /* keep count above k_max (clamped to k_max) */
+  KV_DEVERR_TIMEOUT = 16     /* bounded wait on an asynchronous copy ran out */
+};
+
+/* The paged cache. All pointers are device pointers owned by the caller. */
+typedef struct kv_cache_desc {
+  const void* k_pool;           /* [num_phys_pages][num_kv_heads][page_size][head_dim] */
+  const void* v_pool;           /* same layout as k_pool */
+  int32_t dtype;                /* kv_dtype of k_pool, v_pool, q and stats */
+  int32_t num_phys_pages;
+  int32_t num_kv_heads;
+  int32_t page_size;            /* tokens per page: 16, 32 or 64 */
+  int32_t head_dim;             /* 64 or 128 */
+  int32_t batch;                /* sequences */
+  const int32_t* page_table;    /* [batch][page_table_stride] */
+  int32_t page_table_stride;    /* >= max over b of ceil(seq_lens[b] / page_size) */
+  const int32_t* seq_lens;      /* [batch] tokens, current token included */
+} kv_cache_desc;
+
+/* Human-readable name of a kv_status value (static string, never NULL). */
+const char* kv_status_string(int32_t status);
+
+/* Library interface version (major * 100 + minor). */
+int32_t kv_version(void);
+
+/*
+ * kv_build_page_stats -- [ENTMAX] per-page statistics.
+ * For every mapped page (b, p < ceil(len_b/PS)) and KV head g, writes the element-wise
+ * min and max of the keys of the page's valid tokens (min(PS, len_b - p*PS) of them) to
+ * stats[page_table[b][p]][g][0|1][:]. Values are copied exactly (no rounding). Rows of
+ * unmapped physical pages are not written. Reads every mapped key once; run it after a
+ * prefill, not per step.
+ * stats: device, [num_phys_pages][num_kv_heads][2][head_dim] of the cache dtype.
+ */
+kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStream_t stream);
+
+/*
+ * kv_score_pages -- [ENTMAX] query-aware page score, [SPARDA] summed over a GQA group.
+ * scores[b][g][p] = sum over query heads h of group g, over d, of
+ *                   max(q[b][h][d] * mn[d], q[b][h][d] * mx[d])
+ * with (mn, mx) = stats of physical page page_table[b][p], KV head g. Each term bounds
+ * q_d * k_d for every key of the page, so the per-head sum bounds q.k over the page. The
+ * softmax scale is left out (it does not change the order). Computed in float32.
+ * Entries p >= ceil(len_b / PS) are not written. scores_stride >= page_table_stride.
+ */
+kv_status kv_score_pages(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                         const void* stats, float* scores, int32_t scores_stride,
+                         cudaStream_t stream);
+
+/*
+ * kv_select_topk -- [PRHS], [SPARDA] appendix A: top-k pages of each (b, g) group.
+ * n_b = ceil(seq_lens[b] / page_size). The keep count k_b is
+ *   keep[b]                                   if keep is not NULL (device [batch]),
+ *   min(n_b, budget_pages)                    else if budget_pages > 0,
+ *   n_b                                       else if keep_ratio >= 1,
+ *   min(n_b, max(1, ceil(keep_ratio*n_b - 1e-9)))   otherwise (ratio in (0, 1)),
+ * and 0 when n_b = 0 (the ratio rule is evaluated in double precision, so that e.g.
+ * 0.2 * 5 keeps 1 page, not 2). k_b above k_max is clamped to k_max and flagged
+ * (KV_DEVERR_KEEP); a negative keep[b] is taken as 0.
+ * Pages are ranked by (score descending, page index ascending) -- ties go to the lower
+ * page index -- and the k_b best are written to sel_idx[b][g][0..k_b) in ASCENDING page
+ * order, with sel_cnt[b][g] = k_b. Scores must not be NaN.
+ * scores: device [batch][num_kv_heads][scores_stride] float32 (as kv_score_pages writes).
+ * sel_idx: device [batch][num_kv_heads][k_max]; sel_cnt: device [batch][num_kv_heads].
+ */
+kv_status kv_select_topk(const float* scores, int32_t scores_stride, const int32_t* seq_lens,
+                         int32_t page_size, int32_t batch, int32_t num_kv_heads,
+                         const int32_t* keep, double keep_ratio, int32_t budget_pages,
+                         int32_t k_max, int32_t* sel_idx, int32_t* sel_cnt,
+                         cudaStream_t stream);
+
+/*
+ * kv_sparse_decode_attn -- [BYTEX] split-K decode attention over selected pages.
+ * For each (b, g) the selected list (sel_idx[b][g][0..sel_cnt[b][g]), or every page
+ * 0..n_b-1 when sel_idx is NULL: the dense baseline through the same kernel) is cut into
+ * num_splits consecutive runs: split s takes list positions [s*c, min(cnt, (s+1)*c)) with
+ * c = ceil(cnt / num_splits). For each query head h of the group and split s, over the
+ * valid tokens t of the run's pages (tokens at or past len_b are masked):
+ *   x_t = sm_scale * q[b][h] . k_t,  m = max x_t,  l = sum exp(x_t - m),
+ *   acc = sum exp(x_t - m) v_t
+ * written as part_ml[b][h][s] = (m, l), part_acc[b][h][s][:] = acc. An empty split
+ * writes (m, l) = (-inf, 0) and acc = 0. Accumulation is float32.
+ * num_splits >= 1 (kv_auto_num_splits gives a value that fills the GPU).
+ * sel_stride: row stride of sel_idx (the k_max used by kv_select_topk); ignored when
+ * sel_idx is NULL. sel_cnt may be NULL only when sel_idx is NULL.
+ */
+kv_status kv_sparse_decode_attn(const kv_cache_desc* cache, const void* q,
+                                int32_t num_q_heads, float sm_scale, const int32_t* sel_idx,
+                                const int32_t* sel_cnt, int32_t sel_stride,
+                                int32_t num_splits, float* part_acc, float* part_ml,
+                                cudaStream_t stream);
+
+/*
+ * kv_merge_splits -- log-sum-exp merge of the split partials ([BYTEX] split-K).
+ * M = max_s m_s; L = sum_s l_s exp(m_s - M); out = sum_s acc_s exp(m_s - M) / L;
+ * lse = M + log L (natural log). Splits with m = -inf carry no mass; if every split is
+ * empty, out = 0 and lse = -inf. lse may be NULL.
+ */
+kv_status kv_merge_splits(const float* part_acc, const float* part_ml, int32_t batch,
+                          int32_t num_q_heads, int32_t num_splits, int32_t head_dim,
+                          float* out, float* lse, cudaStream_t stream);
+
+/*
+ * kv_auto_num_splits -- host: a split count that fills every SM of the current device
+ * for a cache of this shape when each (b, g) group keeps about pages_per_group pages.
+ * Returns >= 1, or a negative kv_status on a bad argument.
+ */
+int32_t kv_auto_num_splits(const kv_cache_desc* cache, int32_t num_q_heads,
+                           int32_t pages_per_group);
+
+/*
+ * kv_dropped_mass -- [PRHS], [ENTMAX] diagnostic probe, not part of a decode step.
+ * delta[b][h] = sum over valid tokens of pages NOT in sel_idx[b][g] of exp(x_t - M)
+ *               / sum over all valid tokens of exp(x_t - M),  x_t = sm_scale * q.k_t,
+ * M the max over all valid tokens; 0 for an empty sequence. Reads every key of every
+ * mapped page. workspace: device, at least kv_dropped_mass_workspace_size() bytes.
+ */
+kv_status kv_dropped_mass(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                          float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,
+                          int32_t sel_stride, float* delta, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads);
+
+/*
+ * kv_decode_step -- one sparse decode step: kv_score_pages, kv_select_topk,
+ * kv_sparse_decode_attn and kv_merge_splits on a caller workspace. With keep_ratio >= 1
+ * and budget_pages <= 0 it is the dense step (every page, no scoring or selection).
+ * k_max bounds the keep count (and sizes the workspace); num_splits 0 = automatic.
+ * out: device [batch][num_q_heads][head_dim] float32; lse: [batch][num_q_heads] or NULL.
+ * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned.
+ */
+kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                         float sm_scale, const void* stats, double keep_ratio,
+                         int32_t budget_pages, int32_t k_max, int32_t num_splits,
+                         float* out, float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
+                                     int32_t k_max, int32_t num_splits);
+
+/*
+ * kv_check_device_errors -- synchronises `stream`, reads and clears the current device's
+ * error word. Returns KV_OK, KV_ERR_TIMEOUT (a bounded wait ran out) or KV_ERR_BAD_INDEX
+ * (any other flag). If flags is not NULL (host), the raw KV_DEVERR_* mask is stored.
+ */
+kv_status kv_check_device_errors(cudaStream_t stream, int32_t* flags);
+
+/*
+ * kv_set_wait_limit_ns -- host: limit, in nanoseconds of the GPU's global timer, of every
+ * device-side wait on an asynchronous copy (default 2e9). After it runs out the kernel
+ * flags KV_DEVERR_TIMEOUT, drains its own copies (again bounded) and returns.
+ */
+kv_status kv_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * kv_selftest_wait_timeout -- launches one block that waits, with the production bounded
+ * wait, on a barrier that nothing ever completes, using `limit_ns` as the limit. Used to
+ * test the timeout path: a following kv_check_device_errors() must return KV_ERR_TIMEOUT.
+ */
+kv_status kv_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSEKV_H_ */

@@ -1,0 +1,404 @@
+// Host side of the C interface declared in include/sparsekv.h: argument checks, the
+// per-device error word, split-count choice, workspace carving and kernel launches.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "attn_impl.cuh"
+#include "kv_internal.cuh"
+
+namespace skv {
+namespace {
+
+// Device-side error word (one per device context). Kernels receive its device address.
+__device__ int32_t g_kv_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDroppedSplits = 64;          // page ranges per group in the dropped-mass probe
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int smem_per_sm = 0;
+  int32_t* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+unsigned long long g_wait_ns = 2000000000ull;
+
+kv_status device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kv_error_word) != cudaSuccess) return KV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return KV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               dev) != cudaSuccess)
+      return KV_ERR_CUDA;
+    st.err = static_cast<int32_t*>(p);
+    st.ready = true;
+  }
+  *out = &st;
+  return KV_OK;
+}
+
+kv_status ctx_for_call(DevCtx* ctx, DeviceState** st_out = nullptr) {
+  DeviceState* st = nullptr;
+  kv_status r = device_state(&st);
+  if (r != KV_OK) return r;
+  ctx->err = st->err;
+  ctx->wait_ns = g_wait_ns;
+  if (st_out) *st_out = st;
+  return KV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kv_status check_desc(const kv_cache_desc* d) {
+  if (d == nullptr || d->k_pool == nullptr || d->v_pool == nullptr ||
+      d->page_table == nullptr || d->seq_lens == nullptr)
+    return KV_ERR_INVALID_ARG;
+  if (d->num_phys_pages <= 0 || d->num_kv_heads <= 0 || d->batch <= 0 ||
+      d->page_table_stride <= 0 || d->batch > 65535 || d->num_kv_heads > 65535)
+    return KV_ERR_INVALID_ARG;
+  if (d->dtype != KV_BF16 && d->dtype != KV_FP32) return KV_ERR_UNSUPPORTED;
+  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64) return KV_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if ((long long)d->page_table_stride * d->page_size > INT32_MAX) return KV_ERR_INVALID_ARG;
+  if (!aligned16(d->k_pool) || !aligned16(d->v_pool)) return KV_ERR_MISALIGNED;
+  return KV_OK;
+}
+
+kv_status check_heads(const kv_cache_desc* d, const void* q, int32_t num_q_heads) {
+  if (q == nullptr || num_q_heads <= 0 || num_q_heads % d->num_kv_heads != 0)
+    return KV_ERR_INVALID_ARG;
+  const int G = num_q_heads / d->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
+  if (!aligned16(q)) return KV_ERR_MISALIGNED;
+  return KV_OK;
+}
+
+kv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+size_t attn_smem(const kv_cache_desc* d, int G) {
+  return d->dtype == KV_BF16 ? split_attn_smem_bf16(d->head_dim, G)
+                             : split_attn_smem_fp32(d->head_dim, G);
+}
+
+int min_splits_for(int pages) { return (pages + kMaxSplitPages - 1) / kMaxSplitPages; }
+
+int auto_splits(const kv_cache_desc* d, int G, int pages_per_group, const DeviceState* st) {
+  const size_t smem = attn_smem(d, G);
+  int per_sm = smem > 0 ? (int)(st->smem_per_sm / (smem + 1024)) : 1;
+  per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+  const long groups = (long)d->batch * d->num_kv_heads;
+  const long target = (long)st->sms * per_sm;
+  long S = (target + groups - 1) / groups;
+  const int ppt = kTileTokens / d->page_size;
+  const long cap = pages_per_group / (2 * ppt);            // at least two tiles per split
+  if (S > cap) S = cap;
+  if (S < 1) S = 1;
+  const int lo = min_splits_for(pages_per_group);
+  if (S < lo) S = lo;
+  return (int)S;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct StepLayout {
+  size_t scores, sel, cnt, acc, ml, total;
+};
+
+StepLayout step_layout(const kv_cache_desc* d, int Hq, int k_max, int S) {
+  StepLayout L;
+  const size_t groups = (size_t)d->batch * d->num_kv_heads;
+  L.scores = 0;
+  L.sel = L.scores + round256(groups * d->page_table_stride * sizeof(float));
+  L.cnt = L.sel + round256(groups * (size_t)(k_max > 0 ? k_max : 1) * sizeof(int32_t));
+  L.acc = L.cnt + round256(groups * sizeof(int32_t));
+  L.ml = L.acc + round256((size_t)d->batch * Hq * S * d->head_dim * sizeof(float));
+  L.total = L.ml + round256((size_t)d->batch * Hq * S * 2 * sizeof(float));
+  return L;
+}
+
+bool is_dense(double keep_ratio, int budget_pages) {
+  return budget_pages <= 0 && keep_ratio >= 1.0;
+}
+
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, DevCtx ctx) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);          // expects one arrival that never comes
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+  if (!ok && threadIdx.x == 0) flag(ctx, KV_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_split_attn(const kv_cache_desc& d, const void* q, int Hq, float sm_scale,
+                              const int32_t* sel_idx, const int32_t* sel_cnt, int sel_stride,
+                              int num_splits, float* part_acc, float* part_ml, DevCtx ctx,
+                              cudaStream_t s, int /*num_sms*/) {
+  const int G = Hq / d.num_kv_heads;
+  return d.dtype == KV_BF16
+             ? launch_split_attn_bf16(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride,
+                                      num_splits, part_acc, part_ml, ctx, s)
+             : launch_split_attn_fp32(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride,
+                                      num_splits, part_acc, part_ml, ctx, s);
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, DevCtx ctx, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, ctx);
+  return cudaGetLastError();
+}
+
+}  // namespace skv
+
+using namespace skv;
+
+extern "C" {
+
+const char* kv_status_string(int32_t status) {
+  switch (status) {
+    case KV_OK: return "ok";
+    case KV_ERR_INVALID_ARG: return "invalid argument";
+    case KV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KV_ERR_CUDA: return "CUDA error";
+    case KV_ERR_WORKSPACE: return "workspace missing or too small";
+    case KV_ERR_BAD_INDEX: return "device detected a bad page, length, index or keep count";
+    case KV_ERR_TIMEOUT: return "device wait timed out";
+    case KV_ERR_MISALIGNED: return "buffer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int32_t kv_version(void) { return 100; }
+
+kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if (stats == nullptr) return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(launch_page_stats(*cache, stats, ctx, stream));
+}
+
+kv_status kv_score_pages(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                         const void* stats, float* scores, int32_t scores_stride,
+                         cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (stats == nullptr || scores == nullptr || scores_stride < cache->page_table_stride)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(
+      launch_score_pages(*cache, q, num_q_heads, stats, scores, scores_stride, ctx, stream));
+}
+
+kv_status kv_select_topk(const float* scores, int32_t scores_stride, const int32_t* seq_lens,
+                         int32_t page_size, int32_t batch, int32_t num_kv_heads,
+                         const int32_t* keep, double keep_ratio, int32_t budget_pages,
+                         int32_t k_max, int32_t* sel_idx, int32_t* sel_cnt,
+                         cudaStream_t stream) {
+  if (scores == nullptr || seq_lens == nullptr || sel_idx == nullptr || sel_cnt == nullptr)
+    return KV_ERR_INVALID_ARG;
+  if (scores_stride <= 0 || page_size <= 0 || batch <= 0 || batch > 65535 ||
+      num_kv_heads <= 0 || num_kv_heads > 65535 || k_max <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (keep == nullptr && budget_pages <= 0 && !(keep_ratio > 0.0)) return KV_ERR_INVALID_ARG;
+  if ((long long)scores_stride * page_size > INT32_MAX) return KV_ERR_INVALID_ARG;
+  DevCtx ctx;
+  kv_status r = ctx_for_call(&ctx);
+  if (r != KV_OK) return r;
+  // The row stride bounds every sequence: a longer seq_len is flagged by the kernel.
+  return from_cuda(launch_select_topk(scores, scores_stride, seq_lens, page_size, batch,
+                                      num_kv_heads, keep, keep_ratio, budget_pages, k_max,
+                                      sel_idx, sel_cnt, scores_stride, ctx, stream));
+}
+
+kv_status kv_sparse_decode_attn(const kv_cache_desc* cache, const void* q,
+                                int32_t num_q_heads, float sm_scale, const int32_t* sel_idx,
+                                const int32_t* sel_cnt, int32_t sel_stride,
+                                int32_t num_splits, float* part_acc, float* part_ml,
+                                cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (part_acc == nullptr || part_ml == nullptr || num_splits < 1 || num_splits > 65535 ||
+      !(sm_scale > 0.f) || !isfinite(sm_scale))
+    return KV_ERR_INVALID_ARG;
+  if (sel_idx != nullptr && (sel_cnt == nullptr || sel_stride <= 0)) return KV_ERR_INVALID_ARG;
+  const int bound = sel_idx != nullptr ? sel_stride : cache->page_table_stride;
+  if (num_splits < min_splits_for(bound)) return KV_ERR_INVALID_ARG;
+  DevCtx ctx;
+  DeviceState* st = nullptr;
+  if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
+  return from_cuda(launch_split_attn(*cache, q, num_q_heads, sm_scale, sel_idx, sel_cnt,
+                                     sel_stride, num_splits, part_acc, part_ml, ctx, stream,
+                                     st->sms));
+}
+
+kv_status kv_merge_splits(const float* part_acc, const float* part_ml, int32_t batch,
+                          int32_t num_q_heads, int32_t num_splits, int32_t head_dim,
+                          float* out, float* lse, cudaStream_t stream) {
+  if (part_acc == nullptr || part_ml == nullptr || out == nullptr) return KV_ERR_INVALID_ARG;
+  if (batch <= 0 || num_q_heads <= 0 || num_splits < 1) return KV_ERR_INVALID_ARG;
+  if ((long long)batch * num_q_heads > INT32_MAX) return KV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return KV_ERR_UNSUPPORTED;
+  return from_cuda(
+      launch_merge(part_acc, part_ml, batch, num_q_heads, num_splits, head_dim, out, lse, stream));
+}
+
+int32_t kv_auto_num_splits(const kv_cache_desc* cache, int32_t num_q_heads,
+                           int32_t pages_per_group) {
+  if (cache == nullptr || cache->num_kv_heads <= 0 || cache->batch <= 0 ||
+      num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0 || pages_per_group < 0)
+    return KV_ERR_INVALID_ARG;
+  if (cache->page_size != 16 && cache->page_size != 32 && cache->page_size != 64)
+    return KV_ERR_UNSUPPORTED;
+  DeviceState* st = nullptr;
+  kv_status r = device_state(&st);
+  if (r != KV_OK) return r;
+  return auto_splits(cache, num_q_heads / cache->num_kv_heads, pages_per_group, st);
+}
+
+size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads) {
+  if (cache == nullptr || cache->batch <= 0 || num_q_heads <= 0) return 0;
+  return (size_t)cache->batch * num_q_heads * kDroppedSplits * 3 * sizeof(float);
+}
+
+kv_status kv_dropped_mass(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                          float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,
+                          int32_t sel_stride, float* delta, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (sel_idx == nullptr || sel_cnt == nullptr || sel_stride <= 0 || delta == nullptr ||
+      !(sm_scale > 0.f) || !isfinite(sm_scale))
+    return KV_ERR_INVALID_ARG;
+  if ((long long)cache->page_table_stride > (long long)kDroppedSplits * 65536)
+    return KV_ERR_UNSUPPORTED;
+  if (workspace == nullptr ||
+      workspace_bytes < kv_dropped_mass_workspace_size(cache, num_q_heads))
+    return KV_ERR_WORKSPACE;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(launch_dropped_mass(*cache, q, num_q_heads, sm_scale, sel_idx, sel_cnt,
+                                       sel_stride, kDroppedSplits,
+                                       static_cast<float*>(workspace), delta, ctx, stream));
+}
+
+size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
+                                     int32_t k_max, int32_t num_splits) {
+  if (cache == nullptr || num_q_heads <= 0 || cache->num_kv_heads <= 0 || cache->batch <= 0 ||
+      num_q_heads % cache->num_kv_heads != 0 || cache->head_dim <= 0 ||
+      cache->page_table_stride <= 0 || k_max < 0)
+    return 0;
+  int S = num_splits;
+  if (S <= 0) {
+    DeviceState* st = nullptr;
+    if (device_state(&st) != KV_OK) return 0;
+    const int G = num_q_heads / cache->num_kv_heads;
+    // the larger of the sparse and the dense split counts, so either mode fits
+    const int s1 = auto_splits(cache, G, k_max > 0 ? k_max : 1, st);
+    const int s2 = auto_splits(cache, G, cache->page_table_stride, st);
+    S = s1 > s2 ? s1 : s2;
+  }
+  return step_layout(cache, num_q_heads, k_max, S).total;
+}
+
+kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                         float sm_scale, const void* stats, double keep_ratio,
+                         int32_t budget_pages, int32_t k_max, int32_t num_splits,
+                         float* out, float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (out == nullptr || !(sm_scale > 0.f) || !isfinite(sm_scale)) return KV_ERR_INVALID_ARG;
+  const bool dense = is_dense(keep_ratio, budget_pages);
+  if (!dense && (stats == nullptr || k_max <= 0 || !(keep_ratio > 0.0 || budget_pages > 0)))
+    return KV_ERR_INVALID_ARG;
+  if (!dense && !aligned16(stats)) return KV_ERR_MISALIGNED;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return KV_ERR_WORKSPACE;
+  DevCtx ctx;
+  DeviceState* st = nullptr;
+  if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
+  const int G = num_q_heads / cache->num_kv_heads;
+  int S = num_splits;
+  if (S <= 0) S = auto_splits(cache, G, dense ? cache->page_table_stride : k_max, st);
+  if (S < min_splits_for(dense ? cache->page_table_stride : k_max)) return KV_ERR_INVALID_ARG;
+  const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, S);
+  if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  float* scores = reinterpret_cast<float*>(ws + L.scores);
+  int32_t* sel = reinterpret_cast<int32_t*>(ws + L.sel);
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  float* ml = reinterpret_cast<float*>(ws + L.ml);
+  cudaError_t e;
+  if (!dense) {
+    e = launch_score_pages(*cache, q, num_q_heads, stats, scores, cache->page_table_stride, ctx,
+                           stream);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+    e = launch_select_topk(scores, cache->page_table_stride, cache->seq_lens, cache->page_size,
+                           cache->batch, cache->num_kv_heads, nullptr, keep_ratio,
+                           budget_pages, k_max, sel, cnt, cache->page_table_stride, ctx,
+                           stream);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+  }
+  e = launch_split_attn(*cache, q, num_q_heads, sm_scale, dense ? nullptr : sel,
+                        dense ? nullptr : cnt, dense ? 0 : k_max, S, acc, ml, ctx, stream,
+                        st->sms);
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  return from_cuda(
+      launch_merge(acc, ml, cache->batch, num_q_heads, S, cache->head_dim, out, lse, stream));
+}
+
+kv_status kv_check_device_errors(cudaStream_t stream, int32_t* flags) {
+  DeviceState* st = nullptr;
+  kv_status r = device_state(&st);
+  if (r != KV_OK) return r;
+  int32_t h = 0;
+  const int32_t zero = 0;
+  if (cudaMemcpyAsync(&h, st->err, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return KV_ERR_CUDA;
+  if (cudaMemcpyAsync(st->err, &zero, sizeof(zero), cudaMemcpyHostToDevice, stream) !=
+      cudaSuccess)
+    return KV_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KV_ERR_CUDA;
+  if (flags != nullptr) *flags = h;
+  if (h == 0) return KV_OK;
+  return (h & KV_DEVERR_TIMEOUT) ? KV_ERR_TIMEOUT : KV_ERR_BAD_INDEX;
+}
+
+kv_status kv_set_wait_limit_ns(uint64_t limit_ns) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_wait_ns = (unsigned long long)limit_ns;
+  return KV_OK;
+}
+
+kv_status kv_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  DevCtx ctx;
+  kv_status r = ctx_for_call(&ctx);
+  if (r != KV_OK) return r;
+  return from_cuda(launch_wait_selftest((unsigned long long)limit_ns, ctx, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,19 @@
+// Split-K decode attention kernels for fp32 caches (see attn_impl.cuh).
+#include "attn_impl.cuh"
+
+namespace skv {
+
+cudaError_t launch_split_attn_fp32(const kv_cache_desc& d, const void* q, int G, float sm_scale,
+                                   const int32_t* sel_idx, const int32_t* sel_cnt,
+                                   int sel_stride, int S, float* part_acc, float* part_ml,
+                                   DevCtx ctx, cudaStream_t st) {
+  if (d.head_dim == 128)
+    return launch_split_attn_d<float, 128>(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
+                                          part_acc, part_ml, ctx, st);
+  return launch_split_attn_d<float, 64>(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
+                                       part_acc, part_ml, ctx, st);
+}
+
+size_t split_attn_smem_fp32(int head_dim, int G) { return split_attn_smem_t<float>(head_dim, G); }
+
+}  // namespace skv
