@@ -234,6 +234,28 @@ size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_h
                                      int32_t k_max, int32_t num_splits);
 
 /*
+ * kv_decode_step_static -- kv_decode_step without a workspace argument, for callers that
+ * cannot allocate device memory on the decode path (a plain C or plugin host with no
+ * device allocator of its own, or a serving loop that must not call cudaMalloc per token,
+ * since that can synchronise the device or fail under memory pressure mid-step). The pages
+ * have no counterpart of this call: it only moves the scratch of kv_decode_step into the
+ * library. Inputs, outputs and results are those of kv_decode_step (bit for bit).
+ * Scratch: one file-scope __device__ array of KV_STATIC_SCRATCH_BYTES that every GPU loading
+ * the library holds until exit. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, that device current), so make that first call before any
+ * stream capture. All calls share the array and it keeps the last call's contents: calls
+ * that overlap on the GPU race and must be serialised by the caller. Nothing in it needs to
+ * start at zero. A shape whose scratch (kv_decode_step_workspace_size for the same
+ * arguments) exceeds KV_STATIC_SCRATCH_BYTES returns KV_ERR_WORKSPACE and launches nothing.
+ * This call allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ */
+#define KV_STATIC_SCRATCH_BYTES (8u << 20)
+kv_status kv_decode_step_static(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const void* stats, double keep_ratio,
+                                int32_t budget_pages, int32_t k_max, int32_t num_splits,
+                                float* out, float* lse, cudaStream_t stream);
+
+/*
  * kv_check_device_errors -- synchronises `stream`, reads and clears the current device's
  * error word. Returns KV_OK, KV_ERR_TIMEOUT (a bounded wait ran out) or KV_ERR_BAD_INDEX
  * (any other flag). If flags is not NULL (host), the raw KV_DEVERR_* mask is stored.

@@ -31,7 +31,7 @@ EXPORTS = (
     "kv_select_topk", "kv_sparse_decode_attn", "kv_merge_splits", "kv_auto_num_splits",
     "kv_dropped_mass", "kv_dropped_mass_workspace_size", "kv_decode_step",
     "kv_decode_step_workspace_size", "kv_check_device_errors", "kv_set_wait_limit_ns",
-    "kv_selftest_wait_timeout",
+    "kv_selftest_wait_timeout", "kv_decode_step_static",
 )
 
 
@@ -81,6 +81,7 @@ def _declare(lib):
         "kv_check_device_errors": (I32, [P, ctypes.POINTER(I32)]),
         "kv_set_wait_limit_ns": (I32, [U64]),
         "kv_selftest_wait_timeout": (I32, [U64, P]),
+        "kv_decode_step_static": (I32, [D, P, I32, F32, P, F64, I32, I32, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -361,3 +362,31 @@ def kv_set_wait_limit_ns(limit_ns: int):
 def kv_selftest_wait_timeout(limit_ns: int, stream=None):
     _check("kv_selftest_wait_timeout", lib().kv_selftest_wait_timeout(int(limit_ns),
                                                                       _stream(stream)))
+
+
+STATIC_SCRATCH_BYTES = 8 << 20     # KV_STATIC_SCRATCH_BYTES of include/sparsekv.h
+
+
+def kv_decode_step_static(kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: float = 1.0,
+                          budget_pages: int = 0, k_max: int | None = None, num_splits: int = 0,
+                          out=None, lse=None, stream=None):
+    """kv_decode_step on the library's own static scratch: for callers that cannot allocate
+    device memory on the decode path. Only out and lse are the caller's; calls that overlap
+    on the GPU share the scratch and must be serialised. Raises when the shape needs more
+    scratch than the library holds."""
+    _need(q, "q", kv.dtype)
+    B, Hq, D = q.shape
+    if k_max is None:
+        k_max = max_keep_pages(kv.stride, keep_ratio, budget_pages)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib().kv_decode_step_static(
+        kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(stats), float(keep_ratio),
+        int(budget_pages), int(k_max), int(num_splits), _ptr(out), _ptr(lse), _stream(stream))
+    if st == -4:
+        raise KVError("kv_decode_step_static (the shape needs more than the "
+                      f"{STATIC_SCRATCH_BYTES >> 20} MiB static scratch)", st)
+    _check("kv_decode_step_static", st)
+    return out, lse
