@@ -4,7 +4,7 @@ A step is one sparse decode step over the whole batch: page scores, top-k select
 split-K attention over the selected pages and the log-sum-exp merge (the page statistics
 already exist; their build is timed separately). The dense step is the same attention
 kernel with every page kept, plus the merge. Inputs are resident in HBM; L2 is flushed
-(a 512 MiB write) before every timed step, outside the timed events.
+(a 256 MiB write, twice the L2) before every timed step, outside the timed events.
 
 Prints one JSON line. ``--impl reference`` times the float64 CPU oracle on the same
 workload instead (the reference arm of this comparison).
@@ -33,7 +33,10 @@ METRIC = ("decode-attn µs/step and achieved HBM GB/s vs peak at 32K–1M ctx; "
           "sparse/dense speedup")
 DEFAULT_WORKLOAD = "llama8b_32k"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-ATTN_SOURCE = os.path.join(ROOT, "sparse_kv_cache_build_gb300", "csrc", "attn_impl.cuh")
+CSRC = os.path.join(ROOT, "sparse_kv_cache_build_gb300", "csrc")
+# the attention kernel that runs for each storage dtype, and its source file
+ATTN_KERNEL = {"bf16": ("split_attn_mma_kernel", os.path.join(CSRC, "attn_mma.cuh")),
+               "fp32": ("split_attn_kernel", os.path.join(CSRC, "attn_impl.cuh"))}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -57,20 +60,20 @@ def file_hash(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def committed_traffic(workload, keep_label):
+def committed_traffic(workload, keep_label, dtype):
     """Per-launch DRAM bytes of the attention kernel from a committed ncu summary, if the
     kernel source has not changed since the counters were taken."""
     p = os.path.join(PROFILE_DIR, f"split_attn_{workload}.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("source_hash") != file_hash(ATTN_SOURCE):
+    if d.get("source_hash") != file_hash(ATTN_KERNEL[dtype][1]):
         return None
     return d.get("traffic_bytes_per_launch", {}).get(keep_label)
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -86,7 +89,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -186,7 +189,7 @@ def run_ours(args):
 
     # statistics build (once per cache; timed on its own)
     stats = torch.empty((kv.k_pool.shape[0], Hkv, 2, D), dtype=kv.dtype, device=dev)
-    flush = torch.empty((512 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)   # 2x L2
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     stats_us = []
     for _ in range(3):
@@ -257,12 +260,19 @@ def run_ours(args):
     st, flags = skv.kv_check_device_errors()
     if st != 0:
         raise RuntimeError(f"device error word {flags:#x} after warm-up")
-    g_sparse, g_dense = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # g_sparse is the timed step (kernels back to back, linked by programmatic dependent
+    # launch); g_marked is the same step with event nodes between the kernels, replayed in
+    # its own flushed loop to time each kernel.
+    g_sparse, g_marked, g_dense = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                   torch.cuda.CUDAGraph())
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_sparse, stream=side):
-            sparse_step(in_graph_events)
+            sparse_step(False)
+        if in_graph_events:
+            with torch.cuda.graph(g_marked, stream=side):
+                sparse_step(True)
         with torch.cuda.graph(g_dense, stream=side):
             dense_step()
     stream.wait_stream(side)
@@ -293,7 +303,12 @@ def run_ours(args):
             t1.record()
             torch.cuda.synchronize()
             step_us.append(t0.elapsed_time(t1) * 1e3)
-            if in_graph_events:
+        barrier()
+        if in_graph_events:
+            for _ in range(args.steps):
+                flush.zero_()
+                g_marked.replay()
+                torch.cuda.synchronize()
                 for i, k in enumerate(kern_us):
                     kern_us[k].append(marks[i].elapsed_time(marks[i + 1]) * 1e3)
         barrier()
@@ -382,9 +397,10 @@ def run_ours(args):
             "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "page_size": PS,
             "context_tokens": int(c.seq_lens.sum()), "kv_storage": w.dtype, "keep": label,
             "num_splits": S, "num_splits_dense": S_dense, "parallelism": f"replicas{world}",
-            "l2": "flushed before every timed step (512 MiB write, outside the events)",
-            "graph": "CUDA graph per step" + (" with event nodes between kernels"
-                                               if in_graph_events else ""),
+            "l2": "flushed before every timed step (256 MiB write = 2x L2, outside the events)",
+            "graph": "one CUDA graph per step, kernels linked by programmatic dependent "
+                     "launch; per-kernel times from a copy of the graph with event nodes "
+                     "between kernels, replayed in its own L2-flushed loop",
         },
         "sparse_us": {"median": round(sparse_med, 3), "p10": round(pct(step_us, 10), 3),
                       "p90": round(pct(step_us, 90), 3)},
@@ -401,18 +417,18 @@ def run_ours(args):
         "stats_build_us": round(statistics.median(stats_us), 3),
         "dropped_mass_mean": round(delta_mean, 5),
         "roofline": {
-            "kernel": "split_attn_kernel",
+            "kernel": ATTN_KERNEL[w.dtype][0],
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": committed_traffic(w.name, label),
+            "traffic": committed_traffic(w.name, label, w.dtype),
             "algorithmic_bytes_per_launch": acct["attn_launch"],
             "avg_launch_us": round(attn_us, 3),
         },
-        "gpu_launches": 4 * args.steps + 2 * args.steps,
+        "gpu_launches": 4 * args.steps * (2 if in_graph_events else 1) + 2 * args.steps,
         "clocks": clocks,
     }
     if e2e_us:
@@ -514,7 +530,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

@@ -129,6 +129,22 @@ int32_t kv_version(void);
 kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStream_t stream);
 
 /*
+ * kv_append_token -- [ENTMAX] the cache grows by one token per decode step; this call adds
+ * that token and keeps the page statistics current without re-reading the cache.
+ * For every sequence b with seq_lens[b] > 0 (seq_lens already counts the new token), the
+ * token goes to position t = seq_lens[b] - 1: slot t % page_size of logical page
+ * t / page_size, which page_table must already map. Its key and value rows
+ * k_new[b][g][:], v_new[b][g][:] are written to k_pool and v_pool (the descriptor's pool
+ * pointers are written through), and the page's statistics become the element-wise min/max
+ * of the old ones and the key (a page's first token, slot 0, resets them to the key). The
+ * result equals kv_build_page_stats of the grown cache bit for bit.
+ * k_new, v_new: device [batch][num_kv_heads][head_dim] of the cache dtype.
+ * stats: device [num_phys_pages][num_kv_heads][2][head_dim] of the cache dtype.
+ */
+kv_status kv_append_token(const kv_cache_desc* cache, const void* k_new, const void* v_new,
+                          void* stats, cudaStream_t stream);
+
+/*
  * kv_score_pages -- [ENTMAX] query-aware page score, [SPARDA] summed over a GQA group.
  * scores[b][g][p] = sum over query heads h of group g, over d, of
  *                   max(q[b][h][d] * mn[d], q[b][h][d] * mx[d])

@@ -8,6 +8,7 @@ call does, and raises if it has not been built.
 from . import inputs  # noqa: F401
 from .binding import (  # noqa: F401
     PagedKV,
+    kv_append_token,
     kv_auto_num_splits,
     kv_build_page_stats,
     kv_check_device_errors,

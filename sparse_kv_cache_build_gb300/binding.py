@@ -31,7 +31,7 @@ EXPORTS = (
     "kv_select_topk", "kv_sparse_decode_attn", "kv_merge_splits", "kv_auto_num_splits",
     "kv_dropped_mass", "kv_dropped_mass_workspace_size", "kv_decode_step",
     "kv_decode_step_workspace_size", "kv_check_device_errors", "kv_set_wait_limit_ns",
-    "kv_selftest_wait_timeout", "kv_decode_step_static",
+    "kv_selftest_wait_timeout", "kv_decode_step_static", "kv_append_token",
 )
 
 
@@ -82,6 +82,7 @@ def _declare(lib):
         "kv_set_wait_limit_ns": (I32, [U64]),
         "kv_selftest_wait_timeout": (I32, [U64, P]),
         "kv_decode_step_static": (I32, [D, P, I32, F32, P, F64, I32, I32, I32, P, P, P]),
+        "kv_append_token": (I32, [D, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -206,6 +207,18 @@ def kv_build_page_stats(kv: PagedKV, stats=None, stream=None):
         stats = torch.empty((NP, Hkv, 2, D), dtype=kv.dtype, device=kv.k_pool.device)
     _need(stats, "stats", kv.dtype, (NP, Hkv, 2, D))
     _check("kv_build_page_stats", lib().kv_build_page_stats(kv.ref(), _ptr(stats), _stream(stream)))
+    return stats
+
+
+def kv_append_token(kv: PagedKV, k_new, v_new, stats, stream=None):
+    """Write the new token (position seq_lens[b] - 1) into the pools and fold its key into
+    its page's min/max. k_new, v_new: [B][Hkv][D] of the cache dtype."""
+    shape = (kv.batch, kv.num_kv_heads, kv.head_dim)
+    _need(k_new, "k_new", kv.dtype, shape)
+    _need(v_new, "v_new", kv.dtype, shape)
+    _need(stats, "stats", kv.dtype)
+    _check("kv_append_token", lib().kv_append_token(kv.ref(), _ptr(k_new), _ptr(v_new),
+                                                    _ptr(stats), _stream(stream)))
     return stats
 
 

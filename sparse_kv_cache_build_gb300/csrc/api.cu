@@ -194,6 +194,17 @@ kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStrea
   return from_cuda(launch_page_stats(*cache, stats, ctx, stream));
 }
 
+kv_status kv_append_token(const kv_cache_desc* cache, const void* k_new, const void* v_new,
+                          void* stats, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if (k_new == nullptr || v_new == nullptr || stats == nullptr) return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats) || !aligned16(k_new) || !aligned16(v_new)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(launch_append(*cache, k_new, v_new, stats, ctx, stream));
+}
+
 kv_status kv_score_pages(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                          const void* stats, float* scores, int32_t scores_stride,
                          cudaStream_t stream) {

@@ -1,19 +1,104 @@
-// Split-K decode attention kernels for bf16 caches (see attn_impl.cuh).
+// Split-K decode attention for bf16 caches: the tensor-core kernel of attn_mma.cuh, fed by
+// TMA tensor copies. This file builds the two tensor maps (K and V pools seen as 2-D
+// [NP*Hkv*PS rows][D columns] bf16 arrays, boxes of 64 columns x PS rows, 128-byte swizzle)
+// and launches the kernel.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "attn_impl.cuh"
+#include "attn_mma.cuh"
 
 namespace skv {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool pool_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t rows = (cuuint64_t)d.num_phys_pages * d.num_kv_heads * d.page_size;
+  const cuuint64_t dims[2] = {(cuuint64_t)d.head_dim, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d.head_dim * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)d.page_size};
+  const cuuint32_t elem_strides[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides,
+            box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_mma(const kv_cache_desc& d, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const void* q, float sm_scale, const int32_t* sel_idx,
+                       const int32_t* sel_cnt, int sel_stride, int S, float* part_acc,
+                       float* part_ml, DevCtx ctx, cudaStream_t st) {
+  using C = MmaCfg<D, G>;
+  auto kern = split_attn_mma_kernel<D, G>;
+  static int attr_set_for_device[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set_for_device[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set_for_device[dev] = 1;
+  }
+  dim3 grid(S, d.num_kv_heads, d.batch);
+  return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, mk, mv, d,
+                    static_cast<const uint16_t*>(q), sm_scale * kLog2e, sel_idx, sel_cnt,
+                    sel_stride, S, part_acc, part_ml, ctx);
+}
+
+template <int D>
+cudaError_t launch_mma_d(const kv_cache_desc& d, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const void* q, int G, float sm_scale, const int32_t* sel_idx,
+                         const int32_t* sel_cnt, int sel_stride, int S, float* part_acc,
+                         float* part_ml, DevCtx ctx, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_mma<D, 1>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
+    case 2: return launch_mma<D, 2>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
+    case 4: return launch_mma<D, 4>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
+    case 8: return launch_mma<D, 8>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
 
 cudaError_t launch_split_attn_bf16(const kv_cache_desc& d, const void* q, int G, float sm_scale,
                                    const int32_t* sel_idx, const int32_t* sel_cnt,
                                    int sel_stride, int S, float* part_acc, float* part_ml,
                                    DevCtx ctx, cudaStream_t st) {
+  if ((long long)d.num_phys_pages * d.num_kv_heads * d.page_size >= (1ll << 31))
+    return cudaErrorInvalidValue;                 // TMA row coordinates are 32-bit
+  CUtensorMap mk, mv;
+  if (!pool_map(&mk, d.k_pool, d) || !pool_map(&mv, d.v_pool, d)) return cudaErrorInvalidValue;
   if (d.head_dim == 128)
-    return launch_split_attn_d<bf16_t, 128>(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
-                                          part_acc, part_ml, ctx, st);
-  return launch_split_attn_d<bf16_t, 64>(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
-                                       part_acc, part_ml, ctx, st);
+    return launch_mma_d<128>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
+                             part_acc, part_ml, ctx, st);
+  return launch_mma_d<64>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc,
+                          part_ml, ctx, st);
 }
 
-size_t split_attn_smem_bf16(int head_dim, int G) { return split_attn_smem_t<bf16_t>(head_dim, G); }
+size_t split_attn_smem_bf16(int head_dim, int G) {
+#define SKV_SMEM_CASE(DD, GG) if (head_dim == DD && G == GG) return MmaCfg<DD, GG>::SMEM;
+  SKV_SMEM_CASE(64, 1) SKV_SMEM_CASE(64, 2) SKV_SMEM_CASE(64, 4) SKV_SMEM_CASE(64, 8)
+  SKV_SMEM_CASE(128, 1) SKV_SMEM_CASE(128, 2) SKV_SMEM_CASE(128, 4) SKV_SMEM_CASE(128, 8)
+#undef SKV_SMEM_CASE
+  return 0;
+}
 
 }  // namespace skv

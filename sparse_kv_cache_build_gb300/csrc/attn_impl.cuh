@@ -136,6 +136,8 @@ split_attn_kernel(kv_cache_desc d, const T* __restrict__ q, float qk_scale_log2,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wt = warp % C::NWT, wh = warp / C::NWT;
   const int Hkv = d.num_kv_heads, Hq = Hkv * G, PS = d.page_size;
+  pdl_trigger();
+  pdl_wait();
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, PS);
 
@@ -416,10 +418,8 @@ cudaError_t launch_split_attn_t(const kv_cache_desc& d, const void* q, float sm_
     attr_set_for_device[dev] = 1;
   }
   dim3 grid(S, d.num_kv_heads, d.batch);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(d, static_cast<const T*>(q), sm_scale * kLog2e,
-                                          sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml,
-                                          ctx);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, d, static_cast<const T*>(q),
+                    sm_scale * kLog2e, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx);
 }
 
 template <typename T, int D>

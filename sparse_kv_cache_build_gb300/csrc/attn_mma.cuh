@@ -1,0 +1,350 @@
+// Split-K decode attention for bf16 caches on the tensor cores (GQA-packed q-group x page).
+//
+// Source: "Where Activation Sparsity and KV-Cache Sparsity Cross in LLM Decoding",
+// abstract and Table 11: dense and sparse decoding read the cache through one split-K
+// attention kernel (dense = every page kept). Results are the (m, l, acc) partials of
+// kv_sparse_decode_attn, exactly as the CUDA-core kernel of attn_impl.cuh defines them.
+//
+// Why tensor cores here: per token the work is G dot products of length D for q.k and G
+// more for p.v. On CUDA cores that costs ~1200 warp instructions per 16-token tile and the
+// kernel measured issue/latency-bound at 30-50% of HBM bandwidth. Packing the group's G
+// query heads as the M = 16 rows of an m16n8k16 bf16 MMA cuts it to ~90 instructions:
+//   q.k:  S[h][t] = Q[h][:] . K[t][:]   M = heads, N = 8 tokens x 2, K = D (D/16 steps)
+//   p.v:  O[h][d] += P[h][t] V[t][d]     M = heads, N = 8 columns x D/8, K = 16 tokens
+// The S accumulator fragment of q.k is, register for register, the A fragment of p.v (the
+// FlashAttention-2 register reuse), so probabilities never leave registers. P is rounded to
+// bf16 as a hi part plus a lo part (two MMAs), which keeps p to ~2^-17 relative: products
+// of bf16 inputs are exact and every sum is float32, as on the CUDA-core path.
+//
+// Data movement: pages arrive by TMA tensor copies (cp.async.bulk.tensor.2d) from a 2-D view
+// of the pool, [NP*Hkv*PS rows][D columns], in boxes of 64 columns x PS rows with the
+// 128-byte swizzle, so ldmatrix reads eight consecutive rows at one 16-byte column chunk
+// without bank conflicts. Each stage holds 64 tokens of K and of V; thread 0 keeps NSTAGE
+// stages in flight, completion counted on one mbarrier per stage (bounded waits).
+#pragma once
+
+#include <cuda.h>
+
+#include "kv_internal.cuh"
+
+namespace skv {
+
+template <int D, int G>
+struct MmaCfg {
+  static constexpr int HALVES = D / 64;                    // 64-column (128-byte) halves
+  static constexpr int HALF_BYTES = kTileTokens * 128;     // 64 rows x 128 B
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;   // K (or V) of one stage
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int NSTAGE = 3;
+  static constexpr int THREADS = 128;                      // 4 warps x 16 tokens
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int ONT = D / 8;                        // output n-tiles
+  static constexpr size_t OFF_STAGES = 0;                  // from a 1024-aligned base
+  static constexpr size_t OFF_PHYS = OFF_STAGES + (size_t)NSTAGE * STAGE_BYTES;
+  static constexpr size_t OFF_VALID = OFF_PHYS + 4 * kMaxSplitPages;
+  static constexpr size_t OFF_BAR = OFF_VALID + 2 * kMaxSplitPages;
+  static constexpr size_t SMEM = OFF_BAR + 8 * NSTAGE + 1024;   // + alignment slack
+  static constexpr size_t MERGE_BYTES = 4 * (size_t)4 * G * (D + 2);
+  static_assert(MERGE_BYTES <= (size_t)NSTAGE * STAGE_BYTES, "merge buffers must fit");
+};
+
+// 2-D TMA tile load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                        uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed bf16x2 (round to nearest even), first in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Byte offset, inside one 1024-byte-aligned half, of 16-byte chunk `c` of row `r` under
+// the 128-byte swizzle (chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(MmaCfg<D, G>::THREADS)
+split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, kv_cache_desc d,
+                      const uint16_t* __restrict__ q, float qk_scale_log2,
+                      const int32_t* __restrict__ sel_idx, const int32_t* __restrict__ sel_cnt,
+                      int sel_stride, int S, float* __restrict__ part_acc,
+                      float* __restrict__ part_ml, DevCtx ctx) {
+  using C = MmaCfg<D, G>;
+  extern __shared__ __align__(128) char smem_raw[];
+  char* smem = reinterpret_cast<char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  int32_t* s_phys = reinterpret_cast<int32_t*>(smem + C::OFF_PHYS);
+  int16_t* s_valid = reinterpret_cast<int16_t*>(smem + C::OFF_VALID);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hkv = d.num_kv_heads, Hq = Hkv * G, PS = d.page_size;
+  pdl_trigger();
+  if (tid == 0) {
+    for (int i = 0; i < C::NSTAGE; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  const int len = checked_len(ctx, d, b);
+  const int n_pages = ceil_div(len, PS);
+
+  // ---- this split's run of the page list ------------------------------------------------
+  int cnt = n_pages;
+  const long grp = (long)b * Hkv + g;
+  if (sel_idx != nullptr) {
+    cnt = sel_cnt[grp];
+    if (cnt < 0 || cnt > sel_stride) {
+      if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+      cnt = cnt < 0 ? 0 : sel_stride;
+    }
+  }
+  const int c = cnt > 0 ? ceil_div(cnt, S) : 0;
+  const int pos0 = min(cnt, s * c);
+  int np = min(cnt, pos0 + c) - pos0;
+  if (np > kMaxSplitPages) {
+    if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+    np = kMaxSplitPages;
+  }
+  const int32_t* table = d.page_table + (long)b * d.page_table_stride;
+  for (int i = tid; i < np; i += C::THREADS) {
+    int p = pos0 + i, P = -1, valid = 0;
+    if (sel_idx != nullptr) p = sel_idx[grp * sel_stride + pos0 + i];
+    if (p < 0 || p >= n_pages) {
+      flag(ctx, KV_DEVERR_BAD_SEL);
+    } else {
+      P = table[p];
+      if (P < 0 || P >= d.num_phys_pages) {
+        flag(ctx, KV_DEVERR_BAD_PAGE);
+        P = -1;
+      } else {
+        valid = min(PS, len - p * PS);
+      }
+    }
+    s_phys[i] = P;
+    s_valid[i] = (int16_t)valid;
+  }
+  __syncthreads();
+
+  const int PPT = kTileTokens / PS;
+  const int n_tiles = ceil_div(np, PPT);
+  const uint32_t page_half_bytes = (uint32_t)PS * 128;
+
+  auto issue = [&](int t) {
+    const int st = t % C::NSTAGE;
+    char* kdst = smem + C::OFF_STAGES + (size_t)st * C::STAGE_BYTES;
+    char* vdst = kdst + C::TILE_BYTES;
+    const int i0 = t * PPT, i1 = min(np, i0 + PPT);
+    uint32_t bytes = 0;
+    for (int i = i0; i < i1; ++i)
+      bytes += s_valid[i] > 0 ? 2u * C::HALVES * page_half_bytes : 0u;
+    mbar_arrive_expect_tx(&bars[st], bytes);
+    const uint64_t pol = l2_evict_first_policy();
+    for (int i = i0; i < i1; ++i) {
+      if (s_valid[i] <= 0) continue;
+      const int y = (s_phys[i] * Hkv + g) * PS;
+      const uint32_t off = (uint32_t)(i - i0) * page_half_bytes;
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_load_2d(kdst + h * C::HALF_BYTES + off, &tmK, 64 * h, y, &bars[st], pol);
+        tma_load_2d(vdst + h * C::HALF_BYTES + off, &tmV, 64 * h, y, &bars[st], pol);
+      }
+    }
+  };
+  if (tid == 0) {
+    for (int t = 0; t < C::NSTAGE && t < n_tiles; ++t) issue(t);
+  }
+
+  // ---- q as A fragments: row = lane/4 (query head of the group), rows >= G are zero ----
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t qa0[C::KSTEPS], qa2[C::KSTEPS];
+  {
+    const bool live = gid < G;
+    const uint16_t* qrow = q + ((long)b * Hq + g * G + (live ? gid : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      const uint32_t* p32 = reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
+      qa0[ks] = live ? p32[0] : 0u;
+      qa2[ks] = live ? p32[4] : 0u;
+    }
+  }
+
+  float o[C::ONT][4];
+#pragma unroll
+  for (int nt = 0; nt < C::ONT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_run = -INFINITY, l_lane = 0.f;
+
+  // ldmatrix lane roles
+  const int lm = lane >> 3, lr = lane & 7;
+  bool aborted = false;
+  int t = 0;
+  for (; t < n_tiles; ++t) {
+    const int st = t % C::NSTAGE;
+    const bool ok = mbar_wait_bounded(&bars[st], (uint32_t)((t / C::NSTAGE) & 1), ctx.wait_ns);
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+
+    const int tok_base = warp * kWarpTokens;
+    const int slot = t * PPT + tok_base / PS;
+    int vt = 0;
+    if (slot < np) vt = max(0, min(kWarpTokens, (int)s_valid[slot] - tok_base % PS));
+
+    if (vt > 0) {
+      const uint32_t kbase = smem_addr(smem + C::OFF_STAGES + (size_t)st * C::STAGE_BYTES);
+      const uint32_t vbase = kbase + C::TILE_BYTES;
+      // ---- S = Q K^T for 16 tokens (two n-tiles of 8) ------------------------------------
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        const int row = tok_base + (lm >> 1) * 8 + lr;
+        const int col = ks * 16 + (lm & 1) * 8;              // element column
+        const uint32_t addr = kbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(addr, b00, b01, b10, b11);
+        mma_bf16(sc[0], qa0[ks], 0u, qa2[ks], 0u, b00, b01);
+        mma_bf16(sc[1], qa0[ks], 0u, qa2[ks], 0u, b10, b11);
+      }
+      // ---- online softmax (base 2) for row gid; tokens nt*8 + 2*tig + {0,1} ---------------
+      float x[4];
+      x[0] = (2 * tig < vt) ? sc[0][0] * qk_scale_log2 : -INFINITY;
+      x[1] = (2 * tig + 1 < vt) ? sc[0][1] * qk_scale_log2 : -INFINITY;
+      x[2] = (8 + 2 * tig < vt) ? sc[1][0] * qk_scale_log2 : -INFINITY;
+      x[3] = (8 + 2 * tig + 1 < vt) ? sc[1][1] * qk_scale_log2 : -INFINITY;
+      float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+      const float m_new = fmaxf(m_run, mt);
+      const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = x[i] == -INFINITY ? 0.f : exp2f(x[i] - m_new);
+      l_lane = l_lane * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+      m_run = m_new;
+      if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < C::ONT; ++nt) { o[nt][0] *= alpha; o[nt][1] *= alpha; }
+      }
+      // P as bf16 hi + lo A fragments (rows gid; rows gid + 8 are zero)
+      const uint32_t ph0 = pack_bf16(p[0], p[1]), ph2 = pack_bf16(p[2], p[3]);
+      const uint32_t pl0 = pack_bf16(p[0] - bf16_lo_f(ph0), p[1] - bf16_hi_f(ph0));
+      const uint32_t pl2 = pack_bf16(p[2] - bf16_lo_f(ph2), p[3] - bf16_hi_f(ph2));
+      // masked tokens of a partial page: zero their V elements (may hold any bits)
+      uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+      if (vt < kWarpTokens) {
+        vm0 = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
+        vm1 = (8 + 2 * tig < vt ? 0x0000ffffu : 0u) | (8 + 2 * tig + 1 < vt ? 0xffff0000u : 0u);
+      }
+      // ---- O += P V ------------------------------------------------------------------------
+#pragma unroll
+      for (int np2 = 0; np2 < C::ONT / 2; ++np2) {
+        const int row = tok_base + (lm & 1) * 8 + lr;
+        const int col = np2 * 16 + (lm >> 1) * 8;
+        const uint32_t addr = vbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
+        uint32_t v00, v01, v10, v11;
+        ldsm_x4_t(addr, v00, v01, v10, v11);
+        v00 &= vm0; v01 &= vm1; v10 &= vm0; v11 &= vm1;
+        mma_bf16(o[2 * np2], ph0, 0u, ph2, 0u, v00, v01);
+        mma_bf16(o[2 * np2], pl0, 0u, pl2, 0u, v00, v01);
+        mma_bf16(o[2 * np2 + 1], ph0, 0u, ph2, 0u, v10, v11);
+        mma_bf16(o[2 * np2 + 1], pl0, 0u, pl2, 0u, v10, v11);
+      }
+    }
+    __syncthreads();                                       // stage st is free again
+    if (tid == 0 && t + C::NSTAGE < n_tiles) issue(t + C::NSTAGE);
+  }
+
+  const long out_row = ((long)b * Hq + g * G) * S + s;
+  if (aborted) {
+    if (tid == 0) {
+      flag(ctx, KV_DEVERR_TIMEOUT);
+      for (int u = t; u < n_tiles && u < t + C::NSTAGE; ++u)
+        mbar_wait_bounded(&bars[u % C::NSTAGE], (uint32_t)((u / C::NSTAGE) & 1), ctx.wait_ns);
+    }
+    for (int i = tid; i < G * D; i += C::THREADS) {
+      const int hl = i / D, dd = i % D;
+      part_acc[(out_row + (long)hl * S) * D + dd] = 0.f;
+      if (dd == 0) {
+        part_ml[(out_row + (long)hl * S) * 2 + 0] = -INFINITY;
+        part_ml[(out_row + (long)hl * S) * 2 + 1] = 0.f;
+      }
+    }
+    return;
+  }
+
+  // ---- merge the four token warps ---------------------------------------------------------
+  l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 1);
+  l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 2);
+  float* mg_o = reinterpret_cast<float*>(smem + C::OFF_STAGES);         // [4][G][D]
+  float* mg_m = mg_o + 4 * G * D;                                       // [4][G]
+  float* mg_l = mg_m + 4 * G;
+  if (gid < G) {
+    if (tig == 0) {
+      mg_m[warp * G + gid] = m_run;
+      mg_l[warp * G + gid] = l_lane;
+    }
+#pragma unroll
+    for (int nt = 0; nt < C::ONT; ++nt) {
+      mg_o[(warp * G + gid) * D + nt * 8 + 2 * tig] = o[nt][0];
+      mg_o[(warp * G + gid) * D + nt * 8 + 2 * tig + 1] = o[nt][1];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += C::THREADS) {
+    const int hl = i / D, dd = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, mg_m[w2 * G + hl]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w2 = 0; w2 < 4; ++w2) {
+        const float mw = mg_m[w2 * G + hl];
+        const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        L = fmaf(mg_l[w2 * G + hl], sc, L);
+        A = fmaf(mg_o[(w2 * G + hl) * D + dd], sc, A);
+      }
+    }
+    part_acc[(out_row + (long)hl * S) * D + dd] = A;
+    if (dd == 0) {
+      part_ml[(out_row + (long)hl * S) * 2 + 0] = M == -INFINITY ? -INFINITY : M * kLn2;
+      part_ml[(out_row + (long)hl * S) * 2 + 1] = L;
+    }
+  }
+}
+
+}  // namespace skv

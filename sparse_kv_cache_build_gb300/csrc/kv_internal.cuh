@@ -127,6 +127,36 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 }
 
 // ------------------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel of the library lets the next kernel on the
+// stream start launching as soon as all of its own blocks are running (pdl_trigger), and
+// waits for the previous kernel to finish and flush (pdl_wait) before its first access to
+// global memory, so only launch latency and on-chip set-up overlap. Both are no-ops when the
+// kernel was launched without the programmatic-serialisation attribute.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kern` on `s` with the programmatic-serialisation attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
 // Small math helpers
 // ------------------------------------------------------------------------------------
 constexpr float kLog2e = 1.4426950408889634f;
@@ -169,6 +199,8 @@ cudaError_t launch_dropped_mass(const kv_cache_desc& d, const void* q, int Hq,
                                 const int32_t* sel_cnt, int sel_stride, int num_splits,
                                 float* partials, float* delta, DevCtx ctx, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, DevCtx ctx, cudaStream_t s);
+cudaError_t launch_append(const kv_cache_desc& d, const void* k_new, const void* v_new,
+                          void* stats, DevCtx ctx, cudaStream_t s);
 
 // Dynamic shared memory bytes of the attention kernel for this shape (0 = unsupported).
 size_t split_attn_smem_bytes(int dtype, int head_dim, int group_size);

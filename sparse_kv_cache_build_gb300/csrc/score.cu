@@ -16,17 +16,18 @@
 // its contiguous stats row with that vector.
 //
 // The pass streams the stats array (2*D elements per page and KV head) once: it is
-// HBM-bound. Eight lanes own one page (16-byte chunks j, j+8, ... of the row), so a warp
-// instruction reads four whole rows, and a block covers 128 pages with all loads of a
-// warp's four steps in flight before any arithmetic.
+// HBM-bound, and short, so it is built to put every load in flight in one wave. Eight lanes
+// own one page (16-byte chunks j, j+8, ... of the row), a 128-thread block covers 16 pages,
+// and the grid covers every page of every group. Each block issues its page-table and
+// statistics loads first and only then builds Pos/Neg from q, so the two latency chains
+// overlap.
 #include "kv_internal.cuh"
 
 namespace skv {
 namespace {
 
-constexpr int kScoreWarps = 8;
-constexpr int kScoreSteps = 4;                                    // pages per 8-lane group
-constexpr int kScorePagesPerBlock = kScoreWarps * 4 * kScoreSteps;  // 128
+constexpr int kScoreWarps = 4;
+constexpr int kScorePagesPerBlock = kScoreWarps * 4;   // 16
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kScoreWarps * 32)
@@ -36,6 +37,8 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restric
   constexpr int EPC = 16 / EB;                // elements per 16-byte chunk
   constexpr int CPL = (2 * D * EB / 16) / 8;  // chunks per lane per stats row
   __shared__ __align__(16) float w[2 * D];    // [Neg | Pos], matching a row's [mn | mx]
+  pdl_trigger();
+  pdl_wait();
 
   const int b = blockIdx.z, g = blockIdx.y;
   const int len = checked_len(ctx, d, b);
@@ -44,8 +47,26 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restric
   if (p_block >= n_pages) return;
 
   const int Hkv = d.num_kv_heads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane >> 3, j = lane & 7;
+  const int p = p_block + warp * 4 + grp;
+  uint4 raw[CPL];
+  bool ok = false;
+  if (p < n_pages) {
+    const int P = d.page_table[(long)b * d.page_table_stride + p];
+    if (P >= 0 && P < d.num_phys_pages) {
+      ok = true;
+      const uint4* row = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const char*>(stats) + (((long)P * Hkv + g) * 2 * D) * EB);
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) raw[u] = __ldg(row + j + 8 * u);
+    } else if (j == 0) {
+      flag(ctx, KV_DEVERR_BAD_PAGE);
+    }
+  }
+
   const int Hq = Hkv * G;
-  for (int t = threadIdx.x; t < D; t += blockDim.x) {
+  for (int t = threadIdx.x; t < D; t += kScoreWarps * 32) {
     float pos = 0.f, neg = 0.f;
     for (int h = g * G; h < (g + 1) * G; ++h) {
       const float x = load_elem<T>(q, ((long)b * Hq + h) * D + t);
@@ -57,59 +78,30 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restric
   }
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 3, j = lane & 7;
-  const int32_t* table = d.page_table + (long)b * d.page_table_stride;
-  const char* sbase = reinterpret_cast<const char*>(stats);
-
-  uint4 raw[kScoreSteps][CPL];
-  bool ok[kScoreSteps];
+  float acc = 0.f;
+  if (ok) {
 #pragma unroll
-  for (int st = 0; st < kScoreSteps; ++st) {
-    const int p = p_block + (st * kScoreWarps + warp) * 4 + grp;
-    ok[st] = false;
-    if (p < n_pages) {
-      const int P = table[p];
-      if (P >= 0 && P < d.num_phys_pages) {
-        ok[st] = true;
-        const uint4* row = reinterpret_cast<const uint4*>(
-            sbase + (((long)P * Hkv + g) * 2 * D) * EB);
+    for (int u = 0; u < CPL; ++u) {
+      float f[EPC];
+      chunk_to_f32<T>(raw[u], f);
+      const float* wc = w + (j + 8 * u) * EPC;
 #pragma unroll
-        for (int u = 0; u < CPL; ++u) raw[st][u] = __ldg(row + j + 8 * u);
-      } else if (j == 0) {
-        flag(ctx, KV_DEVERR_BAD_PAGE);
-      }
+      for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
     }
   }
-#pragma unroll
-  for (int st = 0; st < kScoreSteps; ++st) {
-    float acc = 0.f;
-    if (ok[st]) {
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) {
-        float f[EPC];
-        chunk_to_f32<T>(raw[st][u], f);
-        const float* wc = w + (j + 8 * u) * EPC;
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
-      }
-    }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    const int p = p_block + (st * kScoreWarps + warp) * 4 + grp;
-    if (j == 0 && ok[st]) scores[((long)b * Hkv + g) * scores_stride + p] = acc;
-  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  if (j == 0 && ok) scores[((long)b * Hkv + g) * scores_stride + p] = acc;
 }
 
 template <typename T, int D>
 cudaError_t launch_t(const kv_cache_desc& d, const void* q, int Hq, const void* stats,
                      float* scores, int scores_stride, DevCtx ctx, cudaStream_t s) {
   dim3 grid(ceil_div(d.page_table_stride, kScorePagesPerBlock), d.num_kv_heads, d.batch);
-  score_kernel<T, D><<<grid, kScoreWarps * 32, 0, s>>>(
-      d, static_cast<const T*>(q), Hq / d.num_kv_heads, static_cast<const T*>(stats), scores,
-      scores_stride, ctx);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel<T, D>, grid, dim3(kScoreWarps * 32), 0, s, d,
+                    static_cast<const T*>(q), Hq / d.num_kv_heads,
+                    static_cast<const T*>(stats), scores, scores_stride, ctx);
 }
 
 }  // namespace

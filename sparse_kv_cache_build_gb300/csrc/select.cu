@@ -10,19 +10,19 @@
 // page order.
 //
 // One 1024-thread block per group. Scores are mapped to unsigned keys whose integer order
-// is the float order, and a most-significant-digit radix select (four 8-bit passes over
-// the group's scores, histograms in shared memory with warp-aggregated atomics) finds the
-// k-th largest key T and how many keys equal to T are kept (the lowest-indexed ones). A
-// final ordered pass stages 8192 keys at a time in shared memory, each thread scanning 8
-// consecutive keys; one block-wide exclusive scan of (greater-than-T, equal-to-T) counts
-// gives each kept page its output slot, so the output is ascending by construction. The
-// score rows are small (4 bytes per page) and stay in L2 across the passes.
+// is the float order, and a most-significant-digit radix select (up to four 8-bit passes,
+// histograms in shared memory with warp-aggregated atomics) finds the k-th largest key T
+// and how many keys equal to T are kept (the lowest-indexed ones). Groups of up to 16384
+// pages keep their keys in registers (16 per thread) for every pass, so the scores are read
+// from memory once; a pass that finds a digit bin holding exactly the keys still needed
+// ends the search early (every key at or above that bin is kept). The ordered compaction
+// then runs one block-wide exclusive scan of packed (greater-than-T, equal-to-T) counts per
+// 1024 consecutive pages, which gives each kept page its output slot, so the output is
+// ascending by construction. Longer groups take the same steps reading keys from L2.
 #include "kv_internal.cuh"
 
 namespace skv {
 namespace {
-
-constexpr int kItems = kSelectChunk / kSelectThreads;   // 8 keys per thread per chunk
 
 __device__ __forceinline__ uint32_t order_key(float s) {
   const uint32_t u = __float_as_uint(s + 0.0f);          // -0 -> +0: equal scores, equal keys
@@ -71,6 +71,11 @@ __device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t* w
   return warp_tot[warp] + incl - v;
 }
 
+constexpr int kRegKeys = 16;                 // keys per thread kept in registers
+
+// REG: keys live in registers (n <= kRegKeys * kSelectThreads); otherwise each pass
+// re-reads them from the score row (L2-resident).
+template <bool REG>
 __global__ void __launch_bounds__(kSelectThreads)
 select_kernel(const float* __restrict__ scores, int scores_stride,
               const int32_t* __restrict__ seq_lens, int PS, int Hkv,
@@ -78,10 +83,11 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
               int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt, int table_stride,
               DevCtx ctx) {
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t s_prefix, s_remaining;
+  __shared__ uint32_t s_prefix, s_remaining, s_exact;
   __shared__ uint64_t warp_tot[32];
   __shared__ uint64_t s_total;
-  __shared__ uint32_t keys[kSelectChunk];
+  pdl_trigger();
+  pdl_wait();
 
   const int g = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -107,20 +113,40 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
   }
   if (k == 0) return;
 
+  const int nj = ceil_div(n, kSelectThreads);   // key slices of 1024 consecutive pages
+  uint32_t rk[REG ? kRegKeys : 1];
+  if constexpr (REG) {
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      const int i = j * kSelectThreads + tid;
+      rk[j] = i < n ? order_key(row[i]) : 0u;
+    }
+  }
+  auto key_of = [&](int j) -> uint32_t {
+    if constexpr (REG) return rk[j];
+    else return order_key(row[j * kSelectThreads + tid]);
+  };
+
   // ---- radix select of the k-th largest key -------------------------------------------
   uint32_t prefix = 0, mask = 0, remaining = (uint32_t)k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  bool exact = false;
+  for (int shift = 24; shift >= 0 && !exact; shift -= 8) {
     for (int i = tid; i < 256; i += kSelectThreads) hist[i] = 0;
+    if (tid == 0) s_exact = 0;
     __syncthreads();
-    for (int base = 0; base < n; base += kSelectThreads) {
-      const int i = base + tid;
-      uint32_t digit = 256;                  // 256 = not counted in this pass
-      if (i < n) {
-        const uint32_t key = order_key(row[i]);
-        if ((key & mask) == prefix) digit = (key >> shift) & 255u;
+#pragma unroll
+    for (int j = 0; j < (REG ? kRegKeys : 1); ++j) {
+      for (int jj = j; jj < (REG ? j + 1 : nj); ++jj) {
+        if (REG && jj >= nj) break;
+        const int i = jj * kSelectThreads + tid;
+        uint32_t digit = 256;                // 256 = not counted in this pass
+        if (i < n) {
+          const uint32_t key = key_of(jj);
+          if ((key & mask) == prefix) digit = (key >> shift) & 255u;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+        if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
       }
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
     }
     __syncthreads();
     if (warp == 0) {
@@ -140,6 +166,7 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
           if (above + c[e] >= remaining) {
             s_prefix = prefix | ((uint32_t)(lane * 8 + e) << shift);
             s_remaining = remaining - above;
+            s_exact = (above + c[e] == remaining) ? 1u : 0u;
             break;
           }
           above += c[e];
@@ -149,47 +176,36 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
     __syncthreads();
     prefix = s_prefix;
     remaining = s_remaining;
+    exact = s_exact != 0;
     mask |= 255u << shift;
   }
-  const uint32_t T = prefix;                 // the k-th largest key
-  const uint32_t take_eq = remaining;        // keys equal to T that are kept (>= 1)
+  // Keep key > T, and the first take_eq keys equal to T in page order. When a bin held
+  // exactly the keys still needed, every key >= its (zero-extended) prefix is kept.
+  const uint32_t T = prefix;
+  const uint32_t take_eq = exact ? 0xffffffffu : remaining;
 
-  // ---- ordered compaction ---------------------------------------------------------------
+  // ---- ordered compaction, one slice of 1024 pages at a time ------------------------------
   uint32_t carry_gt = 0, carry_eq = 0;
-  for (int c0 = 0; c0 < n; c0 += kSelectChunk) {
-    for (int i = tid; i < kSelectChunk; i += kSelectThreads)
-      keys[i] = (c0 + i < n) ? order_key(row[c0 + i]) : 0u;
-    __syncthreads();
-    uint32_t gt = 0, eq = 0;
+  for (int j = 0; j < nj; ++j) {
+    const int i = j * kSelectThreads + tid;
+    uint32_t key = 0;
+    bool valid = i < n;
+    if constexpr (REG) {
 #pragma unroll
-    for (int e = 0; e < kItems; ++e) {
-      const int idx = tid * kItems + e;
-      if (c0 + idx < n) {
-        const uint32_t key = keys[idx];
-        gt += key > T;
-        eq += key == T;
-      }
+      for (int jj = 0; jj < kRegKeys; ++jj) key = (jj == j) ? rk[jj] : key;
+    } else {
+      if (valid) key = order_key(row[i]);
     }
+    const uint32_t gt = valid && key > T;
+    const uint32_t eq = valid && key == T;
     const uint64_t ex = block_exclusive_scan(((uint64_t)gt << 32) | eq, warp_tot, &s_total);
-    uint32_t gt_before = carry_gt + (uint32_t)(ex >> 32);
-    uint32_t eq_before = carry_eq + (uint32_t)(ex & 0xffffffffu);
-#pragma unroll
-    for (int e = 0; e < kItems; ++e) {
-      const int idx = tid * kItems + e;
-      if (c0 + idx < n) {
-        const uint32_t key = keys[idx];
-        if (key > T) {
-          out[gt_before + min(eq_before, take_eq)] = c0 + idx;
-          ++gt_before;
-        } else if (key == T) {
-          if (eq_before < take_eq) out[gt_before + eq_before] = c0 + idx;
-          ++eq_before;
-        }
-      }
-    }
+    const uint32_t gt_before = carry_gt + (uint32_t)(ex >> 32);
+    const uint32_t eq_before = carry_eq + (uint32_t)(ex & 0xffffffffu);
+    if (gt) out[gt_before + min(eq_before, take_eq)] = i;
+    else if (eq && eq_before < take_eq) out[gt_before + eq_before] = i;
     carry_gt += (uint32_t)(s_total >> 32);
     carry_eq += (uint32_t)(s_total & 0xffffffffu);
-    __syncthreads();                         // keys[] and s_total are reused next chunk
+    __syncthreads();                         // warp_tot / s_total are rewritten next slice
   }
 }
 
@@ -201,10 +217,11 @@ cudaError_t launch_select_topk(const float* scores, int scores_stride, const int
                                int32_t* sel_idx, int32_t* sel_cnt, int page_table_stride,
                                DevCtx ctx, cudaStream_t s) {
   dim3 grid(Hkv, batch);
-  select_kernel<<<grid, kSelectThreads, 0, s>>>(scores, scores_stride, seq_lens, page_size,
-                                                Hkv, keep, keep_ratio, budget_pages, k_max,
-                                                sel_idx, sel_cnt, page_table_stride, ctx);
-  return cudaGetLastError();
+  auto kern = page_table_stride <= kRegKeys * kSelectThreads ? select_kernel<true>
+                                                              : select_kernel<false>;
+  return launch_pdl(kern, grid, dim3(kSelectThreads), 0, s, scores, scores_stride, seq_lens,
+                    page_size, Hkv, keep, keep_ratio, budget_pages, k_max, sel_idx, sel_cnt,
+                    page_table_stride, ctx);
 }
 
 }  // namespace skv
