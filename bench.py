@@ -60,14 +60,14 @@ def file_hash(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def committed_traffic(workload, keep_label, dtype):
-    """Per-launch DRAM bytes of the attention kernel from a committed ncu summary, if the
+def committed_traffic(workload, keep_label, source):
+    """Per-launch DRAM bytes of the timed kernel from a committed ncu summary, if the
     kernel source has not changed since the counters were taken."""
-    p = os.path.join(PROFILE_DIR, f"split_attn_{workload}.json")
+    p = os.path.join(PROFILE_DIR, f"{os.path.basename(source).split('.')[0]}_{workload}.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("source_hash") != file_hash(ATTN_KERNEL[dtype][1]):
+    if d.get("source_hash") != file_hash(source):
         return None
     return d.get("traffic_bytes_per_launch", {}).get(keep_label)
 
@@ -205,10 +205,13 @@ def run_ours(args):
         k_max = keep["keep_pages"]
         keep_t = torch.full((B,), k_max, dtype=torch.int32, device=dev)
         sel_kw = dict(keep=keep_t, k_max=k_max)
+        step_kw = None                 # a fixed per-group keep count has no kv_decode_step form
     else:
         k_max = skv.max_keep_pages(kv.stride, keep.get("keep_ratio"), keep.get("budget_pages"))
         sel_kw = dict(keep_ratio=keep.get("keep_ratio", 0.0),
                       budget_pages=keep.get("budget_pages", 0), k_max=k_max)
+        step_kw = dict(keep_ratio=keep.get("keep_ratio", 1.0),
+                       budget_pages=keep.get("budget_pages", 0))
     S = skv.kv_auto_num_splits(kv, Hq, k_max)
     S_dense = skv.kv_auto_num_splits(kv, Hq, kv.stride)
     scores = torch.empty((B, Hkv, kv.stride), dtype=torch.float32, device=dev)
@@ -222,6 +225,8 @@ def run_ours(args):
     ml_d = torch.empty((B, Hq, S_dense, 2), dtype=torch.float32, device=dev)
     out_d = torch.empty_like(out)
     lse_d = torch.empty_like(lse)
+    ws = torch.empty((skv.kv_decode_step_workspace_size(kv, Hq, k_max),), dtype=torch.uint8,
+                     device=dev)
 
     try:
         marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
@@ -230,7 +235,7 @@ def run_ours(args):
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         in_graph_events = False
 
-    def sparse_step(with_marks):
+    def four_kernel_step(with_marks):
         if with_marks:
             marks[0].record()
         skv.kv_score_pages(kv, c.q, stats, scores)
@@ -247,43 +252,77 @@ def run_ours(args):
         if with_marks:
             marks[4].record()
 
-    def dense_step():
-        skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, None, None, num_splits=S_dense,
-                                  part_acc=acc_d, part_ml=ml_d)
-        skv.kv_merge_splits(acc_d, ml_d, out_d, lse_d)
+    def step():
+        """The call a user makes for one sparse decode step (one launch where possible)."""
+        if step_kw is None:
+            four_kernel_step(False)
+        else:
+            skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
+                               workspace=ws, **step_kw)
 
-    # warm up eagerly, then capture both steps as CUDA graphs
+    def one_launch_step():
+        """The step as one cluster launch (where the shape allows it)."""
+        skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
+                           workspace=ws, num_splits=skv.ONE_LAUNCH, **step_kw)
+
+    def dense_step():
+        """The same call with every page kept: the same kernel, no scoring or selection."""
+        if step_kw is None:
+            skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, None, None, num_splits=S_dense,
+                                      part_acc=acc_d, part_ml=ml_d)
+            skv.kv_merge_splits(acc_d, ml_d, out_d, lse_d)
+        else:
+            skv.kv_decode_step(kv, c.q, w.sm_scale, keep_ratio=1.0, out=out_d, lse=lse_d,
+                               workspace=ws)
+
+    # warm up eagerly (this also fixes each shape's launch configuration)
     for _ in range(max(1, args.warmup)):
-        sparse_step(False)
+        step()
         dense_step()
+        four_kernel_step(False)
     torch.cuda.synchronize()
     st, flags = skv.kv_check_device_errors()
     if st != 0:
         raise RuntimeError(f"device error word {flags:#x} after warm-up")
-    # g_sparse is the timed step (kernels back to back, linked by programmatic dependent
-    # launch); g_marked is the same step with event nodes between the kernels, replayed in
-    # its own flushed loop to time each kernel.
-    g_sparse, g_marked, g_dense = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
-                                   torch.cuda.CUDAGraph())
+    one_launch = one_launch_ran = False
+    if step_kw is not None:            # one launch leaves the score region of ws untouched
+        score_bytes = (B * Hkv * kv.stride * 4 + 255) // 256 * 256
+        for fn in (step, one_launch_step):
+            ws[:score_bytes].fill_(255)
+            fn()
+            torch.cuda.synchronize()
+            ran = bool((ws[:score_bytes] == 255).all())
+            if fn is step:
+                one_launch = ran
+            else:
+                one_launch_ran = ran
+
+    # one CUDA graph per measured step; g_marked is the four-kernel step with event nodes
+    # between its kernels, replayed in its own flushed loop to time each kernel
+    g_step, g_dense, g_four, g_marked, g_one = (torch.cuda.CUDAGraph() for _ in range(5))
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        with torch.cuda.graph(g_sparse, stream=side):
-            sparse_step(False)
-        if in_graph_events:
-            with torch.cuda.graph(g_marked, stream=side):
-                sparse_step(True)
+        with torch.cuda.graph(g_step, stream=side):
+            step()
         with torch.cuda.graph(g_dense, stream=side):
             dense_step()
+        with torch.cuda.graph(g_four, stream=side):
+            four_kernel_step(False)
+        if in_graph_events:
+            with torch.cuda.graph(g_marked, stream=side):
+                four_kernel_step(True)
+        if step_kw is not None:
+            with torch.cuda.graph(g_one, stream=side):
+                one_launch_step()
     stream.wait_stream(side)
     torch.cuda.synchronize()
 
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
-        flush.zero_()
-        g_sparse.replay()
-        flush.zero_()
-        g_dense.replay()
+        for g_ in (g_step, g_dense, g_four):
+            flush.zero_()
+            g_.replay()
     torch.cuda.synchronize()
 
     def barrier():
@@ -292,17 +331,28 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- timed region: K sparse steps (then K dense steps), L2 flushed before each ------
-    step_us, kern_us = [], {"score": [], "select": [], "attn": [], "merge": []}
-    barrier()
-    with ClockSampler(local) as clk:
+    def timed(graph):
+        res = []
         for _ in range(args.steps):
             flush.zero_()
             t0.record()
-            g_sparse.replay()
+            graph.replay()
             t1.record()
             torch.cuda.synchronize()
-            step_us.append(t0.elapsed_time(t1) * 1e3)
+            res.append(t0.elapsed_time(t1) * 1e3)
+        return res
+
+    # ---- timed region: K steps of each kind, L2 flushed before every step ---------------
+    kern_us = {"score": [], "select": [], "attn": [], "merge": []}
+    barrier()
+    with ClockSampler(local) as clk:
+        step_us = timed(g_step)
+        barrier()
+        dense_us = timed(g_dense)
+        barrier()
+        four_us = timed(g_four)
+        barrier()
+        one_us = timed(g_one) if one_launch_ran else []
         barrier()
         if in_graph_events:
             for _ in range(args.steps):
@@ -312,21 +362,12 @@ def run_ours(args):
                 for i, k in enumerate(kern_us):
                     kern_us[k].append(marks[i].elapsed_time(marks[i + 1]) * 1e3)
         barrier()
-        dense_us = []
-        for _ in range(args.steps):
-            flush.zero_()
-            t0.record()
-            g_dense.replay()
-            t1.record()
-            torch.cuda.synchronize()
-            dense_us.append(t0.elapsed_time(t1) * 1e3)
-    barrier()
     clocks = clk.summary()
 
     if not in_graph_events:        # per-kernel times from eager launches instead
         for _ in range(args.steps):
             flush.zero_()
-            sparse_step(True)
+            four_kernel_step(True)
             torch.cuda.synchronize()
             for i, k in enumerate(kern_us):
                 kern_us[k].append(marks[i].elapsed_time(marks[i + 1]) * 1e3)
@@ -334,6 +375,8 @@ def run_ours(args):
     st, flags = skv.kv_check_device_errors()
     if st != 0:
         raise RuntimeError(f"device error word {flags:#x} after the timed region")
+    four_kernel_step(False)
+    torch.cuda.synchronize()
     sel_cnt = cnt.cpu().numpy()
     acct = byte_account(w, n_pages, sel_cnt, S)
 
@@ -345,20 +388,15 @@ def run_ours(args):
     q_host = c.q.detach().cpu().pin_memory()
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(c.q)
-    ws = torch.empty((skv.kv_decode_step_workspace_size(kv, Hq, k_max, S),), dtype=torch.uint8,
-                     device=dev)
-    step_kw = dict(keep_ratio=keep.get("keep_ratio", 1.0), budget_pages=keep.get("budget_pages", 0))
-    if "keep_pages" in keep:
-        step_kw = None                 # a fixed per-group keep count has no fused form
     e2e_us = []
     if step_kw is not None:
-        for i in range(args.warmup + args.steps):
+        for i in range(args.warmup + min(args.steps, 500)):
             flush.zero_()
             torch.cuda.synchronize()
             h0 = time.perf_counter()
             q_dev.copy_(q_host, non_blocking=True)
-            skv.kv_decode_step(kv, q_dev, w.sm_scale, stats, k_max=k_max, num_splits=S, out=out,
-                               lse=lse, workspace=ws, **step_kw)
+            skv.kv_decode_step(kv, q_dev, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
+                               workspace=ws, **step_kw)
             out_host.copy_(out, non_blocking=True)
             torch.cuda.synchronize()
             if i >= args.warmup:
@@ -377,8 +415,17 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     attn_us = statistics.mean(kern_us["attn"]) if kern_us["attn"] else float("nan")
-    achieved = acct["attn_launch"] / (attn_us * 1e-6) / 1e9
     dense_med = statistics.median(dense_us)
+    step_mean = statistics.mean(step_us)
+    dense_mean = statistics.mean(dense_us)
+    if one_launch:
+        # the step is a single kernel: its duration is the event-timed step
+        roof_kernel, roof_bytes, roof_us = "fused_step_kernel", acct["sparse_step"], step_mean
+        roof_source = os.path.join(CSRC, "step_fused.cu")
+    else:
+        roof_kernel, roof_bytes, roof_us = ATTN_KERNEL[w.dtype][0], acct["attn_launch"], attn_us
+        roof_source = ATTN_KERNEL[w.dtype][1]
+    achieved = roof_bytes / (roof_us * 1e-6) / 1e9
     line = {
         "metric": METRIC,
         "value": round(sparse_med, 3),
@@ -396,11 +443,12 @@ def run_ours(args):
             "workload": w.name, "description": w.description, "batch": B,
             "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "page_size": PS,
             "context_tokens": int(c.seq_lens.sum()), "kv_storage": w.dtype, "keep": label,
-            "num_splits": S, "num_splits_dense": S_dense, "parallelism": f"replicas{world}",
+            "step_path": ("one launch: kv_decode_step, a thread-block cluster per (sequence, "
+                          "KV head)" if one_launch else
+                          f"four kernels (score, select, attention, merge), {S} splits"),
+            "num_splits_four_kernel": S, "parallelism": f"replicas{world}",
             "l2": "flushed before every timed step (256 MiB write = 2x L2, outside the events)",
-            "graph": "one CUDA graph per step, kernels linked by programmatic dependent "
-                     "launch; per-kernel times from a copy of the graph with event nodes "
-                     "between kernels, replayed in its own L2-flushed loop",
+            "graph": "one CUDA graph per step, replayed once per timed step",
         },
         "sparse_us": {"median": round(sparse_med, 3), "p10": round(pct(step_us, 10), 3),
                       "p90": round(pct(step_us, 90), 3)},
@@ -410,25 +458,34 @@ def run_ours(args):
         "byte_bound": round(acct["dense_step"] / acct["sparse_step"], 3),
         "step_gbs": {"sparse": round(acct["sparse_step"] / (sparse_med * 1e-6) / 1e9, 1),
                      "dense": round(acct["dense_step"] / (dense_med * 1e-6) / 1e9, 1)},
-        "kernel_us": {k: round(statistics.mean(v), 3) for k, v in kern_us.items() if v},
+        "one_launch_step_us": (round(statistics.median(one_us), 3) if one_us else None),
+        "four_kernel_step_us": {"median": round(statistics.median(four_us), 3),
+                                "kernel_us_marked": {k: round(statistics.mean(v), 3)
+                                                     for k, v in kern_us.items() if v}},
         "kernel_cost_beyond_bytes_us": round(
             sparse_med - dense_med * acct["sparse_step"] / acct["dense_step"], 3),
         "bytes": acct,
         "stats_build_us": round(statistics.median(stats_us), 3),
         "dropped_mass_mean": round(delta_mean, 5),
         "roofline": {
-            "kernel": ATTN_KERNEL[w.dtype][0],
+            "kernel": roof_kernel,
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": committed_traffic(w.name, label, w.dtype),
-            "algorithmic_bytes_per_launch": acct["attn_launch"],
-            "avg_launch_us": round(attn_us, 3),
+            "traffic": committed_traffic(w.name, label, roof_source),
+            "algorithmic_bytes_per_launch": roof_bytes,
+            "avg_launch_us": round(roof_us, 3),
+            "dense_same_kernel": {
+                "achieved": round(acct["dense_step"] / (dense_mean * 1e-6) / 1e9, 1),
+                "frac": round(acct["dense_step"] / (dense_mean * 1e-6) / 1e9 / peak, 4),
+                "avg_launch_us": round(dense_mean, 3)},
         },
-        "gpu_launches": 4 * args.steps * (2 if in_graph_events else 1) + 2 * args.steps,
+        "gpu_launches": args.steps * ((1 if one_launch else 4) + (1 if one_launch else 2)
+                                      + 4 + (4 if in_graph_events else 0)
+                                      + (1 if one_us else 0)),
         "clocks": clocks,
     }
     if e2e_us:

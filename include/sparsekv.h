@@ -87,6 +87,9 @@ typedef enum kv_status {
 
 typedef enum kv_dtype { KV_BF16 = 0, KV_FP32 = 1 } kv_dtype;
 
+/* num_splits value of kv_decode_step that asks for the one-launch step. */
+#define KV_SPLITS_ONE_LAUNCH (-1)
+
 /* Device-side error flags (bit mask) behind kv_check_device_errors(). */
 enum {
   KV_DEVERR_BAD_PAGE = 1,    /* page-table entry outside [0, num_phys_pages) */
@@ -180,6 +183,25 @@ kv_status kv_select_topk(const float* scores, int32_t scores_stride, const int32
                          cudaStream_t stream);
 
 /*
+ * kv_select_structured -- kv_select_topk with forced pages: [SPARDA] section 3.1 and
+ * appendix A join initial blocks, a local window of the most recent blocks and top-k blocks.
+ * For each group the first sink_pages and the last local_pages pages (the set F, clipped to
+ * the group's n pages) are always kept, the keep count becomes max(k_b, |F|) (then clamped
+ * to k_max as in kv_select_topk), and the remaining places go to the best-scoring pages
+ * outside F under kv_select_topk's order. scores may be NULL: every page outside F then ties,
+ * so the lowest-indexed ones fill the remaining places; with sink_pages = 0 and
+ * local_pages = k this is the KV-window baseline of [BYTEX] Tables 3 and 11 (keep the last k
+ * pages, no scoring). Arguments are otherwise those of kv_select_topk; at least one of a
+ * keep rule and a forced page count must be given.
+ */
+kv_status kv_select_structured(const float* scores, int32_t scores_stride,
+                               const int32_t* seq_lens, int32_t page_size, int32_t batch,
+                               int32_t num_kv_heads, const int32_t* keep, double keep_ratio,
+                               int32_t budget_pages, int32_t sink_pages, int32_t local_pages,
+                               int32_t k_max, int32_t* sel_idx, int32_t* sel_cnt,
+                               cudaStream_t stream);
+
+/*
  * kv_sparse_decode_attn -- [BYTEX] split-K decode attention over selected pages.
  * For each (b, g) the selected list (sel_idx[b][g][0..sel_cnt[b][g]), or every page
  * 0..n_b-1 when sel_idx is NULL: the dense baseline through the same kernel) is cut into
@@ -236,9 +258,20 @@ size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_
  * kv_decode_step -- one sparse decode step: kv_score_pages, kv_select_topk,
  * kv_sparse_decode_attn and kv_merge_splits on a caller workspace. With keep_ratio >= 1
  * and budget_pages <= 0 it is the dense step (every page, no scoring or selection).
- * k_max bounds the keep count (and sizes the workspace); num_splits 0 = automatic.
+ * k_max bounds the keep count (and sizes the workspace).
+ * num_splits > 0: the four calls run with that many splits; 0: the four calls with
+ * kv_auto_num_splits' count; KV_SPLITS_ONE_LAUNCH: for bf16 caches whose (sequence, KV head)
+ * groups fit one wave of thread-block clusters, the whole step is ONE launch -- a cluster per
+ * group scores, selects, attends and merges in on-chip memory (distributed shared memory
+ * between the cluster's CTAs), each CTA being one split (other shapes fall back to the four
+ * calls). Both paths give the same selection (bit for bit) and outputs equal up to float32
+ * rounding of the merge.
  * out: device [batch][num_q_heads][head_dim] float32; lse: [batch][num_q_heads] or NULL.
- * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned.
+ * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned. After
+ * a sparse call it holds the step's selection: sel_idx [batch][num_kv_heads][k_max] int32 at
+ * byte offset A = round256(batch * num_kv_heads * page_table_stride * 4), and sel_cnt
+ * [batch][num_kv_heads] int32 at A + round256(batch * num_kv_heads * k_max * 4), where
+ * round256(x) rounds x up to a multiple of 256 (the layout kv_dropped_mass can be fed from).
  */
 kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                          float sm_scale, const void* stats, double keep_ratio,

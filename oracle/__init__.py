@@ -22,6 +22,9 @@ Steps and the passages they follow (page title, then section):
   EntmaxKV abstract (query-aware page scoring); "SparDA: Sparse Decoupled Attention for
   Efficient Long-Context LLM Inference", section 3.1 (per-head relevance is summed within
   a GQA group into one shared score).
+* ``select_structured`` -- forced initial and local-window pages joined to the top-k of
+  the rest (SparDA section 3.1, appendix A); the pure KV window is its score-free case
+  ("Where Activation Sparsity and KV-Cache Sparsity Cross in LLM Decoding", Tables 3, 11).
 * ``keep_count`` / ``select_pages`` -- top-k pages per KV group under a keep ratio or a
   token budget, ties to the lower page index, output ascending. "Near-Oracle KV Selection
   via Pre-hoc Sparsity for Long-Context Inference", abstract (top-k KV selection); SparDA
@@ -51,6 +54,7 @@ from .kvattn import (
     page_scores,
     keep_count,
     select_pages,
+    select_structured,
     select_all_groups,
     gather_tokens,
     attend,
@@ -68,6 +72,7 @@ __all__ = [
     "page_scores",
     "keep_count",
     "select_pages",
+    "select_structured",
     "select_all_groups",
     "gather_tokens",
     "attend",

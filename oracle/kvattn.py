@@ -151,6 +151,31 @@ def select_pages(scores_1d, k: int):
     return np.sort(order[:k]).astype(np.int64)
 
 
+def select_structured(scores_1d, k: int, sink: int = 0, local: int = 0):
+    """Forced initial and local pages joined to a top-k of the rest.
+
+    SparDA section 3.1 describes block-sparse attention over initial blocks, a local window
+    of the most recent blocks and top-k selected blocks (appendix A: B_init, B_local and
+    f_top(., k) joined). Reading used here for a group of n pages and a keep count k: the
+    forced set F is pages [0, sink) and [n - local, n) (clipped to [0, n)); the kept set is F
+    joined with the top max(0, k - |F|) pages outside F by (score descending, page index
+    ascending); the result is ascending. With sink = 0 and local = k it is the KV-window
+    baseline of "Where Activation Sparsity and KV-Cache Sparsity Cross in LLM Decoding",
+    Tables 3 and 11 (keep the last pages, no scores needed).
+    """
+    s = np.asarray(scores_1d, dtype=np.float64)
+    n = s.shape[0]
+    forced = np.zeros(n, dtype=bool)
+    forced[: max(0, min(int(sink), n))] = True
+    if local > 0:
+        forced[max(0, n - int(local)):] = True
+    rest = np.nonzero(~forced)[0]
+    extra = max(0, min(int(k), n) - int(forced.sum()))
+    order = np.lexsort((rest, -s[rest]))
+    chosen = np.concatenate([np.nonzero(forced)[0], rest[order[:extra]]])
+    return np.sort(chosen).astype(np.int64)
+
+
 def select_all_groups(scores, ks):
     """``select_pages`` for every (b, g): ``scores`` as returned by ``page_scores``,
     ``ks[b]`` the keep count of sequence ``b``. Returns ``sel[b][g]`` index arrays."""

@@ -7,6 +7,7 @@ call does, and raises if it has not been built.
 
 from . import inputs  # noqa: F401
 from .binding import (  # noqa: F401
+    ONE_LAUNCH,
     PagedKV,
     kv_append_token,
     kv_auto_num_splits,
@@ -18,6 +19,7 @@ from .binding import (  # noqa: F401
     kv_dropped_mass_workspace_size,
     kv_merge_splits,
     kv_score_pages,
+    kv_select_structured,
     kv_select_topk,
     kv_selftest_wait_timeout,
     kv_set_wait_limit_ns,

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libsparsekv.so")
 
 KV_OK = 0
 KV_BF16, KV_FP32 = 0, 1
+ONE_LAUNCH = -1          # KV_SPLITS_ONE_LAUNCH: kv_decode_step as a single launch
 STATUS = {0: "KV_OK", -1: "KV_ERR_INVALID_ARG", -2: "KV_ERR_UNSUPPORTED", -3: "KV_ERR_CUDA",
           -4: "KV_ERR_WORKSPACE", -5: "KV_ERR_BAD_INDEX", -6: "KV_ERR_TIMEOUT",
           -7: "KV_ERR_MISALIGNED"}
@@ -32,6 +33,7 @@ EXPORTS = (
     "kv_dropped_mass", "kv_dropped_mass_workspace_size", "kv_decode_step",
     "kv_decode_step_workspace_size", "kv_check_device_errors", "kv_set_wait_limit_ns",
     "kv_selftest_wait_timeout", "kv_decode_step_static", "kv_append_token",
+    "kv_select_structured",
 )
 
 
@@ -83,6 +85,8 @@ def _declare(lib):
         "kv_selftest_wait_timeout": (I32, [U64, P]),
         "kv_decode_step_static": (I32, [D, P, I32, F32, P, F64, I32, I32, I32, P, P, P]),
         "kv_append_token": (I32, [D, P, P, P, P]),
+        "kv_select_structured": (I32, [P, I32, P, I32, I32, I32, P, F64, I32, I32, I32, I32, P,
+                                       P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -263,6 +267,33 @@ def kv_select_topk(scores, seq_lens, page_size: int, keep=None, keep_ratio: floa
         _ptr(scores), stride, _ptr(seq_lens), int(page_size), B, Hkv, _ptr(keep),
         float(keep_ratio), int(budget_pages), int(k_max), _ptr(sel_idx), _ptr(sel_cnt),
         _stream(stream)))
+    return sel_idx, sel_cnt
+
+
+def kv_select_structured(scores, seq_lens, page_size: int, batch: int, num_kv_heads: int,
+                         stride: int, sink_pages: int = 0, local_pages: int = 0, keep=None,
+                         keep_ratio: float = 0.0, budget_pages: int = 0, k_max: int | None = None,
+                         sel_idx=None, sel_cnt=None, stream=None):
+    """Forced first sink_pages and last local_pages pages joined to the top-k of the rest;
+    scores may be None (the KV-window baseline when sink_pages = 0)."""
+    if scores is not None:
+        _need(scores, "scores", torch.float32, (batch, num_kv_heads, stride))
+    dev = seq_lens.device
+    if k_max is None:
+        k_max = min(stride, max_keep_pages(stride, keep_ratio if keep_ratio else None,
+                                           budget_pages or None) + sink_pages + local_pages)
+    if sel_idx is None:
+        sel_idx = torch.empty((batch, num_kv_heads, k_max), dtype=torch.int32, device=dev)
+    if sel_cnt is None:
+        sel_cnt = torch.empty((batch, num_kv_heads), dtype=torch.int32, device=dev)
+    _need(sel_idx, "sel_idx", torch.int32, (batch, num_kv_heads, k_max))
+    _need(sel_cnt, "sel_cnt", torch.int32, (batch, num_kv_heads))
+    if keep is not None:
+        _need(keep, "keep", torch.int32, (batch,))
+    _check("kv_select_structured", lib().kv_select_structured(
+        _ptr(scores), int(stride), _ptr(seq_lens), int(page_size), int(batch),
+        int(num_kv_heads), _ptr(keep), float(keep_ratio), int(budget_pages), int(sink_pages),
+        int(local_pages), int(k_max), _ptr(sel_idx), _ptr(sel_cnt), _stream(stream)))
     return sel_idx, sel_cnt
 
 

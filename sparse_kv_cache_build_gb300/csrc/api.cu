@@ -4,7 +4,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "attn_impl.cuh"
 #include "kv_internal.cuh"
@@ -128,6 +130,26 @@ StepLayout step_layout(const kv_cache_desc* d, int Hq, int k_max, int S) {
   return L;
 }
 
+// Cluster size of the one-launch step per (device, shape), decided once (outside any
+// stream capture that follows) and reused.
+int cached_cluster_size(const kv_cache_desc* d, int G, const DeviceState* st) {
+  int dev = -1;
+  cudaGetDevice(&dev);
+  using Key = std::tuple<int, int, int, int, int, int, int, int, int>;
+  static std::map<Key, int> memo;
+  const Key key{dev, d->dtype, d->head_dim, G, d->page_size, d->batch, d->num_kv_heads,
+                d->page_table_stride, d->num_phys_pages};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+  }
+  const int CL = fused_cluster_size(*d, G, st->sms);
+  std::lock_guard<std::mutex> lock(g_mu);
+  memo[key] = CL;
+  return CL;
+}
+
 bool is_dense(double keep_ratio, int budget_pages) {
   return budget_pages <= 0 && keep_ratio >= 1.0;
 }
@@ -237,8 +259,32 @@ kv_status kv_select_topk(const float* scores, int32_t scores_stride, const int32
   if (r != KV_OK) return r;
   // The row stride bounds every sequence: a longer seq_len is flagged by the kernel.
   return from_cuda(launch_select_topk(scores, scores_stride, seq_lens, page_size, batch,
-                                      num_kv_heads, keep, keep_ratio, budget_pages, k_max,
+                                      num_kv_heads, keep, keep_ratio, budget_pages, k_max, 0, 0,
                                       sel_idx, sel_cnt, scores_stride, ctx, stream));
+}
+
+kv_status kv_select_structured(const float* scores, int32_t scores_stride,
+                               const int32_t* seq_lens, int32_t page_size, int32_t batch,
+                               int32_t num_kv_heads, const int32_t* keep, double keep_ratio,
+                               int32_t budget_pages, int32_t sink_pages, int32_t local_pages,
+                               int32_t k_max, int32_t* sel_idx, int32_t* sel_cnt,
+                               cudaStream_t stream) {
+  if (seq_lens == nullptr || sel_idx == nullptr || sel_cnt == nullptr) return KV_ERR_INVALID_ARG;
+  if (scores_stride <= 0 || page_size <= 0 || batch <= 0 || batch > 65535 ||
+      num_kv_heads <= 0 || num_kv_heads > 65535 || k_max <= 0 || sink_pages < 0 ||
+      local_pages < 0)
+    return KV_ERR_INVALID_ARG;
+  if (keep == nullptr && budget_pages <= 0 && !(keep_ratio > 0.0) &&
+      sink_pages + local_pages == 0)
+    return KV_ERR_INVALID_ARG;
+  if ((long long)scores_stride * page_size > INT32_MAX) return KV_ERR_INVALID_ARG;
+  DevCtx ctx;
+  kv_status r = ctx_for_call(&ctx);
+  if (r != KV_OK) return r;
+  return from_cuda(launch_select_topk(scores, scores_stride, seq_lens, page_size, batch,
+                                      num_kv_heads, keep, keep_ratio, budget_pages, k_max,
+                                      sink_pages, local_pages, sel_idx, sel_cnt, scores_stride,
+                                      ctx, stream));
 }
 
 kv_status kv_sparse_decode_attn(const kv_cache_desc* cache, const void* q,
@@ -352,9 +398,23 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   DeviceState* st = nullptr;
   if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
   const int G = num_q_heads / cache->num_kv_heads;
+  if (num_splits == KV_SPLITS_ONE_LAUNCH) {
+    // one launch for the whole step when the shape allows it (bf16, one wave of clusters)
+    const int CL = cached_cluster_size(cache, G, st);
+    if (CL > 0) {
+      const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, 1);
+      if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
+      char* ws = static_cast<char*>(workspace);
+      return from_cuda(launch_fused_step(
+          *cache, G, CL, q, stats, sm_scale, keep_ratio, budget_pages, dense ? 1 : k_max,
+          dense ? 1 : 0, dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.sel),
+          dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.cnt), out, lse, ctx, stream));
+    }
+  }
   int S = num_splits;
   if (S <= 0) S = auto_splits(cache, G, dense ? cache->page_table_stride : k_max, st);
   if (S < min_splits_for(dense ? cache->page_table_stride : k_max)) return KV_ERR_INVALID_ARG;
+  // (a one-launch request whose shape does not allow it runs the four kernels instead)
   const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, S);
   if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -370,7 +430,7 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
     if (e != cudaSuccess) return KV_ERR_CUDA;
     e = launch_select_topk(scores, cache->page_table_stride, cache->seq_lens, cache->page_size,
                            cache->batch, cache->num_kv_heads, nullptr, keep_ratio,
-                           budget_pages, k_max, sel, cnt, cache->page_table_stride, ctx,
+                           budget_pages, k_max, 0, 0, sel, cnt, cache->page_table_stride, ctx,
                            stream);
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }

@@ -44,8 +44,11 @@ struct MmaCfg {
   static constexpr size_t OFF_VALID = OFF_PHYS + 4 * kMaxSplitPages;
   static constexpr size_t OFF_BAR = OFF_VALID + 2 * kMaxSplitPages;
   static constexpr size_t SMEM = OFF_BAR + 8 * NSTAGE + 1024;   // + alignment slack
+  // a CTA partial: acc [G][D], then m [G] (base 2), then l [G]
+  static constexpr size_t PARTIAL_FLOATS = (size_t)G * (D + 2);
   static constexpr size_t MERGE_BYTES = 4 * (size_t)4 * G * (D + 2);
-  static_assert(MERGE_BYTES <= (size_t)NSTAGE * STAGE_BYTES, "merge buffers must fit");
+  static_assert(MERGE_BYTES + 4 * PARTIAL_FLOATS <= (size_t)NSTAGE * STAGE_BYTES,
+                "merge buffers must fit");
 };
 
 // 2-D TMA tile load into shared memory, completion counted on `bar`.
@@ -97,6 +100,219 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Per-warp running state of the online softmax: O accumulator fragments (rows lane/4 are
+// the group's query heads; rows lane/4 + 8 are padding), the row max (base 2) and this
+// lane's share of the row sum.
+template <int D>
+struct WarpAcc {
+  float o[D / 8][4];
+  float m_run;
+  float l_lane;
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    m_run = -INFINITY;
+    l_lane = 0.f;
+  }
+};
+
+// q rows of the group as m16n8k16 A fragments (rows >= G are zero).
+template <int D, int G>
+__device__ __forceinline__ void load_q_frags(const uint16_t* q, long row0, uint32_t* qa0,
+                                             uint32_t* qa2) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const bool live = gid < G;
+  const uint16_t* qrow = q + (row0 + (live ? gid : 0)) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t* p32 = reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
+    qa0[ks] = live ? p32[0] : 0u;
+    qa2[ks] = live ? p32[4] : 0u;
+  }
+}
+
+// Stream a run of np pages (physical ids and valid-token counts in shared memory) through a
+// ring of NST stages of 64 tokens, accumulating attention of the group's query heads into
+// the four warps' WarpAcc. All 128 threads call it; thread 0 issues the TMA copies. Ring use
+// number ring_base + t goes to stage (ring_base + t) % NST with phase parity
+// ((ring_base + t) / NST) & 1, so one ring can serve several runs or phases of a kernel.
+// It consumes ceil(np / (64 / PS)) ring uses. Returns false if a wait ran out (the copies
+// this CTA issued have then been drained, bounded).
+template <int D, int G, int NST>
+__device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char* stages,
+                          uint64_t* bars, uint32_t ring_base, const int32_t* s_phys,
+                          const int16_t* s_valid, int np, int g, int Hkv, int PS,
+                          const uint32_t* qa0, const uint32_t* qa2, float qk_scale_log2,
+                          WarpAcc<D>& acc, unsigned long long wait_ns) {
+  using C = MmaCfg<D, G>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int lm = lane >> 3, lr = lane & 7;
+  const int PPT = kTileTokens / PS;
+  const int n_tiles = ceil_div(np, PPT);
+  const uint32_t page_half_bytes = (uint32_t)PS * 128;
+
+  auto issue = [&](int t) {
+    const uint32_t u = ring_base + (uint32_t)t;
+    const int st = (int)(u % NST);
+    char* kdst = stages + (size_t)st * C::STAGE_BYTES;
+    char* vdst = kdst + C::TILE_BYTES;
+    const int i0 = t * PPT, i1 = min(np, i0 + PPT);
+    uint32_t bytes = 0;
+    for (int i = i0; i < i1; ++i)
+      bytes += s_valid[i] > 0 ? 2u * C::HALVES * page_half_bytes : 0u;
+    mbar_arrive_expect_tx(&bars[st], bytes);
+    const uint64_t pol = l2_evict_first_policy();
+    for (int i = i0; i < i1; ++i) {
+      if (s_valid[i] <= 0) continue;
+      const int y = (s_phys[i] * Hkv + g) * PS;
+      const uint32_t off = (uint32_t)(i - i0) * page_half_bytes;
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_load_2d(kdst + h * C::HALF_BYTES + off, tmK, 64 * h, y, &bars[st], pol);
+        tma_load_2d(vdst + h * C::HALF_BYTES + off, tmV, 64 * h, y, &bars[st], pol);
+      }
+    }
+  };
+  if (tid == 0) {
+    for (int t = 0; t < NST && t < n_tiles; ++t) issue(t);
+  }
+
+  bool aborted = false;
+  int t = 0;
+  for (; t < n_tiles; ++t) {
+    const uint32_t u = ring_base + (uint32_t)t;
+    const int st = (int)(u % NST);
+    const bool ok = mbar_wait_bounded(&bars[st], (u / NST) & 1u, wait_ns);
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+
+    const int tok_base = warp * kWarpTokens;
+    const int slot = t * PPT + tok_base / PS;
+    int vt = 0;
+    if (slot < np) vt = max(0, min(kWarpTokens, (int)s_valid[slot] - tok_base % PS));
+
+    if (vt > 0) {
+      const uint32_t kbase = smem_addr(stages + (size_t)st * C::STAGE_BYTES);
+      const uint32_t vbase = kbase + C::TILE_BYTES;
+      // ---- S = Q K^T for 16 tokens (two n-tiles of 8) ------------------------------------
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        const int row = tok_base + (lm >> 1) * 8 + lr;
+        const int col = ks * 16 + (lm & 1) * 8;              // element column
+        const uint32_t addr = kbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(addr, b00, b01, b10, b11);
+        mma_bf16(sc[0], qa0[ks], 0u, qa2[ks], 0u, b00, b01);
+        mma_bf16(sc[1], qa0[ks], 0u, qa2[ks], 0u, b10, b11);
+      }
+      // ---- online softmax (base 2) for row gid; tokens nt*8 + 2*tig + {0,1} ---------------
+      float x[4];
+      x[0] = (2 * tig < vt) ? sc[0][0] * qk_scale_log2 : -INFINITY;
+      x[1] = (2 * tig + 1 < vt) ? sc[0][1] * qk_scale_log2 : -INFINITY;
+      x[2] = (8 + 2 * tig < vt) ? sc[1][0] * qk_scale_log2 : -INFINITY;
+      x[3] = (8 + 2 * tig + 1 < vt) ? sc[1][1] * qk_scale_log2 : -INFINITY;
+      float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+      const float m_new = fmaxf(acc.m_run, mt);
+      const float alpha = acc.m_run == -INFINITY ? 0.f : exp2f(acc.m_run - m_new);
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = x[i] == -INFINITY ? 0.f : exp2f(x[i] - m_new);
+      acc.l_lane = acc.l_lane * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+      acc.m_run = m_new;
+      if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < C::ONT; ++nt) { acc.o[nt][0] *= alpha; acc.o[nt][1] *= alpha; }
+      }
+      // P as bf16 hi + lo A fragments (rows gid; rows gid + 8 are zero)
+      const uint32_t ph0 = pack_bf16(p[0], p[1]), ph2 = pack_bf16(p[2], p[3]);
+      const uint32_t pl0 = pack_bf16(p[0] - bf16_lo_f(ph0), p[1] - bf16_hi_f(ph0));
+      const uint32_t pl2 = pack_bf16(p[2] - bf16_lo_f(ph2), p[3] - bf16_hi_f(ph2));
+      // masked tokens of a partial page: zero their V elements (may hold any bits)
+      uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+      if (vt < kWarpTokens) {
+        vm0 = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
+        vm1 = (8 + 2 * tig < vt ? 0x0000ffffu : 0u) | (8 + 2 * tig + 1 < vt ? 0xffff0000u : 0u);
+      }
+      // ---- O += P V ------------------------------------------------------------------------
+#pragma unroll
+      for (int np2 = 0; np2 < C::ONT / 2; ++np2) {
+        const int row = tok_base + (lm & 1) * 8 + lr;
+        const int col = np2 * 16 + (lm >> 1) * 8;
+        const uint32_t addr = vbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
+        uint32_t v00, v01, v10, v11;
+        ldsm_x4_t(addr, v00, v01, v10, v11);
+        v00 &= vm0; v01 &= vm1; v10 &= vm0; v11 &= vm1;
+        mma_bf16(acc.o[2 * np2], ph0, 0u, ph2, 0u, v00, v01);
+        mma_bf16(acc.o[2 * np2], pl0, 0u, pl2, 0u, v00, v01);
+        mma_bf16(acc.o[2 * np2 + 1], ph0, 0u, ph2, 0u, v10, v11);
+        mma_bf16(acc.o[2 * np2 + 1], pl0, 0u, pl2, 0u, v10, v11);
+      }
+    }
+    __syncthreads();                                       // the stage is free again
+    if (tid == 0 && t + NST < n_tiles) issue(t + NST);
+  }
+  if (aborted && tid == 0) {
+    // let every copy this CTA issued land before its shared memory is reused or freed
+    for (int v = t; v < n_tiles && v < t + NST; ++v) {
+      const uint32_t u = ring_base + (uint32_t)v;
+      mbar_wait_bounded(&bars[u % NST], (u / NST) & 1u, wait_ns);
+    }
+  }
+  return !aborted;
+}
+
+// Merge the four warps' states into one CTA partial in shared memory `part`:
+// acc [G][D] (relative to m), m [G] in base 2 (-inf when empty), l [G]. `scratch` holds
+// 4*G*(D+2) floats and may alias the stage ring once it is idle. Ends with __syncthreads.
+template <int D, int G>
+__device__ void cta_partial(WarpAcc<D>& acc, float* scratch, float* part) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  float l_row = acc.l_lane;
+  l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+  l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+  float* mg_o = scratch;                                   // [4][G][D]
+  float* mg_m = mg_o + 4 * G * D;                          // [4][G]
+  float* mg_l = mg_m + 4 * G;
+  if (gid < G) {
+    if (tig == 0) {
+      mg_m[warp * G + gid] = acc.m_run;
+      mg_l[warp * G + gid] = l_row;
+    }
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      mg_o[(warp * G + gid) * D + nt * 8 + 2 * tig] = acc.o[nt][0];
+      mg_o[(warp * G + gid) * D + nt * 8 + 2 * tig + 1] = acc.o[nt][1];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    const int hl = i / D, dd = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, mg_m[w2 * G + hl]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w2 = 0; w2 < 4; ++w2) {
+        const float mw = mg_m[w2 * G + hl];
+        const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        L = fmaf(mg_l[w2 * G + hl], sc, L);
+        A = fmaf(mg_o[(w2 * G + hl) * D + dd], sc, A);
+      }
+    }
+    part[hl * D + dd] = A;
+    if (dd == 0) {
+      part[G * D + hl] = M;
+      part[G * D + G + hl] = L;
+    }
+  }
+  __syncthreads();
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(MmaCfg<D, G>::THREADS)
 split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -114,7 +330,7 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int Hkv = d.num_kv_heads, Hq = Hkv * G, PS = d.page_size;
   pdl_trigger();
   if (tid == 0) {
@@ -160,141 +376,18 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     s_phys[i] = P;
     s_valid[i] = (int16_t)valid;
   }
+  uint32_t qa0[C::KSTEPS], qa2[C::KSTEPS];
+  load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
   __syncthreads();
 
-  const int PPT = kTileTokens / PS;
-  const int n_tiles = ceil_div(np, PPT);
-  const uint32_t page_half_bytes = (uint32_t)PS * 128;
-
-  auto issue = [&](int t) {
-    const int st = t % C::NSTAGE;
-    char* kdst = smem + C::OFF_STAGES + (size_t)st * C::STAGE_BYTES;
-    char* vdst = kdst + C::TILE_BYTES;
-    const int i0 = t * PPT, i1 = min(np, i0 + PPT);
-    uint32_t bytes = 0;
-    for (int i = i0; i < i1; ++i)
-      bytes += s_valid[i] > 0 ? 2u * C::HALVES * page_half_bytes : 0u;
-    mbar_arrive_expect_tx(&bars[st], bytes);
-    const uint64_t pol = l2_evict_first_policy();
-    for (int i = i0; i < i1; ++i) {
-      if (s_valid[i] <= 0) continue;
-      const int y = (s_phys[i] * Hkv + g) * PS;
-      const uint32_t off = (uint32_t)(i - i0) * page_half_bytes;
-#pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_2d(kdst + h * C::HALF_BYTES + off, &tmK, 64 * h, y, &bars[st], pol);
-        tma_load_2d(vdst + h * C::HALF_BYTES + off, &tmV, 64 * h, y, &bars[st], pol);
-      }
-    }
-  };
-  if (tid == 0) {
-    for (int t = 0; t < C::NSTAGE && t < n_tiles; ++t) issue(t);
-  }
-
-  // ---- q as A fragments: row = lane/4 (query head of the group), rows >= G are zero ----
-  const int gid = lane >> 2, tig = lane & 3;
-  uint32_t qa0[C::KSTEPS], qa2[C::KSTEPS];
-  {
-    const bool live = gid < G;
-    const uint16_t* qrow = q + ((long)b * Hq + g * G + (live ? gid : 0)) * D;
-#pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      const uint32_t* p32 = reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
-      qa0[ks] = live ? p32[0] : 0u;
-      qa2[ks] = live ? p32[4] : 0u;
-    }
-  }
-
-  float o[C::ONT][4];
-#pragma unroll
-  for (int nt = 0; nt < C::ONT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m_run = -INFINITY, l_lane = 0.f;
-
-  // ldmatrix lane roles
-  const int lm = lane >> 3, lr = lane & 7;
-  bool aborted = false;
-  int t = 0;
-  for (; t < n_tiles; ++t) {
-    const int st = t % C::NSTAGE;
-    const bool ok = mbar_wait_bounded(&bars[st], (uint32_t)((t / C::NSTAGE) & 1), ctx.wait_ns);
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-
-    const int tok_base = warp * kWarpTokens;
-    const int slot = t * PPT + tok_base / PS;
-    int vt = 0;
-    if (slot < np) vt = max(0, min(kWarpTokens, (int)s_valid[slot] - tok_base % PS));
-
-    if (vt > 0) {
-      const uint32_t kbase = smem_addr(smem + C::OFF_STAGES + (size_t)st * C::STAGE_BYTES);
-      const uint32_t vbase = kbase + C::TILE_BYTES;
-      // ---- S = Q K^T for 16 tokens (two n-tiles of 8) ------------------------------------
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < C::KSTEPS; ++ks) {
-        const int row = tok_base + (lm >> 1) * 8 + lr;
-        const int col = ks * 16 + (lm & 1) * 8;              // element column
-        const uint32_t addr = kbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4(addr, b00, b01, b10, b11);
-        mma_bf16(sc[0], qa0[ks], 0u, qa2[ks], 0u, b00, b01);
-        mma_bf16(sc[1], qa0[ks], 0u, qa2[ks], 0u, b10, b11);
-      }
-      // ---- online softmax (base 2) for row gid; tokens nt*8 + 2*tig + {0,1} ---------------
-      float x[4];
-      x[0] = (2 * tig < vt) ? sc[0][0] * qk_scale_log2 : -INFINITY;
-      x[1] = (2 * tig + 1 < vt) ? sc[0][1] * qk_scale_log2 : -INFINITY;
-      x[2] = (8 + 2 * tig < vt) ? sc[1][0] * qk_scale_log2 : -INFINITY;
-      x[3] = (8 + 2 * tig + 1 < vt) ? sc[1][1] * qk_scale_log2 : -INFINITY;
-      float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      const float m_new = fmaxf(m_run, mt);
-      const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
-      float p[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) p[i] = x[i] == -INFINITY ? 0.f : exp2f(x[i] - m_new);
-      l_lane = l_lane * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
-      m_run = m_new;
-      if (!__all_sync(0xffffffffu, alpha == 1.f)) {
-#pragma unroll
-        for (int nt = 0; nt < C::ONT; ++nt) { o[nt][0] *= alpha; o[nt][1] *= alpha; }
-      }
-      // P as bf16 hi + lo A fragments (rows gid; rows gid + 8 are zero)
-      const uint32_t ph0 = pack_bf16(p[0], p[1]), ph2 = pack_bf16(p[2], p[3]);
-      const uint32_t pl0 = pack_bf16(p[0] - bf16_lo_f(ph0), p[1] - bf16_hi_f(ph0));
-      const uint32_t pl2 = pack_bf16(p[2] - bf16_lo_f(ph2), p[3] - bf16_hi_f(ph2));
-      // masked tokens of a partial page: zero their V elements (may hold any bits)
-      uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-      if (vt < kWarpTokens) {
-        vm0 = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
-        vm1 = (8 + 2 * tig < vt ? 0x0000ffffu : 0u) | (8 + 2 * tig + 1 < vt ? 0xffff0000u : 0u);
-      }
-      // ---- O += P V ------------------------------------------------------------------------
-#pragma unroll
-      for (int np2 = 0; np2 < C::ONT / 2; ++np2) {
-        const int row = tok_base + (lm & 1) * 8 + lr;
-        const int col = np2 * 16 + (lm >> 1) * 8;
-        const uint32_t addr = vbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
-        uint32_t v00, v01, v10, v11;
-        ldsm_x4_t(addr, v00, v01, v10, v11);
-        v00 &= vm0; v01 &= vm1; v10 &= vm0; v11 &= vm1;
-        mma_bf16(o[2 * np2], ph0, 0u, ph2, 0u, v00, v01);
-        mma_bf16(o[2 * np2], pl0, 0u, pl2, 0u, v00, v01);
-        mma_bf16(o[2 * np2 + 1], ph0, 0u, ph2, 0u, v10, v11);
-        mma_bf16(o[2 * np2 + 1], pl0, 0u, pl2, 0u, v10, v11);
-      }
-    }
-    __syncthreads();                                       // stage st is free again
-    if (tid == 0 && t + C::NSTAGE < n_tiles) issue(t + C::NSTAGE);
-  }
-
+  WarpAcc<D> acc;
+  acc.init();
+  const bool ok = attend_run<D, G, C::NSTAGE>(&tmK, &tmV, smem + C::OFF_STAGES, bars, 0u,
+                                              s_phys, s_valid, np, g, Hkv, PS, qa0, qa2,
+                                              qk_scale_log2, acc, ctx.wait_ns);
   const long out_row = ((long)b * Hq + g * G) * S + s;
-  if (aborted) {
-    if (tid == 0) {
-      flag(ctx, KV_DEVERR_TIMEOUT);
-      for (int u = t; u < n_tiles && u < t + C::NSTAGE; ++u)
-        mbar_wait_bounded(&bars[u % C::NSTAGE], (uint32_t)((u / C::NSTAGE) & 1), ctx.wait_ns);
-    }
+  if (!ok) {
+    if (tid == 0) flag(ctx, KV_DEVERR_TIMEOUT);
     for (int i = tid; i < G * D; i += C::THREADS) {
       const int hl = i / D, dd = i % D;
       part_acc[(out_row + (long)hl * S) * D + dd] = 0.f;
@@ -305,44 +398,16 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     return;
   }
-
-  // ---- merge the four token warps ---------------------------------------------------------
-  l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 1);
-  l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 2);
-  float* mg_o = reinterpret_cast<float*>(smem + C::OFF_STAGES);         // [4][G][D]
-  float* mg_m = mg_o + 4 * G * D;                                       // [4][G]
-  float* mg_l = mg_m + 4 * G;
-  if (gid < G) {
-    if (tig == 0) {
-      mg_m[warp * G + gid] = m_run;
-      mg_l[warp * G + gid] = l_lane;
-    }
-#pragma unroll
-    for (int nt = 0; nt < C::ONT; ++nt) {
-      mg_o[(warp * G + gid) * D + nt * 8 + 2 * tig] = o[nt][0];
-      mg_o[(warp * G + gid) * D + nt * 8 + 2 * tig + 1] = o[nt][1];
-    }
-  }
-  __syncthreads();
+  float* scratch = reinterpret_cast<float*>(smem + C::OFF_STAGES);
+  float* part = scratch + 4 * G * (D + 2);
+  cta_partial<D, G>(acc, scratch, part);
   for (int i = tid; i < G * D; i += C::THREADS) {
     const int hl = i / D, dd = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, mg_m[w2 * G + hl]);
-    float L = 0.f, A = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2) {
-        const float mw = mg_m[w2 * G + hl];
-        const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        L = fmaf(mg_l[w2 * G + hl], sc, L);
-        A = fmaf(mg_o[(w2 * G + hl) * D + dd], sc, A);
-      }
-    }
-    part_acc[(out_row + (long)hl * S) * D + dd] = A;
+    part_acc[(out_row + (long)hl * S) * D + dd] = part[hl * D + dd];
     if (dd == 0) {
+      const float M = part[G * D + hl];
       part_ml[(out_row + (long)hl * S) * 2 + 0] = M == -INFINITY ? -INFINITY : M * kLn2;
-      part_ml[(out_row + (long)hl * S) * 2 + 1] = L;
+      part_ml[(out_row + (long)hl * S) * 2 + 1] = part[G * D + G + hl];
     }
   }
 }

@@ -185,9 +185,9 @@ cudaError_t launch_score_pages(const kv_cache_desc& d, const void* q, int Hq,
                                DevCtx ctx, cudaStream_t s);
 cudaError_t launch_select_topk(const float* scores, int scores_stride, const int32_t* seq_lens,
                                int page_size, int batch, int Hkv, const int32_t* keep,
-                               double keep_ratio, int budget_pages, int k_max,
-                               int32_t* sel_idx, int32_t* sel_cnt, int page_table_stride,
-                               DevCtx ctx, cudaStream_t s);
+                               double keep_ratio, int budget_pages, int k_max, int sink,
+                               int local, int32_t* sel_idx, int32_t* sel_cnt,
+                               int page_table_stride, DevCtx ctx, cudaStream_t s);
 cudaError_t launch_split_attn(const kv_cache_desc& d, const void* q, int Hq, float sm_scale,
                               const int32_t* sel_idx, const int32_t* sel_cnt, int sel_stride,
                               int num_splits, float* part_acc, float* part_ml, DevCtx ctx,
@@ -201,6 +201,14 @@ cudaError_t launch_dropped_mass(const kv_cache_desc& d, const void* q, int Hq,
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, DevCtx ctx, cudaStream_t s);
 cudaError_t launch_append(const kv_cache_desc& d, const void* k_new, const void* v_new,
                           void* stats, DevCtx ctx, cudaStream_t s);
+
+// The single-launch decode step (bf16): cluster size for this shape on this device
+// (0 = use the four-kernel path), and its launcher.
+int fused_cluster_size(const kv_cache_desc& d, int G, int num_sms);
+cudaError_t launch_fused_step(const kv_cache_desc& d, int G, int CL, const void* q,
+                              const void* stats, float sm_scale, double keep_ratio, int budget,
+                              int k_max, int dense, int32_t* sel_out, int32_t* cnt_out,
+                              float* out, float* lse, DevCtx ctx, cudaStream_t s);
 
 // Dynamic shared memory bytes of the attention kernel for this shape (0 = unsupported).
 size_t split_attn_smem_bytes(int dtype, int head_dim, int group_size);

@@ -9,6 +9,13 @@
 // Order: score descending, then page index ascending. Output: the kept pages in ascending
 // page order.
 //
+// Structured selection (SparDA section 3.1 and appendix A: initial blocks, a local window
+// of recent blocks and top-k blocks joined): the first `sink` and the last `local` pages of
+// a group are forced in by giving them the largest key (no finite score maps to it), and
+// the keep count becomes max(k, forced). Without scores every other page gets the smallest
+// key, which with sink = 0 and local = k is the KV-window baseline ("Where Activation
+// Sparsity and KV-Cache Sparsity Cross in LLM Decoding", Tables 3 and 11).
+//
 // One 1024-thread block per group. Scores are mapped to unsigned keys whose integer order
 // is the float order, and a most-significant-digit radix select (up to four 8-bit passes,
 // histograms in shared memory with warp-aggregated atomics) finds the k-th largest key T
@@ -80,8 +87,8 @@ __global__ void __launch_bounds__(kSelectThreads)
 select_kernel(const float* __restrict__ scores, int scores_stride,
               const int32_t* __restrict__ seq_lens, int PS, int Hkv,
               const int32_t* __restrict__ keep, double keep_ratio, int budget, int k_max,
-              int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt, int table_stride,
-              DevCtx ctx) {
+              int sink, int local, int32_t* __restrict__ sel_idx,
+              int32_t* __restrict__ sel_cnt, int table_stride, DevCtx ctx) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_remaining, s_exact;
   __shared__ uint64_t warp_tot[32];
@@ -98,12 +105,18 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
   }
   const int n = ceil_div(len, PS);
   int k = keep_count(n, keep, b, keep_ratio, budget);
+  const int forced = min(n, max(0, sink) + max(0, local));   // [0, sink) and [n - local, n)
+  k = max(k, forced);
   if (k > k_max) {
     if (tid == 0) flag(ctx, KV_DEVERR_KEEP);
     k = k_max;
   }
   const long grp = (long)b * Hkv + g;
-  const float* row = scores + grp * scores_stride;
+  const float* row = scores != nullptr ? scores + grp * scores_stride : nullptr;
+  auto key_at = [&](int i) -> uint32_t {
+    if (i < sink || i >= n - local) return 0xffffffffu;   // forced in
+    return row != nullptr ? order_key(row[i]) : 0u;
+  };
   int32_t* out = sel_idx + grp * k_max;
   if (tid == 0) sel_cnt[grp] = k;
 
@@ -119,12 +132,12 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
 #pragma unroll
     for (int j = 0; j < kRegKeys; ++j) {
       const int i = j * kSelectThreads + tid;
-      rk[j] = i < n ? order_key(row[i]) : 0u;
+      rk[j] = i < n ? key_at(i) : 0u;
     }
   }
   auto key_of = [&](int j) -> uint32_t {
     if constexpr (REG) return rk[j];
-    else return order_key(row[j * kSelectThreads + tid]);
+    else return key_at(j * kSelectThreads + tid);
   };
 
   // ---- radix select of the k-th largest key -------------------------------------------
@@ -194,7 +207,7 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
 #pragma unroll
       for (int jj = 0; jj < kRegKeys; ++jj) key = (jj == j) ? rk[jj] : key;
     } else {
-      if (valid) key = order_key(row[i]);
+      if (valid) key = key_at(i);
     }
     const uint32_t gt = valid && key > T;
     const uint32_t eq = valid && key == T;
@@ -213,15 +226,15 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
 
 cudaError_t launch_select_topk(const float* scores, int scores_stride, const int32_t* seq_lens,
                                int page_size, int batch, int Hkv, const int32_t* keep,
-                               double keep_ratio, int budget_pages, int k_max,
-                               int32_t* sel_idx, int32_t* sel_cnt, int page_table_stride,
-                               DevCtx ctx, cudaStream_t s) {
+                               double keep_ratio, int budget_pages, int k_max, int sink,
+                               int local, int32_t* sel_idx, int32_t* sel_cnt,
+                               int page_table_stride, DevCtx ctx, cudaStream_t s) {
   dim3 grid(Hkv, batch);
   auto kern = page_table_stride <= kRegKeys * kSelectThreads ? select_kernel<true>
                                                               : select_kernel<false>;
   return launch_pdl(kern, grid, dim3(kSelectThreads), 0, s, scores, scores_stride, seq_lens,
-                    page_size, Hkv, keep, keep_ratio, budget_pages, k_max, sel_idx, sel_cnt,
-                    page_table_stride, ctx);
+                    page_size, Hkv, keep, keep_ratio, budget_pages, k_max, sink, local, sel_idx,
+                    sel_cnt, page_table_stride, ctx);
 }
 
 }  // namespace skv

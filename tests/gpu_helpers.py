@@ -78,3 +78,17 @@ def oracle_group(c, b, g, ratio=None, budget_tokens=None, keep_pages=None, selec
     else:
         k = oracle.keep_count(n, ratio=ratio)
     return dict(q=q, K=K, V=V, table=table, lens=lens, mn=mn, mx=mx, scores=s, k=k)
+
+
+def round256(x: int) -> int:
+    return (x + 255) // 256 * 256
+
+
+def step_selection(workspace, B, Hkv, stride, k_max):
+    """sel_idx and sel_cnt of a sparse kv_decode_step, read from its workspace at the
+    offsets include/sparsekv.h documents."""
+    a = round256(B * Hkv * stride * 4)
+    c = a + round256(B * Hkv * k_max * 4)
+    sel = workspace[a: a + B * Hkv * k_max * 4].view(torch.int32).view(B, Hkv, k_max)
+    cnt = workspace[c: c + B * Hkv * 4].view(torch.int32).view(B, Hkv)
+    return sel.cpu().numpy(), cnt.cpu().numpy()

@@ -457,3 +457,27 @@ def test_physical_placement_does_not_change_results():
         np.testing.assert_array_equal(res[0][0][b], res[1][0][b])
     np.testing.assert_array_equal(res[0][2], res[1][2])
     np.testing.assert_array_equal(res[0][3], res[1][3])
+
+
+# ----------------------------------------------------------------------------- structured
+
+def test_structured_selection_brute_force_and_special_cases():
+    rng = np.random.default_rng(5)
+    for trial in range(40):
+        n = int(rng.integers(1, 60))
+        s = np.round(rng.normal(size=n), 1)
+        k, sink, local = (int(rng.integers(0, n + 3)) for _ in range(3))
+        forced = {p for p in range(n) if p < sink or p >= n - local}
+        rest = sorted((p for p in range(n) if p not in forced), key=lambda p: (-s[p], p))
+        want = sorted(forced | set(rest[:max(0, min(k, n) - len(forced))]))
+        got = oracle.select_structured(s, k, sink, local)
+        assert got.tolist() == want, (n, k, sink, local)
+    s = np.arange(10, dtype=np.float64)[::-1]            # page 0 scores highest
+    # no forced pages: plain top-k
+    assert oracle.select_structured(s, 3).tolist() == oracle.select_pages(s, 3).tolist()
+    # the KV window keeps exactly the last k pages whatever the scores
+    assert oracle.select_structured(s, 4, 0, 4).tolist() == [6, 7, 8, 9]
+    # sink 1 + local 2 + one scored page (page 1 is the best unforced one)
+    assert oracle.select_structured(s, 4, 1, 2).tolist() == [0, 1, 8, 9]
+    # forced pages beyond k are all kept
+    assert oracle.select_structured(s, 1, 2, 2).tolist() == [0, 1, 8, 9]
