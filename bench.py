@@ -140,7 +140,8 @@ def byte_account(w, n_pages, sel_cnt, S):
                   + B*Hq*D*eb [q] + sum_b n_b*4 [table] + sum_{b,g} k_bg*4 [indices]
     attention launch = sum_{b,g} k_bg*(2*PS*D*eb + 8) [pages + index + table entry]
                        + B*Hq*D*eb [q] + B*Hq*S*(D+2)*4 [partials written]
-    dense step = sum_b Hkv*n_b*PS*D*2*eb + q + table + partials.
+    attention + merge launch = sum_{b,g} k_bg*(2*PS*D*eb + 8) + q + B*Hq*(D+1)*4 [out, lse]
+    dense step = sum_b Hkv*n_b*PS*D*2*eb + q + table.
     """
     eb = 2 if w.dtype == "bf16" else 4
     B, Hq, Hkv, D, PS = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size
@@ -150,9 +151,13 @@ def byte_account(w, n_pages, sel_cnt, S):
     sparse = (k_total * PS * D * 2 * eb + n_total * Hkv * 2 * D * eb + q_bytes
               + n_total * 4 + k_total * 4)
     attn = k_total * (2 * PS * D * eb + 8) + q_bytes + B * Hq * S * (D + 2) * 4
+    # the attention + merge kernel of the two-launch step: reads the selected list, the
+    # table entries and pages, and (last CTA of each group) writes out and lse; its split
+    # partials stay an internal round trip and are not counted
+    step_attn = k_total * (2 * PS * D * eb + 8) + q_bytes + B * Hq * (D + 1) * 4
     dense = n_total * Hkv * PS * D * 2 * eb + q_bytes + n_total * 4
-    return dict(sparse_step=sparse, attn_launch=attn, dense_step=dense,
-                selected_pages=k_total, pages=n_total * Hkv)
+    return dict(sparse_step=sparse, attn_launch=attn, step_attn_launch=step_attn,
+                dense_step=dense, selected_pages=k_total, pages=n_total * Hkv)
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -225,15 +230,60 @@ def run_ours(args):
     ml_d = torch.empty((B, Hq, S_dense, 2), dtype=torch.float32, device=dev)
     out_d = torch.empty_like(out)
     lse_d = torch.empty_like(lse)
-    ws = torch.empty((skv.kv_decode_step_workspace_size(kv, Hq, k_max),), dtype=torch.uint8,
+    # the step's workspace starts zero-filled (its per-group counters return to zero)
+    ws = torch.zeros((skv.kv_decode_step_workspace_size(kv, Hq, k_max),), dtype=torch.uint8,
                      device=dev)
+    ctr = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    ctr2 = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    # the two-launch step (score + select, then attention + merge) runs wherever both calls
+    # accept the shape; otherwise the step is four kernels
+    two_launch = in_attn_select = False
+    if step_kw is not None:
+        try:
+            skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
+                                sel_idx=sel, sel_cnt=cnt, **step_kw)
+            skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
+                                     part_ml=ml, counters=ctr2, out=out, lse=lse)
+            two_launch = True
+        except binding.KVError:
+            pass
+        try:                           # the variant that selects inside the attention kernel
+            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
+                                      part_acc=acc, part_ml=ml, counters=ctr2, out=out,
+                                      lse=lse, **step_kw)
+            in_attn_select = True
+        except binding.KVError:
+            pass
+        torch.cuda.synchronize()
 
     try:
         marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        smarks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
         in_graph_events = True
     except TypeError:
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        smarks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         in_graph_events = False
+
+    def two_launch_step(with_marks):
+        """The two kernels kv_decode_step runs, called one by one through the C ABI."""
+        if with_marks:
+            smarks[0].record()
+        skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
+                            sel_idx=sel, sel_cnt=cnt, **step_kw)
+        if with_marks:
+            smarks[1].record()
+        skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
+                                 part_ml=ml, counters=ctr2, out=out, lse=lse)
+        if with_marks:
+            smarks[2].record()
+
+    def in_attn_select_step():
+        """Scores, then the attention kernel selecting each split's run itself."""
+        skv.kv_score_pages(kv, c.q, stats, scores)
+        skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
+                                  part_acc=acc, part_ml=ml, counters=ctr2, out=out, lse=lse,
+                                  **step_kw)
 
     def four_kernel_step(with_marks):
         if with_marks:
@@ -286,20 +336,24 @@ def run_ours(args):
         raise RuntimeError(f"device error word {flags:#x} after warm-up")
     one_launch = one_launch_ran = False
     if step_kw is not None:            # one launch leaves the score region of ws untouched
-        score_bytes = (B * Hkv * kv.stride * 4 + 255) // 256 * 256
+        ctr_bytes = 2 * ((B * Hkv * 4 + 255) // 256 * 256)      # the step's counters
+        score_region = ws[ctr_bytes: ctr_bytes + (B * Hkv * kv.stride * 4 + 255) // 256 * 256]
         for fn in (step, one_launch_step):
-            ws[:score_bytes].fill_(255)
+            score_region.fill_(255)
             fn()
             torch.cuda.synchronize()
-            ran = bool((ws[:score_bytes] == 255).all())
+            ran = bool((score_region == 255).all())
             if fn is step:
                 one_launch = ran
             else:
                 one_launch_ran = ran
 
-    # one CUDA graph per measured step; g_marked is the four-kernel step with event nodes
-    # between its kernels, replayed in its own flushed loop to time each kernel
-    g_step, g_dense, g_four, g_marked, g_one = (torch.cuda.CUDAGraph() for _ in range(5))
+    # one CUDA graph per measured step; g_marked and g_smarked are the four-kernel and the
+    # two-launch steps with event nodes between their kernels, replayed in their own flushed
+    # loops to time each kernel (event nodes sit between the kernels, so their programmatic
+    # launch overlap is lost there: those graphs time kernels, not steps)
+    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_inattn = (torch.cuda.CUDAGraph()
+                                                                     for _ in range(7))
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -312,9 +366,15 @@ def run_ours(args):
         if in_graph_events:
             with torch.cuda.graph(g_marked, stream=side):
                 four_kernel_step(True)
+            if two_launch:
+                with torch.cuda.graph(g_smarked, stream=side):
+                    two_launch_step(True)
         if step_kw is not None:
             with torch.cuda.graph(g_one, stream=side):
                 one_launch_step()
+        if in_attn_select:
+            with torch.cuda.graph(g_inattn, stream=side):
+                in_attn_select_step()
     stream.wait_stream(side)
     torch.cuda.synchronize()
 
@@ -344,6 +404,7 @@ def run_ours(args):
 
     # ---- timed region: K steps of each kind, L2 flushed before every step ---------------
     kern_us = {"score": [], "select": [], "attn": [], "merge": []}
+    step_kern_us = {"score_select": [], "attn_merge": []}
     barrier()
     with ClockSampler(local) as clk:
         step_us = timed(g_step)
@@ -354,6 +415,8 @@ def run_ours(args):
         barrier()
         one_us = timed(g_one) if one_launch_ran else []
         barrier()
+        inattn_us = timed(g_inattn) if in_attn_select else []
+        barrier()
         if in_graph_events:
             for _ in range(args.steps):
                 flush.zero_()
@@ -361,6 +424,12 @@ def run_ours(args):
                 torch.cuda.synchronize()
                 for i, k in enumerate(kern_us):
                     kern_us[k].append(marks[i].elapsed_time(marks[i + 1]) * 1e3)
+            for _ in range(args.steps if two_launch else 0):
+                flush.zero_()
+                g_smarked.replay()
+                torch.cuda.synchronize()
+                for i, k in enumerate(step_kern_us):
+                    step_kern_us[k].append(smarks[i].elapsed_time(smarks[i + 1]) * 1e3)
         barrier()
     clocks = clk.summary()
 
@@ -371,6 +440,12 @@ def run_ours(args):
             torch.cuda.synchronize()
             for i, k in enumerate(kern_us):
                 kern_us[k].append(marks[i].elapsed_time(marks[i + 1]) * 1e3)
+        for _ in range(args.steps if two_launch else 0):
+            flush.zero_()
+            two_launch_step(True)
+            torch.cuda.synchronize()
+            for i, k in enumerate(step_kern_us):
+                step_kern_us[k].append(smarks[i].elapsed_time(smarks[i + 1]) * 1e3)
 
     st, flags = skv.kv_check_device_errors()
     if st != 0:
@@ -422,10 +497,18 @@ def run_ours(args):
         # the step is a single kernel: its duration is the event-timed step
         roof_kernel, roof_bytes, roof_us = "fused_step_kernel", acct["sparse_step"], step_mean
         roof_source = os.path.join(CSRC, "step_fused.cu")
+    elif two_launch:
+        roof_kernel = ATTN_KERNEL[w.dtype][0] + " (attend + merge)"
+        roof_bytes = acct["step_attn_launch"]
+        roof_us = statistics.mean(step_kern_us["attn_merge"])
+        roof_source = ATTN_KERNEL[w.dtype][1]
     else:
         roof_kernel, roof_bytes, roof_us = ATTN_KERNEL[w.dtype][0], acct["attn_launch"], attn_us
         roof_source = ATTN_KERNEL[w.dtype][1]
     achieved = roof_bytes / (roof_us * 1e-6) / 1e9
+    # kernels per replay of each timed graph
+    n_step = 1 if one_launch else (2 if two_launch else 4)
+    n_dense = 1 if (w.dtype == "bf16" and step_kw is not None and two_launch) else 2
     line = {
         "metric": METRIC,
         "value": round(sparse_med, 3),
@@ -445,6 +528,8 @@ def run_ours(args):
             "context_tokens": int(c.seq_lens.sum()), "kv_storage": w.dtype, "keep": label,
             "step_path": ("one launch: kv_decode_step, a thread-block cluster per (sequence, "
                           "KV head)" if one_launch else
+                          f"two kernels (score + select; split-K attention + merge), {S} splits"
+                          if two_launch else
                           f"four kernels (score, select, attention, merge), {S} splits"),
             "num_splits_four_kernel": S, "parallelism": f"replicas{world}",
             "l2": "flushed before every timed step (256 MiB write = 2x L2, outside the events)",
@@ -459,6 +544,10 @@ def run_ours(args):
         "step_gbs": {"sparse": round(acct["sparse_step"] / (sparse_med * 1e-6) / 1e9, 1),
                      "dense": round(acct["dense_step"] / (dense_med * 1e-6) / 1e9, 1)},
         "one_launch_step_us": (round(statistics.median(one_us), 3) if one_us else None),
+        "select_in_attention_step_us": (round(statistics.median(inattn_us), 3)
+                                        if inattn_us else None),
+        "step_kernel_us_marked": ({k: round(statistics.mean(v), 3)
+                                   for k, v in step_kern_us.items() if v} or None),
         "four_kernel_step_us": {"median": round(statistics.median(four_us), 3),
                                 "kernel_us_marked": {k: round(statistics.mean(v), 3)
                                                      for k, v in kern_us.items() if v}},
@@ -483,9 +572,9 @@ def run_ours(args):
                 "frac": round(acct["dense_step"] / (dense_mean * 1e-6) / 1e9 / peak, 4),
                 "avg_launch_us": round(dense_mean, 3)},
         },
-        "gpu_launches": args.steps * ((1 if one_launch else 4) + (1 if one_launch else 2)
-                                      + 4 + (4 if in_graph_events else 0)
-                                      + (1 if one_us else 0)),
+        "gpu_launches": args.steps * (n_step + n_dense + 4 + (4 if in_graph_events else 0)
+                                      + (2 if two_launch else 0) + (1 if one_us else 0)
+                                      + (2 if inattn_us else 0)),
         "clocks": clocks,
     }
     if e2e_us:

@@ -223,6 +223,59 @@ kv_status kv_sparse_decode_attn(const kv_cache_desc* cache, const void* q,
                                 cudaStream_t stream);
 
 /*
+ * kv_score_select -- kv_score_pages followed by kv_select_topk (keep = NULL) in ONE launch.
+ * Writes scores (as kv_score_pages), sel_idx [batch][num_kv_heads][k_max] and sel_cnt
+ * [batch][num_kv_heads] (as kv_select_topk: same keep rule, same order, same ascending
+ * output). The block of each group that finishes its scores last runs the group's
+ * selection. counters: device [batch][num_kv_heads] int32, zero before the first call;
+ * every call returns them to zero. keep_ratio > 0 or budget_pages > 0. The group's keys
+ * must fit one block's shared memory: page_table_stride up to about 50,000 pages on GB300
+ * (KV_ERR_UNSUPPORTED beyond; kv_score_pages + kv_select_topk have no such limit).
+ */
+kv_status kv_score_select(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                          const void* stats, double keep_ratio, int32_t budget_pages,
+                          int32_t k_max, float* scores, int32_t scores_stride,
+                          int32_t* counters, int32_t* sel_idx, int32_t* sel_cnt,
+                          cudaStream_t stream);
+
+/*
+ * kv_decode_attn_merge -- kv_sparse_decode_attn followed by kv_merge_splits in ONE launch,
+ * for bf16 caches. Arguments and per-split results are those of kv_sparse_decode_attn
+ * (sel_idx NULL = every page, the dense baseline); the last of a group's split CTAs to
+ * finish merges the group's partials into out/lse by the formula of kv_merge_splits.
+ * counters: device [batch][num_kv_heads] int32, zero before the first call; every call
+ * returns them to zero. part_acc must be 16-byte and part_ml 8-byte aligned
+ * (KV_ERR_MISALIGNED). num_splits is bounded by the merge's on-chip buffer
+ * (KV_ERR_UNSUPPORTED above it; over 1000 splits for every supported shape).
+ */
+kv_status kv_decode_attn_merge(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                               float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,
+                               int32_t sel_stride, int32_t num_splits, float* part_acc,
+                               float* part_ml, int32_t* counters, float* out, float* lse,
+                               cudaStream_t stream);
+
+/*
+ * kv_select_decode_attn -- kv_select_topk, kv_sparse_decode_attn and kv_merge_splits in ONE
+ * kernel, for bf16 caches. Each of a group's num_splits CTAs selects its own run of the
+ * kept pages from the group's score row (the rule and order of kv_select_topk with keep =
+ * NULL; the run split of kv_sparse_decode_attn), attends over it, writes its partial to
+ * part_acc/part_ml, and the group's last CTA merges the partials into out/lse (the formula
+ * of kv_merge_splits). With scores = NULL every page is kept: the dense baseline through
+ * the same kernel. counters: device [batch][num_kv_heads] int32, zero before the first call;
+ * every call returns them to zero. sel_idx [batch][num_kv_heads][k_max] and sel_cnt
+ * [batch][num_kv_heads] receive the selection when not NULL (sparse calls only). The group's
+ * pages must fit the in-kernel selection (page_table_stride at most 24448 pages for
+ * head_dim 128, 12160 for 64) and the splits its merge; otherwise KV_ERR_UNSUPPORTED.
+ * part_acc must be 16-byte and part_ml 8-byte aligned (KV_ERR_MISALIGNED).
+ */
+kv_status kv_select_decode_attn(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const float* scores, int32_t scores_stride,
+                                double keep_ratio, int32_t budget_pages, int32_t k_max,
+                                int32_t num_splits, float* part_acc, float* part_ml,
+                                int32_t* counters, float* out, float* lse, int32_t* sel_idx,
+                                int32_t* sel_cnt, cudaStream_t stream);
+
+/*
  * kv_merge_splits -- log-sum-exp merge of the split partials ([BYTEX] split-K).
  * M = max_s m_s; L = sum_s l_s exp(m_s - M); out = sum_s acc_s exp(m_s - M) / L;
  * lse = M + log L (natural log). Splits with m = -inf carry no mass; if every split is
@@ -267,11 +320,18 @@ size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_
  * calls). Both paths give the same selection (bit for bit) and outputs equal up to float32
  * rounding of the merge.
  * out: device [batch][num_q_heads][head_dim] float32; lse: [batch][num_q_heads] or NULL.
- * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned. After
- * a sparse call it holds the step's selection: sel_idx [batch][num_kv_heads][k_max] int32 at
- * byte offset A = round256(batch * num_kv_heads * page_table_stride * 4), and sel_cnt
- * [batch][num_kv_heads] int32 at A + round256(batch * num_kv_heads * k_max * 4), where
- * round256(x) rounds x up to a multiple of 256 (the layout kv_dropped_mass can be fed from).
+ * For bf16 caches the four calls collapse into two launches, kv_score_select and
+ * kv_decode_attn_merge (the dense step is the second alone).
+ * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned, ZERO-
+ * FILLED ONCE before its first use: it starts with two int32 counters per group, at offsets
+ * that depend only on batch * num_kv_heads, which the kernels return to zero after every
+ * step, so one workspace serves sparse and dense calls and any k_max or split count (as
+ * long as it is large enough). After a sparse call it holds the step's selection:
+ * sel_idx [batch][num_kv_heads][k_max] int32 at byte offset
+ * A = 2 * round256(batch * num_kv_heads * 4) + round256(batch * num_kv_heads *
+ * page_table_stride * 4), and sel_cnt [batch][num_kv_heads] int32 at
+ * A + round256(batch * num_kv_heads * k_max * 4), where round256(x) rounds x up to a
+ * multiple of 256 (the layout kv_dropped_mass can be fed from).
  */
 kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                          float sm_scale, const void* stats, double keep_ratio,
@@ -288,7 +348,10 @@ size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_h
  * device allocator of its own, or a serving loop that must not call cudaMalloc per token,
  * since that can synchronise the device or fail under memory pressure mid-step). The pages
  * have no counterpart of this call: it only moves the scratch of kv_decode_step into the
- * library. Inputs, outputs and results are those of kv_decode_step (bit for bit).
+ * library. It runs kv_score_pages, kv_select_topk, kv_sparse_decode_attn and kv_merge_splits
+ * (no per-group counters, so nothing in the array has to keep a value between calls): the
+ * selection is kv_decode_step's bit for bit and the outputs equal up to float32 rounding of
+ * the merge.
  * Scratch: one file-scope __device__ array of KV_STATIC_SCRATCH_BYTES that every GPU loading
  * the library holds until exit. The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress, that device current), so make that first call before any

@@ -33,7 +33,8 @@ EXPORTS = (
     "kv_dropped_mass", "kv_dropped_mass_workspace_size", "kv_decode_step",
     "kv_decode_step_workspace_size", "kv_check_device_errors", "kv_set_wait_limit_ns",
     "kv_selftest_wait_timeout", "kv_decode_step_static", "kv_append_token",
-    "kv_select_structured",
+    "kv_select_structured", "kv_select_decode_attn", "kv_score_select",
+    "kv_decode_attn_merge",
 )
 
 
@@ -87,6 +88,10 @@ def _declare(lib):
         "kv_append_token": (I32, [D, P, P, P, P]),
         "kv_select_structured": (I32, [P, I32, P, I32, I32, I32, P, F64, I32, I32, I32, I32, P,
                                        P, P]),
+        "kv_select_decode_attn": (I32, [D, P, I32, F32, P, I32, F64, I32, I32, I32, P, P, P, P,
+                                        P, P, P, P]),
+        "kv_score_select": (I32, [D, P, I32, P, F64, I32, I32, P, I32, P, P, P, P]),
+        "kv_decode_attn_merge": (I32, [D, P, I32, F32, P, P, I32, I32, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -330,6 +335,110 @@ def kv_sparse_decode_attn(kv: PagedKV, q, sm_scale: float, sel_idx=None, sel_cnt
     return part_acc, part_ml
 
 
+def kv_select_decode_attn(kv: PagedKV, q, sm_scale: float, scores=None, keep_ratio: float = 1.0,
+                          budget_pages: int = 0, k_max: int | None = None,
+                          num_splits: int | None = None, part_acc=None, part_ml=None,
+                          counters=None, out=None, lse=None, sel_idx=None, sel_cnt=None,
+                          stream=None):
+    """Selection, split-K attention and merge in one kernel (bf16); scores=None is dense.
+    counters must start at zero (they are returned to zero)."""
+    _need(q, "q", kv.dtype)
+    B, Hq, D = q.shape
+    Hkv = kv.num_kv_heads
+    if k_max is None:
+        k_max = max_keep_pages(kv.stride, keep_ratio, budget_pages) if scores is not None else 1
+    if num_splits is None:
+        num_splits = kv_auto_num_splits(kv, Hq, k_max if scores is not None else kv.stride)
+    S = int(num_splits)
+    dev = q.device
+    if part_acc is None:
+        part_acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=dev)
+    if part_ml is None:
+        part_ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device=dev)
+    if counters is None:
+        counters = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _need(part_acc, "part_acc", torch.float32, (B, Hq, S, D))
+    _need(part_ml, "part_ml", torch.float32, (B, Hq, S, 2))
+    _need(counters, "counters", torch.int32, (B, Hkv))
+    stride = 0
+    if scores is not None:
+        _need(scores, "scores", torch.float32)
+        stride = scores.shape[-1]
+    _check("kv_select_decode_attn", lib().kv_select_decode_attn(
+        kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(scores), stride, float(keep_ratio),
+        int(budget_pages), int(k_max), S, _ptr(part_acc), _ptr(part_ml), _ptr(counters),
+        _ptr(out), _ptr(lse), _ptr(sel_idx), _ptr(sel_cnt), _stream(stream)))
+    return out, lse
+
+
+def kv_score_select(kv: PagedKV, q, stats, keep_ratio: float = 0.0, budget_pages: int = 0,
+                    k_max: int | None = None, scores=None, counters=None, sel_idx=None,
+                    sel_cnt=None, stream=None):
+    """kv_score_pages + kv_select_topk in one launch. counters must start at zero (they are
+    returned to zero). Returns (scores, sel_idx, sel_cnt)."""
+    _need(q, "q", kv.dtype)
+    B, Hkv, stride, dev = kv.batch, kv.num_kv_heads, kv.stride, q.device
+    if k_max is None:
+        k_max = max_keep_pages(stride, keep_ratio, budget_pages)
+    if scores is None:
+        scores = torch.empty((B, Hkv, stride), dtype=torch.float32, device=dev)
+    if counters is None:
+        counters = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    if sel_idx is None:
+        sel_idx = torch.empty((B, Hkv, k_max), dtype=torch.int32, device=dev)
+    if sel_cnt is None:
+        sel_cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    _need(scores, "scores", torch.float32)
+    _need(counters, "counters", torch.int32, (B, Hkv))
+    _need(sel_idx, "sel_idx", torch.int32, (B, Hkv, k_max))
+    _need(sel_cnt, "sel_cnt", torch.int32, (B, Hkv))
+    _check("kv_score_select", lib().kv_score_select(
+        kv.ref(), _ptr(q), q.shape[1], _ptr(stats), float(keep_ratio), int(budget_pages),
+        int(k_max), _ptr(scores), scores.shape[-1], _ptr(counters), _ptr(sel_idx),
+        _ptr(sel_cnt), _stream(stream)))
+    return scores, sel_idx, sel_cnt
+
+
+def kv_decode_attn_merge(kv: PagedKV, q, sm_scale: float, sel_idx=None, sel_cnt=None,
+                         num_splits: int | None = None, part_acc=None, part_ml=None,
+                         counters=None, out=None, lse=None, stream=None):
+    """kv_sparse_decode_attn + kv_merge_splits in one launch (bf16); sel_idx=None is dense.
+    counters must start at zero (they are returned to zero). Returns (out, lse)."""
+    _need(q, "q", kv.dtype)
+    B, Hq, D = q.shape
+    dev = q.device
+    if num_splits is None:
+        bound = sel_idx.shape[-1] if sel_idx is not None else kv.stride
+        num_splits = kv_auto_num_splits(kv, Hq, bound)
+    S = int(num_splits)
+    if part_acc is None:
+        part_acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=dev)
+    if part_ml is None:
+        part_ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device=dev)
+    if counters is None:
+        counters = torch.zeros((B, kv.num_kv_heads), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _need(part_acc, "part_acc", torch.float32, (B, Hq, S, D))
+    _need(part_ml, "part_ml", torch.float32, (B, Hq, S, 2))
+    _need(counters, "counters", torch.int32, (B, kv.num_kv_heads))
+    sel_stride = 0
+    if sel_idx is not None:
+        _need(sel_idx, "sel_idx", torch.int32)
+        _need(sel_cnt, "sel_cnt", torch.int32)
+        sel_stride = sel_idx.shape[-1]
+    _check("kv_decode_attn_merge", lib().kv_decode_attn_merge(
+        kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(sel_idx), _ptr(sel_cnt), sel_stride, S,
+        _ptr(part_acc), _ptr(part_ml), _ptr(counters), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
 def kv_merge_splits(part_acc, part_ml, out=None, lse=None, stream=None):
     _need(part_acc, "part_acc", torch.float32)
     B, Hq, S, D = part_acc.shape
@@ -383,8 +492,8 @@ def kv_decode_step(kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: floa
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     if workspace is None:
-        nbytes = kv_decode_step_workspace_size(kv, Hq, k_max, num_splits)
-        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
+        nbytes = kv_decode_step_workspace_size(kv, Hq, k_max, max(num_splits, 0))
+        workspace = torch.zeros((nbytes,), dtype=torch.uint8, device=q.device)
     _check("kv_decode_step", lib().kv_decode_step(
         kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(stats), float(keep_ratio),
         int(budget_pages), int(k_max), int(num_splits), _ptr(out), _ptr(lse),

@@ -9,6 +9,7 @@
 #include <tuple>
 
 #include "attn_impl.cuh"
+#include "attn_mma.cuh"
 #include "kv_internal.cuh"
 
 namespace skv {
@@ -24,6 +25,7 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int smem_per_sm = 0;
+  int smem_optin = 0;          // largest dynamic shared memory one block may opt into
   int32_t* err = nullptr;
 };
 
@@ -42,6 +44,9 @@ kv_status device_state(DeviceState** out) {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return KV_ERR_CUDA;
     if (cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               dev) != cudaSuccess)
+      return KV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                dev) != cudaSuccess)
       return KV_ERR_CUDA;
     st.err = static_cast<int32_t*>(p);
@@ -115,13 +120,18 @@ int auto_splits(const kv_cache_desc* d, int G, int pages_per_group, const Device
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct StepLayout {
-  size_t scores, sel, cnt, acc, ml, total;
+  size_t scores, sel, cnt, acc, ml, ctr, ctr2, total;
 };
 
+// The per-group counters come first, at offsets that depend only on batch * num_kv_heads,
+// so calls of different shapes (sparse and dense, other k_max or split counts) on one
+// workspace keep finding them where the previous call returned them to zero.
 StepLayout step_layout(const kv_cache_desc* d, int Hq, int k_max, int S) {
   StepLayout L;
   const size_t groups = (size_t)d->batch * d->num_kv_heads;
-  L.scores = 0;
+  L.ctr = 0;
+  L.ctr2 = L.ctr + round256(groups * sizeof(int32_t));
+  L.scores = L.ctr2 + round256(groups * sizeof(int32_t));
   L.sel = L.scores + round256(groups * d->page_table_stride * sizeof(float));
   L.cnt = L.sel + round256(groups * (size_t)(k_max > 0 ? k_max : 1) * sizeof(int32_t));
   L.acc = L.cnt + round256(groups * sizeof(int32_t));
@@ -152,6 +162,12 @@ int cached_cluster_size(const kv_cache_desc* d, int G, const DeviceState* st) {
 
 bool is_dense(double keep_ratio, int budget_pages) {
   return budget_pages <= 0 && keep_ratio >= 1.0;
+}
+
+// The fused score + select launch fits this device for this table stride (its static
+// shared memory is a few KB on top of the dynamic part).
+bool score_select_fits(const kv_cache_desc* d, const DeviceState* st) {
+  return score_select_smem(d->page_table_stride) + 8 * 1024 <= (size_t)st->smem_optin;
 }
 
 __global__ void wait_selftest_kernel(unsigned long long limit_ns, DevCtx ctx) {
@@ -309,6 +325,102 @@ kv_status kv_sparse_decode_attn(const kv_cache_desc* cache, const void* q,
                                      st->sms));
 }
 
+kv_status kv_score_select(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                          const void* stats, double keep_ratio, int32_t budget_pages,
+                          int32_t k_max, float* scores, int32_t scores_stride,
+                          int32_t* counters, int32_t* sel_idx, int32_t* sel_cnt,
+                          cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (stats == nullptr || scores == nullptr || counters == nullptr || sel_idx == nullptr ||
+      sel_cnt == nullptr || scores_stride < cache->page_table_stride || k_max <= 0 ||
+      !(keep_ratio > 0.0 || budget_pages > 0))
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  DeviceState* st = nullptr;
+  if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
+  if (!score_select_fits(cache, st)) return KV_ERR_UNSUPPORTED;
+  return from_cuda(launch_score_select(*cache, q, num_q_heads, stats, scores, scores_stride,
+                                       keep_ratio, budget_pages, k_max, counters, sel_idx,
+                                       sel_cnt, ctx, stream));
+}
+
+kv_status kv_decode_attn_merge(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                               float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,
+                               int32_t sel_stride, int32_t num_splits, float* part_acc,
+                               float* part_ml, int32_t* counters, float* out, float* lse,
+                               cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (cache->dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
+  if (part_acc == nullptr || part_ml == nullptr || counters == nullptr || out == nullptr ||
+      num_splits < 1 || num_splits > 65535 || !(sm_scale > 0.f) || !isfinite(sm_scale))
+    return KV_ERR_INVALID_ARG;
+  if (sel_idx != nullptr && (sel_cnt == nullptr || sel_stride <= 0)) return KV_ERR_INVALID_ARG;
+  if (!aligned16(part_acc) || (reinterpret_cast<uintptr_t>(part_ml) & 7u) != 0)
+    return KV_ERR_MISALIGNED;
+  const int G = num_q_heads / cache->num_kv_heads;
+  int max_sel = 0, max_S = 0;
+  step_attn_limits_bf16(cache->head_dim, G, &max_sel, &max_S);
+  if (num_splits > max_S) return KV_ERR_UNSUPPORTED;
+  if (num_splits < min_splits_for(sel_idx != nullptr ? sel_stride : cache->page_table_stride))
+    return KV_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  StepArgs sa{};
+  sa.counters = counters;
+  sa.out = out;
+  sa.lse = lse;
+  return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, sel_idx, sel_cnt, sel_stride,
+                                         num_splits, part_acc, part_ml, ctx, stream, sa));
+}
+
+kv_status kv_select_decode_attn(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const float* scores, int32_t scores_stride,
+                                double keep_ratio, int32_t budget_pages, int32_t k_max,
+                                int32_t num_splits, float* part_acc, float* part_ml,
+                                int32_t* counters, float* out, float* lse, int32_t* sel_idx,
+                                int32_t* sel_cnt, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (cache->dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
+  if (part_acc == nullptr || part_ml == nullptr || counters == nullptr || out == nullptr ||
+      num_splits < 1 || num_splits > 65535 || !(sm_scale > 0.f) || !isfinite(sm_scale))
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(part_acc) || (reinterpret_cast<uintptr_t>(part_ml) & 7u) != 0)
+    return KV_ERR_MISALIGNED;
+  const bool dense = scores == nullptr;
+  if (!dense && (scores_stride < cache->page_table_stride || k_max <= 0 ||
+                 !(keep_ratio > 0.0 || budget_pages > 0)))
+    return KV_ERR_INVALID_ARG;
+  const int G = num_q_heads / cache->num_kv_heads;
+  int max_sel = 0, max_S = 0;
+  step_attn_limits_bf16(cache->head_dim, G, &max_sel, &max_S);
+  if ((!dense && cache->page_table_stride > max_sel) || num_splits > max_S)
+    return KV_ERR_UNSUPPORTED;
+  if (num_splits < min_splits_for(dense ? cache->page_table_stride : k_max))
+    return KV_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  StepArgs sa{};
+  sa.scores = scores;
+  sa.scores_stride = scores_stride;
+  sa.keep_ratio = keep_ratio;
+  sa.budget = budget_pages;
+  sa.k_max = dense ? 1 : k_max;
+  sa.sel_out = dense ? nullptr : sel_idx;
+  sa.cnt_out = dense ? nullptr : sel_cnt;
+  sa.counters = counters;
+  sa.out = out;
+  sa.lse = lse;
+  return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, nullptr, nullptr, 0,
+                                         num_splits, part_acc, part_ml, ctx, stream, sa));
+}
+
 kv_status kv_merge_splits(const float* part_acc, const float* part_ml, int32_t batch,
                           int32_t num_q_heads, int32_t num_splits, int32_t head_dim,
                           float* out, float* lse, cudaStream_t stream) {
@@ -414,9 +526,36 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   int S = num_splits;
   if (S <= 0) S = auto_splits(cache, G, dense ? cache->page_table_stride : k_max, st);
   if (S < min_splits_for(dense ? cache->page_table_stride : k_max)) return KV_ERR_INVALID_ARG;
-  // (a one-launch request whose shape does not allow it runs the four kernels instead)
+  // (a one-launch request whose shape does not allow it runs the kernels below instead)
   const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, S);
-  if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
+  if (cache->dtype == KV_BF16) {
+    // two launches: scores with the group's top-k in the last block of each group, then
+    // the attention kernel merging the group's partials in its last CTA
+    int max_sel = 0, max_S = 0;
+    step_attn_limits_bf16(cache->head_dim, G, &max_sel, &max_S);
+    if (S <= max_S && (dense || score_select_fits(cache, st))) {
+      if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
+      char* ws = static_cast<char*>(workspace);
+      int32_t* sel = dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.sel);
+      int32_t* cnt = dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.cnt);
+      if (!dense) {
+        cudaError_t e = launch_score_select(
+            *cache, q, num_q_heads, stats, reinterpret_cast<float*>(ws + L.scores),
+            cache->page_table_stride, keep_ratio, budget_pages, k_max,
+            reinterpret_cast<int32_t*>(ws + L.ctr), sel, cnt, ctx, stream);
+        if (e != cudaSuccess) return KV_ERR_CUDA;
+      }
+      StepArgs sa{};
+      sa.counters = reinterpret_cast<int32_t*>(ws + L.ctr2);
+      sa.out = out;
+      sa.lse = lse;
+      return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, sel, cnt,
+                                             dense ? 0 : k_max, S,
+                                             reinterpret_cast<float*>(ws + L.acc),
+                                             reinterpret_cast<float*>(ws + L.ml), ctx, stream,
+                                             sa));
+    }
+  }
   char* ws = static_cast<char*>(workspace);
   float* scores = reinterpret_cast<float*>(ws + L.scores);
   int32_t* sel = reinterpret_cast<int32_t*>(ws + L.sel);

@@ -44,7 +44,7 @@ template <int D, int G>
 cudaError_t launch_mma(const kv_cache_desc& d, const CUtensorMap& mk, const CUtensorMap& mv,
                        const void* q, float sm_scale, const int32_t* sel_idx,
                        const int32_t* sel_cnt, int sel_stride, int S, float* part_acc,
-                       float* part_ml, DevCtx ctx, cudaStream_t st) {
+                       float* part_ml, DevCtx ctx, cudaStream_t st, const StepArgs& sa) {
   using C = MmaCfg<D, G>;
   auto kern = split_attn_mma_kernel<D, G>;
   static int attr_set_for_device[64] = {0};
@@ -59,21 +59,36 @@ cudaError_t launch_mma(const kv_cache_desc& d, const CUtensorMap& mk, const CUte
   dim3 grid(S, d.num_kv_heads, d.batch);
   return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, mk, mv, d,
                     static_cast<const uint16_t*>(q), sm_scale * kLog2e, sel_idx, sel_cnt,
-                    sel_stride, S, part_acc, part_ml, ctx);
+                    sel_stride, S, part_acc, part_ml, ctx, sa);
 }
 
 template <int D>
 cudaError_t launch_mma_d(const kv_cache_desc& d, const CUtensorMap& mk, const CUtensorMap& mv,
                          const void* q, int G, float sm_scale, const int32_t* sel_idx,
                          const int32_t* sel_cnt, int sel_stride, int S, float* part_acc,
-                         float* part_ml, DevCtx ctx, cudaStream_t st) {
+                         float* part_ml, DevCtx ctx, cudaStream_t st, const StepArgs& sa) {
   switch (G) {
-    case 1: return launch_mma<D, 1>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
-    case 2: return launch_mma<D, 2>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
-    case 4: return launch_mma<D, 4>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
-    case 8: return launch_mma<D, 8>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st);
+    case 1: return launch_mma<D, 1>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st, sa);
+    case 2: return launch_mma<D, 2>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st, sa);
+    case 4: return launch_mma<D, 4>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st, sa);
+    case 8: return launch_mma<D, 8>(d, mk, mv, q, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc, part_ml, ctx, st, sa);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_bf16_common(const kv_cache_desc& d, const void* q, int G, float sm_scale,
+                               const int32_t* sel_idx, const int32_t* sel_cnt, int sel_stride,
+                               int S, float* part_acc, float* part_ml, DevCtx ctx,
+                               cudaStream_t st, const StepArgs& sa) {
+  if ((long long)d.num_phys_pages * d.num_kv_heads * d.page_size >= (1ll << 31))
+    return cudaErrorInvalidValue;                 // TMA row coordinates are 32-bit
+  CUtensorMap mk, mv;
+  if (!pool_map(&mk, d.k_pool, d) || !pool_map(&mv, d.v_pool, d)) return cudaErrorInvalidValue;
+  if (d.head_dim == 128)
+    return launch_mma_d<128>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
+                             part_acc, part_ml, ctx, st, sa);
+  return launch_mma_d<64>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc,
+                          part_ml, ctx, st, sa);
 }
 
 }  // namespace
@@ -82,15 +97,31 @@ cudaError_t launch_split_attn_bf16(const kv_cache_desc& d, const void* q, int G,
                                    const int32_t* sel_idx, const int32_t* sel_cnt,
                                    int sel_stride, int S, float* part_acc, float* part_ml,
                                    DevCtx ctx, cudaStream_t st) {
-  if ((long long)d.num_phys_pages * d.num_kv_heads * d.page_size >= (1ll << 31))
-    return cudaErrorInvalidValue;                 // TMA row coordinates are 32-bit
-  CUtensorMap mk, mv;
-  if (!pool_map(&mk, d.k_pool, d) || !pool_map(&mv, d.v_pool, d)) return cudaErrorInvalidValue;
-  if (d.head_dim == 128)
-    return launch_mma_d<128>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
-                             part_acc, part_ml, ctx, st);
-  return launch_mma_d<64>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc,
-                          part_ml, ctx, st);
+  const StepArgs none{};
+  return launch_bf16_common(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc,
+                            part_ml, ctx, st, none);
+}
+
+cudaError_t launch_step_attn_bf16(const kv_cache_desc& d, const void* q, int G, float sm_scale,
+                                  const int32_t* sel_idx, const int32_t* sel_cnt,
+                                  int sel_stride, int S, float* part_acc, float* part_ml,
+                                  DevCtx ctx, cudaStream_t st, const StepArgs& sa) {
+  return launch_bf16_common(d, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S, part_acc,
+                            part_ml, ctx, st, sa);
+}
+
+void step_attn_limits_bf16(int head_dim, int G, int* max_select_pages, int* max_splits) {
+  int sel = 0, ring = 0;
+#define SKV_LIM_CASE(DD, GG)                                                               \
+  if (head_dim == DD && G == GG) {                                                         \
+    sel = MmaCfg<DD, GG>::MAX_SELECT_PAGES;                                                \
+    ring = MmaCfg<DD, GG>::NSTAGE * MmaCfg<DD, GG>::STAGE_BYTES;                           \
+  }
+  SKV_LIM_CASE(64, 1) SKV_LIM_CASE(64, 2) SKV_LIM_CASE(64, 4) SKV_LIM_CASE(64, 8)
+  SKV_LIM_CASE(128, 1) SKV_LIM_CASE(128, 2) SKV_LIM_CASE(128, 4) SKV_LIM_CASE(128, 8)
+#undef SKV_LIM_CASE
+  *max_select_pages = sel;
+  *max_splits = G > 0 ? (ring / 4 - 2 * G) / G : 0;   // merge weights [G][S] in the ring
 }
 
 size_t split_attn_smem_bf16(int head_dim, int G) {

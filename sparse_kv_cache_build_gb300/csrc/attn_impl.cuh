@@ -457,4 +457,12 @@ cudaError_t launch_split_attn_fp32(const kv_cache_desc& d, const void* q, int G,
 size_t split_attn_smem_bf16(int head_dim, int G);
 size_t split_attn_smem_fp32(int head_dim, int G);
 
+// bf16 step mode of the attention kernel (see StepArgs in attn_mma.cuh).
+struct StepArgs;
+cudaError_t launch_step_attn_bf16(const kv_cache_desc& d, const void* q, int G, float sm_scale,
+                                  const int32_t* sel_idx, const int32_t* sel_cnt,
+                                  int sel_stride, int S, float* part_acc, float* part_ml,
+                                  DevCtx ctx, cudaStream_t st, const StepArgs& sa);
+void step_attn_limits_bf16(int head_dim, int G, int* max_select_pages, int* max_splits);
+
 }  // namespace skv

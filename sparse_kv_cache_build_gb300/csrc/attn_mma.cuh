@@ -25,6 +25,7 @@
 
 #include <cuda.h>
 
+#include "cta_topk.cuh"
 #include "kv_internal.cuh"
 
 namespace skv {
@@ -42,8 +43,14 @@ struct MmaCfg {
   static constexpr size_t OFF_STAGES = 0;                  // from a 1024-aligned base
   static constexpr size_t OFF_PHYS = OFF_STAGES + (size_t)NSTAGE * STAGE_BYTES;
   static constexpr size_t OFF_VALID = OFF_PHYS + 4 * kMaxSplitPages;
-  static constexpr size_t OFF_BAR = OFF_VALID + 2 * kMaxSplitPages;
+  static constexpr size_t OFF_HIST = OFF_VALID + 2 * kMaxSplitPages;   // uint32 [kHistWords]
+  static constexpr size_t OFF_MISC = OFF_HIST + 4 * 288;                // uint32 [16]
+  static constexpr size_t OFF_WTOT = OFF_MISC + 64;                     // uint64 [8]
+  static constexpr size_t OFF_BAR = OFF_WTOT + 64;
   static constexpr size_t SMEM = OFF_BAR + 8 * NSTAGE + 1024;   // + alignment slack
+  // largest group whose keys fit the ring for the in-kernel selection
+  static constexpr int MAX_SELECT_PAGES =
+      (int)((NSTAGE * (size_t)STAGE_BYTES / 4) / THREADS - 1) * THREADS;
   // a CTA partial: acc [G][D], then m [G] (base 2), then l [G]
   static constexpr size_t PARTIAL_FLOATS = (size_t)G * (D + 2);
   static constexpr size_t MERGE_BYTES = 4 * (size_t)4 * G * (D + 2);
@@ -100,6 +107,25 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Barrier helpers for a group of `nthreads` threads on named barrier `bar_id`
+// (bar_id 0 = the whole CTA through __syncthreads).
+__device__ __forceinline__ bool group_or(bool pred, int bar_id, int nthreads) {
+  if (bar_id == 0) return __syncthreads_or(pred) != 0;
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"((uint32_t)pred), "r"(bar_id), "r"(nthreads) : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void group_sync(int bar_id, int nthreads) {
+  if (bar_id == 0) __syncthreads();
+  else asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthreads) : "memory");
+}
+
 // Per-warp running state of the online softmax: O accumulator fragments (rows lane/4 are
 // the group's query heads; rows lane/4 + 8 are padding), the row max (base 2) and this
 // lane's share of the row sum.
@@ -138,14 +164,20 @@ __device__ __forceinline__ void load_q_frags(const uint16_t* q, long row0, uint3
 // ((ring_base + t) / NST) & 1, so one ring can serve several runs or phases of a kernel.
 // It consumes ceil(np / (64 / PS)) ring uses. Returns false if a wait ran out (the copies
 // this CTA issued have then been drained, bounded).
+//
+// The group running it is 4 warps (128 threads): by default the whole CTA synchronised with
+// __syncthreads; a CTA may run two independent groups, each with its own stages, barriers,
+// run and named barrier bar_id (gtid = thread index within the group).
 template <int D, int G, int NST>
 __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char* stages,
                           uint64_t* bars, uint32_t ring_base, const int32_t* s_phys,
                           const int16_t* s_valid, int np, int g, int Hkv, int PS,
                           const uint32_t* qa0, const uint32_t* qa2, float qk_scale_log2,
-                          WarpAcc<D>& acc, unsigned long long wait_ns) {
+                          WarpAcc<D>& acc, unsigned long long wait_ns, int bar_id = 0,
+                          int gtid = -1) {
   using C = MmaCfg<D, G>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = gtid >= 0 ? gtid : (int)threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int lm = lane >> 3, lr = lane & 7;
   const int PPT = kTileTokens / PS;
@@ -184,7 +216,7 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
     const uint32_t u = ring_base + (uint32_t)t;
     const int st = (int)(u % NST);
     const bool ok = mbar_wait_bounded(&bars[st], (u / NST) & 1u, wait_ns);
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (group_or(!ok, bar_id, 128)) { aborted = true; break; }
 
     const int tok_base = warp * kWarpTokens;
     const int slot = t * PPT + tok_base / PS;
@@ -251,7 +283,7 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
         mma_bf16(acc.o[2 * np2 + 1], pl0, 0u, pl2, 0u, v10, v11);
       }
     }
-    __syncthreads();                                       // the stage is free again
+    group_sync(bar_id, 128);                               // the stage is free again
     if (tid == 0 && t + NST < n_tiles) issue(t + NST);
   }
   if (aborted && tid == 0) {
@@ -264,19 +296,19 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
   return !aborted;
 }
 
-// Merge the four warps' states into one CTA partial in shared memory `part`:
+// Merge the NW warps' states into one CTA partial in shared memory `part`:
 // acc [G][D] (relative to m), m [G] in base 2 (-inf when empty), l [G]. `scratch` holds
-// 4*G*(D+2) floats and may alias the stage ring once it is idle. Ends with __syncthreads.
-template <int D, int G>
+// NW*G*(D+2) floats and may alias the stage ring once it is idle. Ends with __syncthreads.
+template <int D, int G, int NW = 4>
 __device__ void cta_partial(WarpAcc<D>& acc, float* scratch, float* part) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   float l_row = acc.l_lane;
   l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
   l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-  float* mg_o = scratch;                                   // [4][G][D]
-  float* mg_m = mg_o + 4 * G * D;                          // [4][G]
-  float* mg_l = mg_m + 4 * G;
+  float* mg_o = scratch;                                   // [NW][G][D]
+  float* mg_m = mg_o + NW * G * D;                         // [NW][G]
+  float* mg_l = mg_m + NW * G;
   if (gid < G) {
     if (tig == 0) {
       mg_m[warp * G + gid] = acc.m_run;
@@ -293,11 +325,11 @@ __device__ void cta_partial(WarpAcc<D>& acc, float* scratch, float* part) {
     const int hl = i / D, dd = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, mg_m[w2 * G + hl]);
+    for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, mg_m[w2 * G + hl]);
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2) {
+      for (int w2 = 0; w2 < NW; ++w2) {
         const float mw = mg_m[w2 * G + hl];
         const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
         L = fmaf(mg_l[w2 * G + hl], sc, L);
@@ -313,6 +345,27 @@ __device__ void cta_partial(WarpAcc<D>& acc, float* scratch, float* part) {
   __syncthreads();
 }
 
+// Optional parts of a decode step run inside the attention kernel.
+//  * scores != nullptr: each CTA selects its own run of the group's kept pages from the
+//    score row (keep rule keep_rule(n, ratio, budget) clamped to k_max), instead of reading
+//    a selected list; split 0 also writes the whole list to sel_out[grp][k_max] and the
+//    count to cnt_out[grp] when those are given.
+//  * counters != nullptr: after writing its partial, each CTA counts itself in
+//    counters[grp] (which must start at 0); the last CTA of the group merges the S partials
+//    into out/lse and resets the counter to 0.
+struct StepArgs {
+  const float* scores;
+  int scores_stride;
+  double keep_ratio;
+  int budget;
+  int k_max;
+  int32_t* sel_out;
+  int32_t* cnt_out;
+  int32_t* counters;
+  float* out;
+  float* lse;
+};
+
 template <int D, int G>
 __global__ void __launch_bounds__(MmaCfg<D, G>::THREADS)
 split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -320,7 +373,7 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                       const uint16_t* __restrict__ q, float qk_scale_log2,
                       const int32_t* __restrict__ sel_idx, const int32_t* __restrict__ sel_cnt,
                       int sel_stride, int S, float* __restrict__ part_acc,
-                      float* __restrict__ part_ml, DevCtx ctx) {
+                      float* __restrict__ part_ml, DevCtx ctx, StepArgs sa) {
   using C = MmaCfg<D, G>;
   extern __shared__ __align__(128) char smem_raw[];
   char* smem = reinterpret_cast<char*>(
@@ -342,26 +395,12 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   const int n_pages = ceil_div(len, PS);
 
   // ---- this split's run of the page list ------------------------------------------------
-  int cnt = n_pages;
   const long grp = (long)b * Hkv + g;
-  if (sel_idx != nullptr) {
-    cnt = sel_cnt[grp];
-    if (cnt < 0 || cnt > sel_stride) {
-      if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
-      cnt = cnt < 0 ? 0 : sel_stride;
-    }
-  }
-  const int c = cnt > 0 ? ceil_div(cnt, S) : 0;
-  const int pos0 = min(cnt, s * c);
-  int np = min(cnt, pos0 + c) - pos0;
-  if (np > kMaxSplitPages) {
-    if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
-    np = kMaxSplitPages;
-  }
   const int32_t* table = d.page_table + (long)b * d.page_table_stride;
-  for (int i = tid; i < np; i += C::THREADS) {
-    int p = pos0 + i, P = -1, valid = 0;
-    if (sel_idx != nullptr) p = sel_idx[grp * sel_stride + pos0 + i];
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  // resolve logical page p (list position pos) into run slot i
+  auto resolve = [&](int i, int p) {
+    int P = -1, valid = 0;
     if (p < 0 || p >= n_pages) {
       flag(ctx, KV_DEVERR_BAD_SEL);
     } else {
@@ -375,9 +414,62 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     s_phys[i] = P;
     s_valid[i] = (int16_t)valid;
+  };
+  int cnt = n_pages;
+  if (sa.scores != nullptr) {
+    cnt = keep_rule(n_pages, nullptr, b, sa.keep_ratio, sa.budget);
+    if (cnt > sa.k_max) {
+      if (s == 0 && tid == 0) flag(ctx, KV_DEVERR_KEEP);
+      cnt = sa.k_max;
+    }
+    if (s == 0 && tid == 0 && sa.cnt_out != nullptr) sa.cnt_out[grp] = cnt;
+  } else if (sel_idx != nullptr) {
+    cnt = sel_cnt[grp];
+    if (cnt < 0 || cnt > sel_stride) {
+      if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+      cnt = cnt < 0 ? 0 : sel_stride;
+    }
+  }
+  const int c = cnt > 0 ? ceil_div(cnt, S) : 0;
+  const int pos0 = min(cnt, s * c);
+  int np = min(cnt, pos0 + c) - pos0;
+  if (np > kMaxSplitPages) {
+    if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+    np = kMaxSplitPages;
   }
   uint32_t qa0[C::KSTEPS], qa2[C::KSTEPS];
-  load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
+  if (sa.scores != nullptr && cnt > 0 && cnt < n_pages && n_pages <= C::MAX_SELECT_PAGES) {
+    // select this CTA's run from the group's scores (the ring is free until the first copy);
+    // the page-table row and q are fetched meanwhile
+    for (int j = tid; j * 32 < n_pages; j += C::THREADS) prefetch_l2(table + j * 32);
+    load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
+    uint32_t* ring = reinterpret_cast<uint32_t*>(smem + C::OFF_STAGES);
+    constexpr int kRingWords = (int)((size_t)C::NSTAGE * C::STAGE_BYTES / 4);
+    const CtaKeys K = cta_load_keys<C::THREADS>(sa.scores + grp * sa.scores_stride, n_pages,
+                                                ring, misc + 8);
+    uint32_t T, take_eq;
+    const int used = C::THREADS * K.stride;
+    cta_threshold<C::THREADS>(K, cnt, reinterpret_cast<uint32_t*>(smem + C::OFF_HIST), misc,
+                              ring + used, kRingWords - used, T, take_eq);
+    int32_t* sel_out = (s == 0) ? sa.sel_out : nullptr;
+    cta_compact<C::THREADS>(K, T, take_eq, reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT),
+                            [&](int p, int pos) {
+                              if (sel_out != nullptr) sel_out[grp * sa.k_max + pos] = p;
+                              if (pos >= pos0 && pos < pos0 + np) s_phys[pos - pos0] = p;
+                            });
+    __syncthreads();
+    for (int i = tid; i < np; i += C::THREADS) resolve(i, s_phys[i]);
+  } else {
+    if (sa.scores != nullptr && cnt > 0 && cnt < n_pages) {   // group too long to select here
+      if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+      np = 0;
+    }
+    for (int i = tid; i < np; i += C::THREADS)
+      resolve(i, sel_idx != nullptr ? sel_idx[grp * sel_stride + pos0 + i] : pos0 + i);
+    if (sa.scores != nullptr && s == 0 && sa.sel_out != nullptr)
+      for (int i = tid; i < cnt; i += C::THREADS) sa.sel_out[grp * sa.k_max + i] = i;
+    load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
+  }
   __syncthreads();
 
   WarpAcc<D> acc;
@@ -396,20 +488,110 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
         part_ml[(out_row + (long)hl * S) * 2 + 1] = 0.f;
       }
     }
-    return;
-  }
-  float* scratch = reinterpret_cast<float*>(smem + C::OFF_STAGES);
-  float* part = scratch + 4 * G * (D + 2);
-  cta_partial<D, G>(acc, scratch, part);
-  for (int i = tid; i < G * D; i += C::THREADS) {
-    const int hl = i / D, dd = i % D;
-    part_acc[(out_row + (long)hl * S) * D + dd] = part[hl * D + dd];
-    if (dd == 0) {
-      const float M = part[G * D + hl];
-      part_ml[(out_row + (long)hl * S) * 2 + 0] = M == -INFINITY ? -INFINITY : M * kLn2;
-      part_ml[(out_row + (long)hl * S) * 2 + 1] = part[G * D + G + hl];
+  } else {
+    float* scratch = reinterpret_cast<float*>(smem + C::OFF_STAGES);
+    float* part = scratch + 4 * G * (D + 2);
+    cta_partial<D, G>(acc, scratch, part);
+    for (int i = tid; i < G * D; i += C::THREADS) {
+      const int hl = i / D, dd = i % D;
+      part_acc[(out_row + (long)hl * S) * D + dd] = part[hl * D + dd];
+      if (dd == 0) {
+        const float M = part[G * D + hl];
+        part_ml[(out_row + (long)hl * S) * 2 + 0] = M == -INFINITY ? -INFINITY : M * kLn2;
+        part_ml[(out_row + (long)hl * S) * 2 + 1] = part[G * D + G + hl];
+      }
     }
   }
+  if (sa.counters == nullptr) return;
+
+  // ---- the group's last CTA merges its S partials (log-sum-exp) -------------------------
+  __syncthreads();                                         // this CTA's partials are written
+  if (tid == 0) {
+    __threadfence();
+    const int done = atomicAdd(&sa.counters[grp], 1);
+    misc[3] = (done == S - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (misc[3] == 0u) return;
+  __threadfence();
+  float* wts = reinterpret_cast<float*>(smem + C::OFF_STAGES);   // [G][S], then M[G], L[G]
+  float* Ms = wts + G * S;
+  float* Ls = Ms + G;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int hl = warp; hl < G; hl += C::THREADS / 32) {
+    // one pass over the (m, l) pairs: running max and rescaled sum per lane, then the warp's
+    const float2* ml = reinterpret_cast<const float2*>(part_ml) + ((long)b * Hq + g * G + hl) * S;
+    float M = -INFINITY, L = 0.f;
+    for (int x0 = lane; x0 < S; x0 += 64) {            // two loads in flight per lane
+      float2 v[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        v[u] = x0 + 32 * u < S ? __ldcg(ml + x0 + 32 * u) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (x0 + 32 * u < S) wts[hl * S + x0 + 32 * u] = v[u].x;
+        if (v[u].x != -INFINITY) {
+          if (v[u].x > M) {
+            L = (M == -INFINITY) ? 0.f : L * expf(M - v[u].x);
+            M = v[u].x;
+          }
+          L = fmaf(v[u].y, expf(v[u].x - M), L);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float L2 = __shfl_xor_sync(0xffffffffu, L, o);
+      const float Mn = fmaxf(M, M2);
+      L = (M == -INFINITY ? 0.f : L * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : L2 * expf(M2 - Mn));
+      M = Mn;
+    }
+    __syncwarp();
+    for (int x = lane; x < S; x += 32) {
+      const float m = wts[hl * S + x];
+      wts[hl * S + x] = (m == -INFINITY || M == -INFINITY) ? 0.f : expf(m - M);
+    }
+    if (lane == 0) {
+      Ms[hl] = M;
+      Ls[hl] = L;
+    }
+  }
+  __syncthreads();
+  // out = sum_s w_s acc_s / L, four columns per thread, sixteen splits' loads in flight
+  constexpr int D4 = D / 4;
+  for (int o = tid; o < G * D4; o += C::THREADS) {
+    const int hl = o / D4, d4 = o - hl * D4;
+    const long row = (long)b * Hq + g * G + hl;
+    const float4* a = reinterpret_cast<const float4*>(part_acc + row * S * D) + d4;
+    const float* w = wts + hl * S;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int x = 0; x < S; x += 16) {                  // no serial remainder: guarded lanes
+      float4 v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        v[u] = x + u < S ? __ldcg(a + (long)(x + u) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (x + u < S) {
+          const float ww = w[x + u];
+          A.x = fmaf(v[u].x, ww, A.x);
+          A.y = fmaf(v[u].y, ww, A.y);
+          A.z = fmaf(v[u].z, ww, A.z);
+          A.w = fmaf(v[u].w, ww, A.w);
+        }
+      }
+    }
+    const float M = Ms[hl], L = Ls[hl];
+    float* op = sa.out + row * D + d4 * 4;
+    const bool empty = M == -INFINITY;
+    op[0] = empty ? 0.f : A.x / L;
+    op[1] = empty ? 0.f : A.y / L;
+    op[2] = empty ? 0.f : A.z / L;
+    op[3] = empty ? 0.f : A.w / L;
+    if (d4 == 0 && sa.lse != nullptr) sa.lse[row] = empty ? -INFINITY : M + logf(L);
+  }
+  if (tid == 0) sa.counters[grp] = 0;                      // ready for the next step
 }
 
 }  // namespace skv

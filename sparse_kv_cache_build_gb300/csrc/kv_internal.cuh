@@ -120,6 +120,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // L2 policy for data read exactly once per step (K/V pages): evict first.
+// Hint: bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -164,6 +169,29 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Order-preserving key of a page score: the unsigned order of keys is the float order
+// (-0 and +0 give one key; NaN is not a valid score).
+__device__ __forceinline__ uint32_t score_order_key(float s) {
+  const uint32_t u = __float_as_uint(s + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Pages kept of a group of n: keep[b] if given, else min(n, budget) if budget > 0, else n
+// if ratio >= 1, else min(n, max(1, ceil(ratio * n - 1e-9))) in double; 0 when n == 0.
+__device__ __forceinline__ int keep_rule(int n, const int32_t* keep, int b, double ratio,
+                                         int budget) {
+  if (n <= 0) return 0;
+  if (keep != nullptr) {
+    const int k = keep[b];
+    return k < 0 ? 0 : (k > n ? n : k);
+  }
+  if (budget > 0) return budget < n ? budget : n;
+  if (ratio >= 1.0) return n;
+  int k = (int)ceil(ratio * (double)n - 1e-9);
+  k = k < 1 ? 1 : k;
+  return k < n ? k : n;
+}
+
 // Sequence length of b, clamped into [0, stride * page_size] (flags a bad length).
 __device__ __forceinline__ int checked_len(const DevCtx& c, const kv_cache_desc& d, int b) {
   int len = d.seq_lens[b];
@@ -183,6 +211,15 @@ cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, DevCtx ctx,
 cudaError_t launch_score_pages(const kv_cache_desc& d, const void* q, int Hq,
                                const void* stats, float* scores, int scores_stride,
                                DevCtx ctx, cudaStream_t s);
+// kv_score_pages and the group's top-k (keep ratio / budget) in one launch; counters
+// [batch][Hkv] start at zero and are returned to zero. score_select_smem: dynamic shared
+// bytes the launch needs for a table stride (the caller checks it against the device).
+size_t score_select_smem(int page_table_stride);
+cudaError_t launch_score_select(const kv_cache_desc& d, const void* q, int Hq,
+                                const void* stats, float* scores, int scores_stride,
+                                double keep_ratio, int budget, int k_max, int32_t* counters,
+                                int32_t* sel_idx, int32_t* sel_cnt, DevCtx ctx,
+                                cudaStream_t s);
 cudaError_t launch_select_topk(const float* scores, int scores_stride, const int32_t* seq_lens,
                                int page_size, int batch, int Hkv, const int32_t* keep,
                                double keep_ratio, int budget_pages, int k_max, int sink,

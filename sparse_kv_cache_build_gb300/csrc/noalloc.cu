@@ -15,9 +15,11 @@
 // streams, other host threads) race on it and must be serialised by the caller. Nothing in
 // it needs to start at zero -- every call writes each scratch byte before reading it.
 //
-// The step itself is unchanged: the same public calls (score, select, split-K attention,
-// merge) run on sub-buffers carved from the array exactly as kv_decode_step carves its
-// workspace, so results match kv_decode_step bit for bit.
+// The step runs the four public calls (score, select, split-K attention, merge) on
+// sub-buffers carved from the array like kv_decode_step's workspace. They keep no
+// per-group counters, so no value has to survive from one call to the next; the selection
+// matches kv_decode_step's bit for bit and the outputs match up to float32 rounding of the
+// merge (kv_decode_step merges inside its attention kernel for bf16 caches).
 #include <stdint.h>
 #include <string.h>
 
@@ -70,7 +72,7 @@ extern "C" kv_status kv_decode_step_static(const kv_cache_desc* cache, const voi
     S = kv_auto_num_splits(cache, num_q_heads, dense ? cache->page_table_stride : k_max);
     if (S < 0) return (kv_status)S;
   }
-  // the same carving as kv_decode_step's workspace
+  // carved like kv_decode_step's workspace, less its per-group counters
   const size_t groups = (size_t)cache->batch * cache->num_kv_heads;
   const size_t off_sel = up256(groups * cache->page_table_stride * sizeof(float));
   const size_t off_cnt = off_sel + up256(groups * (size_t)(dense ? 1 : k_max) * sizeof(int32_t));

@@ -21,6 +21,13 @@
 // and the grid covers every page of every group. Each block issues its page-table and
 // statistics loads first and only then builds Pos/Neg from q, so the two latency chains
 // overlap.
+//
+// score_select_kernel is the same pass followed by the group's top-k (the rule of
+// select.cu): 512-thread blocks of 64 pages each; the block of a group that finishes last
+// (a per-group arrival counter, returned to zero) reads the group's scores back from L2
+// and runs the block-wide selection of cta_topk.cuh, so the selection costs no launch of
+// its own and runs once per group.
+#include "cta_topk.cuh"
 #include "kv_internal.cuh"
 
 namespace skv {
@@ -28,23 +35,22 @@ namespace {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScorePagesPerBlock = kScoreWarps * 4;   // 16
+constexpr int kSelWarps = 16;                          // score + select blocks: 512 threads
+constexpr int kSelThreads = kSelWarps * 32;
+constexpr int kSelCandWords = 4096;                    // gathered keys of the threshold bin
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kScoreWarps * 32)
-score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restrict__ stats,
-             float* __restrict__ scores, int scores_stride, DevCtx ctx) {
+// Scores of the WARPS*4 pages of this block for group (b, g) into scores; returns false
+// (block-uniform) if the block has no page of the sequence.
+template <typename T, int D, int WARPS>
+__device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __restrict__ q,
+                                            int G, const T* __restrict__ stats, float* w,
+                                            float* __restrict__ scores, int scores_stride,
+                                            int b, int g, int n_pages, const DevCtx& ctx) {
   constexpr int EB = ElemTraits<T>::bytes;
   constexpr int EPC = 16 / EB;                // elements per 16-byte chunk
   constexpr int CPL = (2 * D * EB / 16) / 8;  // chunks per lane per stats row
-  __shared__ __align__(16) float w[2 * D];    // [Neg | Pos], matching a row's [mn | mx]
-  pdl_trigger();
-  pdl_wait();
-
-  const int b = blockIdx.z, g = blockIdx.y;
-  const int len = checked_len(ctx, d, b);
-  const int n_pages = ceil_div(len, d.page_size);
-  const int p_block = blockIdx.x * kScorePagesPerBlock;
-  if (p_block >= n_pages) return;
+  const int p_block = blockIdx.x * WARPS * 4;
+  if (p_block >= n_pages) return false;
 
   const int Hkv = d.num_kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -66,7 +72,7 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restric
   }
 
   const int Hq = Hkv * G;
-  for (int t = threadIdx.x; t < D; t += kScoreWarps * 32) {
+  for (int t = threadIdx.x; t < D; t += WARPS * 32) {
     float pos = 0.f, neg = 0.f;
     for (int h = g * G; h < (g + 1) * G; ++h) {
       const float x = load_elem<T>(q, ((long)b * Hq + h) * D + t);
@@ -93,6 +99,83 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restric
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   if (j == 0 && ok) scores[((long)b * Hkv + g) * scores_stride + p] = acc;
+  return true;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kScoreWarps * 32)
+score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restrict__ stats,
+             float* __restrict__ scores, int scores_stride, DevCtx ctx) {
+  __shared__ __align__(16) float w[2 * D];    // [Neg | Pos], matching a row's [mn | mx]
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int len = checked_len(ctx, d, b);
+  const int n_pages = ceil_div(len, d.page_size);
+  score_block<T, D, kScoreWarps>(d, q, G, stats, w, scores, scores_stride, b, g, n_pages, ctx);
+}
+
+// Shared words for the keys of a group of up to max_pages pages, laid out as cta_topk.cuh
+// lays them out for kSelThreads threads, plus the gathered-candidate scratch.
+__host__ __device__ constexpr size_t select_key_words(int max_pages) {
+  return (size_t)kSelThreads * (size_t)(((max_pages + kSelThreads - 1) / kSelThreads) | 1);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kSelThreads)
+score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
+                    const T* __restrict__ stats, float* __restrict__ scores, int scores_stride,
+                    double keep_ratio, int budget, int k_max, int32_t* __restrict__ counters,
+                    int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt,
+                    int key_words, DevCtx ctx) {
+  extern __shared__ __align__(16) uint32_t dyn_words[];     // keys, then candidates
+  __shared__ __align__(16) float w[2 * D];
+  __shared__ uint32_t hist[kHistWords];
+  __shared__ uint32_t misc[8 + kSelWarps];
+  __shared__ uint64_t wtot[kSelWarps];
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.z, g = blockIdx.y, tid = threadIdx.x;
+  const int len = checked_len(ctx, d, b);
+  const int n_pages = ceil_div(len, d.page_size);
+  const long grp = (long)b * d.num_kv_heads + g;
+  if (n_pages == 0) {                         // nothing to score or keep
+    if (blockIdx.x == 0 && tid == 0) sel_cnt[grp] = 0;
+    return;
+  }
+  if (!score_block<T, D, kSelWarps>(d, q, G, stats, w, scores, scores_stride, b, g, n_pages,
+                                    ctx))
+    return;
+
+  // ---- the group's last block selects -----------------------------------------------------
+  const int blocks = ceil_div(n_pages, kSelWarps * 4);
+  __syncthreads();                            // this block's scores are written
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(&counters[grp], 1) == blocks - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) counters[grp] = 0;            // ready for the next step
+  int k = keep_rule(n_pages, nullptr, b, keep_ratio, budget);
+  if (k > k_max) {
+    if (tid == 0) flag(ctx, KV_DEVERR_KEEP);
+    k = k_max;
+  }
+  int32_t* out = sel_idx + grp * k_max;
+  if (tid == 0) sel_cnt[grp] = k;
+  if (k >= n_pages) {                         // every page kept
+    for (int i = tid; i < n_pages; i += kSelThreads) out[i] = i;
+    return;
+  }
+  const CtaKeys K = cta_load_keys<kSelThreads>(scores + grp * scores_stride, n_pages, dyn_words,
+                                               misc + 8);
+  uint32_t thr, take_eq;
+  cta_threshold<kSelThreads>(K, k, hist, misc, dyn_words + key_words, kSelCandWords, thr,
+                             take_eq);
+  cta_compact<kSelThreads>(K, thr, take_eq, wtot, [&](int p, int pos) { out[pos] = p; });
 }
 
 template <typename T, int D>
@@ -104,7 +187,47 @@ cudaError_t launch_t(const kv_cache_desc& d, const void* q, int Hq, const void* 
                     static_cast<const T*>(stats), scores, scores_stride, ctx);
 }
 
+template <typename T, int D>
+cudaError_t launch_sel_t(const kv_cache_desc& d, const void* q, int Hq, const void* stats,
+                         float* scores, int scores_stride, double keep_ratio, int budget,
+                         int k_max, int32_t* counters, int32_t* sel_idx, int32_t* sel_cnt,
+                         DevCtx ctx, cudaStream_t s) {
+  const int key_words = (int)select_key_words(d.page_table_stride);
+  const size_t smem = 4 * ((size_t)key_words + kSelCandWords);
+  auto kern = score_select_kernel<T, D>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(ceil_div(d.page_table_stride, kSelWarps * 4), d.num_kv_heads, d.batch);
+  return launch_pdl(kern, grid, dim3(kSelThreads), smem, s, d, static_cast<const T*>(q),
+                    Hq / d.num_kv_heads, static_cast<const T*>(stats), scores, scores_stride,
+                    keep_ratio, budget, k_max, counters, sel_idx, sel_cnt, key_words, ctx);
+}
+
 }  // namespace
+
+size_t score_select_smem(int page_table_stride) {
+  return 4 * (select_key_words(page_table_stride) + kSelCandWords);
+}
+
+cudaError_t launch_score_select(const kv_cache_desc& d, const void* q, int Hq,
+                                const void* stats, float* scores, int scores_stride,
+                                double keep_ratio, int budget, int k_max, int32_t* counters,
+                                int32_t* sel_idx, int32_t* sel_cnt, DevCtx ctx,
+                                cudaStream_t s) {
+  const bool bf = d.dtype == KV_BF16;
+  if (d.head_dim == 128)
+    return bf ? launch_sel_t<bf16_t, 128>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
+                                          budget, k_max, counters, sel_idx, sel_cnt, ctx, s)
+              : launch_sel_t<float, 128>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
+                                         budget, k_max, counters, sel_idx, sel_cnt, ctx, s);
+  return bf ? launch_sel_t<bf16_t, 64>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
+                                       budget, k_max, counters, sel_idx, sel_cnt, ctx, s)
+            : launch_sel_t<float, 64>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
+                                      budget, k_max, counters, sel_idx, sel_cnt, ctx, s);
+}
 
 cudaError_t launch_score_pages(const kv_cache_desc& d, const void* q, int Hq,
                                const void* stats, float* scores, int scores_stride,

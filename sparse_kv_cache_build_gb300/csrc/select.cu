@@ -31,26 +31,6 @@
 namespace skv {
 namespace {
 
-__device__ __forceinline__ uint32_t order_key(float s) {
-  const uint32_t u = __float_as_uint(s + 0.0f);          // -0 -> +0: equal scores, equal keys
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ int keep_count(int n, const int32_t* keep, int b, double ratio,
-                                          int budget) {
-  if (n <= 0) return 0;
-  if (keep != nullptr) {
-    const int k = keep[b];
-    return k < 0 ? 0 : (k > n ? n : k);
-  }
-  if (budget > 0) return budget < n ? budget : n;
-  if (ratio >= 1.0) return n;
-  double c = ceil(ratio * (double)n - 1e-9);
-  int k = (int)c;
-  k = k < 1 ? 1 : k;
-  return k < n ? k : n;
-}
-
 // Block-wide exclusive scan of a 64-bit value (two packed 32-bit counters).
 __device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t* warp_tot,
                                                          uint64_t* total) {
@@ -104,7 +84,7 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
     len = len < 0 ? 0 : table_stride * PS;
   }
   const int n = ceil_div(len, PS);
-  int k = keep_count(n, keep, b, keep_ratio, budget);
+  int k = keep_rule(n, keep, b, keep_ratio, budget);
   const int forced = min(n, max(0, sink) + max(0, local));   // [0, sink) and [n - local, n)
   k = max(k, forced);
   if (k > k_max) {
@@ -115,7 +95,7 @@ select_kernel(const float* __restrict__ scores, int scores_stride,
   const float* row = scores != nullptr ? scores + grp * scores_stride : nullptr;
   auto key_at = [&](int i) -> uint32_t {
     if (i < sink || i >= n - local) return 0xffffffffu;   // forced in
-    return row != nullptr ? order_key(row[i]) : 0u;
+    return row != nullptr ? score_order_key(row[i]) : 0u;
   };
   int32_t* out = sel_idx + grp * k_max;
   if (tid == 0) sel_cnt[grp] = k;

@@ -10,19 +10,24 @@
 //
 // Why one launch: at 32K tokens the step moves ~49 MB, ~7 us at HBM speed, while four
 // dependent launches each pay a ramp-up (first loads, launch latency) of several us. Here a
-// thread-block cluster of CL CTAs (one per SM) owns one (sequence, KV head) group:
-//   1. scores   CTA r scores pages [r*cp, (r+1)*cp): statistics rows come in by bulk
-//               copies through the kernel's mbarrier ring; keys stay in shared memory.
-//   2. select   radix select of the k-th key: every pass each CTA counts its own keys into
-//               a shared histogram and the CL histograms are summed over distributed shared
-//               memory (one cluster barrier per pass, double-buffered histograms).
-//   3. compact  each CTA learns the (greater, equal) counts of the CTAs before it over
-//               DSMEM, scans its keys in page order, and writes each kept page (physical id,
-//               valid tokens) straight into the shared memory of the CTA whose split holds
-//               that list position (split r takes [r*c, (r+1)*c), c = ceil(k / CL), the
-//               split rule of kv_sparse_decode_attn with CL splits).
+// thread-block cluster of CL CTAs (one per SM, 8 warps each) owns one (sequence, KV head)
+// group, and the cluster size is chosen so that every group's cluster is resident at once:
+//   1. scores   CTA r scores pages [r*cp, (r+1)*cp) with all its page-table loads in
+//               flight, then all its statistics-row loads (eight lanes per 512-byte row),
+//               and writes each page's order key and physical id into the shared memory of
+//               every CTA of the cluster (distributed shared memory), so that after one
+//               cluster barrier each CTA holds the whole group.
+//   2. select   each CTA finds the threshold of the k kept keys locally (cta_topk.cuh:
+//               one radix pass from the highest differing bit, then the exact rank of the
+//               threshold bin's keys), the same result in every CTA.
+//   3. compact  each CTA scans the group's keys in page order and keeps only the list
+//               positions of its own split (split r takes [r*c, (r+1)*c), c = ceil(k / CL),
+//               the split rule of kv_sparse_decode_attn with CL splits).
 //   4. attend   the tensor-core attention of attn_mma.cuh over the CTA's run (same device
-//               code as kv_sparse_decode_attn's kernel).
+//               code as kv_sparse_decode_attn's kernel), run by two independent 4-warp
+//               halves of the CTA on the two halves of the run, each with its own two ring
+//               stages and named barrier, so one half computes while the other waits on
+//               copies (the overlap two CTAs per SM give the split kernel).
 //   5. merge    CTA r merges a slice of the G*D outputs from all CL partials over DSMEM.
 // Every CTA of a cluster takes the same branches (they depend only on the group's length,
 // keep count and the summed histograms), so every cluster barrier is reached by all of them;
@@ -31,13 +36,14 @@
 #include <cudaTypedefs.h>
 
 #include "attn_mma.cuh"
+#include "cta_topk.cuh"
 #include "kv_internal.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace skv {
 
-constexpr int kFusedThreads = 128;
+constexpr int kFusedThreads = 256;
 constexpr int kFusedNST = 4;
 constexpr int kFusedMaxRange = 4096;   // pages one CTA scores
 constexpr int kFusedMaxRun = 4096;     // selected pages one CTA attends
@@ -47,58 +53,22 @@ struct FusedCfg {
   using M = MmaCfg<D, G>;
   static constexpr int NST = kFusedNST;
   static constexpr int ROW = 2 * D * 2;                       // bf16 stats row bytes
-  static constexpr int CH = M::STAGE_BYTES / ROW;             // stats rows per ring stage
-  static constexpr size_t OFF_RING = 0;
-  static constexpr size_t OFF_KEYS = OFF_RING + (size_t)NST * M::STAGE_BYTES;
-  static constexpr size_t OFF_RPHYS = OFF_KEYS + 4 * kFusedMaxRange;
+  static constexpr int RING_WORDS = NST * M::STAGE_BYTES / 4;
+  static constexpr size_t OFF_RING = 0;   // keys, physical ids, candidates; then the copies
+  static constexpr size_t OFF_RPHYS = OFF_RING + (size_t)NST * M::STAGE_BYTES;
   static constexpr size_t OFF_RUNP = OFF_RPHYS + 4 * kFusedMaxRange;
   static constexpr size_t OFF_RUNV = OFF_RUNP + 4 * kFusedMaxRun;
   static constexpr size_t OFF_W = OFF_RUNV + 2 * kFusedMaxRun;
-  static constexpr size_t OFF_HIST = OFF_W + 4 * 2 * D;       // uint32 [2][256]
-  static constexpr size_t OFF_GH = OFF_HIST + 4 * 2 * 256;    // uint32 [256]
-  static constexpr size_t OFF_MISC = OFF_GH + 4 * 256;        // uint32 [16] + uint64 [8]
-  static constexpr size_t OFF_BAR = OFF_MISC + 128;
+  static constexpr size_t OFF_HIST = OFF_W + 4 * 2 * D;       // uint32 [kHistWords]
+  static constexpr size_t OFF_MISC = OFF_HIST + 4 * 288;      // uint32 [16] + uint64 [16]
+  static constexpr size_t OFF_MTAB = OFF_MISC + 192;          // float [16 ranks][2G]
+  static constexpr size_t OFF_BAR = OFF_MTAB + 4 * 16 * 2 * G;
   static constexpr size_t SMEM = OFF_BAR + 8 * NST + 1024;    // + alignment slack
-  static_assert(M::MERGE_BYTES + 4 * M::PARTIAL_FLOATS <= (size_t)NST * M::STAGE_BYTES,
+  static_assert(4 * (size_t)8 * G * (D + 2) + 4 * M::PARTIAL_FLOATS <=
+                    (size_t)NST * M::STAGE_BYTES,
                 "merge buffers must fit in the ring");
 };
 
-namespace {
-
-__device__ __forceinline__ uint32_t fused_key(float s) {
-  const uint32_t u = __float_as_uint(s + 0.0f);               // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ int fused_keep(int n, double ratio, int budget) {
-  if (n <= 0) return 0;
-  if (budget > 0) return budget < n ? budget : n;
-  if (ratio >= 1.0) return n;
-  int k = (int)ceil(ratio * (double)n - 1e-9);
-  k = k < 1 ? 1 : k;
-  return k < n ? k : n;
-}
-
-// Exclusive scan over the 128 threads of (gt << 32 | eq); total written to *total.
-__device__ __forceinline__ uint64_t scan128(uint64_t v, uint64_t* wtot, uint64_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wtot[warp] = incl;
-  __syncthreads();
-  uint64_t before = 0;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) before += (w < warp) ? wtot[w] : 0ull;
-  if (threadIdx.x == 0) *total = wtot[0] + wtot[1] + wtot[2] + wtot[3];
-  __syncthreads();
-  return before + incl - v;
-}
-
-}  // namespace
 
 template <int D, int G>
 __global__ void __launch_bounds__(kFusedThreads)
@@ -114,15 +84,14 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   char* smem = reinterpret_cast<char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   char* ring = smem + C::OFF_RING;
-  uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + C::OFF_KEYS);
   int32_t* s_rphys = reinterpret_cast<int32_t*>(smem + C::OFF_RPHYS);
   int32_t* s_runp = reinterpret_cast<int32_t*>(smem + C::OFF_RUNP);
   int16_t* s_runv = reinterpret_cast<int16_t*>(smem + C::OFF_RUNV);
   float* s_w = reinterpret_cast<float*>(smem + C::OFF_W);
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
-  uint32_t* s_gh = reinterpret_cast<uint32_t*>(smem + C::OFF_GH);
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // [0..15]
-  uint64_t* s_misc64 = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC + 64);   // [0..7]
+  uint64_t* s_misc64 = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC + 64);   // [0..15]
+  float* s_mtab = reinterpret_cast<float*>(smem + C::OFF_MTAB);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -140,18 +109,17 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   pdl_wait();
   const int len = checked_len(ctx, d, b);
   const int n = ceil_div(len, PS);
-  int k = dense ? n : fused_keep(n, keep_ratio, budget);
+  int k = dense ? n : keep_rule(n, nullptr, b, keep_ratio, budget);
   if (!dense && k > k_max) {
     if (tid == 0 && r == 0) flag(ctx, KV_DEVERR_KEEP);
     k = k_max;
   }
   const long grp = (long)b * Hkv + g;
   const int32_t* table = d.page_table + (long)b * d.page_table_stride;
-  uint32_t ring_uses = 0;
   int np = 0;
 
   if (!dense && k > 0 && k < n) {
-    // ================= 1. scores of this CTA's page range =================================
+    // ================= 1. scores of this CTA's page range, gathered cluster-wide ==========
     const int cp = ceil_div(n, CL);
     const int p0 = min(n, r * cp);
     int nr = min(n, p0 + cp) - p0;
@@ -159,6 +127,13 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
       nr = kFusedMaxRange;
     }
+    // every CTA of the cluster must have started before its shared memory is written:
+    // arrive now, wait just before the first remote store
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    uint32_t* ring_w = reinterpret_cast<uint32_t*>(ring);
+    CtaKeys K = cta_key_layout<kFusedThreads>(ring_w, n);
+    const int KW = cta_key_words<kFusedThreads>(n);
+    int32_t* s_phys = reinterpret_cast<int32_t*>(ring_w + KW);   // physical ids, key layout
     for (int i = tid; i < nr; i += kFusedThreads) {
       int P = table[p0 + i];
       if (P < 0 || P >= d.num_phys_pages) {
@@ -178,183 +153,80 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       s_w[D + t] = pos;
     }
     __syncthreads();
-    const int nch = ceil_div(nr, C::CH);
-    auto issue_stats = [&](int c) {
-      const uint32_t u = ring_uses + (uint32_t)c;
-      const int st = (int)(u % C::NST);
-      char* dst = ring + (size_t)st * M::STAGE_BYTES;
-      const int i0 = c * C::CH, i1 = min(nr, i0 + C::CH);
-      uint32_t bytes = 0;
-      for (int i = i0; i < i1; ++i) bytes += s_rphys[i] >= 0 ? (uint32_t)C::ROW : 0u;
-      mbar_arrive_expect_tx(&bars[st], bytes);
-      const uint64_t pol = l2_evict_first_policy();
-      for (int i = i0; i < i1; ++i) {
-        const int P = s_rphys[i];
-        if (P < 0) continue;
-        bulk_g2s(dst + (size_t)(i - i0) * C::ROW,
-                 reinterpret_cast<const char*>(stats) + ((size_t)P * Hkv + g) * C::ROW,
-                 (uint32_t)C::ROW, &bars[st], pol);
-      }
-    };
-    if (tid == 0) {
-      for (int c = 0; c < C::NST && c < nch; ++c) issue_stats(c);
-    }
-    bool ok1 = true;
-    int c = 0;
-    for (; c < nch; ++c) {
-      const uint32_t u = ring_uses + (uint32_t)c;
-      const int st = (int)(u % C::NST);
-      const bool ok = mbar_wait_bounded(&bars[st], (u / C::NST) & 1u, ctx.wait_ns);
-      if (__syncthreads_or(!ok)) { ok1 = false; break; }
-      const char* rows = ring + (size_t)st * M::STAGE_BYTES;
-      const int i0 = c * C::CH, cnt = min(C::CH, nr - i0);
-      const int j8 = tid & 7;
-      constexpr int EPC = 8, CPL = (C::ROW / 16) / 8;
-      for (int jj = tid >> 3; jj < ((cnt + 15) & ~15); jj += kFusedThreads / 8) {
-        float acc = 0.f;
-        const bool live = jj < cnt && s_rphys[i0 + jj] >= 0;
-        if (live) {
-          const uint4* row = reinterpret_cast<const uint4*>(rows + (size_t)jj * C::ROW);
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    {
+      constexpr int EPC = 8, CPL = (C::ROW / 16) / 8;   // 16-byte chunks per lane per row
+      constexpr int NG = kFusedThreads / 8;             // 8-lane row groups
+      constexpr int RB = 4;                             // rows per group in flight
+      const int rg = tid >> 3, j8 = tid & 7;
+      for (int base = 0; base < nr; base += NG * RB) {
+        uint4 raw[RB][CPL];
+        int Pu[RB];
 #pragma unroll
-          for (int uu = 0; uu < CPL; ++uu) {
-            float f[EPC];
-            chunk_to_f32<bf16_t>(row[j8 + 8 * uu], f);
-            const float* wc = s_w + (j8 + 8 * uu) * EPC;
+        for (int u = 0; u < RB; ++u) {
+          const int i = base + u * NG + rg;
+          Pu[u] = i < nr ? s_rphys[i] : -1;
+          if (Pu[u] >= 0) {
+            const uint4* row = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const char*>(stats) + ((size_t)Pu[u] * Hkv + g) * C::ROW);
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
+            for (int uu = 0; uu < CPL; ++uu) raw[u][uu] = __ldg(row + j8 + 8 * uu);
           }
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        if (j8 == 0 && jj < cnt) s_keys[i0 + jj] = live ? fused_key(acc) : 0u;
-      }
-      __syncthreads();
-      if (tid == 0 && c + C::NST < nch) issue_stats(c + C::NST);
-    }
-    if (!ok1) {
-      if (tid == 0) {
-        flag(ctx, KV_DEVERR_TIMEOUT);
-        for (int v = c; v < nch && v < c + C::NST; ++v) {
-          const uint32_t u = ring_uses + (uint32_t)v;
-          mbar_wait_bounded(&bars[u % C::NST], (u / C::NST) & 1u, ctx.wait_ns);
-        }
-      }
-      for (int i = tid; i < nr; i += kFusedThreads) s_keys[i] = 0u;
-      __syncthreads();
-    }
-    ring_uses += (uint32_t)nch;
-
-    // ================= 2. radix select across the cluster =================================
-    uint32_t prefix = 0, mask = 0, remaining = (uint32_t)k;
-    bool exact = false;
-    const int iters = ceil_div(nr, kFusedThreads);
-    int pass = 0;
-    for (int shift = 24; shift >= 0 && !exact; shift -= 8, ++pass) {
-      uint32_t* hist = s_hist + (pass & 1) * 256;
-      for (int i = tid; i < 256; i += kFusedThreads) hist[i] = 0u;
-      __syncthreads();
-      for (int it = 0; it < iters; ++it) {
-        const int i = it * kFusedThreads + tid;
-        uint32_t digit = 256;
-        if (i < nr) {
-          const uint32_t key = s_keys[i];
-          if ((key & mask) == prefix) digit = (key >> shift) & 255u;
-        }
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
-      }
-      cluster.sync();                          // every CTA's histogram of this pass is final
-      for (int i = tid; i < 256; i += kFusedThreads) {
-        uint32_t v = 0;
-        for (int rk = 0; rk < CL; ++rk) v += cluster.map_shared_rank(hist, rk)[i];
-        s_gh[i] = v;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        uint32_t cc[8], lane_sum = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { cc[e] = s_gh[lane * 8 + e]; lane_sum += cc[e]; }
-        uint32_t incl = lane_sum;
+        for (int u = 0; u < RB; ++u) {
+          const int i = base + u * NG + rg;
+          float acc = 0.f;
+          if (Pu[u] >= 0) {
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-          if (lane + o < 32) incl += y;
-        }
-        uint32_t above = incl - lane_sum;
-        if (above < remaining && remaining <= incl) {
+            for (int uu = 0; uu < CPL; ++uu) {
+              float f[EPC];
+              chunk_to_f32<bf16_t>(raw[u][uu], f);
+              const float* wc = s_w + (j8 + 8 * uu) * EPC;
 #pragma unroll
-          for (int e = 7; e >= 0; --e) {
-            if (above + cc[e] >= remaining) {
-              s_misc[0] = prefix | ((uint32_t)(lane * 8 + e) << shift);
-              s_misc[1] = remaining - above;
-              s_misc[2] = (above + cc[e] == remaining) ? 1u : 0u;
-              break;
+              for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
             }
-            above += cc[e];
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          if (i < nr) {
+            const uint32_t key = Pu[u] >= 0 ? score_order_key(acc) : 0u;
+            const int sl = K.slot(p0 + i);
+            for (int rk = j8; rk < CL; rk += 8) {      // the 8 lanes share the CL copies
+              cluster.map_shared_rank(K.keys, rk)[sl] = key;
+              cluster.map_shared_rank(s_phys, rk)[sl] = Pu[u];
+            }
           }
         }
       }
-      __syncthreads();
-      prefix = s_misc[0];
-      remaining = s_misc[1];
-      exact = s_misc[2] != 0u;
-      mask |= 255u << shift;
-      __syncthreads();                         // s_misc is rewritten next pass
     }
-    const uint32_t T = prefix;
-    const uint32_t take_eq = exact ? 0xffffffffu : remaining;
+    cluster.sync();                            // every CTA holds every key and physical id
 
-    // ================= 3. ordered compaction into the splits' runs ========================
-    const int ipt = ceil_div(nr, kFusedThreads);          // keys per thread (contiguous)
-    const int a0 = min(nr, tid * ipt), a1 = min(nr, a0 + ipt);
-    uint32_t gt = 0, eq = 0;
-    for (int i = a0; i < a1; ++i) {
-      const uint32_t key = s_keys[i];
-      gt += key > T;
-      eq += key == T;
-    }
-    uint64_t* wtot = s_misc64;                 // [4]
-    uint64_t* total = s_misc64 + 4;
-    const uint64_t ex = scan128(((uint64_t)gt << 32) | eq, wtot, total);
-    uint32_t* pub = s_misc + 4;                // this CTA's (gt, eq) totals for the others
-    if (tid == 0) {
-      pub[0] = (uint32_t)(*total >> 32);
-      pub[1] = (uint32_t)(*total & 0xffffffffu);
-    }
-    cluster.sync();                            // totals published
-    uint32_t gt_b = 0, eq_b = 0;
-    for (int rk = 0; rk < r; ++rk) {
-      const uint32_t* rp = cluster.map_shared_rank(pub, rk);
-      gt_b += rp[0];
-      eq_b += rp[1];
-    }
-    uint32_t gt_before = gt_b + (uint32_t)(ex >> 32);
-    uint32_t eq_before = eq_b + (uint32_t)(ex & 0xffffffffu);
+    // ================= 2. threshold of the k kept keys (the same in every CTA) ============
+    cta_key_diff<kFusedThreads>(K, s_misc + 8);
+    uint32_t T, take_eq;
+    cta_threshold<kFusedThreads>(K, k, s_hist, s_misc, ring_w + 2 * KW, C::RING_WORDS - 2 * KW,
+                                 T, take_eq);
+
+    // ================= 3. this split's run of the ascending kept list =====================
     const int c2 = ceil_div(k, CL);
-    for (int i = a0; i < a1; ++i) {
-      const uint32_t key = s_keys[i];
-      int pos = -1;
-      if (key > T) {
-        pos = (int)(gt_before + min(eq_before, take_eq));
-        ++gt_before;
-      } else if (key == T) {
-        if (eq_before < take_eq) pos = (int)(gt_before + eq_before);
-        ++eq_before;
-      }
-      if (pos >= 0 && pos < k) {
-        const int p = p0 + i;
-        const int owner = pos / c2, idx = pos - owner * c2;
-        const int P = s_rphys[i];
-        cluster.map_shared_rank(s_runp, owner)[idx] = P;
-        cluster.map_shared_rank(s_runv, owner)[idx] =
-            (int16_t)(P >= 0 ? min(PS, len - p * PS) : 0);
+    const int pos0 = min(k, r * c2);
+    np = min(k, pos0 + c2) - pos0;
+    if (np > kFusedMaxRun) {
+      if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+      np = kFusedMaxRun;
+    }
+    cta_compact<kFusedThreads>(K, T, take_eq, s_misc64, [&](int p, int pos) {
+      if (pos >= pos0 && pos < pos0 + np) {
+        const int P = s_phys[K.slot(p)];
+        s_runp[pos - pos0] = P;
+        s_runv[pos - pos0] = (int16_t)(P >= 0 ? min(PS, len - p * PS) : 0);
         if (sel_out != nullptr) sel_out[grp * k_max + pos] = p;
       }
-    }
+    });
     if (cnt_out != nullptr && r == 0 && tid == 0) cnt_out[grp] = k;
-    cluster.sync();                            // every split's run is complete
-    np = min(k, (r + 1) * c2) - min(k, r * c2);
+    __syncthreads();                           // runs written; the ring is free for copies
   } else {
     // dense, nothing kept, or everything kept: split r takes its run of pages directly
     const int kk = (!dense && k == 0) ? 0 : (dense ? n : k);
@@ -382,18 +254,24 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     __syncthreads();
   }
 
-  // ================= 4. attention over this CTA's run ====================================
+  // ================= 4. attention over this CTA's run, two halves ============================
   uint32_t qa0[M::KSTEPS], qa2[M::KSTEPS];
   load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
   WarpAcc<D> acc;
   acc.init();
-  const bool ok4 = attend_run<D, G, C::NST>(&tmK, &tmV, ring, bars, ring_uses, s_runp, s_runv,
-                                            np, g, Hkv, PS, qa0, qa2, qk_scale_log2, acc,
-                                            ctx.wait_ns);
+  const int half = warp >> 2;                  // warps 0-3 and 4-7
+  const int np0 = (np + 1) / 2;
+  const int my_np = half == 0 ? np0 : np - np0;
+  const int my_off = half == 0 ? 0 : np0;
+  const bool ok4 = attend_run<D, G, 2>(&tmK, &tmV, ring + (size_t)half * 2 * M::STAGE_BYTES,
+                                       bars + 2 * half, 0u, s_runp + my_off, s_runv + my_off,
+                                       my_np, g, Hkv, PS, qa0, qa2, qk_scale_log2, acc,
+                                       ctx.wait_ns, 1 + half, tid & 127);
+  const bool ok_all = __syncthreads_and(ok4) != 0;   // both halves done with the ring
   float* scratch = reinterpret_cast<float*>(ring);
-  float* part = scratch + 4 * G * (D + 2);
-  cta_partial<D, G>(acc, scratch, part);
-  if (!ok4) {
+  float* part = scratch + 8 * G * (D + 2);
+  cta_partial<D, G, 8>(acc, scratch, part);
+  if (!ok_all) {
     if (tid == 0) flag(ctx, KV_DEVERR_TIMEOUT);
     for (int i = tid; i < G * D; i += kFusedThreads) part[i] = 0.f;
     if (tid < G) {
@@ -405,21 +283,30 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
   // ================= 5. merge the CL partials over DSMEM ===================================
   cluster.sync();                              // every partial is final
+  for (int i = tid; i < CL * 2 * G; i += kFusedThreads) {
+    const int rk = i / (2 * G), j = i % (2 * G);
+    s_mtab[i] = cluster.map_shared_rank(part, rk)[G * D + j];   // m [G] then l [G]
+  }
+  __syncthreads();
   const int E = ceil_div(G * D, CL);
   const int e0 = min(G * D, r * E), e1 = min(G * D, e0 + E);
   for (int e = e0 + tid; e < e1; e += kFusedThreads) {
     const int hl = e / D, dd = e % D;
     float Mx = -INFINITY;
-    for (int rk = 0; rk < CL; ++rk)
-      Mx = fmaxf(Mx, cluster.map_shared_rank(part, rk)[G * D + hl]);
+    for (int rk = 0; rk < CL; ++rk) Mx = fmaxf(Mx, s_mtab[rk * 2 * G + hl]);
+    float vals[16];
+#pragma unroll
+    for (int rk = 0; rk < 16; ++rk)
+      vals[rk] = rk < CL ? cluster.map_shared_rank(part, rk)[hl * D + dd] : 0.f;
     float L = 0.f, A = 0.f;
     if (Mx != -INFINITY) {
-      for (int rk = 0; rk < CL; ++rk) {
-        const float* rp = cluster.map_shared_rank(part, rk);
-        const float mw = rp[G * D + hl];
+#pragma unroll
+      for (int rk = 0; rk < 16; ++rk) {
+        if (rk >= CL) break;
+        const float mw = s_mtab[rk * 2 * G + hl];
         const float w = mw == -INFINITY ? 0.f : exp2f(mw - Mx);
-        L = fmaf(rp[G * D + G + hl], w, L);
-        A = fmaf(rp[hl * D + dd], w, A);
+        L = fmaf(s_mtab[rk * 2 * G + G + hl], w, L);
+        A = fmaf(vals[rk], w, A);
       }
     }
     const long oi = (long)b * Hq + g * G + hl;
@@ -530,9 +417,12 @@ int fused_cluster_size(const kv_cache_desc& d, int G, int num_sms) {
   if ((long long)d.num_phys_pages * d.num_kv_heads * d.page_size >= (1ll << 31)) return 0;
   const long groups = (long)d.batch * d.num_kv_heads;
   if (groups > num_sms) return 0;                // one CTA per SM: all groups in one wave
-  int CL = 16;
-  while (CL > 1 && groups * CL > num_sms) CL >>= 1;
-  for (; CL >= 1; CL >>= 1) {
+  // the group's keys, physical ids and some candidate room fit the copy ring
+  const int ring_w =
+      d.head_dim == 128 ? FusedCfg<128, 1>::RING_WORDS : FusedCfg<64, 1>::RING_WORDS;
+  if (2 * cta_key_words<kFusedThreads>(d.page_table_stride) + 1024 > ring_w) return 0;
+  for (int CL = 16; CL >= 1; --CL) {
+    if (groups * CL > num_sms) continue;
     // every CTA's score range and page run must fit its shared-memory arrays
     if (ceil_div(d.page_table_stride, CL) > kFusedMaxRange) return 0;
     int max_clusters = 0;
@@ -541,7 +431,7 @@ int fused_cluster_size(const kv_cache_desc& d, int G, int num_sms) {
       cudaGetLastError();
       continue;
     }
-    if (max_clusters >= 1) return CL;
+    if (max_clusters >= groups) return CL;       // every group's cluster resident at once
   }
   return 0;
 }

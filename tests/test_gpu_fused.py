@@ -17,7 +17,7 @@ import sparse_kv_cache_build_gb300 as skv
 from sparse_kv_cache_build_gb300 import inputs
 
 from gpu_helpers import (BF16_TOL, assert_no_device_error, f64, need_gpu, oracle_group,
-                         round256, step_selection, workload)
+                         round256, step_score_region, step_selection, workload)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,13 +51,13 @@ def test_one_launch_step_matches_oracle(dtype, D, G, PS, lens, keep):
     ws = torch.empty((skv.kv_decode_step_workspace_size(kv, Hq, k_max),), dtype=torch.uint8,
                      device="cuda")
     ws.fill_(255)
+    ws[: 2 * round256(B * Hkv * 4)].zero_()           # the step's counters start at zero
     out, lse = skv.kv_decode_step(kv, c.q, w.sm_scale, stats, keep_ratio=ratio if ratio else 1.0,
                                   budget_pages=budget, k_max=k_max, workspace=ws,
                                   num_splits=skv.ONE_LAUNCH)
     assert_no_device_error()
     # one launch ran: the four-kernel path would have written the score region
-    score_bytes = round256(B * Hkv * kv.stride * 4)
-    assert bool((ws[:score_bytes] == 255).all())
+    assert bool((step_score_region(ws, B, Hkv, kv.stride) == 255).all())
     out, lse = f64(out), f64(lse)
 
     if dense:

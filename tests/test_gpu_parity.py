@@ -262,9 +262,10 @@ def test_fused_decode_step_equals_the_separate_calls():
     acc, ml = skv.kv_sparse_decode_attn(r["kv"], c.q, w.sm_scale, num_splits=7)
     dense2, _ = skv.kv_merge_splits(acc, ml)
     assert_no_device_error()
-    np.testing.assert_array_equal(f64(out), r["out"])
-    np.testing.assert_array_equal(f64(lse), r["lse"])
-    assert torch.equal(dense, dense2)
+    # same selection and partials; the merge runs in the attention kernel's last CTA
+    np.testing.assert_allclose(f64(out), r["out"], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(f64(lse), r["lse"], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(f64(dense), f64(dense2), rtol=0, atol=1e-6)
 
 
 def test_physical_placement_is_bit_identical():

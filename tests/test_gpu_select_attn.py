@@ -1,0 +1,164 @@
+"""kv_select_decode_attn: selection, split-K attention and merge in one kernel (bf16).
+
+Its selection must equal kv_select_topk's on the same scores bit for bit, its output must
+match the separate calls (select, attention, merge kernel) within float32 rounding and the
+oracle within the bf16 bar, the dense call must equal dense attention, and the per-group
+counters must be back at zero after every call.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_kv_cache_build_gb300 as skv
+from sparse_kv_cache_build_gb300 import inputs
+
+from gpu_helpers import BF16_TOL, assert_no_device_error, f64, need_gpu, oracle_group, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+    torch.cuda.set_device(0)
+
+
+SHAPES = [(128, 4, 16), (128, 8, 64), (128, 1, 32), (64, 2, 16), (64, 8, 64)]
+LENS = [(1000, 4097, 37), (0, 1, 17, 65, 3000), (30000,)]
+
+
+@pytest.mark.parametrize("D,G,PS", SHAPES)
+@pytest.mark.parametrize("lens", LENS)
+@pytest.mark.parametrize("keep", [dict(keep_ratio=0.3), dict(budget_pages=20),
+                                  dict(keep_ratio=0.02)], ids=["r0.3", "budget20", "r0.02"])
+@pytest.mark.parametrize("S", [1, 5, 40])
+def test_select_attend_merge_in_one_kernel(D, G, PS, lens, keep, S):
+    Hkv = 2
+    w = workload(num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, page_size=PS, dtype="bf16",
+                 seed=13, seq_lens=lens, planted=6)
+    c = inputs.make_cache(w, "cuda", extra_phys_pages=3)
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    scores = skv.kv_score_pages(kv, c.q, stats)
+    ratio, budget = keep.get("keep_ratio", 0.0), keep.get("budget_pages", 0)
+    k_max = skv.max_keep_pages(kv.stride, ratio if not budget else None, budget or None)
+    B = w.batch
+    sel = torch.full((B, Hkv, k_max), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, Hkv), -7, dtype=torch.int32, device="cuda")
+    ctr = torch.zeros((B, Hkv), dtype=torch.int32, device="cuda")
+    outs = []
+    for rep in range(2):                               # counters must be reusable
+        out, lse = skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, keep_ratio=ratio,
+                                             budget_pages=budget, k_max=k_max, num_splits=S,
+                                             counters=ctr, sel_idx=sel, sel_cnt=cnt)
+        assert_no_device_error()
+        assert int(ctr.abs().sum()) == 0
+        outs.append(f64(out))
+    assert (outs[0] == outs[1]).all()
+    out, lse = outs[0], f64(lse)
+    # selection: identical to the separate top-k kernel
+    sel2, cnt2 = skv.kv_select_topk(scores, c.seq_lens, PS, keep_ratio=ratio,
+                                    budget_pages=budget, k_max=k_max)
+    sel, cnt, sel2, cnt2 = (x.cpu().numpy() for x in (sel, cnt, sel2, cnt2))
+    np.testing.assert_array_equal(cnt, cnt2)
+    for b in range(B):
+        for g in range(Hkv):
+            np.testing.assert_array_equal(sel[b, g, : cnt[b, g]], sel2[b, g, : cnt2[b, g]])
+    # output: the separate calls with the same split count, and the oracle
+    acc, ml = skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, torch.from_numpy(sel2).cuda(),
+                                        torch.from_numpy(cnt2).cuda(), num_splits=S)
+    out2, lse2 = skv.kv_merge_splits(acc, ml)
+    np.testing.assert_allclose(out, f64(out2), rtol=0, atol=1e-6)
+    for b, L in enumerate(lens):
+        if L == 0:                                     # nothing to attend to
+            assert (cnt[b] == 0).all() and (out[b] == 0).all() and np.isneginf(lse[b]).all()
+            continue
+        for g in range(Hkv):
+            o = oracle_group(c, b, g, ratio=ratio if not budget else None,
+                             budget_tokens=budget * PS if budget else None)
+            k = int(cnt[b, g])
+            assert k == o["k"]
+            got = sel[b, g, :k]
+            ok, msg = oracle.check_selection(got, o["scores"], k)
+            assert ok, msg
+            ref, ref_lse = oracle.attend(o["q"], o["K"], o["V"], o["table"], o["lens"], PS,
+                                         w.sm_scale, selected=[[got]])
+            hs = slice(g * G, (g + 1) * G)
+            assert np.abs(out[b, hs] - ref[0]).max() < BF16_TOL
+            assert np.abs(lse[b, hs] - ref_lse[0]).max() < 1e-4
+
+
+@pytest.mark.parametrize("S", [1, 7, 38])
+def test_dense_call_is_dense_attention(S):
+    w = workload(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, dtype="bf16",
+                 seed=14, seq_lens=(5000, 33, 0), planted=4)
+    c = inputs.make_cache(w, "cuda")
+    kv = skv.PagedKV.from_cache(c)
+    ctr = torch.zeros((w.batch, 2), dtype=torch.int32, device="cuda")
+    out, lse = skv.kv_select_decode_attn(kv, c.q, w.sm_scale, None, num_splits=S, counters=ctr)
+    assert_no_device_error()
+    assert int(ctr.abs().sum()) == 0
+    ref, _ = oracle.attend(f64(c.q), f64(c.k_pool), f64(c.v_pool), c.page_table.cpu().numpy(),
+                           c.seq_lens.cpu().numpy(), 16, w.sm_scale)
+    assert np.abs(f64(out) - ref).max() < BF16_TOL
+    acc, ml = skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, num_splits=S)
+    out2, _ = skv.kv_merge_splits(acc, ml)
+    np.testing.assert_allclose(f64(out), f64(out2), rtol=0, atol=1e-6)
+
+
+def _score_rows(kind, n, gen):
+    if kind == "coarse":                       # many exact ties, both signs, both zeros
+        s = torch.round(torch.randn(n, generator=gen, dtype=torch.float64) * 4) / 4
+        s[: min(n, 40)] = -0.0
+        return s.float()
+    if kind == "tied":                         # every page equal
+        return torch.full((n,), 1.5)
+    if kind == "outliers":                     # a few huge scores over a narrow band
+        s = 100.0 + torch.rand(n, generator=gen) * 1e-3
+        s[torch.randint(0, n, (min(n, 7),), generator=gen)] = 1e6
+        return s
+    if kind == "ramp":                         # distinct, ascending
+        return torch.arange(n, dtype=torch.float32) * 0.5 - n / 4
+    return torch.randn(n, generator=gen)
+
+
+@pytest.mark.parametrize("n", [5, 300, 2048, 8192, 24448])
+@pytest.mark.parametrize("kind", ["coarse", "tied", "outliers", "ramp", "normal"])
+def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
+    """Arbitrary score rows through the in-kernel selection: the oracle's rule exactly
+    (score descending, lower page first on ties, ascending output)."""
+    PS, D, G, Hkv = 16, 128, 4, 2
+    w = workload(num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, page_size=PS, dtype="bf16",
+                 seed=n, seq_lens=(n * PS, n * PS - 5))
+    c = inputs.make_cache(w, "cuda")
+    kv = skv.PagedKV.from_cache(c)
+    gen = torch.Generator().manual_seed(n * 7 + len(kind))
+    scores = torch.stack([torch.stack([_score_rows(kind, kv.stride, gen) for _ in range(Hkv)])
+                          for _ in range(w.batch)]).contiguous()
+    sh = scores.double().numpy()
+    scores = scores.cuda()
+    for kw in (dict(keep_ratio=0.3), dict(keep_ratio=0.02), dict(budget_pages=max(1, n // 3))):
+        ratio, budget = kw.get("keep_ratio", 0.0), kw.get("budget_pages", 0)
+        k_max = skv.max_keep_pages(kv.stride, ratio if not budget else None, budget or None)
+        sel = torch.full((w.batch, Hkv, k_max), -1, dtype=torch.int32, device="cuda")
+        cnt = torch.full((w.batch, Hkv), -1, dtype=torch.int32, device="cuda")
+        S = min(8, skv.kv_auto_num_splits(kv, w.num_q_heads, k_max))
+        out, _ = skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, keep_ratio=ratio,
+                                           budget_pages=budget, k_max=k_max, num_splits=S,
+                                           sel_idx=sel, sel_cnt=cnt)
+        assert_no_device_error()
+        sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+        for b in range(w.batch):
+            nb = oracle.num_pages(int(c.seq_lens[b]), PS)
+            k = (oracle.keep_count(nb, budget_tokens=budget * PS, page_size=PS) if budget
+                 else oracle.keep_count(nb, ratio=ratio))
+            for g in range(Hkv):
+                assert cnt[b, g] == k
+                np.testing.assert_array_equal(sel[b, g, :k], oracle.select_pages(sh[b, g, :nb], k))
+        # the output is the separate calls' on the same selection
+        acc, ml = skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, torch.from_numpy(sel).cuda(),
+                                            torch.from_numpy(cnt).cuda(), num_splits=S)
+        out2, _ = skv.kv_merge_splits(acc, ml)
+        np.testing.assert_allclose(f64(out), f64(out2), rtol=0, atol=1e-6)
