@@ -157,7 +157,8 @@ def byte_account(w, n_pages, sel_cnt, S):
     step_attn = k_total * (2 * PS * D * eb + 8) + q_bytes + B * Hq * (D + 1) * 4
     dense = n_total * Hkv * PS * D * 2 * eb + q_bytes + n_total * 4
     return dict(sparse_step=sparse, attn_launch=attn, step_attn_launch=step_attn,
-                dense_step=dense, selected_pages=k_total, pages=n_total * Hkv)
+                scores_bytes=n_total * Hkv * 4, dense_step=dense, selected_pages=k_total,
+                pages=n_total * Hkv)
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -235,25 +236,31 @@ def run_ours(args):
                      device=dev)
     ctr = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
     ctr2 = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
-    # the two-launch step (score + select, then attention + merge) runs wherever both calls
-    # accept the shape; otherwise the step is four kernels
-    two_launch = in_attn_select = False
+    # the kernels kv_decode_step runs for this shape (KV_PLAN_*)
+    plan, S_plan = (skv.kv_decode_step_plan(kv, Hq, k_max=k_max, **step_kw)
+                    if step_kw is not None else (0, S))
+    dense_plan, _ = skv.kv_decode_step_plan(kv, Hq, keep_ratio=1.0)
+    two_launch = plan in (1, 2)
+    assert S_plan == S, (S_plan, S)
+    # the other two-launch form, timed beside it where the shape allows
+    alt_plan = None
     if step_kw is not None:
-        try:
-            skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
-                                sel_idx=sel, sel_cnt=cnt, **step_kw)
-            skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
-                                     part_ml=ml, counters=ctr2, out=out, lse=lse)
-            two_launch = True
-        except binding.KVError:
-            pass
-        try:                           # the variant that selects inside the attention kernel
-            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
-                                      part_acc=acc, part_ml=ml, counters=ctr2, out=out,
-                                      lse=lse, **step_kw)
-            in_attn_select = True
-        except binding.KVError:
-            pass
+        for cand in ((2,) if plan == 1 else (1,) if plan == 2 else (1, 2)):
+            try:
+                if cand == 1:
+                    skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores.zero_(), k_max=k_max,
+                                              num_splits=S, part_acc=acc, part_ml=ml,
+                                              counters=ctr2, out=out, lse=lse, **step_kw)
+                else:
+                    skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores,
+                                        counters=ctr, sel_idx=sel, sel_cnt=cnt, **step_kw)
+                    skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S,
+                                             part_acc=acc, part_ml=ml, counters=ctr2, out=out,
+                                             lse=lse)
+                alt_plan = cand
+                break
+            except binding.KVError:
+                continue
         torch.cuda.synchronize()
 
     try:
@@ -265,25 +272,32 @@ def run_ours(args):
         smarks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         in_graph_events = False
 
-    def two_launch_step(with_marks):
-        """The two kernels kv_decode_step runs, called one by one through the C ABI."""
+    def plan_step(which, with_marks=False):
+        """A two-launch plan's kernels, called one by one through the C ABI."""
         if with_marks:
             smarks[0].record()
-        skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
-                            sel_idx=sel, sel_cnt=cnt, **step_kw)
+        if which == 1:
+            skv.kv_score_pages(kv, c.q, stats, scores)
+        else:
+            skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
+                                sel_idx=sel, sel_cnt=cnt, **step_kw)
         if with_marks:
             smarks[1].record()
-        skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
-                                 part_ml=ml, counters=ctr2, out=out, lse=lse)
+        if which == 1:
+            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
+                                      part_acc=acc, part_ml=ml, counters=ctr2, out=out,
+                                      lse=lse, sel_idx=sel, sel_cnt=cnt, **step_kw)
+        else:
+            skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
+                                     part_ml=ml, counters=ctr2, out=out, lse=lse)
         if with_marks:
             smarks[2].record()
 
-    def in_attn_select_step():
-        """Scores, then the attention kernel selecting each split's run itself."""
-        skv.kv_score_pages(kv, c.q, stats, scores)
-        skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
-                                  part_acc=acc, part_ml=ml, counters=ctr2, out=out, lse=lse,
-                                  **step_kw)
+    def two_launch_step(with_marks):
+        plan_step(plan, with_marks)
+
+    def alt_step():
+        plan_step(alt_plan)
 
     def four_kernel_step(with_marks):
         if with_marks:
@@ -334,26 +348,17 @@ def run_ours(args):
     st, flags = skv.kv_check_device_errors()
     if st != 0:
         raise RuntimeError(f"device error word {flags:#x} after warm-up")
-    one_launch = one_launch_ran = False
-    if step_kw is not None:            # one launch leaves the score region of ws untouched
-        ctr_bytes = 2 * ((B * Hkv * 4 + 255) // 256 * 256)      # the step's counters
-        score_region = ws[ctr_bytes: ctr_bytes + (B * Hkv * kv.stride * 4 + 255) // 256 * 256]
-        for fn in (step, one_launch_step):
-            score_region.fill_(255)
-            fn()
-            torch.cuda.synchronize()
-            ran = bool((score_region == 255).all())
-            if fn is step:
-                one_launch = ran
-            else:
-                one_launch_ran = ran
+    one_launch = plan == 5
+    one_launch_ran = (step_kw is not None and
+                      skv.kv_decode_step_plan(kv, Hq, k_max=k_max, num_splits=skv.ONE_LAUNCH,
+                                              **step_kw)[0] == 5)
 
     # one CUDA graph per measured step; g_marked and g_smarked are the four-kernel and the
     # two-launch steps with event nodes between their kernels, replayed in their own flushed
     # loops to time each kernel (event nodes sit between the kernels, so their programmatic
     # launch overlap is lost there: those graphs time kernels, not steps)
-    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_inattn = (torch.cuda.CUDAGraph()
-                                                                     for _ in range(7))
+    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt = (torch.cuda.CUDAGraph()
+                                                                  for _ in range(7))
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -372,9 +377,9 @@ def run_ours(args):
         if step_kw is not None:
             with torch.cuda.graph(g_one, stream=side):
                 one_launch_step()
-        if in_attn_select:
-            with torch.cuda.graph(g_inattn, stream=side):
-                in_attn_select_step()
+        if alt_plan is not None:
+            with torch.cuda.graph(g_alt, stream=side):
+                alt_step()
     stream.wait_stream(side)
     torch.cuda.synchronize()
 
@@ -404,7 +409,7 @@ def run_ours(args):
 
     # ---- timed region: K steps of each kind, L2 flushed before every step ---------------
     kern_us = {"score": [], "select": [], "attn": [], "merge": []}
-    step_kern_us = {"score_select": [], "attn_merge": []}
+    step_kern_us = {"first": [], "attention": []}
     barrier()
     with ClockSampler(local) as clk:
         step_us = timed(g_step)
@@ -415,7 +420,7 @@ def run_ours(args):
         barrier()
         one_us = timed(g_one) if one_launch_ran else []
         barrier()
-        inattn_us = timed(g_inattn) if in_attn_select else []
+        alt_us = timed(g_alt) if alt_plan is not None else []
         barrier()
         if in_graph_events:
             for _ in range(args.steps):
@@ -498,9 +503,10 @@ def run_ours(args):
         roof_kernel, roof_bytes, roof_us = "fused_step_kernel", acct["sparse_step"], step_mean
         roof_source = os.path.join(CSRC, "step_fused.cu")
     elif two_launch:
-        roof_kernel = ATTN_KERNEL[w.dtype][0] + " (attend + merge)"
-        roof_bytes = acct["step_attn_launch"]
-        roof_us = statistics.mean(step_kern_us["attn_merge"])
+        roof_kernel = ATTN_KERNEL[w.dtype][0] + (" (select + attend + merge)" if plan == 1
+                                                 else " (attend + merge)")
+        roof_bytes = acct["step_attn_launch"] + (acct["scores_bytes"] if plan == 1 else 0)
+        roof_us = statistics.mean(step_kern_us["attention"])
         roof_source = ATTN_KERNEL[w.dtype][1]
     else:
         roof_kernel, roof_bytes, roof_us = ATTN_KERNEL[w.dtype][0], acct["attn_launch"], attn_us
@@ -508,7 +514,7 @@ def run_ours(args):
     achieved = roof_bytes / (roof_us * 1e-6) / 1e9
     # kernels per replay of each timed graph
     n_step = 1 if one_launch else (2 if two_launch else 4)
-    n_dense = 1 if (w.dtype == "bf16" and step_kw is not None and two_launch) else 2
+    n_dense = 1 if dense_plan in (3, 5) else 2
     line = {
         "metric": METRIC,
         "value": round(sparse_med, 3),
@@ -526,11 +532,8 @@ def run_ours(args):
             "workload": w.name, "description": w.description, "batch": B,
             "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "page_size": PS,
             "context_tokens": int(c.seq_lens.sum()), "kv_storage": w.dtype, "keep": label,
-            "step_path": ("one launch: kv_decode_step, a thread-block cluster per (sequence, "
-                          "KV head)" if one_launch else
-                          f"two kernels (score + select; split-K attention + merge), {S} splits"
-                          if two_launch else
-                          f"four kernels (score, select, attention, merge), {S} splits"),
+            "step_path": f"kv_decode_step plan {plan}: {binding.PLANS[plan]}, {S} splits",
+            "dense_path": f"kv_decode_step plan {dense_plan}: {binding.PLANS[dense_plan]}",
             "num_splits_four_kernel": S, "parallelism": f"replicas{world}",
             "l2": "flushed before every timed step (256 MiB write = 2x L2, outside the events)",
             "graph": "one CUDA graph per step, replayed once per timed step",
@@ -544,8 +547,9 @@ def run_ours(args):
         "step_gbs": {"sparse": round(acct["sparse_step"] / (sparse_med * 1e-6) / 1e9, 1),
                      "dense": round(acct["dense_step"] / (dense_med * 1e-6) / 1e9, 1)},
         "one_launch_step_us": (round(statistics.median(one_us), 3) if one_us else None),
-        "select_in_attention_step_us": (round(statistics.median(inattn_us), 3)
-                                        if inattn_us else None),
+        "other_two_launch_step_us": ({"plan": binding.PLANS[alt_plan],
+                                      "median": round(statistics.median(alt_us), 3)}
+                                     if alt_us else None),
         "step_kernel_us_marked": ({k: round(statistics.mean(v), 3)
                                    for k, v in step_kern_us.items() if v} or None),
         "four_kernel_step_us": {"median": round(statistics.median(four_us), 3),
@@ -574,7 +578,7 @@ def run_ours(args):
         },
         "gpu_launches": args.steps * (n_step + n_dense + 4 + (4 if in_graph_events else 0)
                                       + (2 if two_launch else 0) + (1 if one_us else 0)
-                                      + (2 if inattn_us else 0)),
+                                      + (2 if alt_us else 0)),
         "clocks": clocks,
     }
     if e2e_us:

@@ -320,8 +320,11 @@ size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_
  * calls). Both paths give the same selection (bit for bit) and outputs equal up to float32
  * rounding of the merge.
  * out: device [batch][num_q_heads][head_dim] float32; lse: [batch][num_q_heads] or NULL.
- * For bf16 caches the four calls collapse into two launches, kv_score_select and
- * kv_decode_attn_merge (the dense step is the second alone).
+ * For bf16 caches the step takes two launches, the merge running in the attention
+ * kernel's last CTA per group: groups of up to 4096 pages (page_table_stride) run
+ * kv_score_pages then kv_select_decode_attn, longer ones kv_score_select then
+ * kv_decode_attn_merge; the dense step is kv_decode_attn_merge alone
+ * (kv_decode_step_plan tells which).
  * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned, ZERO-
  * FILLED ONCE before its first use: it starts with two int32 counters per group, at offsets
  * that depend only on batch * num_kv_heads, which the kernels return to zero after every
@@ -341,6 +344,25 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
 
 size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
                                      int32_t k_max, int32_t num_splits);
+
+/*
+ * kv_decode_step_plan -- host, launches nothing: the kernels kv_decode_step runs for these
+ * arguments (a KV_PLAN_* value, or a negative kv_status), and in *splits (if not NULL) its
+ * split count (the cluster size for KV_PLAN_ONE_LAUNCH). All plans give the same selection
+ * and outputs equal up to float32 rounding of the merge.
+ */
+typedef enum {
+  KV_PLAN_FOUR_KERNELS = 0,            /* kv_score_pages, kv_select_topk,
+                                          kv_sparse_decode_attn, kv_merge_splits */
+  KV_PLAN_SCORE_THEN_SELECT_ATTN = 1,  /* kv_score_pages, kv_select_decode_attn */
+  KV_PLAN_SCORE_SELECT_THEN_ATTN = 2,  /* kv_score_select, kv_decode_attn_merge */
+  KV_PLAN_DENSE_ATTN_MERGE = 3,        /* kv_decode_attn_merge with every page */
+  KV_PLAN_DENSE_TWO_KERNELS = 4,       /* kv_sparse_decode_attn, kv_merge_splits */
+  KV_PLAN_ONE_LAUNCH = 5               /* one thread-block cluster per group */
+} kv_plan;
+int32_t kv_decode_step_plan(const kv_cache_desc* cache, int32_t num_q_heads, double keep_ratio,
+                            int32_t budget_pages, int32_t k_max, int32_t num_splits,
+                            int32_t* splits);
 
 /*
  * kv_decode_step_static -- kv_decode_step without a workspace argument, for callers that

@@ -8,6 +8,7 @@ call does, and raises if it has not been built.
 from . import inputs  # noqa: F401
 from .binding import (  # noqa: F401
     ONE_LAUNCH,
+    PLANS,
     PagedKV,
     kv_append_token,
     kv_auto_num_splits,
@@ -15,6 +16,7 @@ from .binding import (  # noqa: F401
     kv_check_device_errors,
     kv_decode_attn_merge,
     kv_decode_step,
+    kv_decode_step_plan,
     kv_decode_step_workspace_size,
     kv_dropped_mass,
     kv_dropped_mass_workspace_size,

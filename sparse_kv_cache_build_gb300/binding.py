@@ -21,6 +21,10 @@ LIB_PATH = os.path.join(_PKG, "libsparsekv.so")
 KV_OK = 0
 KV_BF16, KV_FP32 = 0, 1
 ONE_LAUNCH = -1          # KV_SPLITS_ONE_LAUNCH: kv_decode_step as a single launch
+# kv_decode_step_plan results (KV_PLAN_*)
+PLANS = {0: "four kernels", 1: "score, then select + attention + merge",
+         2: "score + select, then attention + merge", 3: "dense attention + merge",
+         4: "dense attention, merge", 5: "one launch"}
 STATUS = {0: "KV_OK", -1: "KV_ERR_INVALID_ARG", -2: "KV_ERR_UNSUPPORTED", -3: "KV_ERR_CUDA",
           -4: "KV_ERR_WORKSPACE", -5: "KV_ERR_BAD_INDEX", -6: "KV_ERR_TIMEOUT",
           -7: "KV_ERR_MISALIGNED"}
@@ -34,7 +38,7 @@ EXPORTS = (
     "kv_decode_step_workspace_size", "kv_check_device_errors", "kv_set_wait_limit_ns",
     "kv_selftest_wait_timeout", "kv_decode_step_static", "kv_append_token",
     "kv_select_structured", "kv_select_decode_attn", "kv_score_select",
-    "kv_decode_attn_merge",
+    "kv_decode_attn_merge", "kv_decode_step_plan",
 )
 
 
@@ -92,6 +96,7 @@ def _declare(lib):
                                         P, P, P, P]),
         "kv_score_select": (I32, [D, P, I32, P, F64, I32, I32, P, I32, P, P, P, P]),
         "kv_decode_attn_merge": (I32, [D, P, I32, F32, P, P, I32, I32, P, P, P, P, P, P]),
+        "kv_decode_step_plan": (I32, [D, I32, F64, I32, I32, I32, ctypes.POINTER(I32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -499,6 +504,21 @@ def kv_decode_step(kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: floa
         int(budget_pages), int(k_max), int(num_splits), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
+
+
+def kv_decode_step_plan(kv: PagedKV, num_q_heads: int, keep_ratio: float = 1.0,
+                        budget_pages: int = 0, k_max: int | None = None,
+                        num_splits: int = 0) -> tuple[int, int]:
+    """(KV_PLAN_* value, split count) of kv_decode_step for these arguments; no launch."""
+    if k_max is None:
+        k_max = max_keep_pages(kv.stride, keep_ratio, budget_pages)
+    splits = ctypes.c_int32(0)
+    r = lib().kv_decode_step_plan(kv.ref(), int(num_q_heads), float(keep_ratio),
+                                  int(budget_pages), int(k_max), int(num_splits),
+                                  ctypes.byref(splits))
+    if r < 0:
+        raise KVError("kv_decode_step_plan", r)
+    return int(r), int(splits.value)
 
 
 def kv_check_device_errors(stream=None):

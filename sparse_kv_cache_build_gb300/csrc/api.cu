@@ -20,6 +20,9 @@ __device__ int32_t g_kv_error_word = 0;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDroppedSplits = 64;          // page ranges per group in the dropped-mass probe
+// Longest group (pages) whose selection kv_decode_step leaves to the attention kernel's CTAs;
+// longer groups select once, in the score launch (measured crossover between 2048 and 8192).
+constexpr int kInAttnSelectPages = 4096;
 
 struct DeviceState {
   bool ready = false;
@@ -491,6 +494,86 @@ size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_h
   return step_layout(cache, num_q_heads, k_max, S).total;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The kernels kv_decode_step launches for a shape (KV_PLAN_*), and its split count.
+struct StepPlan {
+  int plan = KV_PLAN_FOUR_KERNELS;
+  int S = 1;
+  int CL = 0;          // cluster size of the one-launch plan
+};
+
+kv_status plan_step(const kv_cache_desc* cache, int num_q_heads, double keep_ratio,
+                    int budget_pages, int k_max, int num_splits, DeviceState* st,
+                    StepPlan* out) {
+  const bool dense = is_dense(keep_ratio, budget_pages);
+  const int G = num_q_heads / cache->num_kv_heads;
+  const int stride = cache->page_table_stride;
+  StepPlan P;
+  if (num_splits == KV_SPLITS_ONE_LAUNCH) {
+    // one launch for the whole step when the shape allows it (bf16, one wave of clusters);
+    // otherwise the plans below with the automatic split count
+    P.CL = cached_cluster_size(cache, G, st);
+    if (P.CL > 0) {
+      P.plan = KV_PLAN_ONE_LAUNCH;
+      P.S = P.CL;
+      *out = P;
+      return KV_OK;
+    }
+    num_splits = 0;
+  }
+  int S = num_splits;
+  if (S <= 0) S = auto_splits(cache, G, dense ? stride : k_max, st);
+  if (S < min_splits_for(dense ? stride : k_max)) return KV_ERR_INVALID_ARG;
+  P.S = S;
+  P.plan = dense ? KV_PLAN_DENSE_TWO_KERNELS : KV_PLAN_FOUR_KERNELS;
+  if (cache->dtype == KV_BF16) {
+    // Two launches at most, the merge in the attention kernel's last CTA per group. Short
+    // groups: the scores, then an attention kernel whose CTAs each select their own run
+    // (redoing a small top-k per CTA is cheaper than a kernel boundary). Long groups: the
+    // scores with the top-k in each group's last score block, then attention over the list.
+    // Dense: the attention kernel alone.
+    int max_sel = 0, max_S = 0;
+    step_attn_limits_bf16(cache->head_dim, G, &max_sel, &max_S);
+    if (S <= max_S) {
+      if (dense)
+        P.plan = KV_PLAN_DENSE_ATTN_MERGE;
+      else if (stride <= kInAttnSelectPages && stride <= max_sel)
+        P.plan = KV_PLAN_SCORE_THEN_SELECT_ATTN;
+      else if (score_select_fits(cache, st))
+        P.plan = KV_PLAN_SCORE_SELECT_THEN_ATTN;
+    }
+  }
+  *out = P;
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kv_decode_step_plan(const kv_cache_desc* cache, int32_t num_q_heads, double keep_ratio,
+                            int32_t budget_pages, int32_t k_max, int32_t num_splits,
+                            int32_t* splits) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return KV_ERR_INVALID_ARG;
+  const int G = num_q_heads / cache->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
+  if (!is_dense(keep_ratio, budget_pages) && (k_max <= 0 || !(keep_ratio > 0.0 || budget_pages > 0)))
+    return KV_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  if ((r = device_state(&st)) != KV_OK) return r;
+  StepPlan P;
+  if ((r = plan_step(cache, num_q_heads, keep_ratio, budget_pages, k_max, num_splits, st, &P)) !=
+      KV_OK)
+    return r;
+  if (splits != nullptr) *splits = P.S;
+  return P.plan;
+}
+
 kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                          float sm_scale, const void* stats, double keep_ratio,
                          int32_t budget_pages, int32_t k_max, int32_t num_splits,
@@ -509,76 +592,69 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   DevCtx ctx;
   DeviceState* st = nullptr;
   if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
+  StepPlan P;
+  if ((r = plan_step(cache, num_q_heads, keep_ratio, budget_pages, k_max, num_splits, st, &P)) !=
+      KV_OK)
+    return r;
   const int G = num_q_heads / cache->num_kv_heads;
-  if (num_splits == KV_SPLITS_ONE_LAUNCH) {
-    // one launch for the whole step when the shape allows it (bf16, one wave of clusters)
-    const int CL = cached_cluster_size(cache, G, st);
-    if (CL > 0) {
-      const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, 1);
-      if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
-      char* ws = static_cast<char*>(workspace);
-      return from_cuda(launch_fused_step(
-          *cache, G, CL, q, stats, sm_scale, keep_ratio, budget_pages, dense ? 1 : k_max,
-          dense ? 1 : 0, dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.sel),
-          dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.cnt), out, lse, ctx, stream));
-    }
-  }
-  int S = num_splits;
-  if (S <= 0) S = auto_splits(cache, G, dense ? cache->page_table_stride : k_max, st);
-  if (S < min_splits_for(dense ? cache->page_table_stride : k_max)) return KV_ERR_INVALID_ARG;
-  // (a one-launch request whose shape does not allow it runs the kernels below instead)
-  const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, S);
-  if (cache->dtype == KV_BF16) {
-    // two launches: scores with the group's top-k in the last block of each group, then
-    // the attention kernel merging the group's partials in its last CTA
-    int max_sel = 0, max_S = 0;
-    step_attn_limits_bf16(cache->head_dim, G, &max_sel, &max_S);
-    if (S <= max_S && (dense || score_select_fits(cache, st))) {
-      if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
-      char* ws = static_cast<char*>(workspace);
-      int32_t* sel = dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.sel);
-      int32_t* cnt = dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.cnt);
-      if (!dense) {
-        cudaError_t e = launch_score_select(
-            *cache, q, num_q_heads, stats, reinterpret_cast<float*>(ws + L.scores),
-            cache->page_table_stride, keep_ratio, budget_pages, k_max,
-            reinterpret_cast<int32_t*>(ws + L.ctr), sel, cnt, ctx, stream);
-        if (e != cudaSuccess) return KV_ERR_CUDA;
-      }
-      StepArgs sa{};
-      sa.counters = reinterpret_cast<int32_t*>(ws + L.ctr2);
-      sa.out = out;
-      sa.lse = lse;
-      return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, sel, cnt,
-                                             dense ? 0 : k_max, S,
-                                             reinterpret_cast<float*>(ws + L.acc),
-                                             reinterpret_cast<float*>(ws + L.ml), ctx, stream,
-                                             sa));
-    }
-  }
+  const int stride = cache->page_table_stride;
+  const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, P.S);
+  if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   float* scores = reinterpret_cast<float*>(ws + L.scores);
-  int32_t* sel = reinterpret_cast<int32_t*>(ws + L.sel);
-  int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+  int32_t* sel = dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.sel);
+  int32_t* cnt = dense ? nullptr : reinterpret_cast<int32_t*>(ws + L.cnt);
   float* acc = reinterpret_cast<float*>(ws + L.acc);
   float* ml = reinterpret_cast<float*>(ws + L.ml);
-  cudaError_t e;
+  StepArgs sa{};
+  sa.counters = reinterpret_cast<int32_t*>(ws + L.ctr2);
+  sa.out = out;
+  sa.lse = lse;
+  cudaError_t e = cudaSuccess;
+  switch (P.plan) {
+    case KV_PLAN_ONE_LAUNCH:
+      return from_cuda(launch_fused_step(*cache, G, P.CL, q, stats, sm_scale, keep_ratio,
+                                         budget_pages, dense ? 1 : k_max, dense ? 1 : 0, sel,
+                                         cnt, out, lse, ctx, stream));
+    case KV_PLAN_DENSE_ATTN_MERGE:
+      return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, nullptr, nullptr, 0, P.S,
+                                             acc, ml, ctx, stream, sa));
+    case KV_PLAN_SCORE_THEN_SELECT_ATTN:
+      e = launch_score_pages(*cache, q, num_q_heads, stats, scores, stride, ctx, stream);
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      sa.scores = scores;
+      sa.scores_stride = stride;
+      sa.keep_ratio = keep_ratio;
+      sa.budget = budget_pages;
+      sa.k_max = k_max;
+      sa.sel_out = sel;
+      sa.cnt_out = cnt;
+      return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, nullptr, nullptr, 0, P.S,
+                                             acc, ml, ctx, stream, sa));
+    case KV_PLAN_SCORE_SELECT_THEN_ATTN:
+      e = launch_score_select(*cache, q, num_q_heads, stats, scores, stride, keep_ratio,
+                              budget_pages, k_max, reinterpret_cast<int32_t*>(ws + L.ctr), sel,
+                              cnt, ctx, stream);
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, sel, cnt, k_max, P.S, acc,
+                                             ml, ctx, stream, sa));
+    default:
+      break;
+  }
+  // four kernels (sparse) or two (dense)
   if (!dense) {
-    e = launch_score_pages(*cache, q, num_q_heads, stats, scores, cache->page_table_stride, ctx,
-                           stream);
+    e = launch_score_pages(*cache, q, num_q_heads, stats, scores, stride, ctx, stream);
     if (e != cudaSuccess) return KV_ERR_CUDA;
-    e = launch_select_topk(scores, cache->page_table_stride, cache->seq_lens, cache->page_size,
-                           cache->batch, cache->num_kv_heads, nullptr, keep_ratio,
-                           budget_pages, k_max, 0, 0, sel, cnt, cache->page_table_stride, ctx,
-                           stream);
+    e = launch_select_topk(scores, stride, cache->seq_lens, cache->page_size, cache->batch,
+                           cache->num_kv_heads, nullptr, keep_ratio, budget_pages, k_max, 0, 0,
+                           sel, cnt, stride, ctx, stream);
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }
-  e = launch_split_attn(*cache, q, num_q_heads, sm_scale, dense ? nullptr : sel,
-                        dense ? nullptr : cnt, dense ? 0 : k_max, S, acc, ml, ctx, stream,
-                        st->sms);
+  e = launch_split_attn(*cache, q, num_q_heads, sm_scale, sel, cnt, dense ? 0 : k_max, P.S, acc,
+                        ml, ctx, stream, st->sms);
   if (e != cudaSuccess) return KV_ERR_CUDA;
   return from_cuda(
-      launch_merge(acc, ml, cache->batch, num_q_heads, S, cache->head_dim, out, lse, stream));
+      launch_merge(acc, ml, cache->batch, num_q_heads, P.S, cache->head_dim, out, lse, stream));
 }
 
 kv_status kv_check_device_errors(cudaStream_t stream, int32_t* flags) {

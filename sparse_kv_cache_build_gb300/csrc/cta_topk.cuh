@@ -65,6 +65,7 @@ __device__ __forceinline__ void cta_key_diff(CtaKeys& K, uint32_t* red) {
   const uint32_t k0 = K.keys[0];
   const int a0 = min(K.n, tid * K.ipt), a1 = min(K.n, a0 + K.ipt);
   uint32_t orv = 0u;
+#pragma unroll 4
   for (int i = a0; i < a1; ++i) orv |= K.keys[tid * K.stride + (i - a0)] ^ k0;
   orv = __reduce_or_sync(0xffffffffu, orv);
   if ((tid & 31) == 0) red[tid >> 5] = orv;
@@ -206,6 +207,7 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
     for (int i = tid; i < kHistWords; i += NT) hist[i] = 0u;
     __syncthreads();
     if (ncand < 0) {
+#pragma unroll 4
       for (int i = a0; i < a1; ++i) {
         const uint32_t key = K.keys[tid * K.stride + (i - a0)];
         if ((key & mask) == prefix) atomicAdd(&hist[hslot((key >> lo) & dmask)], 1u);
@@ -234,6 +236,7 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
     if (ncand < 0 && (int)bin_count <= cand_cap) {
       // gather the bin's keys (page order, through a scan of per-thread counts)
       uint32_t mine = 0u, total = 0u;
+#pragma unroll 4
       for (int i = a0; i < a1; ++i) mine += (K.keys[tid * K.stride + (i - a0)] & mask) == prefix;
       uint32_t at = block_excl_scan<NT>(mine, misc + 8, total);
       for (int i = a0; i < a1 && mine != 0u; ++i) {
@@ -285,6 +288,7 @@ __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int a0 = min(K.n, tid * K.ipt), a1 = min(K.n, a0 + K.ipt);
   uint32_t gt = 0, eq = 0;
+#pragma unroll 4
   for (int i = a0; i < a1; ++i) {
     const uint32_t key = K.keys[tid * K.stride + (i - a0)];
     gt += key > T;
@@ -305,6 +309,7 @@ __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint
   __syncthreads();
   const uint64_t ex = before + incl - v;
   uint32_t gt_before = (uint32_t)(ex >> 32), eq_before = (uint32_t)(ex & 0xffffffffu);
+#pragma unroll 4
   for (int i = a0; i < a1; ++i) {
     const uint32_t key = K.keys[tid * K.stride + (i - a0)];
     if (key > T) {

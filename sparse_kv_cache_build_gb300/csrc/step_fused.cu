@@ -157,7 +157,7 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     {
       constexpr int EPC = 8, CPL = (C::ROW / 16) / 8;   // 16-byte chunks per lane per row
       constexpr int NG = kFusedThreads / 8;             // 8-lane row groups
-      constexpr int RB = 4;                             // rows per group in flight
+      constexpr int RB = 8;                             // rows per group in flight
       const int rg = tid >> 3, j8 = tid & 7;
       for (int base = 0; base < nr; base += NG * RB) {
         uint4 raw[RB][CPL];

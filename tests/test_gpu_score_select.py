@@ -183,3 +183,31 @@ def test_one_workspace_serves_sparse_dense_and_other_k_max():
         assert torch.equal(got_lse, ref_lse), kw
     n = 2 * ((w.batch * w.num_kv_heads * 4 + 255) // 256 * 256)
     assert int(shared[:n].abs().sum()) == 0              # every counter back at zero
+
+
+def test_decode_step_plan_by_shape():
+    """kv_decode_step's plan: short bf16 groups select inside the attention kernel, long ones
+    in the score launch, dense bf16 is the attention kernel alone, fp32 keeps four kernels;
+    the plan's kernels called one by one give kv_decode_step's output."""
+    cases = [("bf16", (1000, 4097, 37), 1), ("bf16", (8200 * 16,), 2), ("fp32", (1000, 37), 0)]
+    for dtype, lens, want in cases:
+        w, c = _make(dtype, 128, 4, 16, lens)
+        kv = skv.PagedKV.from_cache(c)
+        plan, S = skv.kv_decode_step_plan(kv, w.num_q_heads, keep_ratio=0.3)
+        assert plan == want, (dtype, lens, plan)
+        dplan, _ = skv.kv_decode_step_plan(kv, w.num_q_heads, keep_ratio=1.0)
+        assert dplan == (3 if dtype == "bf16" else 4)
+        if dtype != "bf16":
+            continue
+        stats = skv.kv_build_page_stats(kv)
+        out, lse = skv.kv_decode_step(kv, c.q, w.sm_scale, stats, keep_ratio=0.3)
+        k_max = skv.max_keep_pages(kv.stride, 0.3)
+        if plan == 1:
+            scores = skv.kv_score_pages(kv, c.q, stats)
+            out2, lse2 = skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, keep_ratio=0.3,
+                                                   k_max=k_max, num_splits=S)
+        else:
+            _, sel, cnt = skv.kv_score_select(kv, c.q, stats, keep_ratio=0.3, k_max=k_max)
+            out2, lse2 = skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S)
+        assert_no_device_error()
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
