@@ -677,6 +677,40 @@ def run_reference(args):
     }
 
 
+def run_only_step(args):
+    """kv_decode_step alone, for a profiler's launch list or capture of its kernels."""
+    import sparse_kv_cache_build_gb300 as skv
+    from sparse_kv_cache_build_gb300 import binding, inputs
+
+    torch.cuda.set_device(0)
+    binding.lib()
+    w = inputs.workload(args.workload)
+    label, keep = keep_setting(w, args.keep_index)
+    c = inputs.make_cache(w, "cuda")
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    if args.only_step == "dense" or "keep_pages" in keep:
+        kw = dict(keep_ratio=1.0)
+        k_max = 1
+    else:
+        kw = dict(keep_ratio=keep.get("keep_ratio", 1.0), budget_pages=keep.get("budget_pages", 0))
+        k_max = skv.max_keep_pages(kv.stride, keep.get("keep_ratio"), keep.get("budget_pages"))
+    ws = torch.zeros((skv.kv_decode_step_workspace_size(kv, w.num_q_heads, k_max),),
+                     dtype=torch.uint8, device="cuda")
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        flush.zero_()
+        skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    st, flags = skv.kv_check_device_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word {flags:#x}")
+    plan, S = skv.kv_decode_step_plan(kv, w.num_q_heads, k_max=k_max, **kw)
+    print(f"{w.name} {label if args.only_step == 'sparse' else 'dense'}: "
+          f"{args.warmup + args.steps} steps, plan {plan} ({binding.PLANS[plan]}), {S} splits",
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -688,8 +722,14 @@ def main():
                     help="which keep ratio of the workload to run")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-step", choices=["sparse", "dense"],
+                    help="profiling aid: run warm-up + steps plain kv_decode_step calls "
+                         "(L2 flushed before each) and print no benchmark line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.only_step:
+        run_only_step(args)
+        return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
