@@ -39,8 +39,14 @@ Steps and the passages they follow (page title, then section):
 * ``dropped_mass`` -- the dense attention mass of the tokens not selected. "Near-Oracle KV
   Selection via Pre-hoc Sparsity for Long-Context Inference", abstract (delta, the mass of
   the discarded entries); EntmaxKV abstract (output error is governed by delta).
+* ``fp8stats`` -- the page statistics stored as E4M3 bytes with one power-of-two exponent
+  per row, the minimum rounded down and the maximum rounded up so that the score stays an
+  upper bound ("Where Activation Sparsity and KV-Cache Sparsity Cross in LLM Decoding":
+  a selector key cache quantised to few bits; EntmaxKV abstract: the bound).
 
-Parity pins (tests marked ``not gpu``): brute-force loops for the statistics and the
+Parity pins (tests marked ``not gpu``): PyTorch's float8_e4m3fn decoding and rounding for
+the E4M3 table and the outward rounding, the exponent's defining inequalities and the
+upper-bound invariant for FP8 statistics; brute-force loops for the statistics and the
 selection, closed forms and the upper-bound invariant for the score, PyTorch's
 ``scaled_dot_product_attention`` in float64 for attention, partition invariance for the
 merge, and the exact mixture identity for delta. Every function here is pinned; none is
@@ -64,6 +70,7 @@ from .kvattn import (
     dropped_mass,
 )
 from .parity import check_selection
+from . import fp8stats  # noqa: F401
 
 __all__ = [
     "num_pages",
@@ -81,4 +88,5 @@ __all__ = [
     "merge_partials",
     "dropped_mass",
     "check_selection",
+    "fp8stats",
 ]
