@@ -324,6 +324,15 @@ def run_ours(args):
             skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
                                workspace=ws, **step_kw)
 
+    # FP8 statistics (built once, like the bf16 ones): the same step scoring from 1-byte stats
+    stats8 = exps8 = None
+    if step_kw is not None:
+        stats8, exps8 = skv.kv_build_page_stats_fp8(kv)
+
+    def fp8_step():
+        skv.kv_decode_step_fp8(kv, c.q, w.sm_scale, stats8, exps8, k_max=k_max, out=out,
+                               lse=lse, workspace=ws, **step_kw)
+
     def one_launch_step():
         """The step as one cluster launch (where the shape allows it)."""
         skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
@@ -344,6 +353,8 @@ def run_ours(args):
         step()
         dense_step()
         four_kernel_step(False)
+        if step_kw is not None:
+            fp8_step()
     torch.cuda.synchronize()
     st, flags = skv.kv_check_device_errors()
     if st != 0:
@@ -357,8 +368,8 @@ def run_ours(args):
     # two-launch steps with event nodes between their kernels, replayed in their own flushed
     # loops to time each kernel (event nodes sit between the kernels, so their programmatic
     # launch overlap is lost there: those graphs time kernels, not steps)
-    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt = (torch.cuda.CUDAGraph()
-                                                                  for _ in range(7))
+    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt, g_fp8 = (
+        torch.cuda.CUDAGraph() for _ in range(8))
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -377,6 +388,8 @@ def run_ours(args):
         if step_kw is not None:
             with torch.cuda.graph(g_one, stream=side):
                 one_launch_step()
+            with torch.cuda.graph(g_fp8, stream=side):
+                fp8_step()
         if alt_plan is not None:
             with torch.cuda.graph(g_alt, stream=side):
                 alt_step()
@@ -419,6 +432,8 @@ def run_ours(args):
         four_us = timed(g_four)
         barrier()
         one_us = timed(g_one) if one_launch_ran else []
+        barrier()
+        fp8_us = timed(g_fp8) if step_kw is not None else []
         barrier()
         alt_us = timed(g_alt) if alt_plan is not None else []
         barrier()
@@ -547,6 +562,10 @@ def run_ours(args):
         "step_gbs": {"sparse": round(acct["sparse_step"] / (sparse_med * 1e-6) / 1e9, 1),
                      "dense": round(acct["dense_step"] / (dense_med * 1e-6) / 1e9, 1)},
         "one_launch_step_us": (round(statistics.median(one_us), 3) if one_us else None),
+        "fp8_stats_step_us": ({"median": round(statistics.median(fp8_us), 3),
+                               "speedup_vs_dense": round(dense_med / statistics.median(fp8_us), 3),
+                               "stats_bytes_per_step": acct["pages"] * (2 * D + 1)}
+                              if fp8_us else None),
         "other_two_launch_step_us": ({"plan": binding.PLANS[alt_plan],
                                       "median": round(statistics.median(alt_us), 3)}
                                      if alt_us else None),
@@ -578,7 +597,8 @@ def run_ours(args):
         },
         "gpu_launches": args.steps * (n_step + n_dense + 4 + (4 if in_graph_events else 0)
                                       + (2 if two_launch else 0) + (1 if one_us else 0)
-                                      + (2 if alt_us else 0)),
+                                      + (2 if alt_us else 0)
+                                      + (n_step if fp8_us else 0)),
         "clocks": clocks,
     }
     if e2e_us:

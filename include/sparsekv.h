@@ -132,6 +132,23 @@ int32_t kv_version(void);
 kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStream_t stream);
 
 /*
+ * kv_build_page_stats_fp8 -- the statistics of kv_build_page_stats stored in one byte each
+ * (the compressed page statistics motivated by [BYTEX]'s selector key cache quantised to few
+ * bits), with outward rounding so that the score stays an upper bound ([ENTMAX]).
+ * For each mapped (page P, KV head g) row of 2*head_dim values (min row, max row):
+ *   e = smallest integer >= -126 with max |x| <= 448 * 2^e over the row (0 if all zero),
+ *   stats_exp[P][g] = e,
+ *   min byte = E4M3 byte of the largest value v with v * 2^e <= min,
+ *   max byte = E4M3 byte of the smallest value v with v * 2^e >= max,
+ * E4M3 being the OCP "FN" byte (bias 7, 3 mantissa bits, subnormals, largest 448, no
+ * infinity; zero is written as 0x00). Decoded min <= true min and decoded max >= true max.
+ * stats_fp8: device, [num_phys_pages][num_kv_heads][2][head_dim] bytes, 16-byte aligned;
+ * stats_exp: device, [num_phys_pages][num_kv_heads] int8. Unmapped pages are not written.
+ */
+kv_status kv_build_page_stats_fp8(const kv_cache_desc* cache, void* stats_fp8,
+                                  int8_t* stats_exp, cudaStream_t stream);
+
+/*
  * kv_append_token -- [ENTMAX] the cache grows by one token per decode step; this call adds
  * that token and keeps the page statistics current without re-reading the cache.
  * For every sequence b with seq_lens[b] > 0 (seq_lens already counts the new token), the
@@ -159,6 +176,15 @@ kv_status kv_append_token(const kv_cache_desc* cache, const void* k_new, const v
 kv_status kv_score_pages(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                          const void* stats, float* scores, int32_t scores_stride,
                          cudaStream_t stream);
+
+/*
+ * kv_score_pages_fp8 -- kv_score_pages from the statistics of kv_build_page_stats_fp8: the
+ * same formula with mn, mx the decoded values byte * 2^e (an upper bound of the exact-stats
+ * score, as the decoded box contains the exact one). Computed in float32.
+ */
+kv_status kv_score_pages_fp8(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                             const void* stats_fp8, const int8_t* stats_exp, float* scores,
+                             int32_t scores_stride, cudaStream_t stream);
 
 /*
  * kv_select_topk -- [PRHS], [SPARDA] appendix A: top-k pages of each (b, g) group.
@@ -344,6 +370,18 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
 
 size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
                                      int32_t k_max, int32_t num_splits);
+
+/*
+ * kv_decode_step_fp8 -- kv_decode_step scoring from FP8 statistics (kv_build_page_stats_fp8)
+ * instead of statistics in the cache's dtype: the same plans, workspace and outputs, with
+ * kv_score_pages_fp8's scores. KV_SPLITS_ONE_LAUNCH runs the automatic plan instead (the
+ * one-launch kernel reads cache-dtype statistics). Dense calls ignore the statistics.
+ */
+kv_status kv_decode_step_fp8(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                             float sm_scale, const void* stats_fp8, const int8_t* stats_exp,
+                             double keep_ratio, int32_t budget_pages, int32_t k_max,
+                             int32_t num_splits, float* out, float* lse, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * kv_decode_step_plan -- host, launches nothing: the kernels kv_decode_step runs for these

@@ -13,15 +13,18 @@ from .binding import (  # noqa: F401
     kv_append_token,
     kv_auto_num_splits,
     kv_build_page_stats,
+    kv_build_page_stats_fp8,
     kv_check_device_errors,
     kv_decode_attn_merge,
     kv_decode_step,
+    kv_decode_step_fp8,
     kv_decode_step_plan,
     kv_decode_step_workspace_size,
     kv_dropped_mass,
     kv_dropped_mass_workspace_size,
     kv_merge_splits,
     kv_score_pages,
+    kv_score_pages_fp8,
     kv_score_select,
     kv_select_decode_attn,
     kv_select_structured,

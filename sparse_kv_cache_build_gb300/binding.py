@@ -38,7 +38,8 @@ EXPORTS = (
     "kv_decode_step_workspace_size", "kv_check_device_errors", "kv_set_wait_limit_ns",
     "kv_selftest_wait_timeout", "kv_decode_step_static", "kv_append_token",
     "kv_select_structured", "kv_select_decode_attn", "kv_score_select",
-    "kv_decode_attn_merge", "kv_decode_step_plan",
+    "kv_decode_attn_merge", "kv_decode_step_plan", "kv_build_page_stats_fp8",
+    "kv_score_pages_fp8", "kv_decode_step_fp8",
 )
 
 
@@ -97,6 +98,9 @@ def _declare(lib):
         "kv_score_select": (I32, [D, P, I32, P, F64, I32, I32, P, I32, P, P, P, P]),
         "kv_decode_attn_merge": (I32, [D, P, I32, F32, P, P, I32, I32, P, P, P, P, P, P]),
         "kv_decode_step_plan": (I32, [D, I32, F64, I32, I32, I32, ctypes.POINTER(I32)]),
+        "kv_build_page_stats_fp8": (I32, [D, P, P, P]),
+        "kv_score_pages_fp8": (I32, [D, P, I32, P, P, P, I32, P]),
+        "kv_decode_step_fp8": (I32, [D, P, I32, F32, P, P, F64, I32, I32, I32, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -222,6 +226,37 @@ def kv_build_page_stats(kv: PagedKV, stats=None, stream=None):
     _need(stats, "stats", kv.dtype, (NP, Hkv, 2, D))
     _check("kv_build_page_stats", lib().kv_build_page_stats(kv.ref(), _ptr(stats), _stream(stream)))
     return stats
+
+
+def kv_build_page_stats_fp8(kv: PagedKV, stats=None, stats_exp=None, stream=None):
+    """FP8 (E4M3) page statistics with outward rounding: (bytes [NP][Hkv][2][D] uint8,
+    exponents [NP][Hkv] int8)."""
+    NP, Hkv, D = kv.k_pool.shape[0], kv.num_kv_heads, kv.head_dim
+    dev = kv.k_pool.device
+    if stats is None:
+        stats = torch.zeros((NP, Hkv, 2, D), dtype=torch.uint8, device=dev)
+    if stats_exp is None:
+        stats_exp = torch.zeros((NP, Hkv), dtype=torch.int8, device=dev)
+    _need(stats, "stats", torch.uint8, (NP, Hkv, 2, D))
+    _need(stats_exp, "stats_exp", torch.int8, (NP, Hkv))
+    _check("kv_build_page_stats_fp8", lib().kv_build_page_stats_fp8(
+        kv.ref(), _ptr(stats), _ptr(stats_exp), _stream(stream)))
+    return stats, stats_exp
+
+
+def kv_score_pages_fp8(kv: PagedKV, q, stats, stats_exp, scores=None, stream=None):
+    _need(q, "q", kv.dtype)
+    _need(stats, "stats", torch.uint8)
+    _need(stats_exp, "stats_exp", torch.int8)
+    B, Hq, _ = q.shape
+    if scores is None:
+        scores = torch.empty((B, kv.num_kv_heads, kv.stride), dtype=torch.float32,
+                             device=q.device)
+    _need(scores, "scores", torch.float32)
+    _check("kv_score_pages_fp8", lib().kv_score_pages_fp8(
+        kv.ref(), _ptr(q), Hq, _ptr(stats), _ptr(stats_exp), _ptr(scores), scores.shape[-1],
+        _stream(stream)))
+    return scores
 
 
 def kv_append_token(kv: PagedKV, k_new, v_new, stats, stream=None):
@@ -519,6 +554,28 @@ def kv_decode_step_plan(kv: PagedKV, num_q_heads: int, keep_ratio: float = 1.0,
     if r < 0:
         raise KVError("kv_decode_step_plan", r)
     return int(r), int(splits.value)
+
+
+def kv_decode_step_fp8(kv: PagedKV, q, sm_scale: float, stats=None, stats_exp=None,
+                       keep_ratio: float = 1.0, budget_pages: int = 0, k_max: int | None = None,
+                       num_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """kv_decode_step scoring from FP8 statistics (kv_build_page_stats_fp8)."""
+    _need(q, "q", kv.dtype)
+    B, Hq, D = q.shape
+    if k_max is None:
+        k_max = max_keep_pages(kv.stride, keep_ratio, budget_pages)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = kv_decode_step_workspace_size(kv, Hq, k_max, max(num_splits, 0))
+        workspace = torch.zeros((nbytes,), dtype=torch.uint8, device=q.device)
+    _check("kv_decode_step_fp8", lib().kv_decode_step_fp8(
+        kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(stats), _ptr(stats_exp),
+        float(keep_ratio), int(budget_pages), int(k_max), int(num_splits), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, lse
 
 
 def kv_check_device_errors(stream=None):

@@ -232,7 +232,18 @@ kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStrea
   if (!aligned16(stats)) return KV_ERR_MISALIGNED;
   DevCtx ctx;
   if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
-  return from_cuda(launch_page_stats(*cache, stats, ctx, stream));
+  return from_cuda(launch_page_stats(*cache, stats, nullptr, ctx, stream));
+}
+
+kv_status kv_build_page_stats_fp8(const kv_cache_desc* cache, void* stats_fp8,
+                                  int8_t* stats_exp, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if (stats_fp8 == nullptr || stats_exp == nullptr) return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats_fp8)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(launch_page_stats(*cache, stats_fp8, stats_exp, ctx, stream));
 }
 
 kv_status kv_append_token(const kv_cache_desc* cache, const void* k_new, const void* v_new,
@@ -257,8 +268,24 @@ kv_status kv_score_pages(const kv_cache_desc* cache, const void* q, int32_t num_
   if (!aligned16(stats)) return KV_ERR_MISALIGNED;
   DevCtx ctx;
   if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
-  return from_cuda(
-      launch_score_pages(*cache, q, num_q_heads, stats, scores, scores_stride, ctx, stream));
+  return from_cuda(launch_score_pages(*cache, q, num_q_heads, stats, nullptr, scores,
+                                      scores_stride, ctx, stream));
+}
+
+kv_status kv_score_pages_fp8(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                             const void* stats_fp8, const int8_t* stats_exp, float* scores,
+                             int32_t scores_stride, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (stats_fp8 == nullptr || stats_exp == nullptr || scores == nullptr ||
+      scores_stride < cache->page_table_stride)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats_fp8)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(launch_score_pages(*cache, q, num_q_heads, stats_fp8, stats_exp, scores,
+                                      scores_stride, ctx, stream));
 }
 
 kv_status kv_select_topk(const float* scores, int32_t scores_stride, const int32_t* seq_lens,
@@ -345,7 +372,8 @@ kv_status kv_score_select(const kv_cache_desc* cache, const void* q, int32_t num
   DeviceState* st = nullptr;
   if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
   if (!score_select_fits(cache, st)) return KV_ERR_UNSUPPORTED;
-  return from_cuda(launch_score_select(*cache, q, num_q_heads, stats, scores, scores_stride,
+  return from_cuda(launch_score_select(*cache, q, num_q_heads, stats, nullptr, scores,
+                                       scores_stride,
                                        keep_ratio, budget_pages, k_max, counters, sel_idx,
                                        sel_cnt, ctx, stream));
 }
@@ -574,11 +602,17 @@ int32_t kv_decode_step_plan(const kv_cache_desc* cache, int32_t num_q_heads, dou
   return P.plan;
 }
 
-kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
-                         float sm_scale, const void* stats, double keep_ratio,
-                         int32_t budget_pages, int32_t k_max, int32_t num_splits,
-                         float* out, float* lse, void* workspace, size_t workspace_bytes,
-                         cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// kv_decode_step with the statistics in the cache's dtype (stats_exp == NULL) or as FP8
+// bytes with per-row exponents.
+kv_status decode_step_impl(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                           float sm_scale, const void* stats, const int8_t* stats_exp,
+                           double keep_ratio, int32_t budget_pages, int32_t k_max,
+                           int32_t num_splits, float* out, float* lse, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
   kv_status r = check_desc(cache);
   if (r != KV_OK) return r;
   if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
@@ -587,6 +621,8 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   if (!dense && (stats == nullptr || k_max <= 0 || !(keep_ratio > 0.0 || budget_pages > 0)))
     return KV_ERR_INVALID_ARG;
   if (!dense && !aligned16(stats)) return KV_ERR_MISALIGNED;
+  if (!dense && stats_exp != nullptr && num_splits == KV_SPLITS_ONE_LAUNCH)
+    num_splits = 0;                        // the one-launch kernel reads cache-dtype stats
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return KV_ERR_WORKSPACE;
   DevCtx ctx;
@@ -620,7 +656,8 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
       return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, nullptr, nullptr, 0, P.S,
                                              acc, ml, ctx, stream, sa));
     case KV_PLAN_SCORE_THEN_SELECT_ATTN:
-      e = launch_score_pages(*cache, q, num_q_heads, stats, scores, stride, ctx, stream);
+      e = launch_score_pages(*cache, q, num_q_heads, stats, stats_exp, scores, stride, ctx,
+                             stream);
       if (e != cudaSuccess) return KV_ERR_CUDA;
       sa.scores = scores;
       sa.scores_stride = stride;
@@ -632,7 +669,8 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
       return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, nullptr, nullptr, 0, P.S,
                                              acc, ml, ctx, stream, sa));
     case KV_PLAN_SCORE_SELECT_THEN_ATTN:
-      e = launch_score_select(*cache, q, num_q_heads, stats, scores, stride, keep_ratio,
+      e = launch_score_select(*cache, q, num_q_heads, stats, stats_exp, scores, stride,
+                              keep_ratio,
                               budget_pages, k_max, reinterpret_cast<int32_t*>(ws + L.ctr), sel,
                               cnt, ctx, stream);
       if (e != cudaSuccess) return KV_ERR_CUDA;
@@ -643,7 +681,8 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   }
   // four kernels (sparse) or two (dense)
   if (!dense) {
-    e = launch_score_pages(*cache, q, num_q_heads, stats, scores, stride, ctx, stream);
+    e = launch_score_pages(*cache, q, num_q_heads, stats, stats_exp, scores, stride, ctx,
+                           stream);
     if (e != cudaSuccess) return KV_ERR_CUDA;
     e = launch_select_topk(scores, stride, cache->seq_lens, cache->page_size, cache->batch,
                            cache->num_kv_heads, nullptr, keep_ratio, budget_pages, k_max, 0, 0,
@@ -655,6 +694,31 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   if (e != cudaSuccess) return KV_ERR_CUDA;
   return from_cuda(
       launch_merge(acc, ml, cache->batch, num_q_heads, P.S, cache->head_dim, out, lse, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                         float sm_scale, const void* stats, double keep_ratio,
+                         int32_t budget_pages, int32_t k_max, int32_t num_splits,
+                         float* out, float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  return decode_step_impl(cache, q, num_q_heads, sm_scale, stats, nullptr, keep_ratio,
+                          budget_pages, k_max, num_splits, out, lse, workspace, workspace_bytes,
+                          stream);
+}
+
+kv_status kv_decode_step_fp8(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                             float sm_scale, const void* stats_fp8, const int8_t* stats_exp,
+                             double keep_ratio, int32_t budget_pages, int32_t k_max,
+                             int32_t num_splits, float* out, float* lse, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  if (!is_dense(keep_ratio, budget_pages) && stats_exp == nullptr) return KV_ERR_INVALID_ARG;
+  return decode_step_impl(cache, q, num_q_heads, sm_scale, stats_fp8, stats_exp, keep_ratio,
+                          budget_pages, k_max, num_splits, out, lse, workspace, workspace_bytes,
+                          stream);
 }
 
 kv_status kv_check_device_errors(cudaStream_t stream, int32_t* flags) {

@@ -206,20 +206,22 @@ __device__ __forceinline__ int checked_len(const DevCtx& c, const kv_cache_desc&
 // ------------------------------------------------------------------------------------
 // Launchers (one per kernel family; each returns cudaGetLastError()).
 // ------------------------------------------------------------------------------------
-cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, DevCtx ctx,
-                              cudaStream_t s);
+// stats_exp == NULL: statistics in the cache's dtype; otherwise FP8 bytes in stats and one
+// int8 exponent per (page, KV head) in stats_exp (fp8_stats.cuh).
+cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, int8_t* stats_exp,
+                              DevCtx ctx, cudaStream_t s);
 cudaError_t launch_score_pages(const kv_cache_desc& d, const void* q, int Hq,
-                               const void* stats, float* scores, int scores_stride,
-                               DevCtx ctx, cudaStream_t s);
+                               const void* stats, const int8_t* stats_exp, float* scores,
+                               int scores_stride, DevCtx ctx, cudaStream_t s);
 // kv_score_pages and the group's top-k (keep ratio / budget) in one launch; counters
 // [batch][Hkv] start at zero and are returned to zero. score_select_smem: dynamic shared
 // bytes the launch needs for a table stride (the caller checks it against the device).
 size_t score_select_smem(int page_table_stride);
 cudaError_t launch_score_select(const kv_cache_desc& d, const void* q, int Hq,
-                                const void* stats, float* scores, int scores_stride,
-                                double keep_ratio, int budget, int k_max, int32_t* counters,
-                                int32_t* sel_idx, int32_t* sel_cnt, DevCtx ctx,
-                                cudaStream_t s);
+                                const void* stats, const int8_t* stats_exp, float* scores,
+                                int scores_stride, double keep_ratio, int budget, int k_max,
+                                int32_t* counters, int32_t* sel_idx, int32_t* sel_cnt,
+                                DevCtx ctx, cudaStream_t s);
 cudaError_t launch_select_topk(const float* scores, int scores_stride, const int32_t* seq_lens,
                                int page_size, int batch, int Hkv, const int32_t* keep,
                                double keep_ratio, int budget_pages, int k_max, int sink,

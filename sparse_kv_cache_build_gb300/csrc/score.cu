@@ -27,37 +27,70 @@
 // (a per-group arrival counter, returned to zero) reads the group's scores back from L2
 // and runs the block-wide selection of cta_topk.cuh, so the selection costs no launch of
 // its own and runs once per group.
+//
+// FP8 statistics (fp8_stats.cuh): a row is 2*D E4M3 bytes plus the row's exponent e. Four
+// lanes own a row (each keeps the same 64 bytes in flight as a lane of a bf16 row, so a warp
+// covers twice the rows), the bytes convert exactly to half precision two at a time and then
+// to float, and the row's dot product is scaled by 2^e once at the end (a power-of-two
+// scaling commutes with the fp32 rounding of the sum, so this equals summing the decoded
+// values times 2^e).
+#include <cuda_fp8.h>
+
 #include "cta_topk.cuh"
+#include "fp8_stats.cuh"
 #include "kv_internal.cuh"
 
 namespace skv {
 namespace {
 
 constexpr int kScoreWarps = 4;
-constexpr int kScorePagesPerBlock = kScoreWarps * 4;   // 16
+// rows (pages) per warp: eight lanes per row, four for FP8 rows
+template <bool F8>
+constexpr int rows_per_warp() { return F8 ? 8 : 4; }
+
+// The 16 values of a 16-byte chunk of E4M3 bytes, in byte order (exact).
+__device__ __forceinline__ void fp8_chunk_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((w[i] >> (16 * j)) & 0xffffu), __NV_E4M3);
+      const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      f[4 * i + 2 * j] = x.x;
+      f[4 * i + 2 * j + 1] = x.y;
+    }
+  }
+}
 constexpr int kSelWarps = 16;                          // score + select blocks: 512 threads
 constexpr int kSelThreads = kSelWarps * 32;
 constexpr int kSelCandWords = 4096;                    // gathered keys of the threshold bin
 
 // Scores of the WARPS*4 pages of this block for group (b, g) into scores; returns false
-// (block-uniform) if the block has no page of the sequence.
-template <typename T, int D, int WARPS>
+// (block-uniform) if the block has no page of the sequence. F8: stats are E4M3 bytes with
+// one exponent per row in stats_exp; otherwise stats are of the query's type T.
+template <typename T, int D, int WARPS, bool F8>
 __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __restrict__ q,
-                                            int G, const T* __restrict__ stats, float* w,
+                                            int G, const void* __restrict__ stats,
+                                            const int8_t* __restrict__ stats_exp, float* w,
                                             float* __restrict__ scores, int scores_stride,
                                             int b, int g, int n_pages, const DevCtx& ctx) {
-  constexpr int EB = ElemTraits<T>::bytes;
+  constexpr int EB = F8 ? 1 : ElemTraits<T>::bytes;   // bytes per statistic
   constexpr int EPC = 16 / EB;                // elements per 16-byte chunk
-  constexpr int CPL = (2 * D * EB / 16) / 8;  // chunks per lane per stats row
-  const int p_block = blockIdx.x * WARPS * 4;
+  constexpr int RPW = rows_per_warp<F8>();
+  constexpr int LPR = 32 / RPW;               // lanes per row
+  constexpr int CPL = (2 * D * EB / 16) / LPR;  // chunks per lane per stats row
+  const int p_block = blockIdx.x * WARPS * RPW;
   if (p_block >= n_pages) return false;
 
   const int Hkv = d.num_kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 3, j = lane & 7;
-  const int p = p_block + warp * 4 + grp;
+  const int grp = lane / LPR, j = lane % LPR;
+  const int p = p_block + warp * RPW + grp;
   uint4 raw[CPL];
   bool ok = false;
+  int row_exp = 0;
   if (p < n_pages) {
     const int P = d.page_table[(long)b * d.page_table_stride + p];
     if (P >= 0 && P < d.num_phys_pages) {
@@ -65,7 +98,8 @@ __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __r
       const uint4* row = reinterpret_cast<const uint4*>(
           reinterpret_cast<const char*>(stats) + (((long)P * Hkv + g) * 2 * D) * EB);
 #pragma unroll
-      for (int u = 0; u < CPL; ++u) raw[u] = __ldg(row + j + 8 * u);
+      for (int u = 0; u < CPL; ++u) raw[u] = __ldg(row + j + LPR * u);
+      if constexpr (F8) row_exp = __ldg(stats_exp + (long)P * Hkv + g);
     } else if (j == 0) {
       flag(ctx, KV_DEVERR_BAD_PAGE);
     }
@@ -89,30 +123,33 @@ __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __r
 #pragma unroll
     for (int u = 0; u < CPL; ++u) {
       float f[EPC];
-      chunk_to_f32<T>(raw[u], f);
-      const float* wc = w + (j + 8 * u) * EPC;
+      if constexpr (F8) fp8_chunk_to_f32(raw[u], f);
+      else chunk_to_f32<T>(raw[u], f);
+      const float* wc = w + (j + LPR * u) * EPC;
 #pragma unroll
       for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
     }
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if constexpr (F8) acc *= fp8::pow2(row_exp);
   if (j == 0 && ok) scores[((long)b * Hkv + g) * scores_stride + p] = acc;
   return true;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kScoreWarps * 32)
-score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const T* __restrict__ stats,
-             float* __restrict__ scores, int scores_stride, DevCtx ctx) {
+score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const void* __restrict__ stats,
+             const int8_t* __restrict__ stats_exp, float* __restrict__ scores,
+             int scores_stride, DevCtx ctx) {
   __shared__ __align__(16) float w[2 * D];    // [Neg | Pos], matching a row's [mn | mx]
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.z, g = blockIdx.y;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
-  score_block<T, D, kScoreWarps>(d, q, G, stats, w, scores, scores_stride, b, g, n_pages, ctx);
+  score_block<T, D, kScoreWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b, g,
+                                     n_pages, ctx);
 }
 
 // Shared words for the keys of a group of up to max_pages pages, laid out as cta_topk.cuh
@@ -121,10 +158,11 @@ __host__ __device__ constexpr size_t select_key_words(int max_pages) {
   return (size_t)kSelThreads * (size_t)(((max_pages + kSelThreads - 1) / kSelThreads) | 1);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kSelThreads)
 score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
-                    const T* __restrict__ stats, float* __restrict__ scores, int scores_stride,
+                    const void* __restrict__ stats, const int8_t* __restrict__ stats_exp,
+                    float* __restrict__ scores, int scores_stride,
                     double keep_ratio, int budget, int k_max, int32_t* __restrict__ counters,
                     int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt,
                     int key_words, DevCtx ctx) {
@@ -144,12 +182,12 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
     if (blockIdx.x == 0 && tid == 0) sel_cnt[grp] = 0;
     return;
   }
-  if (!score_block<T, D, kSelWarps>(d, q, G, stats, w, scores, scores_stride, b, g, n_pages,
-                                    ctx))
+  if (!score_block<T, D, kSelWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b,
+                                        g, n_pages, ctx))
     return;
 
   // ---- the group's last block selects -----------------------------------------------------
-  const int blocks = ceil_div(n_pages, kSelWarps * 4);
+  const int blocks = ceil_div(n_pages, kSelWarps * rows_per_warp<F8>());
   __syncthreads();                            // this block's scores are written
   if (tid == 0) {
     __threadfence();
@@ -178,32 +216,35 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   cta_compact<kSelThreads>(K, thr, take_eq, wtot, [&](int p, int pos) { out[pos] = p; });
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 cudaError_t launch_t(const kv_cache_desc& d, const void* q, int Hq, const void* stats,
-                     float* scores, int scores_stride, DevCtx ctx, cudaStream_t s) {
-  dim3 grid(ceil_div(d.page_table_stride, kScorePagesPerBlock), d.num_kv_heads, d.batch);
-  return launch_pdl(score_kernel<T, D>, grid, dim3(kScoreWarps * 32), 0, s, d,
-                    static_cast<const T*>(q), Hq / d.num_kv_heads,
-                    static_cast<const T*>(stats), scores, scores_stride, ctx);
+                     const int8_t* stats_exp, float* scores, int scores_stride, DevCtx ctx,
+                     cudaStream_t s) {
+  dim3 grid(ceil_div(d.page_table_stride, kScoreWarps * rows_per_warp<F8>()), d.num_kv_heads,
+            d.batch);
+  return launch_pdl(score_kernel<T, D, F8>, grid, dim3(kScoreWarps * 32), 0, s, d,
+                    static_cast<const T*>(q), Hq / d.num_kv_heads, stats, stats_exp, scores,
+                    scores_stride, ctx);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 cudaError_t launch_sel_t(const kv_cache_desc& d, const void* q, int Hq, const void* stats,
-                         float* scores, int scores_stride, double keep_ratio, int budget,
-                         int k_max, int32_t* counters, int32_t* sel_idx, int32_t* sel_cnt,
-                         DevCtx ctx, cudaStream_t s) {
+                         const int8_t* stats_exp, float* scores, int scores_stride,
+                         double keep_ratio, int budget, int k_max, int32_t* counters,
+                         int32_t* sel_idx, int32_t* sel_cnt, DevCtx ctx, cudaStream_t s) {
   const int key_words = (int)select_key_words(d.page_table_stride);
   const size_t smem = 4 * ((size_t)key_words + kSelCandWords);
-  auto kern = score_select_kernel<T, D>;
+  auto kern = score_select_kernel<T, D, F8>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(ceil_div(d.page_table_stride, kSelWarps * 4), d.num_kv_heads, d.batch);
+  dim3 grid(ceil_div(d.page_table_stride, kSelWarps * rows_per_warp<F8>()), d.num_kv_heads,
+            d.batch);
   return launch_pdl(kern, grid, dim3(kSelThreads), smem, s, d, static_cast<const T*>(q),
-                    Hq / d.num_kv_heads, static_cast<const T*>(stats), scores, scores_stride,
-                    keep_ratio, budget, k_max, counters, sel_idx, sel_cnt, key_words, ctx);
+                    Hq / d.num_kv_heads, stats, stats_exp, scores, scores_stride, keep_ratio,
+                    budget, k_max, counters, sel_idx, sel_cnt, key_words, ctx);
 }
 
 }  // namespace
@@ -213,31 +254,34 @@ size_t score_select_smem(int page_table_stride) {
 }
 
 cudaError_t launch_score_select(const kv_cache_desc& d, const void* q, int Hq,
-                                const void* stats, float* scores, int scores_stride,
-                                double keep_ratio, int budget, int k_max, int32_t* counters,
-                                int32_t* sel_idx, int32_t* sel_cnt, DevCtx ctx,
-                                cudaStream_t s) {
-  const bool bf = d.dtype == KV_BF16;
-  if (d.head_dim == 128)
-    return bf ? launch_sel_t<bf16_t, 128>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
-                                          budget, k_max, counters, sel_idx, sel_cnt, ctx, s)
-              : launch_sel_t<float, 128>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
-                                         budget, k_max, counters, sel_idx, sel_cnt, ctx, s);
-  return bf ? launch_sel_t<bf16_t, 64>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
-                                       budget, k_max, counters, sel_idx, sel_cnt, ctx, s)
-            : launch_sel_t<float, 64>(d, q, Hq, stats, scores, scores_stride, keep_ratio,
-                                      budget, k_max, counters, sel_idx, sel_cnt, ctx, s);
+                                const void* stats, const int8_t* stats_exp, float* scores,
+                                int scores_stride, double keep_ratio, int budget, int k_max,
+                                int32_t* counters, int32_t* sel_idx, int32_t* sel_cnt,
+                                DevCtx ctx, cudaStream_t s) {
+#define SKV_SEL(T, D, F8)                                                                   \
+  return launch_sel_t<T, D, F8>(d, q, Hq, stats, stats_exp, scores, scores_stride, keep_ratio, \
+                                budget, k_max, counters, sel_idx, sel_cnt, ctx, s)
+  const bool bf = d.dtype == KV_BF16, f8 = stats_exp != nullptr, wide = d.head_dim == 128;
+  if (bf && wide) { if (f8) SKV_SEL(bf16_t, 128, true); SKV_SEL(bf16_t, 128, false); }
+  if (bf) { if (f8) SKV_SEL(bf16_t, 64, true); SKV_SEL(bf16_t, 64, false); }
+  if (wide) { if (f8) SKV_SEL(float, 128, true); SKV_SEL(float, 128, false); }
+  if (f8) SKV_SEL(float, 64, true);
+  SKV_SEL(float, 64, false);
+#undef SKV_SEL
 }
 
 cudaError_t launch_score_pages(const kv_cache_desc& d, const void* q, int Hq,
-                               const void* stats, float* scores, int scores_stride,
-                               DevCtx ctx, cudaStream_t s) {
-  const bool bf = d.dtype == KV_BF16;
-  if (d.head_dim == 128)
-    return bf ? launch_t<bf16_t, 128>(d, q, Hq, stats, scores, scores_stride, ctx, s)
-              : launch_t<float, 128>(d, q, Hq, stats, scores, scores_stride, ctx, s);
-  return bf ? launch_t<bf16_t, 64>(d, q, Hq, stats, scores, scores_stride, ctx, s)
-            : launch_t<float, 64>(d, q, Hq, stats, scores, scores_stride, ctx, s);
+                               const void* stats, const int8_t* stats_exp, float* scores,
+                               int scores_stride, DevCtx ctx, cudaStream_t s) {
+#define SKV_SC(T, D, F8) \
+  return launch_t<T, D, F8>(d, q, Hq, stats, stats_exp, scores, scores_stride, ctx, s)
+  const bool bf = d.dtype == KV_BF16, f8 = stats_exp != nullptr, wide = d.head_dim == 128;
+  if (bf && wide) { if (f8) SKV_SC(bf16_t, 128, true); SKV_SC(bf16_t, 128, false); }
+  if (bf) { if (f8) SKV_SC(bf16_t, 64, true); SKV_SC(bf16_t, 64, false); }
+  if (wide) { if (f8) SKV_SC(float, 128, true); SKV_SC(float, 128, false); }
+  if (f8) SKV_SC(float, 64, true);
+  SKV_SC(float, 64, false);
+#undef SKV_SC
 }
 
 }  // namespace skv

@@ -9,7 +9,10 @@
 // Layout: one warp per (physical page, KV head) chunk. The chunk is PS rows of D
 // contiguous elements; lane l owns D/32 consecutive columns, so every row read by the warp
 // is one coalesced 128- or 256-byte access. Values are compared as floats and written back
-// bit for bit in the storage dtype (min and max of exact values are exact).
+// bit for bit in the storage dtype (min and max of exact values are exact), or, in the FP8
+// form (fp8_stats.cuh), as E4M3 bytes rounded outward under the row's power-of-two exponent
+// (the warp finds the row's largest magnitude with one reduction).
+#include "fp8_stats.cuh"
 #include "kv_internal.cuh"
 
 namespace skv {
@@ -55,9 +58,10 @@ __device__ __forceinline__ void store_row(T* p, const float* f) {
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kStatsWarps * 32)
-page_stats_kernel(kv_cache_desc d, T* __restrict__ stats, DevCtx ctx) {
+page_stats_kernel(kv_cache_desc d, T* __restrict__ stats, uint8_t* __restrict__ codes,
+                  int8_t* __restrict__ exps, DevCtx ctx) {
   constexpr int EPL = D / 32;
   const int b = blockIdx.y;
   const int len = checked_len(ctx, d, b);
@@ -92,27 +96,58 @@ page_stats_kernel(kv_cache_desc d, T* __restrict__ stats, DevCtx ctx) {
         mx[e] = v[e] > mx[e] ? v[e] : mx[e];
       }
     }
-    T* dst = stats + (((long)P * Hkv + g) * 2) * D + lane * EPL;
-    store_row<T, EPL>(dst, mn);
-    store_row<T, EPL>(dst + D, mx);
+    if constexpr (F8) {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) m = fmaxf(m, fmaxf(fabsf(mn[e]), fabsf(mx[e])));
+      const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      const int ex = fp8::row_exponent(__uint_as_float(mb));
+      const float inv = fp8::pow2(-ex);
+      uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        lo |= fp8::quantize_down(mn[e], inv) << (8 * e);
+        hi |= fp8::quantize_up(mx[e], inv) << (8 * e);
+      }
+      uint8_t* dst = codes + (((long)P * Hkv + g) * 2) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        *reinterpret_cast<uint32_t*>(dst) = lo;
+        *reinterpret_cast<uint32_t*>(dst + D) = hi;
+      } else {
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)lo;
+        *reinterpret_cast<uint16_t*>(dst + D) = (uint16_t)hi;
+      }
+      if (lane == 0) exps[(long)P * Hkv + g] = (int8_t)ex;
+    } else {
+      T* dst = stats + (((long)P * Hkv + g) * 2) * D + lane * EPL;
+      store_row<T, EPL>(dst, mn);
+      store_row<T, EPL>(dst + D, mx);
+    }
   }
 }
 
 template <typename T, int D>
-cudaError_t launch_t(const kv_cache_desc& d, void* stats, DevCtx ctx, cudaStream_t s) {
+cudaError_t launch_t(const kv_cache_desc& d, void* stats, int8_t* exps, DevCtx ctx,
+                     cudaStream_t s) {
   dim3 grid(ceil_div(d.page_table_stride, kStatsPagesPerBlock), d.batch);
-  page_stats_kernel<T, D><<<grid, kStatsWarps * 32, 0, s>>>(d, static_cast<T*>(stats), ctx);
+  if (exps != nullptr)
+    page_stats_kernel<T, D, true><<<grid, kStatsWarps * 32, 0, s>>>(
+        d, nullptr, static_cast<uint8_t*>(stats), exps, ctx);
+  else
+    page_stats_kernel<T, D, false><<<grid, kStatsWarps * 32, 0, s>>>(
+        d, static_cast<T*>(stats), nullptr, nullptr, ctx);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, DevCtx ctx,
-                              cudaStream_t s) {
+cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, int8_t* stats_exp,
+                              DevCtx ctx, cudaStream_t s) {
   const bool bf = d.dtype == KV_BF16;
-  if (d.head_dim == 128) return bf ? launch_t<bf16_t, 128>(d, stats, ctx, s)
-                                   : launch_t<float, 128>(d, stats, ctx, s);
-  return bf ? launch_t<bf16_t, 64>(d, stats, ctx, s) : launch_t<float, 64>(d, stats, ctx, s);
+  if (d.head_dim == 128) return bf ? launch_t<bf16_t, 128>(d, stats, stats_exp, ctx, s)
+                                   : launch_t<float, 128>(d, stats, stats_exp, ctx, s);
+  return bf ? launch_t<bf16_t, 64>(d, stats, stats_exp, ctx, s)
+            : launch_t<float, 64>(d, stats, stats_exp, ctx, s);
 }
 
 }  // namespace skv
