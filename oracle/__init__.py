@@ -39,12 +39,18 @@ Steps and the passages they follow (page title, then section):
 * ``dropped_mass`` -- the dense attention mass of the tokens not selected. "Near-Oracle KV
   Selection via Pre-hoc Sparsity for Long-Context Inference", abstract (delta, the mass of
   the discarded entries); EntmaxKV abstract (output error is governed by delta).
+* ``entmax`` -- 1.5-entmax attention over selected pages, its dropped mass, per-head page
+  moments and the Gaussian-aware threshold selector ("EntmaxKV: Support-Aware Decoding for
+  Entmax Attention", abstract: exact zeros make sparse decoding exact once the selection
+  holds the support; the selector estimates the entmax threshold from page statistics).
 * ``fp8stats`` -- the page statistics stored as E4M3 bytes with one power-of-two exponent
   per row, the minimum rounded down and the maximum rounded up so that the score stays an
   upper bound ("Where Activation Sparsity and KV-Cache Sparsity Cross in LLM Decoding":
   a selector key cache quantised to few bits; EntmaxKV abstract: the bound).
 
-Parity pins (tests marked ``not gpu``): PyTorch's float8_e4m3fn decoding and rounding for
+Parity pins (tests marked ``not gpu``): bisection on tau, two-value closed forms and
+numerical integration of the Gaussian tail for entmax; PyTorch's float8_e4m3fn decoding and
+rounding for
 the E4M3 table and the outward rounding, the exponent's defining inequalities and the
 upper-bound invariant for FP8 statistics; brute-force loops for the statistics and the
 selection, closed forms and the upper-bound invariant for the score, PyTorch's
@@ -70,7 +76,7 @@ from .kvattn import (
     dropped_mass,
 )
 from .parity import check_selection
-from . import fp8stats  # noqa: F401
+from . import entmax, fp8stats  # noqa: F401
 
 __all__ = [
     "num_pages",
@@ -88,5 +94,6 @@ __all__ = [
     "merge_partials",
     "dropped_mass",
     "check_selection",
+    "entmax",
     "fp8stats",
 ]
