@@ -333,6 +333,22 @@ def run_ours(args):
         skv.kv_decode_step_fp8(kv, c.q, w.sm_scale, stats8, exps8, k_max=k_max, out=out,
                                lse=lse, workspace=ws, **step_kw)
 
+    # entmax decoding (1.5-entmax): the Gaussian-aware selection step and dense entmax
+    ent_ws = torch.empty((skv.kv_entmax_decode_step_workspace_size(kv, Hq, kv.stride),),
+                         dtype=torch.uint8, device=dev)
+    ent_dws = torch.empty((int(binding.lib().kv_entmax_attn_workspace_size(kv.ref(), Hq, 0)),),
+                          dtype=torch.uint8, device=dev)
+    ent_out = torch.empty_like(out)
+    ent_tau = torch.empty_like(lse)
+
+    def entmax_step():
+        skv.kv_entmax_decode_step(kv, c.q, w.sm_scale, stats, k_max=kv.stride, out=ent_out,
+                                  tau=ent_tau, workspace=ent_ws)
+
+    def entmax_dense():
+        skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, out=ent_out, tau=ent_tau,
+                                  workspace=ent_dws)
+
     def one_launch_step():
         """The step as one cluster launch (where the shape allows it)."""
         skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
@@ -355,6 +371,8 @@ def run_ours(args):
         four_kernel_step(False)
         if step_kw is not None:
             fp8_step()
+        entmax_step()
+        entmax_dense()
     torch.cuda.synchronize()
     st, flags = skv.kv_check_device_errors()
     if st != 0:
@@ -368,8 +386,8 @@ def run_ours(args):
     # two-launch steps with event nodes between their kernels, replayed in their own flushed
     # loops to time each kernel (event nodes sit between the kernels, so their programmatic
     # launch overlap is lost there: those graphs time kernels, not steps)
-    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt, g_fp8 = (
-        torch.cuda.CUDAGraph() for _ in range(8))
+    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt, g_fp8, g_ent, g_entd = (
+        torch.cuda.CUDAGraph() for _ in range(10))
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -379,6 +397,10 @@ def run_ours(args):
             dense_step()
         with torch.cuda.graph(g_four, stream=side):
             four_kernel_step(False)
+        with torch.cuda.graph(g_ent, stream=side):
+            entmax_step()
+        with torch.cuda.graph(g_entd, stream=side):
+            entmax_dense()
         if in_graph_events:
             with torch.cuda.graph(g_marked, stream=side):
                 four_kernel_step(True)
@@ -435,6 +457,10 @@ def run_ours(args):
         barrier()
         fp8_us = timed(g_fp8) if step_kw is not None else []
         barrier()
+        ent_us = timed(g_ent)
+        barrier()
+        entd_us = timed(g_entd)
+        barrier()
         alt_us = timed(g_alt) if alt_plan is not None else []
         barrier()
         if in_graph_events:
@@ -474,6 +500,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     sel_cnt = cnt.cpu().numpy()
     acct = byte_account(w, n_pages, sel_cnt, S)
+    # pages the entmax selector kept (read back from the step's workspace)
+    entmax_step()
+    torch.cuda.synchronize()
+    M = (B * Hq * kv.stride * 4 + 255) // 256 * 256
+    cb = 3 * M + (B * Hkv * kv.stride * 4 + 255) // 256 * 256
+    ent_kept = int(ent_ws[cb: cb + B * Hkv * 4].view(torch.int32).sum())
 
     # dropped mass of this step (diagnostic, outside every timed region)
     delta = skv.kv_dropped_mass(kv, c.q, w.sm_scale, sel, cnt)
@@ -562,6 +594,13 @@ def run_ours(args):
         "step_gbs": {"sparse": round(acct["sparse_step"] / (sparse_med * 1e-6) / 1e9, 1),
                      "dense": round(acct["dense_step"] / (dense_med * 1e-6) / 1e9, 1)},
         "one_launch_step_us": (round(statistics.median(one_us), 3) if one_us else None),
+        "entmax": {"step_us": round(statistics.median(ent_us), 3),
+                   "dense_us": round(statistics.median(entd_us), 3),
+                   "speedup_vs_dense": round(statistics.median(entd_us)
+                                             / statistics.median(ent_us), 3),
+                   "kept_pages": ent_kept,
+                   "path": "kv_entmax_decode_step (moments, Gaussian-aware select, logits, "
+                           "threshold + output) vs kv_entmax_decode_attn over every page"},
         "fp8_stats_step_us": ({"median": round(statistics.median(fp8_us), 3),
                                "speedup_vs_dense": round(dense_med / statistics.median(fp8_us), 3),
                                "stats_bytes_per_step": acct["pages"] * (2 * D + 1)}
@@ -598,7 +637,7 @@ def run_ours(args):
         "gpu_launches": args.steps * (n_step + n_dense + 4 + (4 if in_graph_events else 0)
                                       + (2 if two_launch else 0) + (1 if one_us else 0)
                                       + (2 if alt_us else 0)
-                                      + (n_step if fp8_us else 0)),
+                                      + (n_step if fp8_us else 0) + 4 + 2),
         "clocks": clocks,
     }
     if e2e_us:

@@ -428,6 +428,70 @@ kv_status kv_decode_step_static(const kv_cache_desc* cache, const void* q, int32
                                 float* out, float* lse, cudaStream_t stream);
 
 /*
+ * Entmax decoding over selected pages -- the next-step row after [ENTMAX] (abstract):
+ * alpha-entmax gives exact zeros, so attention over the selected pages equals full attention
+ * once the selection holds the support, and a Gaussian-aware selector estimates the entmax
+ * threshold from the page statistics so that the kept budget adapts to the scores.
+ * Readings: alpha = 1.5; with z_t = sm_scale * q . k_t / 2 the weights are
+ * p_t = max(z_t - tau, 0)^2 with sum p_t = 1 over the attended tokens (tau in z units).
+ *
+ * kv_entmax_page_moments -- per query head h and logical page p (stats as kv_build_page_stats):
+ *   zb = (sm_scale/2) sum_d max(q_d mn_d, q_d mx_d)            (upper bound of z over the page)
+ *   cz = (sm_scale/2) q . (mn + mx)/2                          (box-centre z)
+ *   vz = (sm_scale/2)^2 sum_d q_d^2 (mx_d - mn_d)^2 / 12      (within-box variance of z)
+ * written to [batch][num_q_heads][stride] float32 each (entries past a sequence untouched).
+ */
+kv_status kv_entmax_page_moments(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                 const void* stats, float sm_scale, float* zb, float* cz,
+                                 float* vz, int32_t stride, cudaStream_t stream);
+
+/*
+ * kv_entmax_select -- Gaussian-aware threshold selection per (b, g) group: for each query
+ * head, with n_p the valid tokens of page p and N = sum n_p,
+ *   mu = sum n_p cz_p / N,  sigma^2 = sum n_p (cz_p - mu)^2 / N + sum n_p vz_p / N,
+ *   tau_hat solving N * E[max(Z - tau_hat, 0)^2] = 1 for Z ~ N(mu, sigma^2)
+ * (closed form s^2((u^2+1) Phi(u) + u phi(u)), u = (mu - tau)/s, solved by bisection in
+ * double). A page is kept if zb > tau_hat for some head of the group, and each head's
+ * highest-zb page (the lower index on ties) is always kept. Kept pages go to
+ * sel_idx[b][g][...] ascending, their count to sel_cnt[b][g]; more than k_max is flagged
+ * (KV_DEVERR_KEEP) and the first k_max are kept. tau_hat [batch][num_q_heads] may be NULL.
+ */
+kv_status kv_entmax_select(const float* zb, const float* cz, const float* vz, int32_t stride,
+                           const int32_t* seq_lens, int32_t page_size, int32_t batch,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t k_max,
+                           int32_t* sel_idx, int32_t* sel_cnt, float* tau_hat,
+                           cudaStream_t stream);
+
+/*
+ * kv_entmax_decode_attn -- 1.5-entmax attention of each decode query over the valid tokens of
+ * its group's selected pages (sel_idx NULL: every page, the dense entmax baseline):
+ * out[b][h] = sum_t max(z_t - tau, 0)^2 v_t with tau solved exactly over those tokens
+ * (tau[b][h] written if tau is not NULL; NaN and a zero output for a group with no token).
+ * K is read for the attended pages, V only for tokens with a nonzero weight.
+ * workspace: device, kv_entmax_attn_workspace_size() bytes (the logits), 16-byte aligned.
+ */
+size_t kv_entmax_attn_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
+                                     int32_t sel_stride);
+kv_status kv_entmax_decode_attn(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,
+                                int32_t sel_stride, float* out, float* tau, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kv_entmax_decode_step -- kv_entmax_page_moments, kv_entmax_select and kv_entmax_decode_attn
+ * on a caller workspace (256-byte aligned, kv_entmax_decode_step_workspace_size() bytes).
+ * After the call the workspace holds the selection: with M = round256(batch * num_q_heads *
+ * page_table_stride * 4), sel_idx [batch][num_kv_heads][k_max] int32 at byte 3M and sel_cnt
+ * [batch][num_kv_heads] at 3M + round256(batch * num_kv_heads * k_max * 4).
+ */
+size_t kv_entmax_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
+                                            int32_t k_max);
+kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const void* stats, int32_t k_max, float* out,
+                                float* tau, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/*
  * kv_check_device_errors -- synchronises `stream`, reads and clears the current device's
  * error word. Returns KV_OK, KV_ERR_TIMEOUT (a bounded wait ran out) or KV_ERR_BAD_INDEX
  * (any other flag). If flags is not NULL (host), the raw KV_DEVERR_* mask is stored.

@@ -21,6 +21,11 @@ from .binding import (  # noqa: F401
     kv_decode_step_plan,
     kv_decode_step_workspace_size,
     kv_dropped_mass,
+    kv_entmax_decode_attn,
+    kv_entmax_decode_step,
+    kv_entmax_decode_step_workspace_size,
+    kv_entmax_page_moments,
+    kv_entmax_select,
     kv_dropped_mass_workspace_size,
     kv_merge_splits,
     kv_score_pages,

@@ -39,7 +39,9 @@ EXPORTS = (
     "kv_selftest_wait_timeout", "kv_decode_step_static", "kv_append_token",
     "kv_select_structured", "kv_select_decode_attn", "kv_score_select",
     "kv_decode_attn_merge", "kv_decode_step_plan", "kv_build_page_stats_fp8",
-    "kv_score_pages_fp8", "kv_decode_step_fp8",
+    "kv_score_pages_fp8", "kv_decode_step_fp8", "kv_entmax_page_moments", "kv_entmax_select",
+    "kv_entmax_attn_workspace_size", "kv_entmax_decode_attn",
+    "kv_entmax_decode_step_workspace_size", "kv_entmax_decode_step",
 )
 
 
@@ -101,6 +103,12 @@ def _declare(lib):
         "kv_build_page_stats_fp8": (I32, [D, P, P, P]),
         "kv_score_pages_fp8": (I32, [D, P, I32, P, P, P, I32, P]),
         "kv_decode_step_fp8": (I32, [D, P, I32, F32, P, P, F64, I32, I32, I32, P, P, P, SZ, P]),
+        "kv_entmax_page_moments": (I32, [D, P, I32, P, F32, P, P, P, I32, P]),
+        "kv_entmax_select": (I32, [P, P, P, I32, P, I32, I32, I32, I32, I32, P, P, P, P]),
+        "kv_entmax_attn_workspace_size": (SZ, [D, I32, I32]),
+        "kv_entmax_decode_attn": (I32, [D, P, I32, F32, P, P, I32, P, P, P, SZ, P]),
+        "kv_entmax_decode_step_workspace_size": (SZ, [D, I32, I32]),
+        "kv_entmax_decode_step": (I32, [D, P, I32, F32, P, I32, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -576,6 +584,81 @@ def kv_decode_step_fp8(kv: PagedKV, q, sm_scale: float, stats=None, stats_exp=No
         float(keep_ratio), int(budget_pages), int(k_max), int(num_splits), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
+
+
+def kv_entmax_page_moments(kv: PagedKV, q, stats, sm_scale: float, stream=None):
+    """(zb, cz, vz), each [B][Hq][stride] float32: per-head page bound, centre and variance
+    of z = sm_scale * q.k / 2."""
+    _need(q, "q", kv.dtype)
+    B, Hq, _ = q.shape
+    zb, cz, vz = (torch.full((B, Hq, kv.stride), float("nan"), dtype=torch.float32,
+                             device=q.device) for _ in range(3))
+    _check("kv_entmax_page_moments", lib().kv_entmax_page_moments(
+        kv.ref(), _ptr(q), Hq, _ptr(stats), float(sm_scale), _ptr(zb), _ptr(cz), _ptr(vz),
+        kv.stride, _stream(stream)))
+    return zb, cz, vz
+
+
+def kv_entmax_select(zb, cz, vz, seq_lens, page_size: int, num_kv_heads: int,
+                     k_max: int | None = None, stream=None):
+    """Gaussian-aware entmax page selection: (sel_idx, sel_cnt, tau_hat)."""
+    for t, n in ((zb, "zb"), (cz, "cz"), (vz, "vz")):
+        _need(t, n, torch.float32)
+    B, Hq, stride = zb.shape
+    if k_max is None:
+        k_max = stride
+    dev = zb.device
+    sel = torch.empty((B, num_kv_heads, k_max), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, num_kv_heads), dtype=torch.int32, device=dev)
+    tau = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _check("kv_entmax_select", lib().kv_entmax_select(
+        _ptr(zb), _ptr(cz), _ptr(vz), stride, _ptr(seq_lens), int(page_size), B, Hq,
+        int(num_kv_heads), int(k_max), _ptr(sel), _ptr(cnt), _ptr(tau), _stream(stream)))
+    return sel, cnt, tau
+
+
+def kv_entmax_decode_attn(kv: PagedKV, q, sm_scale: float, sel_idx=None, sel_cnt=None,
+                          out=None, tau=None, workspace=None, stream=None):
+    """1.5-entmax attention over the selected pages (sel_idx=None: every page): (out, tau)."""
+    _need(q, "q", kv.dtype)
+    B, Hq, D = q.shape
+    sel_stride = sel_idx.shape[-1] if sel_idx is not None else 0
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if tau is None:
+        tau = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = int(lib().kv_entmax_attn_workspace_size(kv.ref(), Hq, sel_stride))
+        workspace = torch.empty((n,), dtype=torch.uint8, device=q.device)
+    _check("kv_entmax_decode_attn", lib().kv_entmax_decode_attn(
+        kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(sel_idx), _ptr(sel_cnt), sel_stride,
+        _ptr(out), _ptr(tau), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, tau
+
+
+def kv_entmax_decode_step_workspace_size(kv: PagedKV, num_q_heads: int, k_max: int) -> int:
+    return int(lib().kv_entmax_decode_step_workspace_size(kv.ref(), int(num_q_heads),
+                                                          int(k_max)))
+
+
+def kv_entmax_decode_step(kv: PagedKV, q, sm_scale: float, stats, k_max: int | None = None,
+                          out=None, tau=None, workspace=None, stream=None):
+    """Moments, Gaussian-aware selection and entmax attention in one call: (out, tau)."""
+    _need(q, "q", kv.dtype)
+    B, Hq, D = q.shape
+    if k_max is None:
+        k_max = kv.stride
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if tau is None:
+        tau = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty((kv_entmax_decode_step_workspace_size(kv, Hq, k_max),),
+                                dtype=torch.uint8, device=q.device)
+    _check("kv_entmax_decode_step", lib().kv_entmax_decode_step(
+        kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(stats), int(k_max), _ptr(out), _ptr(tau),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, tau
 
 
 def kv_check_device_errors(stream=None):

@@ -721,6 +721,165 @@ kv_status kv_decode_step_fp8(const kv_cache_desc* cache, const void* q, int32_t 
                           stream);
 }
 
+// ------------------------------------------------------------------------- entmax (f4)
+
+kv_status kv_entmax_page_moments(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                 const void* stats, float sm_scale, float* zb, float* cz,
+                                 float* vz, int32_t stride, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (stats == nullptr || zb == nullptr || cz == nullptr || vz == nullptr ||
+      stride < cache->page_table_stride || !(sm_scale > 0.f) || !isfinite(sm_scale))
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  return from_cuda(launch_entmax_moments(*cache, num_q_heads / cache->num_kv_heads, q, stats,
+                                         sm_scale, zb, cz, vz, stride, ctx, stream));
+}
+
+kv_status kv_entmax_select(const float* zb, const float* cz, const float* vz, int32_t stride,
+                           const int32_t* seq_lens, int32_t page_size, int32_t batch,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t k_max,
+                           int32_t* sel_idx, int32_t* sel_cnt, float* tau_hat,
+                           cudaStream_t stream) {
+  if (zb == nullptr || cz == nullptr || vz == nullptr || seq_lens == nullptr ||
+      sel_idx == nullptr || sel_cnt == nullptr)
+    return KV_ERR_INVALID_ARG;
+  if (stride <= 0 || page_size <= 0 || batch <= 0 || batch > 65535 || num_kv_heads <= 0 ||
+      num_kv_heads > 65535 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || k_max <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 8) return KV_ERR_UNSUPPORTED;
+  if ((long long)stride * page_size > INT32_MAX) return KV_ERR_INVALID_ARG;
+  DevCtx ctx;
+  kv_status r = ctx_for_call(&ctx);
+  if (r != KV_OK) return r;
+  return from_cuda(launch_entmax_select(seq_lens, page_size, batch, num_q_heads, num_kv_heads,
+                                        stride, zb, cz, vz, stride, k_max, sel_idx, sel_cnt,
+                                        tau_hat, ctx, stream));
+}
+
+size_t kv_entmax_attn_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
+                                     int32_t sel_stride) {
+  if (cache == nullptr || cache->batch <= 0 || num_q_heads <= 0 || cache->page_size <= 0)
+    return 0;
+  const long long pages = sel_stride > 0 ? sel_stride : cache->page_table_stride;
+  const size_t slots = (size_t)cache->batch * num_q_heads * pages * cache->page_size;
+  const size_t splits = (size_t)cache->batch * num_q_heads * entmax_max_splits();
+  return 3 * round256(slots * 4) + 2 * round256(splits * 4);
+}
+
+}  // extern "C"
+
+namespace {
+
+int entmax_splits(const kv_cache_desc* cache, int pages, const DeviceState* st) {
+  const long groups = (long)cache->batch * cache->num_kv_heads;
+  long S = (4L * st->sms + groups - 1) / groups;
+  const long cap = pages / 4 > 1 ? pages / 4 : 1;
+  if (S > cap) S = cap;
+  if (S > entmax_max_splits()) S = entmax_max_splits();
+  return S < 1 ? 1 : (int)S;
+}
+
+// Carves the entmax attention scratch (kv_entmax_attn_workspace_size's layout).
+EntmaxScratch entmax_scratch(void* base, const kv_cache_desc* cache, int Hq, int pages) {
+  const size_t slots = (size_t)cache->batch * Hq * pages * cache->page_size;
+  const size_t splits = (size_t)cache->batch * Hq * entmax_max_splits();
+  char* p = static_cast<char*>(base);
+  EntmaxScratch w;
+  w.logits = reinterpret_cast<float*>(p);
+  w.cand_z = reinterpret_cast<float*>(p + round256(slots * 4));
+  w.cand_slot = reinterpret_cast<int*>(p + 2 * round256(slots * 4));
+  w.split_max = reinterpret_cast<float*>(p + 3 * round256(slots * 4));
+  w.split_cnt = reinterpret_cast<int*>(p + 3 * round256(slots * 4) + round256(splits * 4));
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status kv_entmax_decode_attn(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,
+                                int32_t sel_stride, float* out, float* tau, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (out == nullptr || !(sm_scale > 0.f) || !isfinite(sm_scale)) return KV_ERR_INVALID_ARG;
+  if (sel_idx != nullptr && (sel_cnt == nullptr || sel_stride <= 0)) return KV_ERR_INVALID_ARG;
+  const int stride = sel_idx != nullptr ? sel_stride : cache->page_table_stride;
+  if ((long long)stride * cache->page_size > INT32_MAX) return KV_ERR_INVALID_ARG;
+  if (workspace == nullptr ||
+      workspace_bytes < kv_entmax_attn_workspace_size(cache, num_q_heads,
+                                                      sel_idx != nullptr ? sel_stride : 0))
+    return KV_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KV_ERR_MISALIGNED;
+  DevCtx ctx;
+  DeviceState* st = nullptr;
+  if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
+  return from_cuda(launch_entmax_attn(*cache, num_q_heads / cache->num_kv_heads, q, sm_scale,
+                                      sel_idx, sel_cnt, sel_idx != nullptr ? sel_stride : 0,
+                                      entmax_splits(cache, stride, st),
+                                      entmax_scratch(workspace, cache, num_q_heads, stride),
+                                      stride * cache->page_size, out, tau, ctx, stream));
+}
+
+size_t kv_entmax_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
+                                            int32_t k_max) {
+  if (cache == nullptr || cache->batch <= 0 || num_q_heads <= 0 || cache->num_kv_heads <= 0 ||
+      cache->page_table_stride <= 0 || k_max <= 0)
+    return 0;
+  const size_t B = cache->batch, Hq = num_q_heads, Hkv = cache->num_kv_heads;
+  return 3 * round256(B * Hq * cache->page_table_stride * sizeof(float)) +
+         round256(B * Hkv * k_max * sizeof(int32_t)) + round256(B * Hkv * sizeof(int32_t)) +
+         kv_entmax_attn_workspace_size(cache, num_q_heads, k_max);
+}
+
+kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
+                                float sm_scale, const void* stats, int32_t k_max, float* out,
+                                float* tau, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  kv_status r = check_desc(cache);
+  if (r != KV_OK) return r;
+  if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (stats == nullptr || out == nullptr || k_max <= 0 || !(sm_scale > 0.f) ||
+      !isfinite(sm_scale))
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(stats)) return KV_ERR_MISALIGNED;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < kv_entmax_decode_step_workspace_size(cache, num_q_heads, k_max))
+    return KV_ERR_WORKSPACE;
+  DevCtx ctx;
+  DeviceState* st = nullptr;
+  if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
+  const size_t B = cache->batch, Hq = num_q_heads, Hkv = cache->num_kv_heads;
+  const int stride = cache->page_table_stride;
+  const size_t mom = round256(B * Hq * stride * sizeof(float));
+  char* ws = static_cast<char*>(workspace);
+  float* zb = reinterpret_cast<float*>(ws);
+  float* cz = reinterpret_cast<float*>(ws + mom);
+  float* vz = reinterpret_cast<float*>(ws + 2 * mom);
+  int32_t* sel = reinterpret_cast<int32_t*>(ws + 3 * mom);
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws + 3 * mom + round256(B * Hkv * k_max * 4));
+  float* logits = reinterpret_cast<float*>(ws + 3 * mom + round256(B * Hkv * k_max * 4) +
+                                           round256(B * Hkv * 4));
+  const int G = num_q_heads / cache->num_kv_heads;
+  cudaError_t e = launch_entmax_moments(*cache, G, q, stats, sm_scale, zb, cz, vz, stride, ctx,
+                                        stream);
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  e = launch_entmax_select(cache->seq_lens, cache->page_size, cache->batch, num_q_heads,
+                           cache->num_kv_heads, stride, zb, cz, vz, stride, k_max, sel, cnt,
+                           nullptr, ctx, stream);
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  return from_cuda(launch_entmax_attn(*cache, G, q, sm_scale, sel, cnt, k_max,
+                                      entmax_splits(cache, k_max, st),
+                                      entmax_scratch(logits, cache, num_q_heads, k_max),
+                                      k_max * cache->page_size, out, tau, ctx, stream));
+}
+
 kv_status kv_check_device_errors(cudaStream_t stream, int32_t* flags) {
   DeviceState* st = nullptr;
   kv_status r = device_state(&st);

@@ -210,6 +210,30 @@ __device__ __forceinline__ int checked_len(const DevCtx& c, const kv_cache_desc&
 // int8 exponent per (page, KV head) in stats_exp (fp8_stats.cuh).
 cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, int8_t* stats_exp,
                               DevCtx ctx, cudaStream_t s);
+// Entmax decoding (entmax.cu). Moments: zb/cz/vz [B][Hq][stride]. Selection: one block per
+// group writes the kept pages ascending. Attention: logits [B][Hq][cap_slots] scratch, then
+// out [B][Hq][D] and tau [B][Hq] (in z = logit/2 units).
+cudaError_t launch_entmax_moments(const kv_cache_desc& d, int G, const void* q,
+                                  const void* stats, float scale, float* zb, float* cz,
+                                  float* vz, int stride, DevCtx ctx, cudaStream_t s);
+cudaError_t launch_entmax_select(const int32_t* seq_lens, int page_size, int batch, int Hq,
+                                 int Hkv, int table_stride, const float* zb, const float* cz,
+                                 const float* vz, int stride, int k_max, int32_t* sel_idx,
+                                 int32_t* sel_cnt, float* tau_hat, DevCtx ctx, cudaStream_t s);
+// Entmax attention scratch: logits, candidate z and slot ([B][Hq][cap_slots] each), and per
+// split the largest logit and the candidate count ([B][Hq][entmax_max_splits()] each).
+struct EntmaxScratch {
+  float* logits;
+  float* cand_z;
+  int* cand_slot;
+  float* split_max;
+  int* split_cnt;
+};
+int entmax_max_splits();
+cudaError_t launch_entmax_attn(const kv_cache_desc& d, int G, const void* q, float scale,
+                               const int32_t* sel, const int32_t* cnt, int sel_stride, int S,
+                               const EntmaxScratch& w, int cap_slots, float* out, float* tau,
+                               DevCtx ctx, cudaStream_t s);
 cudaError_t launch_score_pages(const kv_cache_desc& d, const void* q, int Hq,
                                const void* stats, const int8_t* stats_exp, float* scores,
                                int scores_stride, DevCtx ctx, cudaStream_t s);

@@ -1,0 +1,208 @@
+"""Entmax decoding (1.5-entmax over selected pages, Gaussian-aware selector) through the C ABI,
+against the float64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import entmax as E
+import sparse_kv_cache_build_gb300 as skv
+from sparse_kv_cache_build_gb300 import inputs
+
+from gpu_helpers import assert_no_device_error, f64, need_gpu, out_tol, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+    torch.cuda.set_device(0)
+
+
+SHAPES = [("bf16", 128, 4, 16), ("bf16", 128, 8, 64), ("bf16", 64, 1, 32), ("fp32", 64, 4, 16),
+          ("fp32", 128, 2, 32)]
+
+
+def make(dtype, D, G, PS, lens=(1000, 2049, 37), seed=31, Hkv=2, planted=4):
+    w = workload(num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, page_size=PS, dtype=dtype,
+                 seed=seed, seq_lens=lens, planted=planted)
+    return w, inputs.make_cache(w, "cuda", extra_phys_pages=3)
+
+
+def host(c):
+    return (f64(c.q), f64(c.k_pool), f64(c.v_pool), c.page_table.cpu().numpy(),
+            c.seq_lens.cpu().numpy())
+
+
+@pytest.mark.parametrize("dtype,D,G,PS", SHAPES)
+def test_page_moments_match_oracle(dtype, D, G, PS):
+    w, c = make(dtype, D, G, PS)
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    zb, cz, vz = (f64(t) for t in skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale))
+    assert_no_device_error()
+    q, K, V, table, lens = host(c)
+    mn, mx = oracle.page_stats(K, table, lens, PS)
+    rzb, rc, rv, _ = E.page_moments(q, mn, mx, table, lens, PS, w.sm_scale)
+    for b in range(w.batch):
+        n = rzb[b].shape[1]
+        for got, ref in ((zb, rzb), (cz, rc), (vz, rv)):
+            scale = np.abs(ref[b]).max() + 1e-3
+            assert np.abs(got[b, :, :n] - ref[b]).max() <= 2e-6 * scale
+        assert np.isnan(zb[b, :, n:]).all()
+
+
+@pytest.mark.parametrize("dtype,D,G,PS", SHAPES)
+def test_select_is_the_oracle_rule_on_gpu_moments(dtype, D, G, PS):
+    w, c = make(dtype, D, G, PS, lens=(1000, 2049, 37, 0, 5))
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    zb, cz, vz = skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale)
+    sel, cnt, tau_hat = skv.kv_entmax_select(zb, cz, vz, c.seq_lens, PS, w.num_kv_heads)
+    assert_no_device_error()
+    sel, cnt, tau_hat = sel.cpu().numpy(), cnt.cpu().numpy(), f64(tau_hat)
+    zb, cz, vz = f64(zb), f64(cz), f64(vz)
+    lens = c.seq_lens.cpu().numpy()
+    for b in range(w.batch):
+        n = oracle.num_pages(int(lens[b]), PS)
+        if n == 0:
+            assert (cnt[b] == 0).all() and np.isnan(tau_hat[b]).all()
+            continue
+        nt = np.array([oracle.valid_tokens(int(lens[b]), PS, p) for p in range(n)], dtype=float)
+        ref_sel, ref_tau = E.entmax_select(zb[b, :, :n], cz[b, :, :n], vz[b, :, :n], nt, G)
+        # the GPU estimates in float (the oracle in float64): agreement to float level
+        np.testing.assert_allclose(tau_hat[b], ref_tau, rtol=2e-5, atol=2e-5)
+        for g in range(w.num_kv_heads):
+            got = set(sel[b, g, : cnt[b, g]].tolist())
+            want = set(ref_sel[g].tolist())
+            assert (np.diff(sel[b, g, : cnt[b, g]]) > 0).all()
+            # decisions may differ only for pages whose bound is within the band of tau_hat
+            heads = range(g * G, (g + 1) * G)
+            band = {p for p in range(n) for h in heads
+                    if abs(zb[b, h, p] - ref_tau[h]) <= 2e-5 * (abs(ref_tau[h]) + 1.0)}
+            assert got ^ want <= band, (got ^ want, band)
+
+
+@pytest.mark.parametrize("dtype,D,G,PS", SHAPES)
+@pytest.mark.parametrize("sparse", [True, False], ids=["selected", "dense"])
+def test_entmax_attention_matches_oracle(dtype, D, G, PS, sparse):
+    w, c = make(dtype, D, G, PS, lens=(1000, 2049, 37, 0, 1))
+    kv = skv.PagedKV.from_cache(c)
+    sel = cnt = None
+    if sparse:
+        stats = skv.kv_build_page_stats(kv)
+        zb, cz, vz = skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale)
+        sel, cnt, _ = skv.kv_entmax_select(zb, cz, vz, c.seq_lens, PS, w.num_kv_heads)
+    outs = [skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, sel, cnt) for _ in range(2)]
+    assert_no_device_error()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1].nan_to_num(7.0), outs[1][1].nan_to_num(7.0))   # NaN: empty
+    out, tau = f64(outs[0][0]), f64(outs[0][1])
+    q, K, V, table, lens = host(c)
+    chosen = None
+    if sparse:
+        s_, n_ = sel.cpu().numpy(), cnt.cpu().numpy()
+        chosen = [[s_[b, g, : n_[b, g]] for g in range(w.num_kv_heads)] for b in range(w.batch)]
+    ref, ref_tau = E.entmax_attend(q, K, V, table, lens, PS, w.sm_scale, selected=chosen)
+    for b in range(w.batch):
+        if lens[b] == 0:
+            assert (out[b] == 0).all() and np.isnan(tau[b]).all()
+            continue
+        assert np.abs(out[b] - ref[b]).max() < out_tol(w)
+        assert np.abs(tau[b] - ref_tau[b]).max() < (1e-4 if dtype == "bf16" else 1e-5)
+
+
+def test_selected_support_makes_sparse_entmax_exact():
+    """The pages holding the dense entmax support (found by the oracle), plus unrelated
+    pages, give the dense output: sparse entmax is exact once the support is selected."""
+    w, c = make("bf16", 128, 4, 16, lens=(3000, 1600), seed=41, planted=16)
+    q, K, V, table, lens = host(c)
+    scale = w.sm_scale
+    _, tau_all = E.entmax_attend(q, K, V, table, lens, 16, scale)
+    B, Hkv, G = w.batch, w.num_kv_heads, w.group_size
+    rng = np.random.default_rng(0)
+    chosen = []
+    for b in range(B):
+        n = oracle.num_pages(int(lens[b]), 16)
+        row = []
+        for g in range(Hkv):
+            keep = set(rng.choice(n, 5, replace=False).tolist())
+            for h in range(g * G, (g + 1) * G):
+                for p in range(n):
+                    toks = K[table[b][p], g, :oracle.valid_tokens(int(lens[b]), 16, p)]
+                    if (scale * toks @ q[b, h] / 2 > tau_all[b, h]).any():
+                        keep.add(p)
+            row.append(np.array(sorted(keep), dtype=np.int32))
+        chosen.append(row)
+    k_max = max(len(r) for row in chosen for r in row)
+    sel = np.zeros((B, Hkv, k_max), dtype=np.int32)
+    cnt = np.zeros((B, Hkv), dtype=np.int32)
+    for b in range(B):
+        for g in range(Hkv):
+            sel[b, g, : len(chosen[b][g])] = chosen[b][g]
+            cnt[b, g] = len(chosen[b][g])
+    assert cnt.max() < oracle.num_pages(int(lens.max()), 16)      # a real subset
+    out, tau = skv.kv_entmax_decode_attn(kv := skv.PagedKV.from_cache(c), c.q, scale,
+                                         torch.from_numpy(sel).cuda(), torch.from_numpy(cnt).cuda())
+    dense, dtau = skv.kv_entmax_decode_attn(kv, c.q, scale)
+    assert_no_device_error()
+    np.testing.assert_allclose(f64(out), f64(dense), rtol=0, atol=2e-6)
+    np.testing.assert_allclose(f64(tau), f64(dtau), rtol=0, atol=2e-6)
+
+
+def test_selector_adapts_to_gaussian_scores():
+    """Keys whose page means vary widely with tight pages (the regime of the Gaussian reading):
+    the one-call step keeps a strict subset of pages, the same set kv_entmax_select gives, and
+    its output is entmax over that set."""
+    w, c = make("bf16", 128, 4, 16, lens=(4000, 2500), seed=43, planted=0)
+    g_ = torch.Generator(device="cuda").manual_seed(43)
+    NP, Hkv, PS, D = c.k_pool.shape
+    page_mean = torch.randn((NP, Hkv, 1, D), generator=g_, device="cuda")
+    k = page_mean + 0.02 * torch.randn((NP, Hkv, PS, D), generator=g_, device="cuda")
+    c.k_pool.copy_(k.to(c.k_pool.dtype))
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    k_max = kv.stride
+    ws = torch.empty((skv.kv_entmax_decode_step_workspace_size(kv, w.num_q_heads, k_max),),
+                     dtype=torch.uint8, device="cuda")
+    out, tau = skv.kv_entmax_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, workspace=ws)
+    zb, cz, vz = skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale)
+    sel, cnt, _ = skv.kv_entmax_select(zb, cz, vz, c.seq_lens, 16, Hkv, k_max=k_max)
+    out2, tau2 = skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, sel, cnt)
+    assert_no_device_error()
+    assert torch.equal(out, out2) and torch.equal(tau, tau2)
+    B, Hq = w.batch, w.num_q_heads
+    cnt_h = cnt.cpu().numpy()
+    for b in range(B):
+        n = oracle.num_pages(int(c.seq_lens[b]), 16)
+        assert (cnt_h[b] > 0).all() and (cnt_h[b] < n // 2).all(), cnt_h[b]
+    q, K, V, table, lens = host(c)
+    s_ = sel.cpu().numpy()
+    chosen = [[s_[b, g, : cnt_h[b, g]] for g in range(Hkv)] for b in range(B)]
+    ref, ref_tau = E.entmax_attend(q, K, V, table, lens, 16, w.sm_scale, selected=chosen)
+    assert np.abs(f64(out) - ref).max() < 2e-3
+    delta = E.entmax_dropped_mass(q, K, table, lens, 16, w.sm_scale, chosen)
+    print(f"kept {cnt_h.sum()} of {sum(oracle.num_pages(int(x), 16) for x in lens) * Hkv} "
+          f"pages, entmax dropped mass max {delta.max():.3g} mean {delta.mean():.3g}")
+
+
+def test_flat_logits_take_the_global_candidate_path():
+    """A zero query ties every logit: every token is a candidate (more than the shared-memory
+    buffer holds) and entmax is uniform: out = mean of V, tau = -1/sqrt(n)."""
+    w, c = make("bf16", 128, 4, 16, lens=(20000 + 7,), seed=44, planted=0)
+    kv = skv.PagedKV.from_cache(c)
+    q0 = torch.zeros_like(c.q)
+    out, tau = skv.kv_entmax_decode_attn(kv, q0, w.sm_scale)
+    assert_no_device_error()
+    n = 20007
+    q, K, V, table, lens = host(c)
+    for g in range(w.num_kv_heads):
+        Vt = oracle.gather_tokens(V, table, n, 16, 0, g, range(oracle.num_pages(n, 16)))
+        mean = Vt.mean(axis=0)
+        for h in range(g * w.group_size, (g + 1) * w.group_size):
+            assert np.abs(f64(out)[0, h] - mean).max() < 1e-5
+            assert f64(tau)[0, h] == pytest.approx(-1 / math.sqrt(n), abs=1e-6)
