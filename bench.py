@@ -48,6 +48,17 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of each rank's values over the process group (any backend);
+    the values themselves when there is one rank. Every rank gets the result."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -532,11 +543,7 @@ def run_ours(args):
     # ---- max over ranks ------------------------------------------------------------------
     sparse_med = statistics.median(step_us)
     mean_us = sum(step_us) / len(step_us)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([mean_us, sparse_med], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_us, sparse_med = float(tt[0]), float(tt[1])
+    mean_us, sparse_med = max_over_ranks([mean_us, sparse_med], world, dev)
     if rank != 0:
         return None
 
