@@ -272,7 +272,7 @@ kv_status kv_score_select(const kv_cache_desc* cache, const void* q, int32_t num
  * counters: device [batch][num_kv_heads] int32, zero before the first call; every call
  * returns them to zero. part_acc must be 16-byte and part_ml 8-byte aligned
  * (KV_ERR_MISALIGNED). num_splits is bounded by the merge's on-chip buffer
- * (KV_ERR_UNSUPPORTED above it; over 1000 splits for every supported shape).
+ * (KV_ERR_UNSUPPORTED above it; over 700 splits for every supported shape).
  */
 kv_status kv_decode_attn_merge(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                                float sm_scale, const int32_t* sel_idx, const int32_t* sel_cnt,

@@ -121,7 +121,7 @@ void step_attn_limits_bf16(int head_dim, int G, int* max_select_pages, int* max_
   SKV_LIM_CASE(128, 1) SKV_LIM_CASE(128, 2) SKV_LIM_CASE(128, 4) SKV_LIM_CASE(128, 8)
 #undef SKV_LIM_CASE
   *max_select_pages = sel;
-  *max_splits = G > 0 ? (ring / 4 - 2 * G) / G : 0;   // merge weights [G][S] in the ring
+  *max_splits = G > 0 ? (ring / 4 - 2 * G) / (2 * G) : 0;   // merge: [G][S] weights and l
 }
 
 size_t split_attn_smem_bf16(int head_dim, int G) {

@@ -507,51 +507,59 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   // ---- the group's last CTA merges its S partials (log-sum-exp) -------------------------
   __syncthreads();                                         // this CTA's partials are written
   if (tid == 0) {
-    __threadfence();
+    __threadfence();                                       // release: the partials first
     const int done = atomicAdd(&sa.counters[grp], 1);
+    __threadfence();                                       // acquire: the others' partials
     misc[3] = (done == S - 1) ? 1u : 0u;
   }
-  __syncthreads();
+  __syncthreads();                                         // orders every thread after it
   if (misc[3] == 0u) return;
-  __threadfence();
-  float* wts = reinterpret_cast<float*>(smem + C::OFF_STAGES);   // [G][S], then M[G], L[G]
-  float* Ms = wts + G * S;
+  float* wts = reinterpret_cast<float*>(smem + C::OFF_STAGES);   // [G][S] weights, M[G],
+  float* Ms = wts + G * S;                                        // L[G], l values [G][S]
   float* Ls = Ms + G;
+  float* lv = Ls + G;
   const int warp = tid >> 5, lane = tid & 31;
-  for (int hl = warp; hl < G; hl += C::THREADS / 32) {
-    // one pass over the (m, l) pairs: running max and rescaled sum per lane, then the warp's
-    const float2* ml = reinterpret_cast<const float2*>(part_ml) + ((long)b * Hq + g * G + hl) * S;
-    float M = -INFINITY, L = 0.f;
-    for (int x0 = lane; x0 < S; x0 += 64) {            // two loads in flight per lane
-      float2 v[2];
+  // The first splits' partial sums of this thread's first output columns do not depend on the
+  // weights: their loads go out now and land while the weights are computed.
+  constexpr int D4 = D / 4;
+  constexpr int PB = 24;
+  float4 pre[PB];
+  if (tid < G * D4) {
+    const int hl = tid / D4, d4 = tid - hl * D4;
+    const float4* a = reinterpret_cast<const float4*>(part_acc + ((long)b * Hq + g * G + hl) * S * D) + d4;
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-        v[u] = x0 + 32 * u < S ? __ldcg(ml + x0 + 32 * u) : make_float2(-INFINITY, 0.f);
+    for (int u = 0; u < PB; ++u)
+      pre[u] = u < S ? __ldcg(a + (long)u * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int hl = warp; hl < G; hl += C::THREADS / 32) {
+    // the (m, l) pairs, two per lane in flight; M = max m by shuffles alone, then one
+    // exponential per split and a plain sum (a short dependency chain)
+    const float2* ml = reinterpret_cast<const float2*>(part_ml) + ((long)b * Hq + g * G + hl) * S;
+    float M = -INFINITY;
+    for (int x0 = lane; x0 < S; x0 += 64) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        if (x0 + 32 * u < S) wts[hl * S + x0 + 32 * u] = v[u].x;
-        if (v[u].x != -INFINITY) {
-          if (v[u].x > M) {
-            L = (M == -INFINITY) ? 0.f : L * expf(M - v[u].x);
-            M = v[u].x;
-          }
-          L = fmaf(v[u].y, expf(v[u].x - M), L);
+        const int x = x0 + 32 * u;
+        if (x < S) {
+          const float2 v = __ldcg(ml + x);
+          wts[hl * S + x] = v.x;                          // m for now, the weight below
+          lv[hl * S + x] = v.y;
+          M = fmaxf(M, v.x);
         }
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
-      const float L2 = __shfl_xor_sync(0xffffffffu, L, o);
-      const float Mn = fmaxf(M, M2);
-      L = (M == -INFINITY ? 0.f : L * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : L2 * expf(M2 - Mn));
-      M = Mn;
-    }
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     __syncwarp();
+    float L = 0.f;
     for (int x = lane; x < S; x += 32) {
       const float m = wts[hl * S + x];
-      wts[hl * S + x] = (m == -INFINITY || M == -INFINITY) ? 0.f : expf(m - M);
+      const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : expf(m - M);
+      wts[hl * S + x] = w;
+      L = fmaf(lv[hl * S + x], w, L);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     if (lane == 0) {
       Ms[hl] = M;
       Ls[hl] = L;
@@ -559,14 +567,27 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   }
   __syncthreads();
   // out = sum_s w_s acc_s / L, four columns per thread, sixteen splits' loads in flight
-  constexpr int D4 = D / 4;
   for (int o = tid; o < G * D4; o += C::THREADS) {
     const int hl = o / D4, d4 = o - hl * D4;
     const long row = (long)b * Hq + g * G + hl;
     const float4* a = reinterpret_cast<const float4*>(part_acc + row * S * D) + d4;
     const float* w = wts + hl * S;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int x = 0; x < S; x += 16) {                  // no serial remainder: guarded lanes
+    int x0 = 0;
+    if (o == tid) {                                    // the prefetched first splits
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        if (u < S) {
+          const float ww = w[u];
+          A.x = fmaf(pre[u].x, ww, A.x);
+          A.y = fmaf(pre[u].y, ww, A.y);
+          A.z = fmaf(pre[u].z, ww, A.z);
+          A.w = fmaf(pre[u].w, ww, A.w);
+        }
+      }
+      x0 = PB;
+    }
+    for (int x = x0; x < S; x += 16) {                 // no serial remainder: guarded lanes
       float4 v[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u)

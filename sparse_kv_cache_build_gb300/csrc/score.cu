@@ -190,12 +190,12 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   const int blocks = ceil_div(n_pages, kSelWarps * rows_per_warp<F8>());
   __syncthreads();                            // this block's scores are written
   if (tid == 0) {
-    __threadfence();
+    __threadfence();                          // release: this block's scores first
     s_last = atomicAdd(&counters[grp], 1) == blocks - 1;
+    __threadfence();                          // acquire: the other blocks' scores
   }
-  __syncthreads();
+  __syncthreads();                            // orders every thread after it
   if (!s_last) return;
-  __threadfence();
   if (tid == 0) counters[grp] = 0;            // ready for the next step
   int k = keep_rule(n_pages, nullptr, b, keep_ratio, budget);
   if (k > k_max) {
