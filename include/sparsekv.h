@@ -290,8 +290,8 @@ kv_status kv_decode_attn_merge(const kv_cache_desc* cache, const void* q, int32_
  * the same kernel. counters: device [batch][num_kv_heads] int32, zero before the first call;
  * every call returns them to zero. sel_idx [batch][num_kv_heads][k_max] and sel_cnt
  * [batch][num_kv_heads] receive the selection when not NULL (sparse calls only). The group's
- * pages must fit the in-kernel selection (page_table_stride at most 24448 pages for
- * head_dim 128, 12160 for 64) and the splits its merge; otherwise KV_ERR_UNSUPPORTED.
+ * pages must fit the in-kernel selection (page_table_stride at most 23552 pages for
+ * head_dim 128, 11264 for 64) and the splits its merge; otherwise KV_ERR_UNSUPPORTED.
  * part_acc must be 16-byte and part_ml 8-byte aligned (KV_ERR_MISALIGNED).
  */
 kv_status kv_select_decode_attn(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
@@ -358,9 +358,9 @@ size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_
  * long as it is large enough). After a sparse call it holds the step's selection:
  * sel_idx [batch][num_kv_heads][k_max] int32 at byte offset
  * A = 2 * round256(batch * num_kv_heads * 4) + round256(batch * num_kv_heads *
- * page_table_stride * 4), and sel_cnt [batch][num_kv_heads] int32 at
- * A + round256(batch * num_kv_heads * k_max * 4), where round256(x) rounds x up to a
- * multiple of 256 (the layout kv_dropped_mass can be fed from).
+ * round4(page_table_stride) * 4), and sel_cnt [batch][num_kv_heads] int32 at
+ * A + round256(batch * num_kv_heads * k_max * 4), where round256(x) and round4(x) round x
+ * up to a multiple of 256 and of 4 (the layout kv_dropped_mass can be fed from).
  */
 kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
                          float sm_scale, const void* stats, double keep_ratio,

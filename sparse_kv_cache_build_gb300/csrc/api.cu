@@ -21,8 +21,9 @@ __device__ int32_t g_kv_error_word = 0;
 constexpr int kMaxDevices = 64;
 constexpr int kDroppedSplits = 64;          // page ranges per group in the dropped-mass probe
 // Longest group (pages) whose selection kv_decode_step leaves to the attention kernel's CTAs;
-// longer groups select once, in the score launch (measured crossover between 2048 and 8192).
-constexpr int kInAttnSelectPages = 4096;
+// longer groups select once, in the score launch (at 8192 pages the in-CTA selection, with
+// its rows copied in bulk, measured 75.9 us a step against 83-85 us for selecting once).
+constexpr int kInAttnSelectPages = 8192;
 
 struct DeviceState {
   bool ready = false;
@@ -129,13 +130,19 @@ struct StepLayout {
 // The per-group counters come first, at offsets that depend only on batch * num_kv_heads,
 // so calls of different shapes (sparse and dense, other k_max or split counts) on one
 // workspace keep finding them where the previous call returned them to zero.
+// Row stride of the step's scores: page_table_stride rounded up to four floats, so that every
+// row starts 16-byte aligned and can be copied into shared memory in bulk.
+size_t step_scores_stride(const kv_cache_desc* d) {
+  return ((size_t)d->page_table_stride + 3) & ~(size_t)3;
+}
+
 StepLayout step_layout(const kv_cache_desc* d, int Hq, int k_max, int S) {
   StepLayout L;
   const size_t groups = (size_t)d->batch * d->num_kv_heads;
   L.ctr = 0;
   L.ctr2 = L.ctr + round256(groups * sizeof(int32_t));
   L.scores = L.ctr2 + round256(groups * sizeof(int32_t));
-  L.sel = L.scores + round256(groups * d->page_table_stride * sizeof(float));
+  L.sel = L.scores + round256(groups * step_scores_stride(d) * sizeof(float));
   L.cnt = L.sel + round256(groups * (size_t)(k_max > 0 ? k_max : 1) * sizeof(int32_t));
   L.acc = L.cnt + round256(groups * sizeof(int32_t));
   L.ml = L.acc + round256((size_t)d->batch * Hq * S * d->head_dim * sizeof(float));
@@ -633,7 +640,7 @@ kv_status decode_step_impl(const kv_cache_desc* cache, const void* q, int32_t nu
       KV_OK)
     return r;
   const int G = num_q_heads / cache->num_kv_heads;
-  const int stride = cache->page_table_stride;
+  const int stride = (int)step_scores_stride(cache);     // of the scores rows
   const StepLayout L = step_layout(cache, num_q_heads, dense ? 1 : k_max, P.S);
   if (workspace_bytes < L.total) return KV_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -686,7 +693,7 @@ kv_status decode_step_impl(const kv_cache_desc* cache, const void* q, int32_t nu
     if (e != cudaSuccess) return KV_ERR_CUDA;
     e = launch_select_topk(scores, stride, cache->seq_lens, cache->page_size, cache->batch,
                            cache->num_kv_heads, nullptr, keep_ratio, budget_pages, k_max, 0, 0,
-                           sel, cnt, stride, ctx, stream);
+                           sel, cnt, cache->page_table_stride, ctx, stream);
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }
   e = launch_split_attn(*cache, q, num_q_heads, sm_scale, sel, cnt, dense ? 0 : k_max, P.S, acc,

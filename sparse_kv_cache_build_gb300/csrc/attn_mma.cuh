@@ -47,10 +47,12 @@ struct MmaCfg {
   static constexpr size_t OFF_MISC = OFF_HIST + 4 * 288;                // uint32 [16]
   static constexpr size_t OFF_WTOT = OFF_MISC + 64;                     // uint64 [8]
   static constexpr size_t OFF_BAR = OFF_WTOT + 64;
-  static constexpr size_t SMEM = OFF_BAR + 8 * NSTAGE + 1024;   // + alignment slack
-  // largest group whose keys fit the ring for the in-kernel selection
-  static constexpr int MAX_SELECT_PAGES =
-      (int)((NSTAGE * (size_t)STAGE_BYTES / 4) / THREADS - 1) * THREADS;
+  static constexpr size_t SMEM = OFF_BAR + 8 * (NSTAGE + 1) + 1024;   // + alignment slack
+  // the in-kernel selection keeps the group's keys (and, copied in bulk, its page-table
+  // row) in the ring, with at least SELECT_CAND_MIN words left for gathered candidates
+  static constexpr int RING_WORDS = (int)((size_t)NSTAGE * STAGE_BYTES / 4);
+  static constexpr int SELECT_CAND_MIN = 1024;
+  static constexpr int MAX_SELECT_PAGES = RING_WORDS - SELECT_CAND_MIN;
   // a CTA partial: acc [G][D], then m [G] (base 2), then l [G]
   static constexpr size_t PARTIAL_FLOATS = (size_t)G * (D + 2);
   static constexpr size_t MERGE_BYTES = 4 * (size_t)4 * G * (D + 2);
@@ -387,24 +389,41 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   const int Hkv = d.num_kv_heads, Hq = Hkv * G, PS = d.page_size;
   pdl_trigger();
   if (tid == 0) {
-    for (int i = 0; i < C::NSTAGE; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i <= C::NSTAGE; ++i) mbar_init(&bars[i], 1);   // stages + row copies
     fence_mbar_init();
   }
+  __syncthreads();                           // the barriers are initialised for every thread
   pdl_wait();
+  const long grp = (long)b * Hkv + g;
+  const int32_t* table = d.page_table + (long)b * d.page_table_stride;
+  uint32_t* ring = reinterpret_cast<uint32_t*>(smem + C::OFF_STAGES);
+  // Step mode: the group's score row, and where it fits beside it the page-table row
+  // (page_table_stride entries each, of which the first n_pages are used), are copied into
+  // the ring in bulk at once, before the sequence length is known, where the rows allow it.
+  const float* srow = sa.scores != nullptr ? sa.scores + grp * sa.scores_stride : nullptr;
+  const int KW = cta_key_words(d.page_table_stride);
+  const bool keys_bulk = srow != nullptr && KW + C::SELECT_CAND_MIN <= C::RING_WORDS &&
+                         cta_row_bulk_ok(srow, sa.scores_stride);
+  const bool table_bulk = keys_bulk && 2 * KW + C::SELECT_CAND_MIN <= C::RING_WORDS &&
+                          cta_row_bulk_ok(table, d.page_table_stride);
+  if (keys_bulk && tid == 0) {
+    mbar_arrive_expect_tx(&bars[C::NSTAGE], (table_bulk ? 8u : 4u) * (uint32_t)KW);
+    cta_bulk_copy(ring, srow, 4u * (uint32_t)KW, &bars[C::NSTAGE]);
+    if (table_bulk) cta_bulk_copy(ring + KW, table, 4u * (uint32_t)KW, &bars[C::NSTAGE]);
+  }
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, PS);
 
   // ---- this split's run of the page list ------------------------------------------------
-  const long grp = (long)b * Hkv + g;
-  const int32_t* table = d.page_table + (long)b * d.page_table_stride;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  const int32_t* tab = table;                // the page-table row, in global or shared memory
   // resolve logical page p (list position pos) into run slot i
   auto resolve = [&](int i, int p) {
     int P = -1, valid = 0;
     if (p < 0 || p >= n_pages) {
       flag(ctx, KV_DEVERR_BAD_SEL);
     } else {
-      P = table[p];
+      P = tab[p];
       if (P < 0 || P >= d.num_phys_pages) {
         flag(ctx, KV_DEVERR_BAD_PAGE);
         P = -1;
@@ -438,19 +457,27 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     np = kMaxSplitPages;
   }
   uint32_t qa0[C::KSTEPS], qa2[C::KSTEPS];
+  bool rows_waited = false;
   if (sa.scores != nullptr && cnt > 0 && cnt < n_pages && n_pages <= C::MAX_SELECT_PAGES) {
     // select this CTA's run from the group's scores (the ring is free until the first copy);
-    // the page-table row and q are fetched meanwhile
-    for (int j = tid; j * 32 < n_pages; j += C::THREADS) prefetch_l2(table + j * 32);
+    // q is fetched meanwhile
     load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
-    uint32_t* ring = reinterpret_cast<uint32_t*>(smem + C::OFF_STAGES);
-    constexpr int kRingWords = (int)((size_t)C::NSTAGE * C::STAGE_BYTES / 4);
-    const CtaKeys K = cta_load_keys<C::THREADS>(sa.scores + grp * sa.scores_stride, n_pages,
-                                                ring, misc + 8);
+    if (!table_bulk)
+      for (int j = tid; j * 32 < n_pages; j += C::THREADS) prefetch_l2(table + j * 32);
+    int used;
+    if (keys_bulk) {
+      if (!mbar_wait_bounded(&bars[C::NSTAGE], 0u, ctx.wait_ns) && tid == 0)
+        flag(ctx, KV_DEVERR_TIMEOUT);
+      rows_waited = true;
+      used = table_bulk ? 2 * KW : KW;
+    } else {
+      cta_fill_loads<C::THREADS>(ring, srow, n_pages);
+      used = cta_key_words(n_pages);
+    }
+    const CtaKeys K = cta_keys_finish<C::THREADS>(ring, n_pages, misc + 8);
     uint32_t T, take_eq;
-    const int used = C::THREADS * K.stride;
     cta_threshold<C::THREADS>(K, cnt, reinterpret_cast<uint32_t*>(smem + C::OFF_HIST), misc,
-                              ring + used, kRingWords - used, T, take_eq);
+                              ring + used, C::RING_WORDS - used, T, take_eq);
     int32_t* sel_out = (s == 0) ? sa.sel_out : nullptr;
     cta_compact<C::THREADS>(K, T, take_eq, reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT),
                             [&](int p, int pos) {
@@ -458,6 +485,7 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                               if (pos >= pos0 && pos < pos0 + np) s_phys[pos - pos0] = p;
                             });
     __syncthreads();
+    if (table_bulk) tab = reinterpret_cast<const int32_t*>(ring + KW);
     for (int i = tid; i < np; i += C::THREADS) resolve(i, s_phys[i]);
   } else {
     if (sa.scores != nullptr && cnt > 0 && cnt < n_pages) {   // group too long to select here
@@ -470,6 +498,9 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
       for (int i = tid; i < cnt; i += C::THREADS) sa.sel_out[grp * sa.k_max + i] = i;
     load_q_frags<D, G>(q, (long)b * Hq + g * G, qa0, qa2);
   }
+  if (keys_bulk && !rows_waited &&                // the ring is reused for the pages next
+      !mbar_wait_bounded(&bars[C::NSTAGE], 0u, ctx.wait_ns) && tid == 0)
+    flag(ctx, KV_DEVERR_TIMEOUT);
   __syncthreads();
 
   WarpAcc<D> acc;

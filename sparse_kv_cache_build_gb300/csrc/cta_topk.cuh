@@ -3,23 +3,29 @@
 // split CTA of the attention kernel can pick its own run of the selected list without a
 // separate launch. The scores of a group are small (4 B per page) and L2-resident after the
 // score pass, so each of the group's S CTAs redoing this work costs less than a kernel
-// boundary, provided the work is latency-lean:
+// boundary, provided the work is latency-lean. Measured on this part, what costs is the
+// number of dependent steps, not the arithmetic:
 //
-//   * keys are loaded in batches of sixteen independent loads per thread;
-//   * the load also ORs (key ^ key of page 0), so the bits above the highest differing
-//     bit are known to be common and the first radix digit starts there;
-//   * after one 8-bit pass the keys of the threshold's bin are gathered (order does not
+//   * the keys arrive by one bulk asynchronous copy of the score row into shared memory
+//     where the row allows it (16-byte aligned, a multiple of four floats per row): one
+//     request instead of n/NT load instructions per thread (a 16K-page row lands in
+//     ~0.7 us, against ~5.7 us for per-thread loads from 128 threads); otherwise by
+//     per-thread loads, sixteen in flight;
+//   * keys are stored contiguously in page order; thread t visits pages t, t + NT, ...
+//     (conflict-free), and every pass first loads a batch of sixteen keys into registers,
+//     so no shared-memory load waits behind a shared store or atomic it might alias;
+//   * the bits on which keys differ are OR ^ AND over the keys, so the first 8-bit radix
+//     digit starts at the highest of them;
+//   * after one digit pass the keys of the threshold's bin are gathered (order does not
 //     matter for the threshold), and if they are at most one per thread each finds its
 //     exact rank among them directly; larger bins take further radix passes over the
 //     gathered keys only;
 //   * histograms take plain shared-memory atomics into a bank-padded array (warp-wide
-//     match instructions cost hundreds of cycles when a warp holds many distinct digits),
-//     and the gather writes through a block scan of per-thread counts, with no atomic whose
-//     result a thread waits on.
-//
-// Layout: thread t owns the contiguous pages [t*ipt, (t+1)*ipt) (ipt = ceil(n / NT)), stored
-// at word offset t*stride with an odd stride, so that the NT threads walking their own
-// chunks in step hit NT different banks.
+//     match instructions cost hundreds of cycles when a warp holds many distinct digits);
+//   * block reductions read the per-warp words one per lane and reduce with warp
+//     instructions, rather than every thread reading every warp's word;
+//   * the ordered compaction gives each warp a contiguous segment of pages, walked 32 at a
+//     time with ballots, after one scan of the per-warp counts.
 #pragma once
 
 #include "kv_internal.cuh"
@@ -27,92 +33,124 @@
 namespace skv {
 
 struct CtaKeys {
-  uint32_t* keys;   // shared, NT * stride words
-  int n, ipt, stride;
-  uint32_t key0;    // key of page 0
-  uint32_t diff;    // OR over the pages of (key ^ key0): the bits on which the keys differ
-  // word index of page i
-  __device__ __forceinline__ int slot(int i) const {
-    const int t = i / ipt;
-    return t * stride + (i - t * ipt);
-  }
+  uint32_t* keys;   // shared: keys[i] is the key of page i, i < n
+  int n;
+  uint32_t common;  // AND over the keys: every bit on which they agree has its shared value
+  uint32_t diff;    // OR ^ AND over the keys: the bits on which they differ
 };
 
-// The padded layout of n keys over NT threads (keys not loaded).
+// Shared words the keys of n pages take (bulk copies move whole 16-byte chunks).
+__host__ __device__ constexpr int cta_key_words(int n) { return (n + 3) & ~3; }
+
+// Shared words of the reduction scratch (`red`) that cta_keys_finish needs.
 template <int NT>
-__device__ __forceinline__ CtaKeys cta_key_layout(uint32_t* smem_words, int n) {
-  CtaKeys K;
-  K.keys = smem_words;
-  K.n = n;
-  K.ipt = ceil_div(n, NT);
-  K.stride = K.ipt | 1;
-  K.key0 = 0u;
-  K.diff = 0u;
-  return K;
+__host__ __device__ constexpr int cta_red_words() { return 2 * (NT / 32); }
+
+// Whether a row of 4-byte entries can be bulk-copied: the row 16-byte aligned and the row
+// stride a multiple of four entries (so the copy's rounding up to 16 bytes stays inside the
+// row).
+__device__ __forceinline__ bool cta_row_bulk_ok(const void* row, long row_stride) {
+  return (reinterpret_cast<uintptr_t>(row) & 15u) == 0 && (row_stride & 3) == 0;
 }
 
-// Shared words the layout of n keys over NT threads spans.
-template <int NT>
-__host__ __device__ constexpr int cta_key_words(int n) {
-  return NT * (((n + NT - 1) / NT) | 1);
+// One thread: copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// memory into shared memory, completion counted on bar, whose expected transaction count the
+// caller raised by `bytes` (mbar_arrive_expect_tx) in the same phase.
+__device__ __forceinline__ void cta_bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  constexpr uint32_t kChunk = 32768;
+  for (uint32_t off = 0; off < bytes; off += kChunk) {
+    const uint32_t len = bytes - off < kChunk ? bytes - off : kChunk;
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(reinterpret_cast<char*>(dst) + off)),
+          "l"(reinterpret_cast<const char*>(src) + off), "r"(len), "r"(smem_addr(bar))
+        : "memory");
+  }
 }
 
-// Fill K.key0 and K.diff from keys already in the layout (visible to every thread); red:
-// NT/32 words of scratch. Ends with __syncthreads.
-template <int NT>
-__device__ __forceinline__ void cta_key_diff(CtaKeys& K, uint32_t* red) {
+// One thread: start the copy of the raw bits of row[0, cta_key_words(n)) into keys, counted
+// on bar (initialised with count 1 and visible to the block). The row must pass
+// cta_row_bulk_ok.
+__device__ __forceinline__ void cta_fill_bulk_issue(uint32_t* keys, const float* row, int n,
+                                                    uint64_t* bar) {
+  const uint32_t bytes = 4u * (uint32_t)cta_key_words(n);
+  mbar_arrive_expect_tx(bar, bytes);
+  if (bytes != 0u) cta_bulk_copy(keys, row, bytes, bar);
+}
+
+// Every thread: copy the raw bits of row[0, n) into keys with loads, kBatch in flight per
+// thread. Thread t writes the pages cta_keys_finish has it read, so no barrier is needed
+// between the two.
+template <int NT, int kBatch = 16>
+__device__ __forceinline__ void cta_fill_loads(uint32_t* keys, const float* row, int n) {
   const int tid = threadIdx.x;
-  const uint32_t k0 = K.keys[0];
-  const int a0 = min(K.n, tid * K.ipt), a1 = min(K.n, a0 + K.ipt);
-  uint32_t orv = 0u;
-#pragma unroll 4
-  for (int i = a0; i < a1; ++i) orv |= K.keys[tid * K.stride + (i - a0)] ^ k0;
-  orv = __reduce_or_sync(0xffffffffu, orv);
-  if ((tid & 31) == 0) red[tid >> 5] = orv;
-  __syncthreads();
-  uint32_t diff = 0u;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) diff |= red[w];
-  K.key0 = k0;
-  K.diff = diff;
-}
-
-// Load the n scores of a row as order keys into the padded layout; red: NT/32 words of
-// scratch. Ends with __syncthreads (the keys and K.diff are then visible to every thread).
-template <int NT>
-__device__ __forceinline__ CtaKeys cta_load_keys(const float* row, int n, uint32_t* smem_words,
-                                                 uint32_t* red) {
-  constexpr int kBatch = 16;
-  CtaKeys K = cta_key_layout<NT>(smem_words, n);
-  const int tid = threadIdx.x;
-  const uint32_t k0 = score_order_key(__ldcg(row));
-  uint32_t orv = 0u;
   for (int base = 0; base < n; base += NT * kBatch) {
-    float v[kBatch];
+    uint32_t v[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * NT + tid;
-      v[u] = i < n ? __ldcg(row + i) : 0.f;
+      v[u] = i < n ? __float_as_uint(__ldcg(row + i)) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * NT + tid;
+      if (i < n) keys[i] = v[u];
+    }
+  }
+}
+
+// Make keys[0, n) final and find the bits on which they differ. CONVERT: the words hold raw
+// score bits and become fix(i, score_order_key(score_i)); otherwise they already are keys.
+// red: cta_red_words<NT>() words. Ends with __syncthreads (the keys are then visible to every
+// thread).
+template <int NT, bool CONVERT, typename Fix>
+__device__ __forceinline__ CtaKeys cta_keys_finish(uint32_t* keys, int n, uint32_t* red, Fix fix) {
+  constexpr int kB = 16, NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t orv = 0u, andv = 0xffffffffu;
+  for (int base = 0; base < n; base += NT * kB) {
+    uint32_t v[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * NT + tid;
+      v[u] = i < n ? keys[i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * NT + tid;
       if (i < n) {
-        const uint32_t key = score_order_key(v[u]);
-        K.keys[K.slot(i)] = key;
-        orv |= key ^ k0;
+        uint32_t key = v[u];
+        if constexpr (CONVERT) {
+          key = fix(i, score_order_key(__uint_as_float(key)));
+          keys[i] = key;
+        }
+        orv |= key;
+        andv &= key;
       }
     }
   }
   orv = __reduce_or_sync(0xffffffffu, orv);
-  if ((tid & 31) == 0) red[tid >> 5] = orv;
+  andv = __reduce_and_sync(0xffffffffu, andv);
+  if (lane == 0) {
+    red[warp] = orv;
+    red[NW + warp] = andv;
+  }
   __syncthreads();
-  uint32_t diff = 0u;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) diff |= red[w];
-  K.key0 = k0;
-  K.diff = diff;
+  const uint32_t o = __reduce_or_sync(0xffffffffu, lane < NW ? red[lane] : 0u);
+  const uint32_t a = __reduce_and_sync(0xffffffffu, lane < NW ? red[NW + lane] : 0xffffffffu);
+  CtaKeys K;
+  K.keys = keys;
+  K.n = n;
+  K.common = a;
+  K.diff = o ^ a;
   return K;
+}
+
+// The raw score bits in keys become their order keys.
+template <int NT>
+__device__ __forceinline__ CtaKeys cta_keys_finish(uint32_t* keys, int n, uint32_t* red) {
+  return cta_keys_finish<NT, true>(keys, n, red, [](int, uint32_t key) { return key; });
 }
 
 // Histogram words: 256 bins, one pad word after every 32 (conflict-free reads of eight
@@ -121,12 +159,15 @@ constexpr int kHistWords = 256 + 8;
 
 namespace topk_detail {
 
+constexpr int kB = 16;   // keys per thread per register batch
+
 __device__ __forceinline__ int hslot(uint32_t bin) { return (int)(bin + (bin >> 5)); }
 
 // Exclusive block scan of one count per thread; wsum: NT/32 words. Every thread gets the
 // total. Ends with the block synchronised once (wsum is not reused before the next sync).
 template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
@@ -136,15 +177,9 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   }
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  uint32_t before = 0u, all = 0u;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) {
-    const uint32_t x = wsum[w];
-    before += w < warp ? x : 0u;
-    all += x;
-  }
-  total = all;
-  return before + incl - v;
+  const uint32_t wv = lane < NW ? wsum[lane] : 0u;
+  total = __reduce_add_sync(0xffffffffu, wv);
+  return __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + incl - v;
 }
 
 // Warp 0: from the top bin down, the bin holding the remaining-th largest key.
@@ -190,32 +225,36 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
                               uint32_t* cand, int cand_cap, uint32_t& T, uint32_t& take_eq) {
   using namespace topk_detail;
   const int tid = threadIdx.x;
+  const uint32_t* keys = K.keys;
+  const int n = K.n;
   if (K.diff == 0u) {                        // every key equal: the first k pages
-    T = K.key0;
+    T = K.common;
     take_eq = (uint32_t)k;
     return;
   }
   int top = 31 - __clz(K.diff);              // highest bit on which keys differ
   uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
-  uint32_t prefix = K.key0 & mask;           // the bits every key shares
+  uint32_t prefix = K.common & mask;         // the bits every key shares
   uint32_t remaining = (uint32_t)k;
-  int ncand = -1;                            // -1: histogram the chunks, else cand[0, ncand)
-  const int a0 = min(K.n, tid * K.ipt), a1 = min(K.n, a0 + K.ipt);
+  int ncand = -1;                            // -1: histogram every key, else cand[0, ncand)
   for (;;) {
     const int lo = top >= 7 ? top - 7 : 0;
     const uint32_t dmask = (2u << (top - lo)) - 1u;      // digit bits [lo, top]
     for (int i = tid; i < kHistWords; i += NT) hist[i] = 0u;
     __syncthreads();
-    if (ncand < 0) {
-#pragma unroll 4
-      for (int i = a0; i < a1; ++i) {
-        const uint32_t key = K.keys[tid * K.stride + (i - a0)];
-        if ((key & mask) == prefix) atomicAdd(&hist[hslot((key >> lo) & dmask)], 1u);
+    const uint32_t* src = ncand < 0 ? keys : cand;
+    const int m = ncand < 0 ? n : ncand;
+    for (int base = 0; base < m; base += NT * kB) {
+      uint32_t v[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int i = base + u * NT + tid;
+        v[u] = i < m ? src[i] : 0u;
       }
-    } else {
-      for (int i = tid; i < ncand; i += NT) {
-        const uint32_t key = cand[i];
-        if ((key & mask) == prefix) atomicAdd(&hist[hslot((key >> lo) & dmask)], 1u);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int i = base + u * NT + tid;
+        if (i < m && (v[u] & mask) == prefix) atomicAdd(&hist[hslot((v[u] >> lo) & dmask)], 1u);
       }
     }
     __syncthreads();
@@ -234,16 +273,32 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
     }
     top = lo - 1;
     if (ncand < 0 && (int)bin_count <= cand_cap) {
-      // gather the bin's keys (page order, through a scan of per-thread counts)
+      // gather the bin's keys (any order), through a scan of per-thread counts
       uint32_t mine = 0u, total = 0u;
-#pragma unroll 4
-      for (int i = a0; i < a1; ++i) mine += (K.keys[tid * K.stride + (i - a0)] & mask) == prefix;
+      for (int base = 0; base < n; base += NT * kB) {
+        uint32_t v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int i = base + u * NT + tid;
+          v[u] = i < n ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) mine += (base + u * NT + tid < n) && (v[u] & mask) == prefix;
+      }
       uint32_t at = block_excl_scan<NT>(mine, misc + 8, total);
-      for (int i = a0; i < a1 && mine != 0u; ++i) {
-        const uint32_t key = K.keys[tid * K.stride + (i - a0)];
-        if ((key & mask) == prefix) {
-          cand[at++] = key;
-          --mine;
+      for (int base = 0; base < n && mine != 0u; base += NT * kB) {
+        uint32_t v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int i = base + u * NT + tid;
+          v[u] = i < n ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          if ((base + u * NT + tid < n) && (v[u] & mask) == prefix) {
+            cand[at++] = v[u];
+            --mine;
+          }
         }
       }
       __syncthreads();
@@ -280,44 +335,60 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
 }
 
 // Ordered compaction: calls emit(page, pos) for every kept page, pos = its position in the
-// ascending kept list. wtot: NT/32 doublewords of scratch.
+// ascending kept list. Warp w walks the pages [w * seg, (w + 1) * seg) 32 at a time (seg a
+// multiple of 32), so ballots order the pages inside each step. wtot: NT/32 doublewords.
 template <int NT, typename F>
 __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint64_t* wtot,
                             F&& emit) {
+  using topk_detail::kB;
   constexpr int NW = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int a0 = min(K.n, tid * K.ipt), a1 = min(K.n, a0 + K.ipt);
-  uint32_t gt = 0, eq = 0;
-#pragma unroll 4
-  for (int i = a0; i < a1; ++i) {
-    const uint32_t key = K.keys[tid * K.stride + (i - a0)];
-    gt += key > T;
-    eq += key == T;
-  }
-  const uint64_t v = ((uint64_t)gt << 32) | eq;
-  uint64_t incl = v;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t* keys = K.keys;
+  const int seg = ((K.n + NW - 1) / NW + 31) & ~31;
+  const int s0 = min(K.n, warp * seg), s1 = min(K.n, s0 + seg);
+  uint32_t gt = 0u, eq = 0u;
+  for (int base = s0; base < s1; base += 32 * kB) {
+    uint32_t v[kB];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wtot[warp] = incl;
-  __syncthreads();
-  uint64_t before = 0;
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * 32 + lane;
+      v[u] = i < s1 ? keys[i] : 0u;
+    }
 #pragma unroll
-  for (int w = 0; w < NW; ++w) before += (w < warp) ? wtot[w] : 0ull;
+    for (int u = 0; u < kB; ++u) {
+      const bool in = base + u * 32 + lane < s1;
+      gt += in && v[u] > T;
+      eq += in && v[u] == T;
+    }
+  }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  if (lane == 0) wtot[warp] = ((uint64_t)gt << 32) | eq;
   __syncthreads();
-  const uint64_t ex = before + incl - v;
-  uint32_t gt_before = (uint32_t)(ex >> 32), eq_before = (uint32_t)(ex & 0xffffffffu);
-#pragma unroll 4
-  for (int i = a0; i < a1; ++i) {
-    const uint32_t key = K.keys[tid * K.stride + (i - a0)];
-    if (key > T) {
-      emit(i, (int)(gt_before + min(eq_before, take_eq)));
-      ++gt_before;
-    } else if (key == T) {
-      if (eq_before < take_eq) emit(i, (int)(gt_before + eq_before));
-      ++eq_before;
+  const uint64_t wv = lane < NW ? wtot[lane] : 0ull;
+  uint32_t gt_before = __reduce_add_sync(0xffffffffu, lane < warp ? (uint32_t)(wv >> 32) : 0u);
+  uint32_t eq_before = __reduce_add_sync(0xffffffffu, lane < warp ? (uint32_t)wv : 0u);
+  const uint32_t below = (1u << lane) - 1u;
+  for (int base = s0; base < s1; base += 32 * kB) {
+    uint32_t v[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * 32 + lane;
+      v[u] = i < s1 ? keys[i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * 32 + lane;
+      const bool in = i < s1;
+      const bool is_gt = in && v[u] > T, is_eq = in && v[u] == T;
+      const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
+      const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
+      const uint32_t g_me = gt_before + __popc(bg & below);
+      const uint32_t e_me = eq_before + __popc(be & below);
+      if (is_gt) emit(i, (int)(g_me + min(e_me, take_eq)));
+      else if (is_eq && e_me < take_eq) emit(i, (int)(g_me + e_me));
+      gt_before += __popc(bg);
+      eq_before += __popc(be);
     }
   }
 }

@@ -75,13 +75,14 @@ __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __r
                                             int G, const void* __restrict__ stats,
                                             const int8_t* __restrict__ stats_exp, float* w,
                                             float* __restrict__ scores, int scores_stride,
-                                            int b, int g, int n_pages, const DevCtx& ctx) {
+                                            int b, int g, int chunk, int n_pages,
+                                            const DevCtx& ctx) {
   constexpr int EB = F8 ? 1 : ElemTraits<T>::bytes;   // bytes per statistic
   constexpr int EPC = 16 / EB;                // elements per 16-byte chunk
   constexpr int RPW = rows_per_warp<F8>();
   constexpr int LPR = 32 / RPW;               // lanes per row
   constexpr int CPL = (2 * D * EB / 16) / LPR;  // chunks per lane per stats row
-  const int p_block = blockIdx.x * WARPS * RPW;
+  const int p_block = chunk * WARPS * RPW;
   if (p_block >= n_pages) return false;
 
   const int Hkv = d.num_kv_heads;
@@ -145,17 +146,16 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const void* __rest
   __shared__ __align__(16) float w[2 * D];    // [Neg | Pos], matching a row's [mn | mx]
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.z, g = blockIdx.y;
+  const int b = blockIdx.z, g = blockIdx.y, chunk = blockIdx.x;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
   score_block<T, D, kScoreWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b, g,
-                                     n_pages, ctx);
+                                     chunk, n_pages, ctx);
 }
 
-// Shared words for the keys of a group of up to max_pages pages, laid out as cta_topk.cuh
-// lays them out for kSelThreads threads, plus the gathered-candidate scratch.
+// Shared words for the keys of a group of up to max_pages pages (cta_topk.cuh).
 __host__ __device__ constexpr size_t select_key_words(int max_pages) {
-  return (size_t)kSelThreads * (size_t)(((max_pages + kSelThreads - 1) / kSelThreads) | 1);
+  return (size_t)cta_key_words(max_pages);
 }
 
 template <typename T, int D, bool F8>
@@ -170,20 +170,23 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   __shared__ __align__(16) float w[2 * D];
   __shared__ uint32_t hist[kHistWords];
   __shared__ uint32_t misc[8 + kSelWarps];
+  __shared__ uint32_t red[cta_red_words<kSelThreads>()];
   __shared__ uint64_t wtot[kSelWarps];
+  __shared__ __align__(8) uint64_t s_bar;
   __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.z, g = blockIdx.y, tid = threadIdx.x;
+  const int b = blockIdx.z, tid = threadIdx.x;
+  const int g = blockIdx.y, chunk = blockIdx.x;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
   const long grp = (long)b * d.num_kv_heads + g;
   if (n_pages == 0) {                         // nothing to score or keep
-    if (blockIdx.x == 0 && tid == 0) sel_cnt[grp] = 0;
+    if (chunk == 0 && tid == 0) sel_cnt[grp] = 0;
     return;
   }
   if (!score_block<T, D, kSelWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b,
-                                        g, n_pages, ctx))
+                                        g, chunk, n_pages, ctx))
     return;
 
   // ---- the group's last block selects -----------------------------------------------------
@@ -208,8 +211,23 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
     for (int i = tid; i < n_pages; i += kSelThreads) out[i] = i;
     return;
   }
-  const CtaKeys K = cta_load_keys<kSelThreads>(scores + grp * scores_stride, n_pages, dyn_words,
-                                               misc + 8);
+  // the group's scores into shared memory: one bulk copy where the row allows it (the other
+  // blocks' stores were made visible by the acquire above; the proxy fence orders them before
+  // the asynchronous copy), else loads
+  const float* srow = scores + grp * scores_stride;
+  if (cta_row_bulk_ok(srow, scores_stride)) {
+    if (tid == 0) {
+      mbar_init(&s_bar, 1);
+      fence_mbar_init();
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      cta_fill_bulk_issue(dyn_words, srow, n_pages, &s_bar);
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded(&s_bar, 0u, ctx.wait_ns) && tid == 0) flag(ctx, KV_DEVERR_TIMEOUT);
+  } else {
+    cta_fill_loads<kSelThreads>(dyn_words, srow, n_pages);
+  }
+  const CtaKeys K = cta_keys_finish<kSelThreads>(dyn_words, n_pages, red);
   uint32_t thr, take_eq;
   cta_threshold<kSelThreads>(K, k, hist, misc, dyn_words + key_words, kSelCandWords, thr,
                              take_eq);
@@ -235,11 +253,10 @@ cudaError_t launch_sel_t(const kv_cache_desc& d, const void* q, int Hq, const vo
   const int key_words = (int)select_key_words(d.page_table_stride);
   const size_t smem = 4 * ((size_t)key_words + kSelCandWords);
   auto kern = score_select_kernel<T, D, F8>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  // always: the kernel's static shared memory counts against the 48 KB default too
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(ceil_div(d.page_table_stride, kSelWarps * rows_per_warp<F8>()), d.num_kv_heads,
             d.batch);
   return launch_pdl(kern, grid, dim3(kSelThreads), smem, s, d, static_cast<const T*>(q),

@@ -17,7 +17,13 @@
 // Sparsity and KV-Cache Sparsity Cross in LLM Decoding", Tables 3 and 11).
 //
 // One 1024-thread block per group. Scores are mapped to unsigned keys whose integer order
-// is the float order, and a most-significant-digit radix select (up to four 8-bit passes,
+// is the float order. Groups whose keys fit in shared memory (up to ~48K pages) take the
+// block top-k of cta_topk.cuh: the score row arrives in shared memory by one bulk copy
+// (loads where the row is not 16-byte aligned), the first radix digit starts at the highest
+// bit on which the keys differ, the threshold bin's keys are gathered and ranked, and the
+// kept pages are written in order by warp ballots after one scan of per-warp counts.
+// Longer groups take the original form below: a most-significant-digit radix select (up to
+// four 8-bit passes,
 // histograms in shared memory with warp-aggregated atomics) finds the k-th largest key T
 // and how many keys equal to T are kept (the lowest-indexed ones). Groups of up to 16384
 // pages keep their keys in registers (16 per thread) for every pass, so the scores are read
@@ -26,10 +32,90 @@
 // then runs one block-wide exclusive scan of packed (greater-than-T, equal-to-T) counts per
 // 1024 consecutive pages, which gives each kept page its output slot, so the output is
 // ascending by construction. Longer groups take the same steps reading keys from L2.
+#include "cta_topk.cuh"
 #include "kv_internal.cuh"
 
 namespace skv {
 namespace {
+
+constexpr int kSelCand = 4096;               // gathered keys of the threshold's bin
+constexpr size_t kSelectCtaSmemLimit = 227 * 1024;   // shared memory a block may opt into
+
+// Shared words of the block top-k for groups of up to max_pages pages: keys, then candidates.
+constexpr size_t select_cta_words(int max_pages) {
+  return (size_t)cta_key_words(max_pages) + kSelCand;
+}
+
+// Keep count of group (b, g) and its page count n; flags a bad length or keep count.
+__device__ __forceinline__ int select_count(const int32_t* seq_lens, int PS, int table_stride,
+                                            const int32_t* keep, double keep_ratio, int budget,
+                                            int k_max, int sink, int local, int b, int& n,
+                                            const DevCtx& ctx) {
+  int len = seq_lens[b];
+  if (len < 0 || len > table_stride * PS) {
+    if (threadIdx.x == 0) flag(ctx, KV_DEVERR_BAD_LEN);
+    len = len < 0 ? 0 : table_stride * PS;
+  }
+  n = ceil_div(len, PS);
+  int k = keep_rule(n, keep, b, keep_ratio, budget);
+  const int forced = min(n, max(0, sink) + max(0, local));   // [0, sink) and [n - local, n)
+  k = max(k, forced);
+  if (k > k_max) {
+    if (threadIdx.x == 0) flag(ctx, KV_DEVERR_KEEP);
+    k = k_max;
+  }
+  return k;
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+select_cta_kernel(const float* __restrict__ scores, int scores_stride,
+                  const int32_t* __restrict__ seq_lens, int PS, int Hkv,
+                  const int32_t* __restrict__ keep, double keep_ratio, int budget, int k_max,
+                  int sink, int local, int32_t* __restrict__ sel_idx,
+                  int32_t* __restrict__ sel_cnt, int table_stride, int key_words, DevCtx ctx) {
+  extern __shared__ __align__(16) uint32_t words[];           // keys, then candidates
+  __shared__ uint32_t hist[kHistWords];
+  __shared__ uint32_t misc[8 + kSelectThreads / 32];
+  __shared__ uint32_t red[cta_red_words<kSelectThreads>()];
+  __shared__ uint64_t wtot[kSelectThreads / 32];
+  __shared__ __align__(8) uint64_t s_bar;
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  const int g = blockIdx.x, b = blockIdx.y;
+  int n = 0;
+  const int k = select_count(seq_lens, PS, table_stride, keep, keep_ratio, budget, k_max, sink,
+                             local, b, n, ctx);
+  const long grp = (long)b * Hkv + g;
+  int32_t* out = sel_idx + grp * k_max;
+  if (threadIdx.x == 0) sel_cnt[grp] = k;
+  if (k >= n) {                              // keep every page (also n == 0)
+    for (int i = threadIdx.x; i < n; i += kSelectThreads) out[i] = i;
+    return;
+  }
+  if (k == 0) return;
+  const float* row = scores != nullptr ? scores + grp * scores_stride : nullptr;
+  const bool have_row = row != nullptr;
+  if (have_row && cta_row_bulk_ok(row, scores_stride)) {   // one bulk copy of the row
+    if (threadIdx.x == 0) cta_fill_bulk_issue(words, row, n, &s_bar);
+    if (!mbar_wait_bounded(&s_bar, 0u, ctx.wait_ns) && threadIdx.x == 0)
+      flag(ctx, KV_DEVERR_TIMEOUT);
+  } else if (have_row) {
+    cta_fill_loads<kSelectThreads>(words, row, n);
+  }
+  const CtaKeys K = cta_keys_finish<kSelectThreads, true>(
+      words, n, red, [&](int i, uint32_t key) -> uint32_t {
+        if (i < sink || i >= n - local) return 0xffffffffu;   // forced in
+        return have_row ? key : 0u;
+      });
+  uint32_t T, take_eq;
+  cta_threshold<kSelectThreads>(K, k, hist, misc, words + key_words, kSelCand, T, take_eq);
+  cta_compact<kSelectThreads>(K, T, take_eq, wtot, [&](int p, int pos) { out[pos] = p; });
+}
 
 // Block-wide exclusive scan of a 64-bit value (two packed 32-bit counters).
 __device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t* warp_tot,
@@ -210,6 +296,19 @@ cudaError_t launch_select_topk(const float* scores, int scores_stride, const int
                                int local, int32_t* sel_idx, int32_t* sel_cnt,
                                int page_table_stride, DevCtx ctx, cudaStream_t s) {
   dim3 grid(Hkv, batch);
+  const size_t words = select_cta_words(page_table_stride);
+  const size_t smem = 4 * words;
+  if (smem + 4 * (kHistWords + 8 + kSelectThreads / 32) + 8 * (kSelectThreads / 32) <=
+      kSelectCtaSmemLimit) {
+    // always: the kernel's static shared memory counts against the 48 KB default too
+    cudaError_t e = cudaFuncSetAttribute(select_cta_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_cta_kernel, grid, dim3(kSelectThreads), smem, s, scores,
+                      scores_stride, seq_lens, page_size, Hkv, keep, keep_ratio, budget_pages,
+                      k_max, sink, local, sel_idx, sel_cnt, page_table_stride,
+                      (int)(words - kSelCand), ctx);
+  }
   auto kern = page_table_stride <= kRegKeys * kSelectThreads ? select_kernel<true>
                                                               : select_kernel<false>;
   return launch_pdl(kern, grid, dim3(kSelectThreads), 0, s, scores, scores_stride, seq_lens,

@@ -131,9 +131,8 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // arrive now, wait just before the first remote store
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     uint32_t* ring_w = reinterpret_cast<uint32_t*>(ring);
-    CtaKeys K = cta_key_layout<kFusedThreads>(ring_w, n);
-    const int KW = cta_key_words<kFusedThreads>(n);
-    int32_t* s_phys = reinterpret_cast<int32_t*>(ring_w + KW);   // physical ids, key layout
+    const int KW = cta_key_words(n);           // keys [KW], then physical ids [KW], by page
+    int32_t* s_phys = reinterpret_cast<int32_t*>(ring_w + KW);
     for (int i = tid; i < nr; i += kFusedThreads) {
       int P = table[p0 + i];
       if (P < 0 || P >= d.num_phys_pages) {
@@ -192,9 +191,9 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           acc += __shfl_xor_sync(0xffffffffu, acc, 1);
           if (i < nr) {
             const uint32_t key = Pu[u] >= 0 ? score_order_key(acc) : 0u;
-            const int sl = K.slot(p0 + i);
+            const int sl = p0 + i;
             for (int rk = j8; rk < CL; rk += 8) {      // the 8 lanes share the CL copies
-              cluster.map_shared_rank(K.keys, rk)[sl] = key;
+              cluster.map_shared_rank(ring_w, rk)[sl] = key;
               cluster.map_shared_rank(s_phys, rk)[sl] = Pu[u];
             }
           }
@@ -204,7 +203,8 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     cluster.sync();                            // every CTA holds every key and physical id
 
     // ================= 2. threshold of the k kept keys (the same in every CTA) ============
-    cta_key_diff<kFusedThreads>(K, s_misc + 8);
+    const CtaKeys K = cta_keys_finish<kFusedThreads, false>(
+        ring_w, n, reinterpret_cast<uint32_t*>(s_misc64), [](int, uint32_t key) { return key; });
     uint32_t T, take_eq;
     cta_threshold<kFusedThreads>(K, k, s_hist, s_misc, ring_w + 2 * KW, C::RING_WORDS - 2 * KW,
                                  T, take_eq);
@@ -219,7 +219,7 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     }
     cta_compact<kFusedThreads>(K, T, take_eq, s_misc64, [&](int p, int pos) {
       if (pos >= pos0 && pos < pos0 + np) {
-        const int P = s_phys[K.slot(p)];
+        const int P = s_phys[p];
         s_runp[pos - pos0] = P;
         s_runv[pos - pos0] = (int16_t)(P >= 0 ? min(PS, len - p * PS) : 0);
         if (sel_out != nullptr) sel_out[grp * k_max + pos] = p;
@@ -420,7 +420,7 @@ int fused_cluster_size(const kv_cache_desc& d, int G, int num_sms) {
   // the group's keys, physical ids and some candidate room fit the copy ring
   const int ring_w =
       d.head_dim == 128 ? FusedCfg<128, 1>::RING_WORDS : FusedCfg<64, 1>::RING_WORDS;
-  if (2 * cta_key_words<kFusedThreads>(d.page_table_stride) + 1024 > ring_w) return 0;
+  if (2 * cta_key_words(d.page_table_stride) + 1024 > ring_w) return 0;
   for (int CL = 16; CL >= 1; --CL) {
     if (groups * CL > num_sms) continue;
     // every CTA's score range and page run must fit its shared-memory arrays

@@ -84,10 +84,14 @@ def round256(x: int) -> int:
     return (x + 255) // 256 * 256
 
 
+def round4(x: int) -> int:
+    return (x + 3) // 4 * 4
+
+
 def step_selection(workspace, B, Hkv, stride, k_max):
     """sel_idx and sel_cnt of a sparse kv_decode_step, read from its workspace at the
     offsets include/sparsekv.h documents."""
-    a = 2 * round256(B * Hkv * 4) + round256(B * Hkv * stride * 4)
+    a = 2 * round256(B * Hkv * 4) + round256(B * Hkv * round4(stride) * 4)
     c = a + round256(B * Hkv * k_max * 4)
     sel = workspace[a: a + B * Hkv * k_max * 4].view(torch.int32).view(B, Hkv, k_max)
     cnt = workspace[c: c + B * Hkv * 4].view(torch.int32).view(B, Hkv)
@@ -98,4 +102,4 @@ def step_score_region(workspace, B, Hkv, stride):
     """The byte range of a kv_decode_step workspace that holds the step's scores (after the
     two per-group counter arrays)."""
     a = 2 * round256(B * Hkv * 4)
-    return workspace[a: a + round256(B * Hkv * stride * 4)]
+    return workspace[a: a + round256(B * Hkv * round4(stride) * 4)]

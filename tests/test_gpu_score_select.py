@@ -106,12 +106,23 @@ def test_score_select_on_tied_scores():
 
 
 def test_score_select_long_group():
-    """A 24448-page group (the longest that the keys of a 512-thread block hold with room)."""
+    """A 24448-page group: its keys (98 KB) in one 512-thread block's shared memory."""
     w, c = _make("bf16", 128, 4, 16, (24448 * 16, 1000 * 16 + 1), Hkv=1)
     kv = skv.PagedKV.from_cache(c)
     stats = skv.kv_build_page_stats(kv)
     for keep in (dict(keep_ratio=0.3), dict(budget_pages=2048)):
         _compare_with_separate_calls(kv, c.q, stats, c.seq_lens, 16, keep, reps=1)
+
+
+@pytest.mark.parametrize("pages", [8191, 8192, 8193])
+def test_selection_at_the_shared_memory_default(pages):
+    """Groups whose keys and candidate scratch take 48 KB of dynamic shared memory, the
+    per-block default (the kernels' static shared memory then needs the opt-in as well), next
+    to strides that are no multiple of four (per-thread loads instead of one bulk copy)."""
+    w, c = _make("bf16", 128, 4, 16, (pages * 16, 1000 * 16 + 3), Hkv=1)
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    _compare_with_separate_calls(kv, c.q, stats, c.seq_lens, 16, dict(keep_ratio=0.3), reps=1)
 
 
 @pytest.mark.parametrize("D,G,PS", [(128, 4, 16), (128, 8, 64), (128, 1, 32), (64, 2, 16),
