@@ -478,11 +478,12 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     uint32_t T, take_eq;
     cta_threshold<C::THREADS>(K, cnt, reinterpret_cast<uint32_t*>(smem + C::OFF_HIST), misc,
                               ring + used, C::RING_WORDS - used, T, take_eq);
-    int32_t* sel_out = (s == 0) ? sa.sel_out : nullptr;
+    // this CTA's run only; each CTA also writes its run's part of the selection output
+    int32_t* sel_out = sa.sel_out;
     cta_compact<C::THREADS>(K, T, take_eq, reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT),
-                            [&](int p, int pos) {
+                            pos0, pos0 + np, [&](int p, int pos) {
                               if (sel_out != nullptr) sel_out[grp * sa.k_max + pos] = p;
-                              if (pos >= pos0 && pos < pos0 + np) s_phys[pos - pos0] = p;
+                              s_phys[pos - pos0] = p;
                             });
     __syncthreads();
     if (table_bulk) tab = reinterpret_cast<const int32_t*>(ring + KW);

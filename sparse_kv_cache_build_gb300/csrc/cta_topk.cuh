@@ -334,12 +334,15 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
   }
 }
 
-// Ordered compaction: calls emit(page, pos) for every kept page, pos = its position in the
-// ascending kept list. Warp w walks the pages [w * seg, (w + 1) * seg) 32 at a time (seg a
-// multiple of 32), so ballots order the pages inside each step. wtot: NT/32 doublewords.
+// Ordered compaction: calls emit(page, pos) for every kept page whose position pos in the
+// ascending kept list lies in [w0, w1) (a CTA that needs one run of the list asks for that
+// window; 0 and k give the whole list). Warp w walks the pages [w * seg, (w + 1) * seg) 32 at
+// a time (seg a multiple of 32), so ballots order the pages inside each step; a warp whose
+// positions miss the window does nothing after the count, and a warp stops once past it. The
+// ballots of a batch of rounds are taken before any emit branches. wtot: NT/32 doublewords.
 template <int NT, typename F>
 __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint64_t* wtot,
-                            F&& emit) {
+                            int w0, int w1, F&& emit) {
   using topk_detail::kB;
   constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -368,9 +371,12 @@ __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint
   const uint64_t wv = lane < NW ? wtot[lane] : 0ull;
   uint32_t gt_before = __reduce_add_sync(0xffffffffu, lane < warp ? (uint32_t)(wv >> 32) : 0u);
   uint32_t eq_before = __reduce_add_sync(0xffffffffu, lane < warp ? (uint32_t)wv : 0u);
+  const uint32_t first = gt_before + min(eq_before, take_eq);
+  const uint32_t last = gt_before + gt + min(eq_before + eq, take_eq);   // exclusive
+  if (last <= (uint32_t)w0 || first >= (uint32_t)w1) return;           // warp-uniform
   const uint32_t below = (1u << lane) - 1u;
   for (int base = s0; base < s1; base += 32 * kB) {
-    uint32_t v[kB];
+    uint32_t v[kB], bg[kB], be[kB];
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
       const int i = base + u * 32 + lane;
@@ -378,18 +384,23 @@ __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint
     }
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
-      const int i = base + u * 32 + lane;
-      const bool in = i < s1;
-      const bool is_gt = in && v[u] > T, is_eq = in && v[u] == T;
-      const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
-      const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
-      const uint32_t g_me = gt_before + __popc(bg & below);
-      const uint32_t e_me = eq_before + __popc(be & below);
-      if (is_gt) emit(i, (int)(g_me + min(e_me, take_eq)));
-      else if (is_eq && e_me < take_eq) emit(i, (int)(g_me + e_me));
-      gt_before += __popc(bg);
-      eq_before += __popc(be);
+      const bool in = base + u * 32 + lane < s1;
+      bg[u] = __ballot_sync(0xffffffffu, in && v[u] > T);
+      be[u] = __ballot_sync(0xffffffffu, in && v[u] == T);
     }
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * 32 + lane;
+      const uint32_t g_me = gt_before + __popc(bg[u] & below);
+      const uint32_t e_me = eq_before + __popc(be[u] & below);
+      int pos = -1;
+      if ((bg[u] >> lane) & 1u) pos = (int)(g_me + min(e_me, take_eq));
+      else if (((be[u] >> lane) & 1u) && e_me < take_eq) pos = (int)(g_me + e_me);
+      if (pos >= w0 && pos < w1) emit(i, pos);
+      gt_before += __popc(bg[u]);
+      eq_before += __popc(be[u]);
+    }
+    if (gt_before + min(eq_before, take_eq) >= (uint32_t)w1) break;    // past the window
   }
 }
 

@@ -231,7 +231,7 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   uint32_t thr, take_eq;
   cta_threshold<kSelThreads>(K, k, hist, misc, dyn_words + key_words, kSelCandWords, thr,
                              take_eq);
-  cta_compact<kSelThreads>(K, thr, take_eq, wtot, [&](int p, int pos) { out[pos] = p; });
+  cta_compact<kSelThreads>(K, thr, take_eq, wtot, 0, k, [&](int p, int pos) { out[pos] = p; });
 }
 
 template <typename T, int D, bool F8>

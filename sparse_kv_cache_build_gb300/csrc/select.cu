@@ -114,7 +114,7 @@ select_cta_kernel(const float* __restrict__ scores, int scores_stride,
       });
   uint32_t T, take_eq;
   cta_threshold<kSelectThreads>(K, k, hist, misc, words + key_words, kSelCand, T, take_eq);
-  cta_compact<kSelectThreads>(K, T, take_eq, wtot, [&](int p, int pos) { out[pos] = p; });
+  cta_compact<kSelectThreads>(K, T, take_eq, wtot, 0, k, [&](int p, int pos) { out[pos] = p; });
 }
 
 // Block-wide exclusive scan of a 64-bit value (two packed 32-bit counters).

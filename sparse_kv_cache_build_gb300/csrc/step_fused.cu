@@ -217,7 +217,7 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
       np = kFusedMaxRun;
     }
-    cta_compact<kFusedThreads>(K, T, take_eq, s_misc64, [&](int p, int pos) {
+    cta_compact<kFusedThreads>(K, T, take_eq, s_misc64, pos0, pos0 + np, [&](int p, int pos) {
       if (pos >= pos0 && pos < pos0 + np) {
         const int P = s_phys[p];
         s_runp[pos - pos0] = P;
