@@ -368,8 +368,9 @@ struct StepArgs {
   float* lse;
 };
 
+// Two CTAs per SM (shared memory allows no more), so up to 255 registers a thread.
 template <int D, int G>
-__global__ void __launch_bounds__(MmaCfg<D, G>::THREADS)
+__global__ void __launch_bounds__(MmaCfg<D, G>::THREADS, 2)
 split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, kv_cache_desc d,
                       const uint16_t* __restrict__ q, float qk_scale_log2,
@@ -539,9 +540,11 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   // ---- the group's last CTA merges its S partials (log-sum-exp) -------------------------
   __syncthreads();                                         // this CTA's partials are written
   if (tid == 0) {
-    __threadfence();                                       // release: the partials first
-    const int done = atomicAdd(&sa.counters[grp], 1);
-    __threadfence();                                       // acquire: the others' partials
+    // one acquire-release atomic: the partials this CTA wrote (ordered before it by the
+    // barrier above) are visible to whoever counts after it, and the others' to this CTA
+    int done;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(done) : "l"(&sa.counters[grp]) : "memory");
     misc[3] = (done == S - 1) ? 1u : 0u;
   }
   __syncthreads();                                         // orders every thread after it
@@ -554,7 +557,7 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   // The first splits' partial sums of this thread's first output columns do not depend on the
   // weights: their loads go out now and land while the weights are computed.
   constexpr int D4 = D / 4;
-  constexpr int PB = 24;
+  constexpr int PB = 40;
   float4 pre[PB];
   if (tid < G * D4) {
     const int hl = tid / D4, d4 = tid - hl * D4;
