@@ -290,8 +290,8 @@ kv_status kv_decode_attn_merge(const kv_cache_desc* cache, const void* q, int32_
  * the same kernel. counters: device [batch][num_kv_heads] int32, zero before the first call;
  * every call returns them to zero. sel_idx [batch][num_kv_heads][k_max] and sel_cnt
  * [batch][num_kv_heads] receive the selection when not NULL (sparse calls only). The group's
- * pages must fit the in-kernel selection (page_table_stride at most 23552 pages for
- * head_dim 128, 11264 for 64) and the splits its merge; otherwise KV_ERR_UNSUPPORTED.
+ * pages must fit the in-kernel selection (page_table_stride at most 21440 pages for
+ * head_dim 128, 9152 for 64) and the splits its merge; otherwise KV_ERR_UNSUPPORTED.
  * part_acc must be 16-byte and part_ml 8-byte aligned (KV_ERR_MISALIGNED).
  */
 kv_status kv_select_decode_attn(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,

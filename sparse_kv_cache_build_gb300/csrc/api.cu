@@ -21,9 +21,10 @@ __device__ int32_t g_kv_error_word = 0;
 constexpr int kMaxDevices = 64;
 constexpr int kDroppedSplits = 64;          // page ranges per group in the dropped-mass probe
 // Longest group (pages) whose selection kv_decode_step leaves to the attention kernel's CTAs;
-// longer groups select once, in the score launch (at 8192 pages the in-CTA selection, with
-// its rows copied in bulk, measured 75.9 us a step against 83-85 us for selecting once).
-constexpr int kInAttnSelectPages = 8192;
+// longer groups select once, in the score launch. Measured with the bulk-copied rows and
+// 11-bit digits: 70.8 against 81.0 us a step at 8192 pages (128K context), 81.1 against
+// 85.1 us at 16384 pages (1M context, page size 64).
+constexpr int kInAttnSelectPages = 16384;
 
 struct DeviceState {
   bool ready = false;
@@ -177,7 +178,8 @@ bool is_dense(double keep_ratio, int budget_pages) {
 // The fused score + select launch fits this device for this table stride (its static
 // shared memory is a few KB on top of the dynamic part).
 bool score_select_fits(const kv_cache_desc* d, const DeviceState* st) {
-  return score_select_smem(d->page_table_stride) + 8 * 1024 <= (size_t)st->smem_optin;
+  // + the kernel's static shared memory (histogram, q-side vector, scratch): under 16 KB
+  return score_select_smem(d->page_table_stride) + 16 * 1024 <= (size_t)st->smem_optin;
 }
 
 __global__ void wait_selftest_kernel(unsigned long long limit_ns, DevCtx ctx) {

@@ -43,16 +43,16 @@ struct MmaCfg {
   static constexpr size_t OFF_STAGES = 0;                  // from a 1024-aligned base
   static constexpr size_t OFF_PHYS = OFF_STAGES + (size_t)NSTAGE * STAGE_BYTES;
   static constexpr size_t OFF_VALID = OFF_PHYS + 4 * kMaxSplitPages;
-  static constexpr size_t OFF_HIST = OFF_VALID + 2 * kMaxSplitPages;   // uint32 [kHistWords]
-  static constexpr size_t OFF_MISC = OFF_HIST + 4 * 288;                // uint32 [16]
+  static constexpr size_t OFF_MISC = OFF_VALID + 2 * kMaxSplitPages;   // uint32 [16]
   static constexpr size_t OFF_WTOT = OFF_MISC + 64;                     // uint64 [8]
   static constexpr size_t OFF_BAR = OFF_WTOT + 64;
   static constexpr size_t SMEM = OFF_BAR + 8 * (NSTAGE + 1) + 1024;   // + alignment slack
   // the in-kernel selection keeps the group's keys (and, copied in bulk, its page-table
-  // row) in the ring, with at least SELECT_CAND_MIN words left for gathered candidates
+  // row) in the ring, then the histogram, with at least SELECT_CAND_MIN words left for
+  // gathered candidates
   static constexpr int RING_WORDS = (int)((size_t)NSTAGE * STAGE_BYTES / 4);
   static constexpr int SELECT_CAND_MIN = 1024;
-  static constexpr int MAX_SELECT_PAGES = RING_WORDS - SELECT_CAND_MIN;
+  static constexpr int MAX_SELECT_PAGES = RING_WORDS - kHistWords - SELECT_CAND_MIN;
   // a CTA partial: acc [G][D], then m [G] (base 2), then l [G]
   static constexpr size_t PARTIAL_FLOATS = (size_t)G * (D + 2);
   static constexpr size_t MERGE_BYTES = 4 * (size_t)4 * G * (D + 2);
@@ -403,9 +403,9 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
   // the ring in bulk at once, before the sequence length is known, where the rows allow it.
   const float* srow = sa.scores != nullptr ? sa.scores + grp * sa.scores_stride : nullptr;
   const int KW = cta_key_words(d.page_table_stride);
-  const bool keys_bulk = srow != nullptr && KW + C::SELECT_CAND_MIN <= C::RING_WORDS &&
+  const bool keys_bulk = srow != nullptr && KW <= C::MAX_SELECT_PAGES &&
                          cta_row_bulk_ok(srow, sa.scores_stride);
-  const bool table_bulk = keys_bulk && 2 * KW + C::SELECT_CAND_MIN <= C::RING_WORDS &&
+  const bool table_bulk = keys_bulk && 2 * KW <= C::MAX_SELECT_PAGES &&
                           cta_row_bulk_ok(table, d.page_table_stride);
   if (keys_bulk && tid == 0) {
     mbar_arrive_expect_tx(&bars[C::NSTAGE], (table_bulk ? 8u : 4u) * (uint32_t)KW);
@@ -477,8 +477,8 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     const CtaKeys K = cta_keys_finish<C::THREADS>(ring, n_pages, misc + 8);
     uint32_t T, take_eq;
-    cta_threshold<C::THREADS>(K, cnt, reinterpret_cast<uint32_t*>(smem + C::OFF_HIST), misc,
-                              ring + used, C::RING_WORDS - used, T, take_eq);
+    cta_threshold<C::THREADS>(K, cnt, ring + used, misc, ring + used + kHistWords,
+                              C::RING_WORDS - used - kHistWords, T, take_eq);
     // this CTA's run only; each CTA also writes its run's part of the selection output
     int32_t* sel_out = sa.sel_out;
     cta_compact<C::THREADS>(K, T, take_eq, reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT),

@@ -14,8 +14,10 @@
 //   * keys are stored contiguously in page order; thread t visits pages t, t + NT, ...
 //     (conflict-free), and every pass first loads a batch of sixteen keys into registers,
 //     so no shared-memory load waits behind a shared store or atomic it might alias;
-//   * the bits on which keys differ are OR ^ AND over the keys, so the first 8-bit radix
-//     digit starts at the highest of them;
+//   * the bits on which keys differ are OR ^ AND over the keys, so the first radix digit
+//     starts at the highest of them; digits are 11 bits wide, so that after the first pass
+//     the threshold's bin usually holds fewer keys than the block has threads (a pass
+//     costs several block-wide steps; more bins cost only a wider histogram);
 //   * after one digit pass the keys of the threshold's bin are gathered (order does not
 //     matter for the threshold), and if they are at most one per thread each finds its
 //     exact rank among them directly; larger bins take further radix passes over the
@@ -153,9 +155,10 @@ __device__ __forceinline__ CtaKeys cta_keys_finish(uint32_t* keys, int n, uint32
   return cta_keys_finish<NT, true>(keys, n, red, [](int, uint32_t key) { return key; });
 }
 
-// Histogram words: 256 bins, one pad word after every 32 (conflict-free reads of eight
-// consecutive bins per lane).
-constexpr int kHistWords = 256 + 8;
+// Radix digits of kDigitBits bits; histogram words: one pad word after every 32 bins.
+constexpr int kDigitBits = 11;
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kHistWords = kBins + kBins / 32;
 
 namespace topk_detail {
 
@@ -182,34 +185,34 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   return __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + incl - v;
 }
 
-// Warp 0: from the top bin down, the bin holding the remaining-th largest key.
-// misc[0] = bin, misc[1] = rank still needed inside it, misc[2] = the bin's count.
+// Every thread: from the top bin down, the bin holding the remaining-th largest key. Thread t
+// owns kBins / NT consecutive bins, the highest for t = 0, so one exclusive block scan of the
+// per-thread sums gives the keys above each thread's bins. misc[0] = bin, misc[1] = rank still
+// needed inside it, misc[2] = the bin's count; misc + 8: NT/32 words of scan scratch.
+template <int NT>
 __device__ __forceinline__ void pick_bin(const uint32_t* hist, uint32_t remaining,
                                          uint32_t* misc) {
-  const int lane = threadIdx.x & 31;
-  uint32_t c[8], lane_sum = 0u;
+  constexpr int B = kBins / NT;
+  static_assert(B >= 1 && B * NT == kBins, "bins per thread");
+  const int hi = kBins - 1 - (int)threadIdx.x * B;     // this thread's highest bin
+  uint32_t c[B], sum = 0u;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    c[e] = hist[hslot((uint32_t)(lane * 8 + e))];
-    lane_sum += c[e];
+  for (int j = 0; j < B; ++j) {
+    c[j] = hist[hslot((uint32_t)(hi - j))];
+    sum += c[j];
   }
-  uint32_t incl = lane_sum;                 // this lane's bins and every higher lane's
+  uint32_t total;
+  uint32_t above = block_excl_scan<NT>(sum, misc + 8, total);
+  if (above < remaining && remaining <= above + sum) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-    if (lane + o < 32) incl += y;
-  }
-  uint32_t above = incl - lane_sum;
-  if (above < remaining && remaining <= incl) {
-#pragma unroll
-    for (int e = 7; e >= 0; --e) {
-      if (above + c[e] >= remaining) {
-        misc[0] = (uint32_t)(lane * 8 + e);
+    for (int j = 0; j < B; ++j) {
+      if (above + c[j] >= remaining) {
+        misc[0] = (uint32_t)(hi - j);
         misc[1] = remaining - above;
-        misc[2] = c[e];
+        misc[2] = c[j];
         break;
       }
-      above += c[e];
+      above += c[j];
     }
   }
 }
@@ -219,7 +222,7 @@ __device__ __forceinline__ void pick_bin(const uint32_t* hist, uint32_t remainin
 // Threshold of the top k keys (0 < k < n). On return (block-uniform) the kept keys are those
 // > T and the first take_eq keys == T in page order. hist: kHistWords words; misc: 8 +
 // NT/32 words; cand: cand_cap words of 16-byte aligned scratch for the gathered keys of
-// the threshold's bin.
+// the threshold's bin. NT divides kBins.
 template <int NT>
 __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t* misc,
                               uint32_t* cand, int cand_cap, uint32_t& T, uint32_t& take_eq) {
@@ -238,7 +241,7 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
   uint32_t remaining = (uint32_t)k;
   int ncand = -1;                            // -1: histogram every key, else cand[0, ncand)
   for (;;) {
-    const int lo = top >= 7 ? top - 7 : 0;
+    const int lo = top >= kDigitBits - 1 ? top - (kDigitBits - 1) : 0;
     const uint32_t dmask = (2u << (top - lo)) - 1u;      // digit bits [lo, top]
     for (int i = tid; i < kHistWords; i += NT) hist[i] = 0u;
     __syncthreads();
@@ -258,7 +261,7 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
       }
     }
     __syncthreads();
-    if (tid < 32) pick_bin(hist, remaining, misc);
+    pick_bin<NT>(hist, remaining, misc);
     __syncthreads();
     const uint32_t bin = misc[0];
     remaining = misc[1];

@@ -60,7 +60,7 @@ struct FusedCfg {
   static constexpr size_t OFF_RUNV = OFF_RUNP + 4 * kFusedMaxRun;
   static constexpr size_t OFF_W = OFF_RUNV + 2 * kFusedMaxRun;
   static constexpr size_t OFF_HIST = OFF_W + 4 * 2 * D;       // uint32 [kHistWords]
-  static constexpr size_t OFF_MISC = OFF_HIST + 4 * 288;      // uint32 [16] + uint64 [16]
+  static constexpr size_t OFF_MISC = OFF_HIST + 4 * kHistWords;   // uint32 [16] + uint64 [16]
   static constexpr size_t OFF_MTAB = OFF_MISC + 192;          // float [16 ranks][2G]
   static constexpr size_t OFF_BAR = OFF_MTAB + 4 * 16 * 2 * G;
   static constexpr size_t SMEM = OFF_BAR + 8 * NST + 1024;    // + alignment slack

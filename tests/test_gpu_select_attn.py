@@ -124,7 +124,7 @@ def _score_rows(kind, n, gen):
     return torch.randn(n, generator=gen)
 
 
-@pytest.mark.parametrize("n", [5, 300, 2048, 8192, 23552])
+@pytest.mark.parametrize("n", [5, 300, 2048, 8192, 21440])
 @pytest.mark.parametrize("kind", ["coarse", "tied", "outliers", "ramp", "normal"])
 def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
     """Arbitrary score rows through the in-kernel selection: the oracle's rule exactly
