@@ -128,15 +128,15 @@ struct StepLayout {
   size_t scores, sel, cnt, acc, ml, ctr, ctr2, total;
 };
 
-// The per-group counters come first, at offsets that depend only on batch * num_kv_heads,
-// so calls of different shapes (sparse and dense, other k_max or split counts) on one
-// workspace keep finding them where the previous call returned them to zero.
 // Row stride of the step's scores: page_table_stride rounded up to four floats, so that every
 // row starts 16-byte aligned and can be copied into shared memory in bulk.
 size_t step_scores_stride(const kv_cache_desc* d) {
   return ((size_t)d->page_table_stride + 3) & ~(size_t)3;
 }
 
+// The per-group counters come first, at offsets that depend only on batch * num_kv_heads,
+// so calls of different shapes (sparse and dense, other k_max or split counts) on one
+// workspace keep finding them where the previous call returned them to zero.
 StepLayout step_layout(const kv_cache_desc* d, int Hq, int k_max, int S) {
   StepLayout L;
   const size_t groups = (size_t)d->batch * d->num_kv_heads;
