@@ -46,15 +46,20 @@ cudaError_t launch_mma(const kv_cache_desc& d, const CUtensorMap& mk, const CUte
                        const int32_t* sel_cnt, int sel_stride, int S, float* part_acc,
                        float* part_ml, DevCtx ctx, cudaStream_t st, const StepArgs& sa) {
   using C = MmaCfg<D, G>;
-  auto kern = split_attn_mma_kernel<D, G>;
-  static int attr_set_for_device[64] = {0};
+  // the filtering instantiation only where the in-kernel selection can use it: long tables
+  // keeping at most a sixteenth of their pages (cta_threshold)
+  const bool is_long = sa.scores != nullptr &&
+                       d.page_table_stride >= topk_detail::kPrefilterMinPages &&
+                       16L * sa.k_max <= (long)d.page_table_stride;
+  auto kern = is_long ? split_attn_mma_kernel<D, G, true> : split_attn_mma_kernel<D, G, false>;
+  static int attr_set_for_device[2][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set_for_device[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set_for_device[is_long][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set_for_device[dev] = 1;
+    attr_set_for_device[is_long][dev] = 1;
   }
   dim3 grid(S, d.num_kv_heads, d.batch);
   return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, mk, mv, d,

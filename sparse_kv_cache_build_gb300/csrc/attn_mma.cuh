@@ -180,7 +180,7 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
   using C = MmaCfg<D, G>;
   const int tid = gtid >= 0 ? gtid : (int)threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int gid = lane >> 2, tig = lane & 3;
+  const int tig = lane & 3;
   const int lm = lane >> 3, lr = lane & 7;
   const int PPT = kTileTokens / PS;
   const int n_tiles = ceil_div(np, PPT);
@@ -368,8 +368,10 @@ struct StepArgs {
   float* lse;
 };
 
-// Two CTAs per SM (shared memory allows no more), so up to 255 registers a thread.
-template <int D, int G>
+// Two CTAs per SM (shared memory allows no more), so up to 255 registers a thread. LONG: the
+// in-kernel selection may filter the keys by a sample first (cta_threshold); launched for
+// page tables of at least topk_detail::kPrefilterMinPages pages keeping at most a sixteenth.
+template <int D, int G, bool LONG>
 __global__ void __launch_bounds__(MmaCfg<D, G>::THREADS, 2)
 split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, kv_cache_desc d,
@@ -477,8 +479,8 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     const CtaKeys K = cta_keys_finish<C::THREADS>(ring, n_pages, misc + 8);
     uint32_t T, take_eq;
-    cta_threshold<C::THREADS>(K, cnt, ring + used, misc, ring + used + kHistWords,
-                              C::RING_WORDS - used - kHistWords, T, take_eq);
+    cta_threshold<C::THREADS, LONG>(K, cnt, ring + used, misc, ring + used + kHistWords,
+                                    C::RING_WORDS - used - kHistWords, T, take_eq);
     // this CTA's run only; each CTA also writes its run's part of the selection output
     int32_t* sel_out = sa.sel_out;
     cta_compact<C::THREADS>(K, T, take_eq, reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT),

@@ -219,27 +219,20 @@ __device__ __forceinline__ void pick_bin(const uint32_t* hist, uint32_t remainin
 
 }  // namespace topk_detail
 
-// Threshold of the top k keys (0 < k < n). On return (block-uniform) the kept keys are those
-// > T and the first take_eq keys == T in page order. hist: kHistWords words; misc: 8 +
-// NT/32 words; cand: cand_cap words of 16-byte aligned scratch for the gathered keys of
-// the threshold's bin. NT divides kBins.
+namespace topk_detail {
+
+// The k-th largest of keys[0, n) (0 < k <= n) by radix passes, every key known to share the
+// bits `mask` with `prefix` and the highest bit of the remaining search being `top`. Returns
+// (block-uniform) T and take_eq as cta_threshold does. gather: after the first pass the bin's
+// keys may be gathered into cand (keys must then not be cand) and ranked directly when they
+// are at most one per thread; otherwise every pass runs over keys.
 template <int NT>
-__device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t* misc,
-                              uint32_t* cand, int cand_cap, uint32_t& T, uint32_t& take_eq) {
-  using namespace topk_detail;
+__device__ __forceinline__ void radix_kth(const uint32_t* keys, int n, int k, int top, uint32_t mask,
+                          uint32_t prefix, bool gather, uint32_t* hist, uint32_t* misc,
+                          uint32_t* cand, int cand_cap, uint32_t& T, uint32_t& take_eq) {
   const int tid = threadIdx.x;
-  const uint32_t* keys = K.keys;
-  const int n = K.n;
-  if (K.diff == 0u) {                        // every key equal: the first k pages
-    T = K.common;
-    take_eq = (uint32_t)k;
-    return;
-  }
-  int top = 31 - __clz(K.diff);              // highest bit on which keys differ
-  uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
-  uint32_t prefix = K.common & mask;         // the bits every key shares
   uint32_t remaining = (uint32_t)k;
-  int ncand = -1;                            // -1: histogram every key, else cand[0, ncand)
+  int ncand = -1;                            // -1: histogram keys, else cand[0, ncand)
   for (;;) {
     const int lo = top >= kDigitBits - 1 ? top - (kDigitBits - 1) : 0;
     const uint32_t dmask = (2u << (top - lo)) - 1u;      // digit bits [lo, top]
@@ -275,7 +268,7 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
       return;
     }
     top = lo - 1;
-    if (ncand < 0 && (int)bin_count <= cand_cap) {
+    if (gather && ncand < 0 && (int)bin_count <= cand_cap) {
       // gather the bin's keys (any order), through a scan of per-thread counts
       uint32_t mine = 0u, total = 0u;
       for (int base = 0; base < n; base += NT * kB) {
@@ -337,11 +330,110 @@ __device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t*
   }
 }
 
+// The search window (highest bit, mask, prefix) of keys known to lie in [lo_key, hi_key].
+__device__ __forceinline__ int window_of(uint32_t lo_key, uint32_t hi_key, uint32_t& mask,
+                                         uint32_t& prefix) {
+  const int top = 31 - __clz(lo_key ^ hi_key);
+  mask = top == 31 ? 0u : ~((2u << top) - 1u);
+  prefix = lo_key & mask;
+  return top;
+}
+
+constexpr int kSample = 512;            // prefilter sample size
+constexpr int kPrefilterMinPages = 4096;
+
+}  // namespace topk_detail
+
+// Threshold of the top k keys (0 < k < n). On return (block-uniform) the kept keys are those
+// > T and the first take_eq keys == T in page order. hist: kHistWords words; misc: 8 +
+// NT/32 words; cand: cand_cap words of 16-byte aligned scratch for the gathered keys of
+// the threshold's bin. NT divides kBins.
+//
+// Histogram passes cost what the shared-memory atomics cost (~1.6 keys per clock per SM), so
+// a long group keeping few pages (n >= 4096, k <= n/16) is first filtered: a strided sample
+// of 512 keys gives, by the same radix search, a key L that about four standard deviations of
+// the sample rank more than k keys should reach; one compare pass counts the keys >= L, and
+// if they are at least k and fit in cand they are gathered and searched alone (every key
+// > T or == T is among them, since T >= L). Otherwise the search runs over every key.
+// PREFILTER = false compiles the filter out: merely present, it measured ~4 us slower on
+// 2048-page groups in the attention kernel, where it never runs.
+template <int NT, bool PREFILTER = true>
+__device__ void cta_threshold(const CtaKeys& K, int k, uint32_t* hist, uint32_t* misc,
+                              uint32_t* cand, int cand_cap, uint32_t& T, uint32_t& take_eq) {
+  using namespace topk_detail;
+  const int tid = threadIdx.x;
+  const uint32_t* keys = K.keys;
+  const int n = K.n;
+  if (K.diff == 0u) {                        // every key equal: the first k pages
+    T = K.common;
+    take_eq = (uint32_t)k;
+    return;
+  }
+  const uint32_t key_or = K.common | K.diff;  // >= every key
+  uint32_t mask, prefix;
+  const int top = window_of(K.common, key_or, mask, prefix);
+  if (PREFILTER && n >= kPrefilterMinPages && 16 * k <= n && cand_cap >= kSample) {
+    const float mu = (float)k * kSample / (float)n;
+    const int ks = (int)ceilf(mu + 4.f * sqrtf(mu * (1.f - (float)k / (float)n)) + 4.f);
+    if (ks < kSample) {
+      const int st = (n / kSample) | 1;
+      for (int j = tid; j < kSample; j += NT) cand[j] = keys[(int)(((long)j * st) % n)];
+      __syncthreads();
+      uint32_t L, te;
+      radix_kth<NT>(cand, kSample, ks, top, mask, prefix, false, hist, misc, cand, 0, L, te);
+      // count the keys >= L (each thread its own, for the gather's offsets)
+      uint32_t mine = 0u, total = 0u;
+      for (int base = 0; base < n; base += NT * kB) {
+        uint32_t v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int i = base + u * NT + tid;
+          v[u] = i < n ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) mine += (base + u * NT + tid < n) && v[u] >= L;
+      }
+      uint32_t at = block_excl_scan<NT>(mine, misc + 8, total);
+      if (total >= (uint32_t)k && total <= (uint32_t)cand_cap) {
+        for (int base = 0; base < n && mine != 0u; base += NT * kB) {
+          uint32_t v[kB];
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            const int i = base + u * NT + tid;
+            v[u] = i < n ? keys[i] : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            if ((base + u * NT + tid < n) && v[u] >= L) {
+              cand[at++] = v[u];
+              --mine;
+            }
+          }
+        }
+        __syncthreads();
+        if (L == key_or) {                   // every candidate equals L: the first k pages
+          T = L;
+          take_eq = (uint32_t)k;
+          return;
+        }
+        uint32_t cmask, cprefix;
+        const int ctop = window_of(L, key_or, cmask, cprefix);
+        radix_kth<NT>(cand, (int)total, k, ctop, cmask, cprefix, false, hist, misc, cand, 0, T,
+                      take_eq);
+        return;
+      }
+      __syncthreads();                       // misc + 8 is reused below
+    }
+  }
+  radix_kth<NT>(keys, n, k, top, mask, prefix, true, hist, misc, cand, cand_cap, T, take_eq);
+}
+
 // Ordered compaction: calls emit(page, pos) for every kept page whose position pos in the
 // ascending kept list lies in [w0, w1) (a CTA that needs one run of the list asks for that
 // window; 0 and k give the whole list). Warp w walks the pages [w * seg, (w + 1) * seg) 32 at
 // a time (seg a multiple of 32), so ballots order the pages inside each step; a warp whose
-// positions miss the window does nothing after the count, and a warp stops once past it. The
+// positions miss the window does nothing after the count, a batch of rounds whose kept pages
+// all precede the window only advances the counts, and a warp stops once past the window. The
 // ballots of a batch of rounds are taken before any emit branches. wtot: NT/32 doublewords.
 template <int NT, typename F>
 __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint64_t* wtot,
@@ -385,11 +477,20 @@ __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint
       const int i = base + u * 32 + lane;
       v[u] = i < s1 ? keys[i] : 0u;
     }
+    uint32_t batch_gt = 0u, batch_eq = 0u;
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
       const bool in = base + u * 32 + lane < s1;
       bg[u] = __ballot_sync(0xffffffffu, in && v[u] > T);
       be[u] = __ballot_sync(0xffffffffu, in && v[u] == T);
+      batch_gt += __popc(bg[u]);
+      batch_eq += __popc(be[u]);
+    }
+    // a batch whose kept pages all come before the window only advances the counts
+    if (gt_before + batch_gt + min(eq_before + batch_eq, take_eq) <= (uint32_t)w0) {
+      gt_before += batch_gt;
+      eq_before += batch_eq;
+      continue;
     }
 #pragma unroll
     for (int u = 0; u < kB; ++u) {

@@ -16,9 +16,9 @@
 // key, which with sink = 0 and local = k is the KV-window baseline ("Where Activation
 // Sparsity and KV-Cache Sparsity Cross in LLM Decoding", Tables 3 and 11).
 //
-// One 1024-thread block per group. Scores are mapped to unsigned keys whose integer order
-// is the float order. Groups whose keys fit in shared memory (up to ~48K pages) take the
-// block top-k of cta_topk.cuh: the score row arrives in shared memory by one bulk copy
+// One block per group (512 threads for the block top-k, 1024 for the original form). Scores
+// are mapped to unsigned keys whose integer order is the float order. Groups whose keys fit
+// in shared memory (up to ~48K pages) take the block top-k of cta_topk.cuh: the score row arrives in shared memory by one bulk copy
 // (loads where the row is not 16-byte aligned), the first radix digit starts at the highest
 // bit on which the keys differ, the threshold bin's keys are gathered and ranked, and the
 // kept pages are written in order by warp ballots after one scan of per-warp counts.
@@ -39,6 +39,7 @@ namespace skv {
 namespace {
 
 constexpr int kSelCand = 4096;               // gathered keys of the threshold's bin
+constexpr int kSelectCtaThreads = 512;       // threads of the block top-k kernel
 constexpr size_t kSelectCtaSmemLimit = 227 * 1024;   // shared memory a block may opt into
 
 // Shared words of the block top-k for groups of up to max_pages pages: keys, then candidates.
@@ -67,7 +68,7 @@ __device__ __forceinline__ int select_count(const int32_t* seq_lens, int PS, int
   return k;
 }
 
-__global__ void __launch_bounds__(kSelectThreads)
+__global__ void __launch_bounds__(kSelectCtaThreads)
 select_cta_kernel(const float* __restrict__ scores, int scores_stride,
                   const int32_t* __restrict__ seq_lens, int PS, int Hkv,
                   const int32_t* __restrict__ keep, double keep_ratio, int budget, int k_max,
@@ -75,9 +76,9 @@ select_cta_kernel(const float* __restrict__ scores, int scores_stride,
                   int32_t* __restrict__ sel_cnt, int table_stride, int key_words, DevCtx ctx) {
   extern __shared__ __align__(16) uint32_t words[];           // keys, then candidates
   __shared__ uint32_t hist[kHistWords];
-  __shared__ uint32_t misc[8 + kSelectThreads / 32];
-  __shared__ uint32_t red[cta_red_words<kSelectThreads>()];
-  __shared__ uint64_t wtot[kSelectThreads / 32];
+  __shared__ uint32_t misc[8 + kSelectCtaThreads / 32];
+  __shared__ uint32_t red[cta_red_words<kSelectCtaThreads>()];
+  __shared__ uint64_t wtot[kSelectCtaThreads / 32];
   __shared__ __align__(8) uint64_t s_bar;
   pdl_trigger();
   if (threadIdx.x == 0) {
@@ -94,7 +95,7 @@ select_cta_kernel(const float* __restrict__ scores, int scores_stride,
   int32_t* out = sel_idx + grp * k_max;
   if (threadIdx.x == 0) sel_cnt[grp] = k;
   if (k >= n) {                              // keep every page (also n == 0)
-    for (int i = threadIdx.x; i < n; i += kSelectThreads) out[i] = i;
+    for (int i = threadIdx.x; i < n; i += kSelectCtaThreads) out[i] = i;
     return;
   }
   if (k == 0) return;
@@ -105,16 +106,16 @@ select_cta_kernel(const float* __restrict__ scores, int scores_stride,
     if (!mbar_wait_bounded(&s_bar, 0u, ctx.wait_ns) && threadIdx.x == 0)
       flag(ctx, KV_DEVERR_TIMEOUT);
   } else if (have_row) {
-    cta_fill_loads<kSelectThreads>(words, row, n);
+    cta_fill_loads<kSelectCtaThreads>(words, row, n);
   }
-  const CtaKeys K = cta_keys_finish<kSelectThreads, true>(
+  const CtaKeys K = cta_keys_finish<kSelectCtaThreads, true>(
       words, n, red, [&](int i, uint32_t key) -> uint32_t {
         if (i < sink || i >= n - local) return 0xffffffffu;   // forced in
         return have_row ? key : 0u;
       });
   uint32_t T, take_eq;
-  cta_threshold<kSelectThreads>(K, k, hist, misc, words + key_words, kSelCand, T, take_eq);
-  cta_compact<kSelectThreads>(K, T, take_eq, wtot, 0, k, [&](int p, int pos) { out[pos] = p; });
+  cta_threshold<kSelectCtaThreads>(K, k, hist, misc, words + key_words, kSelCand, T, take_eq);
+  cta_compact<kSelectCtaThreads>(K, T, take_eq, wtot, 0, k, [&](int p, int pos) { out[pos] = p; });
 }
 
 // Block-wide exclusive scan of a 64-bit value (two packed 32-bit counters).
@@ -298,13 +299,13 @@ cudaError_t launch_select_topk(const float* scores, int scores_stride, const int
   dim3 grid(Hkv, batch);
   const size_t words = select_cta_words(page_table_stride);
   const size_t smem = 4 * words;
-  if (smem + 4 * (kHistWords + 8 + kSelectThreads / 32) + 8 * (kSelectThreads / 32) <=
-      kSelectCtaSmemLimit) {
+  if (smem + 4 * (kHistWords + 8 + kSelectCtaThreads / 32) + 8 * (kSelectCtaThreads / 32) +
+          1024 <= kSelectCtaSmemLimit) {
     // always: the kernel's static shared memory counts against the 48 KB default too
     cudaError_t e = cudaFuncSetAttribute(select_cta_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_cta_kernel, grid, dim3(kSelectThreads), smem, s, scores,
+    return launch_pdl(select_cta_kernel, grid, dim3(kSelectCtaThreads), smem, s, scores,
                       scores_stride, seq_lens, page_size, Hkv, keep, keep_ratio, budget_pages,
                       k_max, sink, local, sel_idx, sel_cnt, page_table_stride,
                       (int)(words - kSelCand), ctx);

@@ -206,8 +206,8 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const CtaKeys K = cta_keys_finish<kFusedThreads, false>(
         ring_w, n, reinterpret_cast<uint32_t*>(s_misc64), [](int, uint32_t key) { return key; });
     uint32_t T, take_eq;
-    cta_threshold<kFusedThreads>(K, k, s_hist, s_misc, ring_w + 2 * KW, C::RING_WORDS - 2 * KW,
-                                 T, take_eq);
+    cta_threshold<kFusedThreads, false>(K, k, s_hist, s_misc, ring_w + 2 * KW,
+                                        C::RING_WORDS - 2 * KW, T, take_eq);
 
     // ================= 3. this split's run of the ascending kept list =====================
     const int c2 = ceil_div(k, CL);

@@ -197,10 +197,12 @@ def test_one_workspace_serves_sparse_dense_and_other_k_max():
 
 
 def test_decode_step_plan_by_shape():
-    """kv_decode_step's plan: short bf16 groups select inside the attention kernel, long ones
-    in the score launch, dense bf16 is the attention kernel alone, fp32 keeps four kernels;
+    """kv_decode_step's plan: bf16 groups of up to 16384 pages select inside the attention
+    kernel, longer ones in the score launch, dense bf16 is the attention kernel alone, fp32
+    keeps four kernels;
     the plan's kernels called one by one give kv_decode_step's output."""
-    cases = [("bf16", (1000, 4097, 37), 1), ("bf16", (8200 * 16,), 2), ("fp32", (1000, 37), 0)]
+    cases = [("bf16", (1000, 4097, 37), 1), ("bf16", (8200 * 16,), 1), ("bf16", (16400 * 16,), 2),
+             ("fp32", (1000, 37), 0)]
     for dtype, lens, want in cases:
         w, c = _make(dtype, 128, 4, 16, lens)
         kv = skv.PagedKV.from_cache(c)
