@@ -114,6 +114,16 @@ def test_score_select_long_group():
         _compare_with_separate_calls(kv, c.q, stats, c.seq_lens, 16, keep, reps=1)
 
 
+def test_score_select_long_group_keeping_few():
+    """A 5000-page group keeping 2 %: the last score block's top-k filters the keys by a
+    sample first; the separate calls and the oracle's rule on the same scores agree."""
+    w, c = _make("bf16", 128, 4, 16, (5000 * 16, 4500 * 16 - 5), Hkv=2)
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    for keep in (dict(keep_ratio=0.02), dict(budget_pages=200)):
+        _compare_with_separate_calls(kv, c.q, stats, c.seq_lens, 16, keep, reps=1)
+
+
 @pytest.mark.parametrize("pages", [8191, 8192, 8193])
 def test_selection_at_the_shared_memory_default(pages):
     """Groups whose keys and candidate scratch take 48 KB of dynamic shared memory, the

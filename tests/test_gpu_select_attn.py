@@ -162,3 +162,31 @@ def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
                                             torch.from_numpy(cnt).cuda(), num_splits=S)
         out2, _ = skv.kv_merge_splits(acc, ml)
         np.testing.assert_allclose(f64(out), f64(out2), rtol=0, atol=1e-6)
+
+
+@pytest.mark.parametrize("n", [4096, 9001, 20000])
+@pytest.mark.parametrize("kind", ["coarse", "outliers", "ramp", "normal"])
+def test_select_topk_long_groups_keeping_few(n, kind):
+    """Groups of 4096 pages or more keeping at most a sixteenth, where the block top-k first
+    filters the keys by a sample: the oracle's rule exactly (score descending, lower page
+    first on ties, ascending output), ties, outliers and ramps included."""
+    PS, Hkv, B = 16, 2, 2
+    gen = torch.Generator().manual_seed(n + 31 * len(kind))
+    scores = torch.stack([torch.stack([_score_rows(kind, n, gen) for _ in range(Hkv)])
+                          for _ in range(B)]).contiguous()
+    lens = torch.tensor([n * PS, n * PS - 7 * PS - 3], dtype=torch.int32)
+    sh = scores.double().numpy()
+    for kw in (dict(keep_ratio=0.02), dict(budget_pages=max(1, n // 40))):
+        ratio, budget = kw.get("keep_ratio", 0.0), kw.get("budget_pages", 0)
+        k_max = skv.max_keep_pages(n, ratio if not budget else None, budget or None)
+        sel, cnt = skv.kv_select_topk(scores.cuda(), lens.cuda(), PS, keep_ratio=ratio,
+                                      budget_pages=budget, k_max=k_max)
+        assert_no_device_error()
+        sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+        for b in range(B):
+            nb = oracle.num_pages(int(lens[b]), PS)
+            k = (oracle.keep_count(nb, budget_tokens=budget * PS, page_size=PS) if budget
+                 else oracle.keep_count(nb, ratio=ratio))
+            for g in range(Hkv):
+                assert cnt[b, g] == k
+                np.testing.assert_array_equal(sel[b, g, :k], oracle.select_pages(sh[b, g, :nb], k))
