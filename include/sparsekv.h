@@ -347,9 +347,9 @@ size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_
  * rounding of the merge.
  * out: device [batch][num_q_heads][head_dim] float32; lse: [batch][num_q_heads] or NULL.
  * For bf16 caches the step takes two launches, the merge running in the attention
- * kernel's last CTA per group: groups of up to 4096 pages (page_table_stride) run
- * kv_score_pages then kv_select_decode_attn, longer ones kv_score_select then
- * kv_decode_attn_merge; the dense step is kv_decode_attn_merge alone
+ * kernel's last CTA per group: groups of up to 16384 pages (page_table_stride, and within
+ * kv_select_decode_attn's limit) run kv_score_pages then kv_select_decode_attn, longer ones
+ * kv_score_select then kv_decode_attn_merge; the dense step is kv_decode_attn_merge alone
  * (kv_decode_step_plan tells which).
  * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned, ZERO-
  * FILLED ONCE before its first use: it starts with two int32 counters per group, at offsets
