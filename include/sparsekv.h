@@ -312,8 +312,10 @@ kv_status kv_merge_splits(const float* part_acc, const float* part_ml, int32_t b
                           float* out, float* lse, cudaStream_t stream);
 
 /*
- * kv_auto_num_splits -- host: a split count that fills every SM of the current device
- * for a cache of this shape when each (b, g) group keeps about pages_per_group pages.
+ * kv_auto_num_splits -- host: a split count for a cache of this shape when each (b, g) group
+ * keeps about pages_per_group pages: the most splits whose CTAs (batch * num_kv_heads * S)
+ * all fit the device's resident CTA slots at once (no partial second wave), at least one,
+ * at most one per two 64-token tiles, and at least what the merge's split limit needs.
  * Returns >= 1, or a negative kv_status on a bad argument.
  */
 int32_t kv_auto_num_splits(const kv_cache_desc* cache, int32_t num_q_heads,
