@@ -24,10 +24,14 @@
 //     gathered keys only;
 //   * histograms take plain shared-memory atomics into a bank-padded array (warp-wide
 //     match instructions cost hundreds of cycles when a warp holds many distinct digits);
+//     their throughput (~1.6 keys per clock per SM) is what a pass over many keys costs, so
+//     long groups keeping few pages histogram only the keys at or above a bound taken from
+//     a sample (cta_threshold);
 //   * block reductions read the per-warp words one per lane and reduce with warp
 //     instructions, rather than every thread reading every warp's word;
 //   * the ordered compaction gives each warp a contiguous segment of pages, walked 32 at a
-//     time with ballots, after one scan of the per-warp counts.
+//     time with ballots, after one scan of the per-warp counts, and emits only a requested
+//     window of positions (one attention CTA's run).
 #pragma once
 
 #include "kv_internal.cuh"
@@ -350,11 +354,13 @@ constexpr int kPrefilterMinPages = 4096;
 // the threshold's bin. NT divides kBins.
 //
 // Histogram passes cost what the shared-memory atomics cost (~1.6 keys per clock per SM), so
-// a long group keeping few pages (n >= 4096, k <= n/16) is first filtered: a strided sample
-// of 512 keys gives, by the same radix search, a key L that about four standard deviations of
-// the sample rank more than k keys should reach; one compare pass counts the keys >= L, and
-// if they are at least k and fit in cand they are gathered and searched alone (every key
-// > T or == T is among them, since T >= L). Otherwise the search runs over every key.
+// a long group keeping few pages (n >= 4096, k <= n/16) is first filtered: from a strided
+// sample of 512 keys the same radix search takes the ks-th largest key L, ks lying about four
+// standard deviations of the sample rank above the rank the k-th largest key is expected to
+// have there, so that at least k keys are >= L but not many more; one compare pass counts the
+// keys >= L, and if they are at least k and fit in cand they are gathered and searched alone
+// (every key > T or == T is among them, since T >= L). Otherwise the search runs over every
+// key, so the sample decides the speed, never the result.
 // PREFILTER = false compiles the filter out: merely present, it measured ~4 us slower on
 // 2048-page groups in the attention kernel, where it never runs.
 template <int NT, bool PREFILTER = true>
