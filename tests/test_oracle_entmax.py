@@ -172,3 +172,107 @@ def test_entmax_select_invariants_and_adaptive_budget():
             delta = E.entmax_dropped_mass(q, kk, table, lens, PS, 0.125, [sel])
             assert np.abs(delta).max() < 1e-12
     assert sum(map(len, kept["flat"])) > 3 * sum(map(len, kept["planted"]))
+
+
+# ---------------------------------------------------------------------------------------
+# Pins of the selector's moments and of its token weighting (hand-worked cases, quadrature,
+# Monte Carlo): a slip in the within-box variance (the 1/12, the q_d^2 weights, the
+# (scale/2)^2 factor) or page- instead of token-weighting of mu and sigma^2 fails here.
+
+import json
+import os
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "entmax_cases.json")
+
+
+def _one_page(q, mn, mx):
+    """Arrays for page_moments: one sequence, one KV head, one query head, one full page."""
+    D = len(q)
+    PS = 16
+    qa = np.asarray(q, dtype=np.float64).reshape(1, 1, D)
+    mna = np.asarray(mn, dtype=np.float64).reshape(1, 1, D)
+    mxa = np.asarray(mx, dtype=np.float64).reshape(1, 1, D)
+    return qa, mna, mxa, np.array([[0]]), np.array([PS]), PS
+
+
+def test_page_moments_golden():
+    for case in json.load(open(GOLDEN))["moments"]:
+        q, mn, mx, table, lens, PS = _one_page(case["q"], case["mn"], case["mx"])
+        zb, c, v, nt = E.page_moments(q, mn, mx, table, lens, PS, case["scale"])
+        assert zb[0][0, 0] == pytest.approx(case["expected_zb"], abs=1e-15)
+        assert c[0][0, 0] == pytest.approx(case["expected_c"], abs=1e-15)
+        assert v[0][0, 0] == pytest.approx(case["expected_v"], rel=1e-14)
+        assert nt[0][0] == PS
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_page_moments_match_monte_carlo_uniform_keys(seed):
+    """Keys drawn uniformly in the box, coordinate by coordinate: the sample mean and
+    variance of z = (scale/2) q.k land within six standard errors of c and v. The query's
+    coordinates span 0.1 to 3 in magnitude with both signs and the box widths 0 to 3, so
+    weighting by |q_d| or q_d, another divisor than 12, or (scale/2) unsquared all miss."""
+    rng = np.random.default_rng(100 + seed)
+    D = 12
+    q = rng.choice([-1.0, 1.0], D) * rng.uniform(0.1, 3.0, D)
+    mn = rng.normal(0.0, 1.0, D)
+    mx = mn + rng.uniform(0.0, 3.0, D)
+    mx[0] = mn[0]                                      # one degenerate (zero-width) side
+    scale = 0.35
+    qa, mna, mxa, table, lens, PS = _one_page(q, mn, mx)
+    zb, c, v, _ = E.page_moments(qa, mna, mxa, table, lens, PS, scale)
+    n = 400_000
+    keys = rng.uniform(mn, mx, size=(n, D))
+    z = (scale / 2.0) * keys @ q
+    se_mean = math.sqrt(v[0][0, 0] / n)
+    assert abs(z.mean() - c[0][0, 0]) < 6 * se_mean
+    # variance of the sample variance: (m4 - sigma^4) / n, with m4 the sample's 4th moment
+    dz = z - z.mean()
+    s2 = float((dz ** 2).mean())
+    se_var = math.sqrt(max(float((dz ** 4).mean()) - s2 * s2, 0.0) / n)
+    assert abs(s2 - v[0][0, 0]) < 6 * se_var
+    assert zb[0][0, 0] >= z.max()
+
+
+def _tau_by_quadrature(mu, sigma2, count):
+    """tau with count * int (x - tau)^2 N(x; mu, sigma2) dx over x > tau = 1, by adaptive
+    quadrature and Brent's root finder (independent of the oracle's closed form)."""
+    from scipy import integrate, optimize
+    s = math.sqrt(sigma2)
+
+    def tail(t):
+        f = lambda x: (x - t) ** 2 * math.exp(-0.5 * ((x - mu) / s) ** 2) / (s * math.sqrt(2 * math.pi))  # noqa: E731
+        return integrate.quad(f, t, mu + 60 * s, limit=400, epsabs=1e-15, epsrel=1e-13)[0]
+
+    return optimize.brentq(lambda t: count * tail(t) - 1.0, mu - 1.0 - 50 * s,
+                           mu + 50 * s + 1.0, xtol=1e-15, rtol=1e-14)
+
+
+def test_entmax_select_golden_token_weighted_threshold():
+    for case in json.load(open(GOLDEN))["select"]:
+        G = case["G"]
+        zb, c, v = (np.asarray(case[k], dtype=np.float64) for k in ("zb", "c", "v"))
+        nt = np.asarray(case["n_tok"], dtype=np.float64)
+        assert nt.sum() == case["expected_count"]
+        sel, tau_hat = E.entmax_select(zb, c, v, nt, G)
+        for h in range(zb.shape[0]):
+            want = _tau_by_quadrature(case["expected_mu"][h], case["expected_sigma2"][h],
+                                      case["expected_count"])
+            assert tau_hat[h] == pytest.approx(want, abs=1e-9)
+        assert [list(map(int, pages)) for pages in sel] == [case["expected_pages"]]
+
+
+def test_entmax_select_weights_pages_by_their_tokens():
+    """Splitting a page into two half pages with the same box (same c and v, half the
+    tokens each) changes nothing under token weighting; under page weighting it would."""
+    rng = np.random.default_rng(9)
+    n = 12
+    c = rng.normal(0.0, 1.0, (1, n))
+    v = rng.uniform(0.0, 0.2, (1, n))
+    zb = c + rng.uniform(0.5, 2.0, (1, n))
+    nt = rng.integers(2, 9, n).astype(np.float64) * 2.0
+    _, tau = E.entmax_select(zb, c, v, nt, 1)
+    split = lambda a: np.concatenate([a, a[:, :1]], axis=1)  # noqa: E731
+    nt2 = np.concatenate([nt, nt[:1] / 2.0])
+    nt2[0] /= 2.0
+    _, tau2 = E.entmax_select(split(zb), split(c), split(v), nt2, 1)
+    assert tau2[0] == pytest.approx(tau[0], abs=1e-12)
