@@ -6,6 +6,14 @@ already exist; their build is timed separately). The dense step is the same atte
 kernel with every page kept, plus the merge. Inputs are resident in HBM; L2 is flushed
 (a 256 MiB write, twice the L2) before every timed step, outside the timed events.
 
+The headline (``value``) is the 32K workload. The same line carries ``configs``: the
+128K workload at both keep ratios, the batched-serving workload and the 1M workload, each
+with its sparse and dense steps, FP8-statistics step, KV-window step, attention-kernel
+roofline, byte bound, dropped mass and a bounded oracle baseline; and ``blocks``: the
+headline sparse/dense pair timed in fresh processes, with paired ratios and resampled
+intervals. ``e2e`` goes through the captured step (``kv_decode_step_graph_*``) with the
+query and output copied between pinned host memory and the device inside the timing.
+
 Prints one JSON line. ``--impl reference`` times the float64 CPU oracle on the same
 workload instead (the reference arm of this comparison).
 """
@@ -172,6 +180,353 @@ def byte_account(w, n_pages, sel_cnt, S):
                 pages=n_total * Hkv)
 
 
+
+# ----------------------------------------------------------------------------- shared timing
+
+# Configurations measured after the headline one (workload, index of its keep ratio): the rest
+# of the metric's 32K-1M range.
+EXTRA_CONFIGS = (("llama8b_128k", 0), ("llama8b_128k", 1), ("batched_serving", 0),
+                 ("llama70b_1m", 0))
+
+
+def capture_graph(fn):
+    """One CUDA graph of fn() (captured on a side stream, as torch requires)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(graph, steps, flush):
+    """Event-timed replays of graph, L2 flushed before each (outside the events); µs."""
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = []
+    for _ in range(steps):
+        flush.zero_()
+        t0.record()
+        graph.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        res.append(t0.elapsed_time(t1) * 1e3)
+    return res
+
+
+def spread(xs):
+    return {"median": round(statistics.median(xs), 3), "p10": round(pct(xs, 10), 3),
+            "p90": round(pct(xs, 90), 3)}
+
+
+def window_byte_account(w, k_total, n_total):
+    """Algorithmic bytes of the KV-window step (the last k pages of every group, no scoring):
+    selected K+V, q, table entries and indices; no statistics."""
+    eb = 2 if w.dtype == "bf16" else 4
+    return (k_total * w.page_size * w.head_dim * 2 * eb
+            + w.batch * w.num_q_heads * w.head_dim * eb + n_total * 4 + k_total * 4)
+
+
+def oracle_group_baseline(c, w, keep, budget_s, b=0, g=0):
+    """The float64 oracle's sparse step (scores, top-k, attention; statistics prebuilt) on ONE
+    (sequence, KV head) group of the workload, repeated for about budget_s seconds, scaled to a
+    whole step by the pages of every group over the pages of this one."""
+    import oracle
+    PS, G = w.page_size, w.group_size
+    n = oracle.num_pages(int(c.seq_lens[b]), PS)
+    phys = c.page_table[b, :n].to(torch.int64)
+    f32 = lambda t: t.detach().cpu().to(torch.float32).numpy()  # noqa: E731
+    K = f32(c.k_pool.index_select(0, phys)[:, g:g + 1])
+    V = f32(c.v_pool.index_select(0, phys)[:, g:g + 1])
+    q = f32(c.q[b:b + 1, g * G:(g + 1) * G]).astype(np.float64)
+    table = np.arange(n, dtype=np.int64)[None, :]
+    lens = np.array([int(c.seq_lens[b])])
+    mn, mx = oracle.page_stats(K, table, lens, PS)
+    if "keep_pages" in keep:
+        k = min(n, keep["keep_pages"])
+    elif "budget_pages" in keep:
+        k = oracle.keep_count(n, budget_tokens=keep["budget_pages"] * PS, page_size=PS)
+    else:
+        k = oracle.keep_count(n, ratio=keep["keep_ratio"])
+    times, cpu_t = [], []
+    t_end = time.perf_counter() + budget_s
+    while not times or time.perf_counter() < t_end:
+        c0, w0 = time.process_time(), time.perf_counter()
+        sc = oracle.page_scores(q, mn, mx, table, lens, PS)
+        sel = oracle.select_all_groups(sc, [k])
+        oracle.attend(q, K, V, table, lens, PS, w.sm_scale, selected=sel)
+        times.append((time.perf_counter() - w0) * 1e6)
+        cpu_t.append((time.process_time() - c0) * 1e6)
+    total_pages = sum(c.pages_per_seq) * w.num_kv_heads
+    scale = total_pages / max(n, 1)
+    cores = max(1, round(sum(cpu_t) / sum(times)))
+    return {"value": round(statistics.median(times) * scale, 1), "unit": "us/step",
+            "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} runs of the float64 oracle's sparse step on one (sequence, "
+                      f"KV head) group of {w.name} ({n} pages, statistics prebuilt); value "
+                      f"scaled to the whole step by the {total_pages} pages of all groups / "
+                      f"{n}"}
+
+
+def measure_config(name, keep_index, args, dev, flush, peak, peak_kind):
+    """One configuration of the metric's range: the sparse step and the dense step through
+    kv_decode_step (L2 flushed before each), the FP8-statistics step, the KV-window step
+    through the same attention kernel, the attention kernel's roofline, the dropped mass and a
+    bounded oracle baseline."""
+    import sparse_kv_cache_build_gb300 as skv
+    from sparse_kv_cache_build_gb300 import binding, inputs
+
+    w = inputs.workload(name)
+    label, keep = keep_setting(w, keep_index)
+    c = inputs.make_cache(w, dev)
+    kv = skv.PagedKV.from_cache(c)
+    B, Hq, Hkv, D, PS = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size
+    stats = skv.kv_build_page_stats(kv)
+    stats8, exps8 = skv.kv_build_page_stats_fp8(kv)
+    step_kw = dict(keep_ratio=keep.get("keep_ratio", 1.0), budget_pages=keep.get("budget_pages", 0))
+    k_max = skv.max_keep_pages(kv.stride, keep.get("keep_ratio"), keep.get("budget_pages"))
+    ws = torch.zeros((skv.kv_decode_step_workspace_size(kv, Hq, k_max),), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    plan, S = skv.kv_decode_step_plan(kv, Hq, k_max=k_max, **step_kw)
+    dense_plan, S_dense = skv.kv_decode_step_plan(kv, Hq, keep_ratio=1.0)
+    scores = torch.empty((B, Hkv, kv.stride), dtype=torch.float32, device=dev)
+    sel = torch.empty((B, Hkv, k_max), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=dev)
+    ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device=dev)
+    ctr = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    ctr2 = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+
+    def sparse():
+        skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
+                           workspace=ws, **step_kw)
+
+    def dense():
+        skv.kv_decode_step(kv, c.q, w.sm_scale, keep_ratio=1.0, out=out, lse=lse, workspace=ws)
+
+    def fp8():
+        skv.kv_decode_step_fp8(kv, c.q, w.sm_scale, stats8, exps8, k_max=k_max, out=out, lse=lse,
+                               workspace=ws, **step_kw)
+
+    # the KV window: the last k pages of every group, no scoring, same attention kernel
+    local = k_max
+    sel_w = torch.empty((B, Hkv, local), dtype=torch.int32, device=dev)
+    cnt_w = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    S_w = skv.kv_auto_num_splits(kv, Hq, local)
+    acc_w = torch.empty((B, Hq, S_w, D), dtype=torch.float32, device=dev)
+    ml_w = torch.empty((B, Hq, S_w, 2), dtype=torch.float32, device=dev)
+    ctr_w = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+
+    def window():
+        skv.kv_select_structured(None, c.seq_lens, PS, B, Hkv, kv.stride, sink_pages=0,
+                                 local_pages=local, k_max=local, sel_idx=sel_w, sel_cnt=cnt_w)
+        skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel_w, cnt_w, num_splits=S_w,
+                                 part_acc=acc_w, part_ml=ml_w, counters=ctr_w, out=out, lse=lse)
+
+    # the step's kernels one by one with events between them (kernel durations)
+    marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+    two_launch = plan in (1, 2, 6, 7)
+
+    def marked():
+        marks[0].record()
+        if plan in (1, 6):
+            skv.kv_score_pages(kv, c.q, stats, scores)
+        else:
+            skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
+                                sel_idx=sel, sel_cnt=cnt, **step_kw)
+        marks[1].record()
+        if plan in (1, 6):
+            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
+                                      part_acc=acc, part_ml=ml, counters=ctr2, out=out,
+                                      lse=lse, sel_idx=sel, sel_cnt=cnt, merge=plan == 1,
+                                      **step_kw)
+        elif plan == 2:
+            skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
+                                     part_ml=ml, counters=ctr2, out=out, lse=lse)
+        else:
+            skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, sel, cnt, num_splits=S,
+                                      part_acc=acc, part_ml=ml)
+        marks[2].record()
+        if plan in (6, 7):
+            skv.kv_merge_splits(acc, ml, out, lse)
+
+    fns = [sparse, dense, fp8, window] + ([marked] if two_launch else [])
+    for _ in range(max(1, args.warmup)):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    st, flags = skv.kv_check_device_errors()
+    if st != 0:
+        raise RuntimeError(f"{name}: device error word {flags:#x} after warm-up")
+    graphs = [capture_graph(f) for f in fns]
+    for _ in range(args.warmup):
+        for g in graphs:
+            flush.zero_()
+            g.replay()
+    torch.cuda.synchronize()
+    steps = args.steps
+    sparse_us = time_replays(graphs[0], steps, flush)
+    dense_us = time_replays(graphs[1], steps, flush)
+    fp8_us = time_replays(graphs[2], steps, flush)
+    window_us = time_replays(graphs[3], steps, flush)
+    attn_us = []
+    if two_launch:
+        for _ in range(steps):
+            flush.zero_()
+            graphs[4].replay()
+            torch.cuda.synchronize()
+            attn_us.append(marks[1].elapsed_time(marks[2]) * 1e3)
+    st, flags = skv.kv_check_device_errors()
+    if st != 0:
+        raise RuntimeError(f"{name}: device error word {flags:#x} after the timed region")
+
+    # bytes, roofline, dropped mass (outside the timed regions)
+    marked()
+    window()
+    torch.cuda.synchronize()
+    sel_cnt = cnt.cpu().numpy()
+    acct = byte_account(w, c.pages_per_seq, sel_cnt, S)
+    w_bytes = window_byte_account(w, int(cnt_w.sum()), int(sum(c.pages_per_seq)))
+    delta = float(skv.kv_dropped_mass(kv, c.q, w.sm_scale, sel, cnt).mean())
+    sparse_med, dense_med = statistics.median(sparse_us), statistics.median(dense_us)
+    window_med = statistics.median(window_us)
+    res = {
+        "workload": w.name, "description": w.description, "keep": label,
+        "context_tokens": int(c.seq_lens.sum()),
+        "step_path": f"kv_decode_step plan {plan}: {binding.PLANS[plan]}, {S} splits",
+        "dense_path": f"kv_decode_step plan {dense_plan}: {binding.PLANS[dense_plan]}, "
+                      f"{S_dense} splits",
+        "sparse_us": spread(sparse_us), "dense_us": spread(dense_us),
+        "speedup_vs_dense": round(dense_med / sparse_med, 3),
+        "byte_bound": round(acct["dense_step"] / acct["sparse_step"], 3),
+        "step_gbs": {"sparse": round(acct["sparse_step"] / (sparse_med * 1e-6) / 1e9, 1),
+                     "dense": round(acct["dense_step"] / (dense_med * 1e-6) / 1e9, 1)},
+        "kernel_cost_beyond_bytes_us": round(
+            sparse_med - dense_med * acct["sparse_step"] / acct["dense_step"], 3),
+        "fp8_stats_step_us": spread(fp8_us),
+        "kv_window": {"us": spread(window_us), "pages_per_group": local,
+                      "speedup_vs_dense": round(dense_med / window_med, 3),
+                      "byte_bound": round(acct["dense_step"] / w_bytes, 3),
+                      "path": "kv_select_structured (sink 0, last k pages, no scores), then "
+                              f"kv_decode_attn_merge, {S_w} splits"},
+        "dropped_mass_mean": round(delta, 5),
+        "bytes": {"sparse_step": acct["sparse_step"], "dense_step": acct["dense_step"],
+                  "kv_window_step": w_bytes},
+    }
+    if attn_us:
+        roof_bytes = ((acct["step_attn_launch"] if plan in (1, 2) else acct["attn_launch"])
+                      + (acct["scores_bytes"] if plan in (1, 6) else 0))
+        a_us = statistics.mean(attn_us)
+        ach = roof_bytes / (a_us * 1e-6) / 1e9
+        dense_mean = statistics.mean(dense_us)
+        res["roofline"] = {
+            "kernel": "split_attn_mma_kernel" + {1: " (select + attend + merge)",
+                                                 2: " (attend + merge)", 6: " (select + attend)",
+                                                 7: " (attend)"}[plan],
+            "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "peak_kind": peak_kind,
+            "unit": "GB/s", "frac": round(ach / peak, 4),
+            "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_us": round(a_us, 3),
+            "dense_same_kernel": {
+                "achieved": round(acct["dense_step"] / (dense_mean * 1e-6) / 1e9, 1),
+                "frac": round(acct["dense_step"] / (dense_mean * 1e-6) / 1e9 / peak, 4),
+                "avg_launch_us": round(dense_mean, 3)}}
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = oracle_group_baseline(c, w, keep, args.config_cpu_seconds)
+    n_step = 3 if plan in (6, 7) else (2 if plan in (1, 2) else 4)
+    res["gpu_launches"] = steps * (n_step + (1 if dense_plan in (3, 5) else 2) + n_step + 2
+                                   + (n_step if attn_us else 0))
+    del c, kv, stats, stats8, exps8, ws, graphs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_block_child(args):
+    """One fresh-process block: the headline sparse and dense steps, replayed alternately
+    (L2 flushed before each), printed as one JSON line for the parent."""
+    import sparse_kv_cache_build_gb300 as skv
+    from sparse_kv_cache_build_gb300 import binding, inputs
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    binding.lib()
+    w = inputs.workload(args.workload)
+    label, keep = keep_setting(w, args.keep_index)
+    c = inputs.make_cache(w, dev)
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    step_kw = dict(keep_ratio=keep.get("keep_ratio", 1.0), budget_pages=keep.get("budget_pages", 0))
+    k_max = skv.max_keep_pages(kv.stride, keep.get("keep_ratio"), keep.get("budget_pages"))
+    ws = torch.zeros((skv.kv_decode_step_workspace_size(kv, w.num_q_heads, k_max),),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def sparse():
+        skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, workspace=ws,
+                           **step_kw)
+
+    def dense():
+        skv.kv_decode_step(kv, c.q, w.sm_scale, keep_ratio=1.0, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        sparse()
+        dense()
+    gs, gd = capture_graph(sparse), capture_graph(dense)
+    for _ in range(args.warmup):
+        time_replays(gs, 1, flush)
+        time_replays(gd, 1, flush)
+    sp, de = [], []
+    for _ in range(args.steps):
+        sp += time_replays(gs, 1, flush)
+        de += time_replays(gd, 1, flush)
+    st, flags = skv.kv_check_device_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word {flags:#x}")
+    print(json.dumps({"sparse_us": sp, "dense_us": de}), flush=True)
+
+
+def run_blocks(args, n_blocks):
+    """n_blocks fresh processes, each timing the headline sparse and dense steps alternately:
+    per-block medians, paired dense/sparse ratios, and 95 % intervals of the mean over blocks
+    from 10,000 resamples of the blocks."""
+    per = []
+    for i in range(n_blocks):
+        cmd = [sys.executable, os.path.abspath(__file__), "--block-child", "--workload",
+               args.workload, "--keep-index", str(args.keep_index), "--steps",
+               str(args.block_steps), "--warmup", str(args.warmup)]
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+        if r.returncode != 0:
+            raise RuntimeError(f"block {i} failed: {r.stderr[-2000:]}")
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        per.append((statistics.median(d["sparse_us"]), statistics.median(d["dense_us"])))
+    sp = np.array([p[0] for p in per])
+    de = np.array([p[1] for p in per])
+    ratio = de / sp
+    rng = np.random.default_rng(12345)
+    idx = rng.integers(0, n_blocks, size=(10000, n_blocks))
+
+    def ci(x):
+        m = x[idx].mean(axis=1)
+        return [round(float(np.percentile(m, 2.5)), 3), round(float(np.percentile(m, 97.5)), 3)]
+
+    return {"blocks": n_blocks, "steps_per_block": args.block_steps,
+            "sparse_us_per_block": [round(float(x), 3) for x in sp],
+            "dense_us_per_block": [round(float(x), 3) for x in de],
+            "paired_speedup_per_block": [round(float(x), 4) for x in ratio],
+            "sparse_us_mean": round(float(sp.mean()), 3), "sparse_us_ci95": ci(sp),
+            "dense_us_mean": round(float(de.mean()), 3), "dense_us_ci95": ci(de),
+            "paired_speedup_mean": round(float(ratio.mean()), 4),
+            "paired_speedup_ci95": ci(ratio),
+            "method": "fresh process per block (sub-process); within a block the sparse and "
+                      "dense steps alternate, L2 flushed before each; ratio = dense median / "
+                      "sparse median of the block; interval = 2.5/97.5 percentiles of the mean "
+                      "over 10,000 resamples of the blocks"}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def keep_setting(w, which=0):
@@ -247,27 +602,53 @@ def run_ours(args):
                      device=dev)
     ctr = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
     ctr2 = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    def plan_kernels(which, ev=None):
+        """Plan `which`'s kernels one by one (ev: events recorded between them)."""
+        if ev is not None:
+            ev[0].record()
+        if which in (1, 6):
+            skv.kv_score_pages(kv, c.q, stats, scores)
+        else:
+            skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
+                                sel_idx=sel, sel_cnt=cnt, **step_kw)
+        if ev is not None:
+            ev[1].record()
+        if which == 1:
+            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
+                                      part_acc=acc, part_ml=ml, counters=ctr2, out=out,
+                                      lse=lse, sel_idx=sel, sel_cnt=cnt, **step_kw)
+        elif which == 6:
+            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
+                                      part_acc=acc, part_ml=ml, sel_idx=sel, sel_cnt=cnt,
+                                      merge=False, **step_kw)
+        elif which == 2:
+            skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
+                                     part_ml=ml, counters=ctr2, out=out, lse=lse)
+        else:
+            skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, sel, cnt, num_splits=S,
+                                      part_acc=acc, part_ml=ml)
+        if ev is not None:
+            ev[2].record()
+        if which in (6, 7):
+            skv.kv_merge_splits(acc, ml, out, lse)
+        if ev is not None:
+            ev[3].record()
+
     # the kernels kv_decode_step runs for this shape (KV_PLAN_*)
     plan, S_plan = (skv.kv_decode_step_plan(kv, Hq, k_max=k_max, **step_kw)
                     if step_kw is not None else (0, S))
     dense_plan, _ = skv.kv_decode_step_plan(kv, Hq, keep_ratio=1.0)
-    two_launch = plan in (1, 2)
+    # the staged plans: score (+ select), the attention kernel, and for plans 6 and 7 a
+    # merge kernel of its own
+    two_launch = plan in (1, 2, 6, 7)
     assert S_plan == S, (S_plan, S)
-    # the other two-launch form, timed beside it where the shape allows
+    # another staged form, timed beside it where the shape allows (for plans 6 and 7: the
+    # same kernels with the merge in the attention kernel's last CTA)
     alt_plan = None
     if step_kw is not None:
-        for cand in ((2,) if plan == 1 else (1,) if plan == 2 else (1, 2)):
+        for cand in {1: (2,), 2: (1,), 6: (1, 7), 7: (2,)}.get(plan, (1, 2)):
             try:
-                if cand == 1:
-                    skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores.zero_(), k_max=k_max,
-                                              num_splits=S, part_acc=acc, part_ml=ml,
-                                              counters=ctr2, out=out, lse=lse, **step_kw)
-                else:
-                    skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores,
-                                        counters=ctr, sel_idx=sel, sel_cnt=cnt, **step_kw)
-                    skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S,
-                                             part_acc=acc, part_ml=ml, counters=ctr2, out=out,
-                                             lse=lse)
+                plan_kernels(cand)
                 alt_plan = cand
                 break
             except binding.KVError:
@@ -276,33 +657,16 @@ def run_ours(args):
 
     try:
         marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-        smarks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        smarks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
         in_graph_events = True
     except TypeError:
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        smarks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        smarks = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         in_graph_events = False
 
     def plan_step(which, with_marks=False):
-        """A two-launch plan's kernels, called one by one through the C ABI."""
-        if with_marks:
-            smarks[0].record()
-        if which == 1:
-            skv.kv_score_pages(kv, c.q, stats, scores)
-        else:
-            skv.kv_score_select(kv, c.q, stats, k_max=k_max, scores=scores, counters=ctr,
-                                sel_idx=sel, sel_cnt=cnt, **step_kw)
-        if with_marks:
-            smarks[1].record()
-        if which == 1:
-            skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, k_max=k_max, num_splits=S,
-                                      part_acc=acc, part_ml=ml, counters=ctr2, out=out,
-                                      lse=lse, sel_idx=sel, sel_cnt=cnt, **step_kw)
-        else:
-            skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S, part_acc=acc,
-                                     part_ml=ml, counters=ctr2, out=out, lse=lse)
-        if with_marks:
-            smarks[2].record()
+        """A staged plan's kernels, called one by one through the C ABI."""
+        plan_kernels(which, smarks if with_marks else None)
 
     def two_launch_step(with_marks):
         plan_step(plan, with_marks)
@@ -360,6 +724,22 @@ def run_ours(args):
         skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, out=ent_out, tau=ent_tau,
                                   workspace=ent_dws)
 
+    # the KV window: the last k pages of every group (no scoring) through the same kernel
+    sel_w = torch.empty((B, Hkv, k_max), dtype=torch.int32, device=dev)
+    cnt_w = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    S_w = skv.kv_auto_num_splits(kv, Hq, k_max)
+    acc_w = torch.empty((B, Hq, S_w, D), dtype=torch.float32, device=dev)
+    ml_w = torch.empty((B, Hq, S_w, 2), dtype=torch.float32, device=dev)
+    ctr_w = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    out_w, lse_w = torch.empty_like(out), torch.empty_like(lse)
+
+    def window_step():
+        skv.kv_select_structured(None, c.seq_lens, PS, B, Hkv, kv.stride, sink_pages=0,
+                                 local_pages=k_max, k_max=k_max, sel_idx=sel_w, sel_cnt=cnt_w)
+        skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel_w, cnt_w, num_splits=S_w,
+                                 part_acc=acc_w, part_ml=ml_w, counters=ctr_w, out=out_w,
+                                 lse=lse_w)
+
     def one_launch_step():
         """The step as one cluster launch (where the shape allows it)."""
         skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
@@ -384,6 +764,8 @@ def run_ours(args):
             fp8_step()
         entmax_step()
         entmax_dense()
+        if step_kw is not None:
+            window_step()
     torch.cuda.synchronize()
     st, flags = skv.kv_check_device_errors()
     if st != 0:
@@ -397,8 +779,8 @@ def run_ours(args):
     # two-launch steps with event nodes between their kernels, replayed in their own flushed
     # loops to time each kernel (event nodes sit between the kernels, so their programmatic
     # launch overlap is lost there: those graphs time kernels, not steps)
-    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt, g_fp8, g_ent, g_entd = (
-        torch.cuda.CUDAGraph() for _ in range(10))
+    g_step, g_dense, g_four, g_marked, g_one, g_smarked, g_alt, g_fp8, g_ent, g_entd, g_win = (
+        torch.cuda.CUDAGraph() for _ in range(11))
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -423,6 +805,8 @@ def run_ours(args):
                 one_launch_step()
             with torch.cuda.graph(g_fp8, stream=side):
                 fp8_step()
+            with torch.cuda.graph(g_win, stream=side):
+                window_step()
         if alt_plan is not None:
             with torch.cuda.graph(g_alt, stream=side):
                 alt_step()
@@ -455,7 +839,7 @@ def run_ours(args):
 
     # ---- timed region: K steps of each kind, L2 flushed before every step ---------------
     kern_us = {"score": [], "select": [], "attn": [], "merge": []}
-    step_kern_us = {"first": [], "attention": []}
+    step_kern_us = {"first": [], "attention": [], "merge": []}
     barrier()
     with ClockSampler(local) as clk:
         step_us = timed(g_step)
@@ -467,6 +851,8 @@ def run_ours(args):
         one_us = timed(g_one) if one_launch_ran else []
         barrier()
         fp8_us = timed(g_fp8) if step_kw is not None else []
+        barrier()
+        win_us = timed(g_win) if step_kw is not None else []
         barrier()
         ent_us = timed(g_ent)
         barrier()
@@ -486,7 +872,8 @@ def run_ours(args):
                 g_smarked.replay()
                 torch.cuda.synchronize()
                 for i, k in enumerate(step_kern_us):
-                    step_kern_us[k].append(smarks[i].elapsed_time(smarks[i + 1]) * 1e3)
+                    if k != "merge" or plan in (6, 7):
+                        step_kern_us[k].append(smarks[i].elapsed_time(smarks[i + 1]) * 1e3)
         barrier()
     clocks = clk.summary()
 
@@ -502,7 +889,8 @@ def run_ours(args):
             two_launch_step(True)
             torch.cuda.synchronize()
             for i, k in enumerate(step_kern_us):
-                step_kern_us[k].append(smarks[i].elapsed_time(smarks[i + 1]) * 1e3)
+                if k != "merge" or plan in (6, 7):
+                    step_kern_us[k].append(smarks[i].elapsed_time(smarks[i + 1]) * 1e3)
 
     st, flags = skv.kv_check_device_errors()
     if st != 0:
@@ -518,27 +906,45 @@ def run_ours(args):
     cb = 3 * M + (B * Hkv * kv.stride * 4 + 255) // 256 * 256
     ent_kept = int(ent_ws[cb: cb + B * Hkv * 4].view(torch.int32).sum())
 
+    win_bytes = None
+    if step_kw is not None:
+        window_step()
+        torch.cuda.synchronize()
+        win_bytes = window_byte_account(w, int(cnt_w.sum()), int(sum(n_pages)))
+
     # dropped mass of this step (diagnostic, outside every timed region)
     delta = skv.kv_dropped_mass(kv, c.q, w.sm_scale, sel, cnt)
     delta_mean = float(delta.mean())
 
-    # ---- end to end through the public call, host buffers, copies inside the timing -----
+    # ---- end to end through the public API, host buffers, copies inside the timing -------
+    # (1) the captured step (kv_decode_step_graph_*), the call a serving loop makes per token:
+    #     the query copied from pinned host memory into the captured query buffer, one graph
+    #     launch, the output copied back to pinned host memory, then the host waits;
+    # (2) the same with a direct kv_decode_step call instead of the graph launch.
     q_host = c.q.detach().cpu().pin_memory()
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(c.q)
-    e2e_us = []
+    e2e_us, e2e_direct_us = [], []
     if step_kw is not None:
-        for i in range(args.warmup + min(args.steps, 500)):
-            flush.zero_()
-            torch.cuda.synchronize()
-            h0 = time.perf_counter()
-            q_dev.copy_(q_host, non_blocking=True)
-            skv.kv_decode_step(kv, q_dev, w.sm_scale, stats, k_max=k_max, out=out, lse=lse,
-                               workspace=ws, **step_kw)
-            out_host.copy_(out, non_blocking=True)
-            torch.cuda.synchronize()
-            if i >= args.warmup:
-                e2e_us.append((time.perf_counter() - h0) * 1e6)
+        ws_g = torch.zeros_like(ws)
+        sg = skv.DecodeStepGraph(kv, q_dev, w.sm_scale, stats, k_max=k_max, workspace=ws_g,
+                                 **step_kw)
+        for graph_call, res in ((True, e2e_us), (False, e2e_direct_us)):
+            for i in range(args.warmup + min(args.steps, 500)):
+                flush.zero_()
+                torch.cuda.synchronize()
+                h0 = time.perf_counter()
+                q_dev.copy_(q_host, non_blocking=True)
+                if graph_call:
+                    g_out, _ = sg.launch()
+                else:
+                    g_out, _ = skv.kv_decode_step(kv, q_dev, w.sm_scale, stats, k_max=k_max,
+                                                  out=out, lse=lse, workspace=ws, **step_kw)
+                out_host.copy_(g_out, non_blocking=True)
+                torch.cuda.synchronize()
+                if i >= args.warmup:
+                    res.append((time.perf_counter() - h0) * 1e6)
+        sg.close()
 
     # ---- max over ranks ------------------------------------------------------------------
     sparse_med = statistics.median(step_us)
@@ -557,9 +963,11 @@ def run_ours(args):
         roof_kernel, roof_bytes, roof_us = "fused_step_kernel", acct["sparse_step"], step_mean
         roof_source = os.path.join(CSRC, "step_fused.cu")
     elif two_launch:
-        roof_kernel = ATTN_KERNEL[w.dtype][0] + (" (select + attend + merge)" if plan == 1
-                                                 else " (attend + merge)")
-        roof_bytes = acct["step_attn_launch"] + (acct["scores_bytes"] if plan == 1 else 0)
+        roof_kernel = ATTN_KERNEL[w.dtype][0] + {1: " (select + attend + merge)",
+                                                 2: " (attend + merge)",
+                                                 6: " (select + attend)", 7: " (attend)"}[plan]
+        roof_bytes = ((acct["step_attn_launch"] if plan in (1, 2) else acct["attn_launch"])
+                      + (acct["scores_bytes"] if plan in (1, 6) else 0))
         roof_us = statistics.mean(step_kern_us["attention"])
         roof_source = ATTN_KERNEL[w.dtype][1]
     else:
@@ -567,7 +975,7 @@ def run_ours(args):
         roof_source = ATTN_KERNEL[w.dtype][1]
     achieved = roof_bytes / (roof_us * 1e-6) / 1e9
     # kernels per replay of each timed graph
-    n_step = 1 if one_launch else (2 if two_launch else 4)
+    n_step = 1 if one_launch else ((3 if plan in (6, 7) else 2) if two_launch else 4)
     n_dense = 1 if dense_plan in (3, 5) else 2
     line = {
         "metric": METRIC,
@@ -620,6 +1028,11 @@ def run_ours(args):
         "four_kernel_step_us": {"median": round(statistics.median(four_us), 3),
                                 "kernel_us_marked": {k: round(statistics.mean(v), 3)
                                                      for k, v in kern_us.items() if v}},
+        "kv_window": ({"us": spread(win_us), "pages_per_group": k_max,
+                       "speedup_vs_dense": round(dense_med / statistics.median(win_us), 3),
+                       "byte_bound": round(acct["dense_step"] / win_bytes, 3),
+                       "path": "kv_select_structured (sink 0, last k pages, no scores), then "
+                               f"kv_decode_attn_merge, {S_w} splits"} if win_us else None),
         "kernel_cost_beyond_bytes_us": round(
             sparse_med - dense_med * acct["sparse_step"] / acct["dense_step"], 3),
         "bytes": acct,
@@ -642,18 +1055,34 @@ def run_ours(args):
                 "avg_launch_us": round(dense_mean, 3)},
         },
         "gpu_launches": args.steps * (n_step + n_dense + 4 + (4 if in_graph_events else 0)
-                                      + (2 if two_launch else 0) + (1 if one_us else 0)
-                                      + (2 if alt_us else 0)
-                                      + (n_step if fp8_us else 0) + 4 + 2),
+                                      + (n_step if two_launch else 0) + (1 if one_us else 0)
+                                      + ({1: 2, 2: 2, 6: 3, 7: 3}.get(alt_plan, 0) if alt_us
+                                         else 0)
+                                      + (n_step if fp8_us else 0) + 4 + 2
+                                      + (2 if win_us else 0)),
         "clocks": clocks,
     }
     if e2e_us:
         line["e2e"] = {"value": round(statistics.median(e2e_us), 3), "unit": "us/step",
                        "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
                        "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
-                       "api": "kv_decode_step"}
+                       "api": "kv_decode_step_graph_launch (the step captured once by "
+                              "kv_decode_step_graph_create; query copied in, output copied "
+                              "out, host waits)",
+                       "direct_call_us": round(statistics.median(e2e_direct_us), 3),
+                       "direct_call_api": "kv_decode_step through the Python binding"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(c, w, keep, budget_s=args.cpu_seconds)
+    if world == 1 and not args.no_configs:
+        # the rest of the metric's range, each configuration on its own (the headline cache
+        # stays resident; each configuration's cache is freed before the next)
+        line["configs"] = {}
+        for name, ki in EXTRA_CONFIGS:
+            r = measure_config(name, ki, args, dev, flush, peak, peak_kind)
+            line["configs"][f"{name}:{r['keep']}"] = r
+            line["gpu_launches"] += r.pop("gpu_launches")
+    if world == 1 and args.blocks > 0:
+        line["blocks"] = run_blocks(args, args.blocks)
     return line
 
 
@@ -788,11 +1217,22 @@ def main():
                     help="which keep ratio of the workload to run")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure the headline workload only")
+    ap.add_argument("--config-cpu-seconds", type=float, default=6.0,
+                    help="oracle time budget of each extra configuration's cpu_baseline")
+    ap.add_argument("--blocks", type=int, default=5,
+                    help="fresh-process blocks of the headline sparse/dense pair (0: none)")
+    ap.add_argument("--block-steps", type=int, default=50)
+    ap.add_argument("--block-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--only-step", choices=["sparse", "dense"],
                     help="profiling aid: run warm-up + steps plain kv_decode_step calls "
                          "(L2 flushed before each) and print no benchmark line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.block_child:
+        run_block_child(args)
+        return
     if args.only_step:
         run_only_step(args)
         return

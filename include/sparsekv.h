@@ -128,8 +128,17 @@ int32_t kv_version(void);
  * unmapped physical pages are not written. Reads every mapped key once; run it after a
  * prefill, not per step.
  * stats: device, [num_phys_pages][num_kv_heads][2][head_dim] of the cache dtype.
+ * phys_pages: NULL to build every mapped page; otherwise device int32[n_phys], STRICTLY
+ * ASCENDING physical page indices, and only the mapped pages whose physical index is in the
+ * list are (re)built (e.g. the pages a chunked prefill just wrote); every other row of
+ * stats is left as it was, and listed pages that no sequence maps are not written. Cost:
+ * one page-table read per mapped page plus the keys of the listed ones. A list entry outside
+ * [0, num_phys_pages) or out of order is flagged (KV_DEVERR_BAD_PAGE; which pages are then
+ * rebuilt is unspecified). n_phys outside [0, num_phys_pages] returns KV_ERR_INVALID_ARG;
+ * n_phys = 0 with a list does nothing.
  */
-kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStream_t stream);
+kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats,
+                              const int32_t* phys_pages, int32_t n_phys, cudaStream_t stream);
 
 /*
  * kv_build_page_stats_fp8 -- the statistics of kv_build_page_stats stored in one byte each
@@ -288,7 +297,8 @@ kv_status kv_decode_attn_merge(const kv_cache_desc* cache, const void* q, int32_
  * part_acc/part_ml, and the group's last CTA merges the partials into out/lse (the formula
  * of kv_merge_splits). With scores = NULL every page is kept: the dense baseline through
  * the same kernel. counters: device [batch][num_kv_heads] int32, zero before the first call;
- * every call returns them to zero. sel_idx [batch][num_kv_heads][k_max] and sel_cnt
+ * every call returns them to zero. counters = NULL: no merge -- the call only writes the
+ * partials (for kv_merge_splits to merge) and out/lse are not touched (they may be NULL). sel_idx [batch][num_kv_heads][k_max] and sel_cnt
  * [batch][num_kv_heads] receive the selection when not NULL (sparse calls only). The group's
  * pages must fit the in-kernel selection (page_table_stride at most 21440 pages for
  * head_dim 128, 9152 for 64) and the splits its merge; otherwise KV_ERR_UNSUPPORTED.
@@ -348,10 +358,12 @@ size_t kv_dropped_mass_workspace_size(const kv_cache_desc* cache, int32_t num_q_
  * calls). Both paths give the same selection (bit for bit) and outputs equal up to float32
  * rounding of the merge.
  * out: device [batch][num_q_heads][head_dim] float32; lse: [batch][num_q_heads] or NULL.
- * For bf16 caches the step takes two launches, the merge running in the attention
- * kernel's last CTA per group: groups of up to 16384 pages (page_table_stride, and within
- * kv_select_decode_attn's limit) run kv_score_pages then kv_select_decode_attn, longer ones
- * kv_score_select then kv_decode_attn_merge; the dense step is kv_decode_attn_merge alone
+ * For bf16 caches: groups of up to 16384 pages (page_table_stride, and within
+ * kv_select_decode_attn's limit) run kv_score_pages, then an attention kernel whose CTAs each
+ * select their own run; longer ones kv_score_select, then the attention over the list; the
+ * dense step is the attention kernel alone. With fewer than 8 splits the attention kernel's
+ * last CTA per group merges (two launches, one for the dense step); with 8 or more the merge
+ * is a kernel of its own, chained to the attention kernel by programmatic dependent launch
  * (kv_decode_step_plan tells which).
  * workspace: device, at least kv_decode_step_workspace_size() bytes, 256-byte aligned, ZERO-
  * FILLED ONCE before its first use: it starts with two int32 counters per group, at offsets
@@ -372,6 +384,33 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
 
 size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
                                      int32_t k_max, int32_t num_splits);
+
+/*
+ * kv_decode_step_graph_create / _launch / _destroy -- kv_decode_step captured once into a CUDA
+ * graph, for a serving loop that runs the same step every token: each launch then costs the
+ * host one graph launch instead of the argument checks, planning and kernel launches of
+ * kv_decode_step. create makes one uncaptured kv_decode_step call (checking the arguments
+ * and doing every first-use set-up; the workspace must therefore be zero-filled as for
+ * kv_decode_step), then captures the same call on a private stream and instantiates it.
+ * Every pointer and size is baked into the graph: the caller keeps all the buffers (cache
+ * descriptor's pools, page table, lengths, q, stats, out, lse, workspace) alive and in place
+ * while the graph exists, and changes only their CONTENTS between launches (the new query,
+ * appended tokens and grown lengths, within the page table's capacity). The step's plan and
+ * split count are those of the capture. launch runs the step on `stream` (asynchronous, like
+ * kv_decode_step); launches of one graph must not overlap on the GPU (they share the
+ * workspace). destroy frees the graph (NULL is accepted). create returns kv_decode_step's
+ * status for bad arguments, KV_ERR_CUDA if capture or instantiation fails; *graph is NULL
+ * then. The graph holds host and driver resources only; no device buffer is allocated.
+ */
+typedef struct kv_step_graph kv_step_graph;
+kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
+                                      int32_t num_q_heads, float sm_scale, const void* stats,
+                                      double keep_ratio, int32_t budget_pages, int32_t k_max,
+                                      int32_t num_splits, float* out, float* lse,
+                                      void* workspace, size_t workspace_bytes,
+                                      kv_step_graph** graph);
+kv_status kv_decode_step_graph_launch(kv_step_graph* graph, cudaStream_t stream);
+kv_status kv_decode_step_graph_destroy(kv_step_graph* graph);
 
 /*
  * kv_decode_step_fp8 -- kv_decode_step scoring from FP8 statistics (kv_build_page_stats_fp8)
@@ -398,7 +437,11 @@ typedef enum {
   KV_PLAN_SCORE_SELECT_THEN_ATTN = 2,  /* kv_score_select, kv_decode_attn_merge */
   KV_PLAN_DENSE_ATTN_MERGE = 3,        /* kv_decode_attn_merge with every page */
   KV_PLAN_DENSE_TWO_KERNELS = 4,       /* kv_sparse_decode_attn, kv_merge_splits */
-  KV_PLAN_ONE_LAUNCH = 5               /* one thread-block cluster per group */
+  KV_PLAN_ONE_LAUNCH = 5,              /* one thread-block cluster per group */
+  KV_PLAN_SCORE_THEN_SELECT_ATTN_THEN_MERGE = 6,  /* kv_score_pages, the attention kernel
+                                          selecting per CTA (partials only), kv_merge_splits */
+  KV_PLAN_SCORE_SELECT_THEN_ATTN_THEN_MERGE = 7   /* kv_score_select, kv_sparse_decode_attn
+                                          over the list, kv_merge_splits */
 } kv_plan;
 int32_t kv_decode_step_plan(const kv_cache_desc* cache, int32_t num_q_heads, double keep_ratio,
                             int32_t budget_pages, int32_t k_max, int32_t num_splits,
@@ -413,15 +456,21 @@ int32_t kv_decode_step_plan(const kv_cache_desc* cache, int32_t num_q_heads, dou
  * library. It runs kv_score_pages, kv_select_topk, kv_sparse_decode_attn and kv_merge_splits
  * (no per-group counters, so nothing in the array has to keep a value between calls): the
  * selection is kv_decode_step's bit for bit and the outputs equal up to float32 rounding of
- * the merge.
+ * the merge. num_splits <= 0 (KV_SPLITS_ONE_LAUNCH included) means kv_auto_num_splits' count.
  * Scratch: one file-scope __device__ array of KV_STATIC_SCRATCH_BYTES that every GPU loading
- * the library holds until exit. The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress, that device current), so make that first call before any
+ * the library holds until exit. CUDA loads the module holding it lazily, so the first call on
+ * a device loads that module, reserves the array (which can fail under memory pressure,
+ * returning KV_ERR_CUDA, or synchronise) and looks up its device address
+ * (cudaGetSymbolAddress, that device current): make that first call at start-up, before any
  * stream capture. All calls share the array and it keeps the last call's contents: calls
  * that overlap on the GPU race and must be serialised by the caller. Nothing in it needs to
- * start at zero. A shape whose scratch (kv_decode_step_workspace_size for the same
- * arguments) exceeds KV_STATIC_SCRATCH_BYTES returns KV_ERR_WORKSPACE and launches nothing.
- * This call allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * start at zero. Limit: this call's own scratch -- batch * num_kv_heads * page_table_stride
+ * float32 scores, batch * num_kv_heads * k_max int32 indices (1 for a dense call),
+ * batch * num_kv_heads int32 counts, and batch * num_q_heads * S * (head_dim + 2) float32
+ * split partials, each rounded up to a multiple of 256 bytes -- above
+ * KV_STATIC_SCRATCH_BYTES returns KV_ERR_WORKSPACE and launches nothing. Once its array is
+ * in place, a call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
  */
 #define KV_STATIC_SCRATCH_BYTES (8u << 20)
 kv_status kv_decode_step_static(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
@@ -492,6 +541,26 @@ kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32
                                 float sm_scale, const void* stats, int32_t k_max, float* out,
                                 float* tau, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
+
+/*
+ * kv_workspace_size -- host, launches nothing: the bytes of device workspace that call `op`
+ * needs for these arguments -- the same value as that call's own *_workspace_size function,
+ * which it dispatches to (KV_OP_DECODE_STEP: kv_decode_step_workspace_size(cache,
+ * num_q_heads, k_max, num_splits), also for kv_decode_step_fp8; KV_OP_DROPPED_MASS:
+ * kv_dropped_mass_workspace_size(cache, num_q_heads); KV_OP_ENTMAX_DECODE_ATTN:
+ * kv_entmax_attn_workspace_size(cache, num_q_heads, k_max as sel_stride, 0 = every page);
+ * KV_OP_ENTMAX_DECODE_STEP: kv_entmax_decode_step_workspace_size(cache, num_q_heads,
+ * k_max)). Arguments a given op does not use are ignored. Every other call of this library
+ * takes no workspace. Returns 0 for an unknown op or a bad argument.
+ */
+typedef enum {
+  KV_OP_DECODE_STEP = 0,
+  KV_OP_DROPPED_MASS = 1,
+  KV_OP_ENTMAX_DECODE_ATTN = 2,
+  KV_OP_ENTMAX_DECODE_STEP = 3
+} kv_op;
+size_t kv_workspace_size(int32_t op, const kv_cache_desc* cache, int32_t num_q_heads,
+                         int32_t k_max, int32_t num_splits);
 
 /*
  * kv_check_device_errors -- synchronises `stream`, reads and clears the current device's

@@ -9,6 +9,7 @@ from . import inputs  # noqa: F401
 from .binding import (  # noqa: F401
     ONE_LAUNCH,
     PLANS,
+    DecodeStepGraph,
     PagedKV,
     kv_append_token,
     kv_auto_num_splits,
@@ -38,5 +39,6 @@ from .binding import (  # noqa: F401
     kv_set_wait_limit_ns,
     kv_sparse_decode_attn,
     kv_version,
+    kv_workspace_size,
     max_keep_pages,
 )

@@ -24,7 +24,9 @@ ONE_LAUNCH = -1          # KV_SPLITS_ONE_LAUNCH: kv_decode_step as a single laun
 # kv_decode_step_plan results (KV_PLAN_*)
 PLANS = {0: "four kernels", 1: "score, then select + attention + merge",
          2: "score + select, then attention + merge", 3: "dense attention + merge",
-         4: "dense attention, merge", 5: "one launch"}
+         4: "dense attention, merge", 5: "one launch",
+         6: "score, then select + attention, then merge",
+         7: "score + select, then attention, then merge"}
 STATUS = {0: "KV_OK", -1: "KV_ERR_INVALID_ARG", -2: "KV_ERR_UNSUPPORTED", -3: "KV_ERR_CUDA",
           -4: "KV_ERR_WORKSPACE", -5: "KV_ERR_BAD_INDEX", -6: "KV_ERR_TIMEOUT",
           -7: "KV_ERR_MISALIGNED"}
@@ -41,7 +43,8 @@ EXPORTS = (
     "kv_decode_attn_merge", "kv_decode_step_plan", "kv_build_page_stats_fp8",
     "kv_score_pages_fp8", "kv_decode_step_fp8", "kv_entmax_page_moments", "kv_entmax_select",
     "kv_entmax_attn_workspace_size", "kv_entmax_decode_attn",
-    "kv_entmax_decode_step_workspace_size", "kv_entmax_decode_step",
+    "kv_entmax_decode_step_workspace_size", "kv_entmax_decode_step", "kv_workspace_size",
+    "kv_decode_step_graph_create", "kv_decode_step_graph_launch", "kv_decode_step_graph_destroy",
 )
 
 
@@ -78,7 +81,12 @@ def _declare(lib):
     sig = {
         "kv_status_string": (ctypes.c_char_p, [I32]),
         "kv_version": (I32, []),
-        "kv_build_page_stats": (I32, [D, P, P]),
+        "kv_build_page_stats": (I32, [D, P, P, I32, P]),
+        "kv_workspace_size": (SZ, [I32, D, I32, I32, I32]),
+        "kv_decode_step_graph_create": (I32, [D, P, I32, F32, P, F64, I32, I32, I32, P, P, P, SZ,
+                                              ctypes.POINTER(P)]),
+        "kv_decode_step_graph_launch": (I32, [P, P]),
+        "kv_decode_step_graph_destroy": (I32, [P]),
         "kv_score_pages": (I32, [D, P, I32, P, P, I32, P]),
         "kv_select_topk": (I32, [P, I32, P, I32, I32, I32, P, F64, I32, I32, P, P, P]),
         "kv_sparse_decode_attn": (I32, [D, P, I32, F32, P, P, I32, I32, P, P, P]),
@@ -227,12 +235,21 @@ def kv_version() -> int:
     return lib().kv_version()
 
 
-def kv_build_page_stats(kv: PagedKV, stats=None, stream=None):
+def kv_build_page_stats(kv: PagedKV, stats=None, phys_pages=None, stream=None):
+    """Page statistics of every mapped page, or (phys_pages: a strictly ascending int32
+    tensor of physical page indices) of the mapped pages in that subset only."""
     NP, Hkv, PS, D = kv.k_pool.shape
     if stats is None:
         stats = torch.empty((NP, Hkv, 2, D), dtype=kv.dtype, device=kv.k_pool.device)
     _need(stats, "stats", kv.dtype, (NP, Hkv, 2, D))
-    _check("kv_build_page_stats", lib().kv_build_page_stats(kv.ref(), _ptr(stats), _stream(stream)))
+    n_phys = 0
+    if phys_pages is not None:
+        _need(phys_pages, "phys_pages", torch.int32)
+        n_phys = phys_pages.numel()
+        if n_phys == 0:              # an empty list (whose data pointer may be NULL): no work
+            return stats
+    _check("kv_build_page_stats", lib().kv_build_page_stats(
+        kv.ref(), _ptr(stats), _ptr(phys_pages), n_phys, _stream(stream)))
     return stats
 
 
@@ -387,9 +404,10 @@ def kv_select_decode_attn(kv: PagedKV, q, sm_scale: float, scores=None, keep_rat
                           budget_pages: int = 0, k_max: int | None = None,
                           num_splits: int | None = None, part_acc=None, part_ml=None,
                           counters=None, out=None, lse=None, sel_idx=None, sel_cnt=None,
-                          stream=None):
+                          merge: bool = True, stream=None):
     """Selection, split-K attention and merge in one kernel (bf16); scores=None is dense.
-    counters must start at zero (they are returned to zero)."""
+    counters must start at zero (they are returned to zero). merge=False: the kernel only
+    writes the partials, returned as (part_acc, part_ml)."""
     _need(q, "q", kv.dtype)
     B, Hq, D = q.shape
     Hkv = kv.num_kv_heads
@@ -403,15 +421,18 @@ def kv_select_decode_attn(kv: PagedKV, q, sm_scale: float, scores=None, keep_rat
         part_acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=dev)
     if part_ml is None:
         part_ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device=dev)
-    if counters is None:
-        counters = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
-    if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
-    if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    if merge:
+        if counters is None:
+            counters = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+        if lse is None:
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        _need(counters, "counters", torch.int32, (B, Hkv))
+    else:
+        counters = out = lse = None
     _need(part_acc, "part_acc", torch.float32, (B, Hq, S, D))
     _need(part_ml, "part_ml", torch.float32, (B, Hq, S, 2))
-    _need(counters, "counters", torch.int32, (B, Hkv))
     stride = 0
     if scores is not None:
         _need(scores, "scores", torch.float32)
@@ -420,7 +441,7 @@ def kv_select_decode_attn(kv: PagedKV, q, sm_scale: float, scores=None, keep_rat
         kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(scores), stride, float(keep_ratio),
         int(budget_pages), int(k_max), S, _ptr(part_acc), _ptr(part_ml), _ptr(counters),
         _ptr(out), _ptr(lse), _ptr(sel_idx), _ptr(sel_cnt), _stream(stream)))
-    return out, lse
+    return (out, lse) if merge else (part_acc, part_ml)
 
 
 def kv_score_select(kv: PagedKV, q, stats, keep_ratio: float = 0.0, budget_pages: int = 0,
@@ -522,6 +543,15 @@ def kv_dropped_mass(kv: PagedKV, q, sm_scale: float, sel_idx, sel_cnt, delta=Non
     return delta
 
 
+KV_OP = {"decode_step": 0, "dropped_mass": 1, "entmax_decode_attn": 2, "entmax_decode_step": 3}
+
+
+def kv_workspace_size(op: str, kv: PagedKV, num_q_heads: int, k_max: int = 0,
+                      num_splits: int = 0) -> int:
+    return int(lib().kv_workspace_size(KV_OP[op], kv.ref(), int(num_q_heads), int(k_max),
+                                       int(num_splits)))
+
+
 def kv_decode_step_workspace_size(kv: PagedKV, num_q_heads: int, k_max: int,
                                   num_splits: int = 0) -> int:
     return int(lib().kv_decode_step_workspace_size(kv.ref(), int(num_q_heads), int(k_max),
@@ -547,6 +577,50 @@ def kv_decode_step(kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: floa
         int(budget_pages), int(k_max), int(num_splits), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
+
+
+class DecodeStepGraph:
+    """kv_decode_step captured once (kv_decode_step_graph_create): launch() runs the step with
+    the buffers given here, whose contents (q, the cache) the caller updates in place."""
+
+    def __init__(self, kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: float = 1.0,
+                 budget_pages: int = 0, k_max: int | None = None, num_splits: int = 0,
+                 out=None, lse=None, workspace=None):
+        _need(q, "q", kv.dtype)
+        B, Hq, D = q.shape
+        if k_max is None:
+            k_max = max_keep_pages(kv.stride, keep_ratio, budget_pages)
+        self.out = out if out is not None else torch.empty((B, Hq, D), dtype=torch.float32,
+                                                           device=q.device)
+        self.lse = lse if lse is not None else torch.empty((B, Hq), dtype=torch.float32,
+                                                           device=q.device)
+        if workspace is None:
+            nbytes = kv_decode_step_workspace_size(kv, Hq, k_max, max(num_splits, 0))
+            workspace = torch.zeros((nbytes,), dtype=torch.uint8, device=q.device)
+        # the buffers must outlive the graph: keep them referenced
+        self._keep = (kv, q, stats, workspace)
+        handle = ctypes.c_void_p()
+        _check("kv_decode_step_graph_create", lib().kv_decode_step_graph_create(
+            kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(stats), float(keep_ratio),
+            int(budget_pages), int(k_max), int(num_splits), _ptr(self.out), _ptr(self.lse),
+            _ptr(workspace), workspace.numel(), ctypes.byref(handle)))
+        self._handle = handle
+
+    def launch(self, stream=None):
+        _check("kv_decode_step_graph_launch",
+               lib().kv_decode_step_graph_launch(self._handle, _stream(stream)))
+        return self.out, self.lse
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None and self._handle.value is not None:
+            lib().kv_decode_step_graph_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def kv_decode_step_plan(kv: PagedKV, num_q_heads: int, keep_ratio: float = 1.0,

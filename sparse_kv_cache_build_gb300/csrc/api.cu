@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <map>
+#include <new>
 #include <mutex>
 #include <tuple>
 
@@ -25,6 +26,11 @@ constexpr int kDroppedSplits = 64;          // page ranges per group in the drop
 // 11-bit digits: 70.8 against 81.0 us a step at 8192 pages (128K context), 81.1 against
 // 85.1 us at 16384 pages (1M context, page size 64).
 constexpr int kInAttnSelectPages = 16384;
+// Split count from which the step merges in a separate kernel (chained by programmatic
+// dependent launch) rather than in the attention kernel's last CTA per group. Measured on
+// this part: with 38 splits the separate merge saved 2.0 us at 32K and 128K and 5.1 us at 1M
+// context; with one split per group (batched serving) it cost 2.0 us.
+constexpr int kSeparateMergeMinSplits = 8;
 
 struct DeviceState {
   bool ready = false;
@@ -235,16 +241,20 @@ const char* kv_status_string(int32_t status) {
   }
 }
 
-int32_t kv_version(void) { return 100; }
+int32_t kv_version(void) { return 101; }
 
-kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats, cudaStream_t stream) {
+kv_status kv_build_page_stats(const kv_cache_desc* cache, void* stats,
+                              const int32_t* phys_pages, int32_t n_phys, cudaStream_t stream) {
   kv_status r = check_desc(cache);
   if (r != KV_OK) return r;
   if (stats == nullptr) return KV_ERR_INVALID_ARG;
+  if (phys_pages != nullptr && (n_phys < 0 || n_phys > cache->num_phys_pages))
+    return KV_ERR_INVALID_ARG;
   if (!aligned16(stats)) return KV_ERR_MISALIGNED;
+  if (phys_pages != nullptr && n_phys == 0) return KV_OK;     // nothing to rebuild
   DevCtx ctx;
   if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
-  return from_cuda(launch_page_stats(*cache, stats, nullptr, ctx, stream));
+  return from_cuda(launch_page_stats(*cache, stats, nullptr, phys_pages, n_phys, ctx, stream));
 }
 
 kv_status kv_build_page_stats_fp8(const kv_cache_desc* cache, void* stats_fp8,
@@ -255,7 +265,7 @@ kv_status kv_build_page_stats_fp8(const kv_cache_desc* cache, void* stats_fp8,
   if (!aligned16(stats_fp8)) return KV_ERR_MISALIGNED;
   DevCtx ctx;
   if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
-  return from_cuda(launch_page_stats(*cache, stats_fp8, stats_exp, ctx, stream));
+  return from_cuda(launch_page_stats(*cache, stats_fp8, stats_exp, nullptr, 0, ctx, stream));
 }
 
 kv_status kv_append_token(const kv_cache_desc* cache, const void* k_new, const void* v_new,
@@ -431,7 +441,7 @@ kv_status kv_select_decode_attn(const kv_cache_desc* cache, const void* q, int32
   if (r != KV_OK) return r;
   if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
   if (cache->dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
-  if (part_acc == nullptr || part_ml == nullptr || counters == nullptr || out == nullptr ||
+  if (part_acc == nullptr || part_ml == nullptr || (counters != nullptr && out == nullptr) ||
       num_splits < 1 || num_splits > 65535 || !(sm_scale > 0.f) || !isfinite(sm_scale))
     return KV_ERR_INVALID_ARG;
   if (!aligned16(part_acc) || (reinterpret_cast<uintptr_t>(part_ml) & 7u) != 0)
@@ -585,6 +595,13 @@ kv_status plan_step(const kv_cache_desc* cache, int num_q_heads, double keep_rat
       else if (score_select_fits(cache, st))
         P.plan = KV_PLAN_SCORE_SELECT_THEN_ATTN;
     }
+    if (S >= kSeparateMergeMinSplits) {
+      if (P.plan == KV_PLAN_DENSE_ATTN_MERGE) P.plan = KV_PLAN_DENSE_TWO_KERNELS;
+      else if (P.plan == KV_PLAN_SCORE_THEN_SELECT_ATTN)
+        P.plan = KV_PLAN_SCORE_THEN_SELECT_ATTN_THEN_MERGE;
+      else if (P.plan == KV_PLAN_SCORE_SELECT_THEN_ATTN)
+        P.plan = KV_PLAN_SCORE_SELECT_THEN_ATTN_THEN_MERGE;
+    }
   }
   *out = P;
   return KV_OK;
@@ -688,6 +705,35 @@ kv_status decode_step_impl(const kv_cache_desc* cache, const void* q, int32_t nu
       if (e != cudaSuccess) return KV_ERR_CUDA;
       return from_cuda(launch_step_attn_bf16(*cache, q, G, sm_scale, sel, cnt, k_max, P.S, acc,
                                              ml, ctx, stream, sa));
+    case KV_PLAN_SCORE_THEN_SELECT_ATTN_THEN_MERGE:
+      // as plan 1, but the attention kernel only writes the partials (no counters) and the
+      // merge is a kernel of its own
+      e = launch_score_pages(*cache, q, num_q_heads, stats, stats_exp, scores, stride, ctx,
+                             stream);
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      sa.scores = scores;
+      sa.scores_stride = stride;
+      sa.keep_ratio = keep_ratio;
+      sa.budget = budget_pages;
+      sa.k_max = k_max;
+      sa.sel_out = sel;
+      sa.cnt_out = cnt;
+      sa.counters = nullptr;
+      e = launch_step_attn_bf16(*cache, q, G, sm_scale, nullptr, nullptr, 0, P.S, acc, ml, ctx,
+                                stream, sa);
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      return from_cuda(launch_merge(acc, ml, cache->batch, num_q_heads, P.S, cache->head_dim,
+                                    out, lse, stream));
+    case KV_PLAN_SCORE_SELECT_THEN_ATTN_THEN_MERGE:
+      e = launch_score_select(*cache, q, num_q_heads, stats, stats_exp, scores, stride,
+                              keep_ratio, budget_pages, k_max,
+                              reinterpret_cast<int32_t*>(ws + L.ctr), sel, cnt, ctx, stream);
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      e = launch_split_attn(*cache, q, num_q_heads, sm_scale, sel, cnt, k_max, P.S, acc, ml, ctx,
+                            stream, st->sms);
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      return from_cuda(launch_merge(acc, ml, cache->batch, num_q_heads, P.S, cache->head_dim,
+                                    out, lse, stream));
     default:
       break;
   }
@@ -720,6 +766,66 @@ kv_status kv_decode_step(const kv_cache_desc* cache, const void* q, int32_t num_
   return decode_step_impl(cache, q, num_q_heads, sm_scale, stats, nullptr, keep_ratio,
                           budget_pages, k_max, num_splits, out, lse, workspace, workspace_bytes,
                           stream);
+}
+
+// ----------------------------------------------------------------- captured decode step
+
+struct kv_step_graph {
+  cudaGraphExec_t exec = nullptr;
+};
+
+kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
+                                      int32_t num_q_heads, float sm_scale, const void* stats,
+                                      double keep_ratio, int32_t budget_pages, int32_t k_max,
+                                      int32_t num_splits, float* out, float* lse,
+                                      void* workspace, size_t workspace_bytes,
+                                      kv_step_graph** graph) {
+  if (graph == nullptr) return KV_ERR_INVALID_ARG;
+  *graph = nullptr;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KV_ERR_CUDA;
+  // one uncaptured call first: it checks the arguments and does every first-use set-up
+  // (device state, kernel attributes, tensor maps) outside the capture
+  kv_status r = kv_decode_step(cache, q, num_q_heads, sm_scale, stats, keep_ratio, budget_pages, k_max,
+                     num_splits, out, lse, workspace, workspace_bytes, s);
+  if (r == KV_OK && cudaStreamSynchronize(s) != cudaSuccess) r = KV_ERR_CUDA;
+  cudaGraph_t g = nullptr;
+  if (r == KV_OK) {
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      r = KV_ERR_CUDA;
+    } else {
+      r = kv_decode_step(cache, q, num_q_heads, sm_scale, stats, keep_ratio, budget_pages,
+                         k_max, num_splits, out, lse, workspace, workspace_bytes, s);
+      const cudaError_t e = cudaStreamEndCapture(s, &g);
+      if (r == KV_OK && e != cudaSuccess) r = KV_ERR_CUDA;
+    }
+  }
+  kv_step_graph* h = nullptr;
+  if (r == KV_OK) {
+    h = new (std::nothrow) kv_step_graph;
+    if (h == nullptr) r = KV_ERR_CUDA;
+    else if (cudaGraphInstantiate(&h->exec, g, 0) != cudaSuccess) r = KV_ERR_CUDA;
+  }
+  if (g != nullptr) cudaGraphDestroy(g);
+  cudaStreamDestroy(s);
+  if (r != KV_OK) {
+    delete h;
+    return r;
+  }
+  *graph = h;
+  return KV_OK;
+}
+
+kv_status kv_decode_step_graph_launch(kv_step_graph* graph, cudaStream_t stream) {
+  if (graph == nullptr || graph->exec == nullptr) return KV_ERR_INVALID_ARG;
+  return from_cuda(cudaGraphLaunch(graph->exec, stream));
+}
+
+kv_status kv_decode_step_graph_destroy(kv_step_graph* graph) {
+  if (graph == nullptr) return KV_OK;
+  const cudaError_t e = graph->exec != nullptr ? cudaGraphExecDestroy(graph->exec) : cudaSuccess;
+  delete graph;
+  return from_cuda(e);
 }
 
 kv_status kv_decode_step_fp8(const kv_cache_desc* cache, const void* q, int32_t num_q_heads,
@@ -890,6 +996,22 @@ kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32
                                       entmax_splits(cache, k_max, st),
                                       entmax_scratch(logits, cache, num_q_heads, k_max),
                                       k_max * cache->page_size, out, tau, ctx, stream));
+}
+
+size_t kv_workspace_size(int32_t op, const kv_cache_desc* cache, int32_t num_q_heads,
+                         int32_t k_max, int32_t num_splits) {
+  switch (op) {
+    case KV_OP_DECODE_STEP:
+      return kv_decode_step_workspace_size(cache, num_q_heads, k_max, num_splits);
+    case KV_OP_DROPPED_MASS:
+      return kv_dropped_mass_workspace_size(cache, num_q_heads);
+    case KV_OP_ENTMAX_DECODE_ATTN:
+      return kv_entmax_attn_workspace_size(cache, num_q_heads, k_max);
+    case KV_OP_ENTMAX_DECODE_STEP:
+      return kv_entmax_decode_step_workspace_size(cache, num_q_heads, k_max);
+    default:
+      return 0;
+  }
 }
 
 kv_status kv_check_device_errors(cudaStream_t stream, int32_t* flags) {

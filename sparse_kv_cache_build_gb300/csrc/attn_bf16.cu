@@ -1,9 +1,11 @@
 // Split-K decode attention for bf16 caches: the tensor-core kernel of attn_mma.cuh, fed by
 // TMA tensor copies. This file builds the two tensor maps (K and V pools seen as 2-D
-// [NP*Hkv*PS rows][D columns] bf16 arrays, boxes of 64 columns x PS rows, 128-byte swizzle)
-// and launches the kernel.
+// [NP*Hkv*PS rows][D columns] bf16 arrays, boxes of 64 columns x PS rows, 128-byte swizzle),
+// keeps the maps of recently used pools so that a launch does not re-encode them, and
+// launches the kernel.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "attn_impl.cuh"
@@ -26,7 +28,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool pool_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d) {
+bool encode_pool_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t rows = (cuuint64_t)d.num_phys_pages * d.num_kv_heads * d.page_size;
@@ -40,6 +42,55 @@ bool pool_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d) {
          CUDA_SUCCESS;
 }
 
+// Encoded maps of recently used pools: a map depends only on the pool's address and shape,
+// so a decode loop over one cache encodes its two maps once instead of on every launch.
+struct MapEntry {
+  bool used = false;
+  int device = -1;
+  const void* pool = nullptr;
+  int head_dim = 0, page_size = 0;
+  long long rows = 0;
+  CUtensorMap map;
+};
+constexpr int kMapCacheEntries = 32;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCacheEntries];
+int g_map_next = 0;
+
+}  // namespace
+
+bool pool_tensor_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const long long rows = (long long)d.num_phys_pages * d.num_kv_heads * d.page_size;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry& e : g_maps) {
+      if (e.used && e.device == dev && e.pool == pool && e.head_dim == d.head_dim &&
+          e.page_size == d.page_size && e.rows == rows) {
+        *map = e.map;
+        return true;
+      }
+    }
+  }
+  CUtensorMap m;
+  if (!encode_pool_map(&m, pool, d)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry& e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCacheEntries;
+  e.used = true;
+  e.device = dev;
+  e.pool = pool;
+  e.head_dim = d.head_dim;
+  e.page_size = d.page_size;
+  e.rows = rows;
+  e.map = m;
+  *map = m;
+  return true;
+}
+
+namespace {
+
 template <int D, int G>
 cudaError_t launch_mma(const kv_cache_desc& d, const CUtensorMap& mk, const CUtensorMap& mv,
                        const void* q, float sm_scale, const int32_t* sel_idx,
@@ -52,14 +103,17 @@ cudaError_t launch_mma(const kv_cache_desc& d, const CUtensorMap& mk, const CUte
                        d.page_table_stride >= topk_detail::kPrefilterMinPages &&
                        16L * sa.k_max <= (long)d.page_table_stride;
   auto kern = is_long ? split_attn_mma_kernel<D, G, true> : split_attn_mma_kernel<D, G, false>;
-  static int attr_set_for_device[2][64] = {{0}};
+  // set once per device and instantiation; atomic so that concurrent first calls from several
+  // host threads are well defined (both may set the attribute, which is idempotent)
+  static std::atomic<int> attr_set_for_device[2][64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set_for_device[is_long][dev]) {
+  if (dev >= 0 && dev < 64 &&
+      !attr_set_for_device[is_long][dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set_for_device[is_long][dev] = 1;
+    attr_set_for_device[is_long][dev].store(1, std::memory_order_release);
   }
   dim3 grid(S, d.num_kv_heads, d.batch);
   return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, mk, mv, d,
@@ -88,7 +142,8 @@ cudaError_t launch_bf16_common(const kv_cache_desc& d, const void* q, int G, flo
   if ((long long)d.num_phys_pages * d.num_kv_heads * d.page_size >= (1ll << 31))
     return cudaErrorInvalidValue;                 // TMA row coordinates are 32-bit
   CUtensorMap mk, mv;
-  if (!pool_map(&mk, d.k_pool, d) || !pool_map(&mv, d.v_pool, d)) return cudaErrorInvalidValue;
+  if (!pool_tensor_map(&mk, d.k_pool, d) || !pool_tensor_map(&mv, d.v_pool, d))
+    return cudaErrorInvalidValue;
   if (d.head_dim == 128)
     return launch_mma_d<128>(d, mk, mv, q, G, sm_scale, sel_idx, sel_cnt, sel_stride, S,
                              part_acc, part_ml, ctx, st, sa);

@@ -483,11 +483,12 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                                     C::RING_WORDS - used - kHistWords, T, take_eq);
     // this CTA's run only; each CTA also writes its run's part of the selection output
     int32_t* sel_out = sa.sel_out;
-    cta_compact<C::THREADS>(K, T, take_eq, reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT),
-                            pos0, pos0 + np, [&](int p, int pos) {
-                              if (sel_out != nullptr) sel_out[grp * sa.k_max + pos] = p;
-                              s_phys[pos - pos0] = p;
-                            });
+    cta_compact_window<C::THREADS>(K, T, take_eq,
+                                   reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT), misc, pos0,
+                                   pos0 + np, [&](int p, int pos) {
+                                     if (sel_out != nullptr) sel_out[grp * sa.k_max + pos] = p;
+                                     s_phys[pos - pos0] = p;
+                                   });
     __syncthreads();
     if (table_bulk) tab = reinterpret_cast<const int32_t*>(ring + KW);
     for (int i = tid; i < np; i += C::THREADS) resolve(i, s_phys[i]);

@@ -11,17 +11,19 @@
 //     request instead of n/NT load instructions per thread (a 16K-page row lands in
 //     ~0.7 us, against ~5.7 us for per-thread loads from 128 threads); otherwise by
 //     per-thread loads, sixteen in flight;
-//   * keys are stored contiguously in page order; thread t visits pages t, t + NT, ...
-//     (conflict-free), and every pass first loads a batch of sixteen keys into registers,
-//     so no shared-memory load waits behind a shared store or atomic it might alias;
+//   * keys are stored contiguously in page order; a pass has thread t read the 16-byte
+//     groups t, t + NT, ... of four keys (conflict-free), a batch of four groups into
+//     registers before any shared store or atomic, so no shared-memory load waits behind a
+//     store or atomic it might alias;
 //   * the bits on which keys differ are OR ^ AND over the keys, so the first radix digit
 //     starts at the highest of them; digits are 11 bits wide, so that after the first pass
 //     the threshold's bin usually holds fewer keys than the block has threads (a pass
 //     costs several block-wide steps; more bins cost only a wider histogram);
-//   * after one digit pass the keys of the threshold's bin are gathered (order does not
-//     matter for the threshold), and if they are at most one per thread each finds its
-//     exact rank among them directly; larger bins take further radix passes over the
-//     gathered keys only;
+//   * after one digit pass the keys of the threshold's bin are gathered through one
+//     shared counter (order does not matter for the threshold, and the bin holds few keys,
+//     so this costs one pass and no block scan), and if they are at most one per thread
+//     each finds its exact rank among them directly; larger bins take further radix passes
+//     over the gathered keys only;
 //   * histograms take plain shared-memory atomics into a bank-padded array (warp-wide
 //     match instructions cost hundreds of cycles when a warp holds many distinct digits);
 //     their throughput (~1.6 keys per clock per SM) is what a pass over many keys costs, so
@@ -29,9 +31,12 @@
 //     a sample (cta_threshold);
 //   * block reductions read the per-warp words one per lane and reduce with warp
 //     instructions, rather than every thread reading every warp's word;
-//   * the ordered compaction gives each warp a contiguous segment of pages, walked 32 at a
-//     time with ballots, after one scan of the per-warp counts, and emits only a requested
-//     window of positions (one attention CTA's run).
+//   * the ordered compaction of the whole list gives each warp a contiguous segment of
+//     pages, walked 32 at a time with ballots, after one scan of the per-warp counts; the
+//     compaction of a short window of positions (one attention CTA's run) gives each thread
+//     a contiguous segment instead, counted with a rotated start (no bank conflicts) and
+//     one block scan, and only the few threads whose segments overlap the window walk
+//     theirs, so its cost does not depend on where the window lies.
 #pragma once
 
 #include "kv_internal.cuh"
@@ -39,8 +44,8 @@
 namespace skv {
 
 struct CtaKeys {
-  uint32_t* keys;   // shared: keys[i] is the key of page i, i < n
-  int n;
+  uint32_t* keys;   // shared, 16-byte aligned, cta_key_words(n) words: keys[i] is page i's
+  int n;            // key for i < n
   uint32_t common;  // AND over the keys: every bit on which they agree has its shared value
   uint32_t diff;    // OR ^ AND over the keys: the bits on which they differ
 };
@@ -85,23 +90,56 @@ __device__ __forceinline__ void cta_fill_bulk_issue(uint32_t* keys, const float*
   if (bytes != 0u) cta_bulk_copy(keys, row, bytes, bar);
 }
 
-// Every thread: copy the raw bits of row[0, n) into keys with loads, kBatch in flight per
-// thread. Thread t writes the pages cta_keys_finish has it read, so no barrier is needed
-// between the two.
-template <int NT, int kBatch = 16>
+// Every thread: copy the raw bits of row[0, n) (any alignment) into keys with loads, sixteen in
+// flight per thread. Thread t writes the 16-byte groups of keys t, t + NT, ..., the ones
+// cta_keys_finish has it read, so no barrier is needed between the two (padding past n is 0).
+template <int NT>
 __device__ __forceinline__ void cta_fill_loads(uint32_t* keys, const float* row, int n) {
+  constexpr int kB4 = 4;
   const int tid = threadIdx.x;
-  for (int base = 0; base < n; base += NT * kBatch) {
-    uint32_t v[kBatch];
+  const int n4 = (n + 3) >> 2;
+  uint4* k4 = reinterpret_cast<uint4*>(keys);
+  for (int base = 0; base < n4; base += NT * kB4) {
+    uint32_t v[kB4][4];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * NT + tid;
-      v[u] = i < n ? __float_as_uint(__ldcg(row + i)) : 0u;
+    for (int u = 0; u < kB4; ++u) {
+      const int j = base + u * NT + tid;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[u][e] = 4 * j + e < n ? __float_as_uint(__ldcg(row + 4 * j + e)) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * NT + tid;
-      if (i < n) keys[i] = v[u];
+    for (int u = 0; u < kB4; ++u) {
+      const int j = base + u * NT + tid;
+      if (j < n4) k4[j] = make_uint4(v[u][0], v[u][1], v[u][2], v[u][3]);
+    }
+  }
+}
+
+// Every thread: f(i, key) for its share of keys[0, n) (16-byte aligned, cta_key_words(n)
+// words), read four at a time: thread t takes the 16-byte groups t, t + NT, ...; the loads of
+// a batch are all issued before f runs on any of them (f may store or do atomics). The order
+// in which a thread visits its keys is not page order.
+template <int NT, typename F>
+__device__ __forceinline__ void cta_for_keys4(const uint32_t* keys, int n, F&& f) {
+  constexpr int kB4 = 4;
+  const int tid = threadIdx.x;
+  const int n4 = (n + 3) >> 2;
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  for (int base = 0; base < n4; base += NT * kB4) {
+    uint4 v[kB4];
+#pragma unroll
+    for (int u = 0; u < kB4; ++u) {
+      const int j = base + u * NT + tid;
+      v[u] = j < n4 ? k4[j] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kB4; ++u) {
+      const int i = 4 * (base + u * NT + tid);
+      if (i < n) f(i, v[u].x);
+      if (i + 1 < n) f(i + 1, v[u].y);
+      if (i + 2 < n) f(i + 2, v[u].z);
+      if (i + 3 < n) f(i + 3, v[u].w);
     }
   }
 }
@@ -112,27 +150,33 @@ __device__ __forceinline__ void cta_fill_loads(uint32_t* keys, const float* row,
 // thread).
 template <int NT, bool CONVERT, typename Fix>
 __device__ __forceinline__ CtaKeys cta_keys_finish(uint32_t* keys, int n, uint32_t* red, Fix fix) {
-  constexpr int kB = 16, NW = NT / 32;
+  constexpr int kB4 = 4, NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t orv = 0u, andv = 0xffffffffu;
-  for (int base = 0; base < n; base += NT * kB) {
-    uint32_t v[kB];
+  const int n4 = (n + 3) >> 2;
+  uint4* k4 = reinterpret_cast<uint4*>(keys);
+  for (int base = 0; base < n4; base += NT * kB4) {
+    uint4 v[kB4];
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
-      const int i = base + u * NT + tid;
-      v[u] = i < n ? keys[i] : 0u;
+    for (int u = 0; u < kB4; ++u) {
+      const int j = base + u * NT + tid;
+      v[u] = j < n4 ? k4[j] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
-      const int i = base + u * NT + tid;
-      if (i < n) {
-        uint32_t key = v[u];
-        if constexpr (CONVERT) {
-          key = fix(i, score_order_key(__uint_as_float(key)));
-          keys[i] = key;
+    for (int u = 0; u < kB4; ++u) {
+      const int j = base + u * NT + tid;
+      if (j < n4) {
+        uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * j + e;
+          if (i < n) {
+            if constexpr (CONVERT) w[e] = fix(i, score_order_key(__uint_as_float(w[e])));
+            orv |= w[e];
+            andv &= w[e];
+          }
         }
-        orv |= key;
-        andv &= key;
+        if constexpr (CONVERT) k4[j] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }
@@ -241,29 +285,20 @@ __device__ __forceinline__ void radix_kth(const uint32_t* keys, int n, int k, in
     const int lo = top >= kDigitBits - 1 ? top - (kDigitBits - 1) : 0;
     const uint32_t dmask = (2u << (top - lo)) - 1u;      // digit bits [lo, top]
     for (int i = tid; i < kHistWords; i += NT) hist[i] = 0u;
+    if (tid == 0) misc[4] = 0u;              // the gather's counter
     __syncthreads();
     const uint32_t* src = ncand < 0 ? keys : cand;
     const int m = ncand < 0 ? n : ncand;
-    for (int base = 0; base < m; base += NT * kB) {
-      uint32_t v[kB];
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int i = base + u * NT + tid;
-        v[u] = i < m ? src[i] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int i = base + u * NT + tid;
-        if (i < m && (v[u] & mask) == prefix) atomicAdd(&hist[hslot((v[u] >> lo) & dmask)], 1u);
-      }
-    }
+    cta_for_keys4<NT>(src, m, [&](int, uint32_t v) {
+      if ((v & mask) == prefix) atomicAdd(&hist[hslot((v >> lo) & dmask)], 1u);
+    });
     __syncthreads();
     pick_bin<NT>(hist, remaining, misc);
     __syncthreads();
     const uint32_t bin = misc[0];
     remaining = misc[1];
     const uint32_t bin_count = misc[2];
-    __syncthreads();                         // misc is rewritten below
+    // misc[0..2] are next written by the following pass's pick_bin, two barriers later
     prefix |= bin << lo;
     mask |= dmask << lo;
     if (remaining == bin_count || lo == 0) { // the whole bin is kept, or the key is complete
@@ -272,35 +307,11 @@ __device__ __forceinline__ void radix_kth(const uint32_t* keys, int n, int k, in
       return;
     }
     top = lo - 1;
-    if (gather && ncand < 0 && (int)bin_count <= cand_cap) {
-      // gather the bin's keys (any order), through a scan of per-thread counts
-      uint32_t mine = 0u, total = 0u;
-      for (int base = 0; base < n; base += NT * kB) {
-        uint32_t v[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const int i = base + u * NT + tid;
-          v[u] = i < n ? keys[i] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < kB; ++u) mine += (base + u * NT + tid < n) && (v[u] & mask) == prefix;
-      }
-      uint32_t at = block_excl_scan<NT>(mine, misc + 8, total);
-      for (int base = 0; base < n && mine != 0u; base += NT * kB) {
-        uint32_t v[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const int i = base + u * NT + tid;
-          v[u] = i < n ? keys[i] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          if ((base + u * NT + tid < n) && (v[u] & mask) == prefix) {
-            cand[at++] = v[u];
-            --mine;
-          }
-        }
-      }
+    if (gather && ncand < 0 && (int)bin_count <= (cand_cap & ~3)) {
+      // gather the bin's keys, in any order, through one shared counter (few keys match)
+      cta_for_keys4<NT>(keys, n, [&](int, uint32_t v) {
+        if ((v & mask) == prefix) cand[atomicAdd(&misc[4], 1u)] = v;
+      });
       __syncthreads();
       ncand = (int)bin_count;
       if (ncand <= NT) {
@@ -352,6 +363,7 @@ constexpr int kPrefilterMinPages = 4096;
 // > T and the first take_eq keys == T in page order. hist: kHistWords words; misc: 8 +
 // NT/32 words; cand: cand_cap words of 16-byte aligned scratch for the gathered keys of
 // the threshold's bin. NT divides kBins.
+
 //
 // Histogram passes cost what the shared-memory atomics cost (~1.6 keys per clock per SM), so
 // a long group keeping few pages (n >= 4096, k <= n/16) is first filtered: from a strided
@@ -511,6 +523,90 @@ __device__ void cta_compact(const CtaKeys& K, uint32_t T, uint32_t take_eq, uint
       eq_before += __popc(be[u]);
     }
     if (gt_before + min(eq_before, take_eq) >= (uint32_t)w1) break;    // past the window
+  }
+}
+
+// Ordered compaction of a window: calls emit(page, pos) for every kept page whose position
+// pos in the ascending kept list lies in [w0, w1), like cta_compact, for windows much shorter
+// than the list (one attention CTA's run), at a cost that does not depend on where the window
+// lies. Thread t counts the kept pages of its segment [t * seg, (t + 1) * seg), seg =
+// ceil(n / NT), starting at a rotated offset (t mod seg) so that the threads of a warp read
+// different banks; one block scan of the (> T, == T) counts gives each segment its first
+// position; the thread whose segment holds position w0 publishes where that segment starts
+// and the counts before it, and warp 0 walks the pages from there 32 at a time with ballots
+// until it passes w1. wtot: NT/32 doublewords; misc2: 4 words. Ends with the emits done by
+// warp 0 only: the caller synchronises before reading what emit wrote.
+template <int NT, typename F>
+__device__ void cta_compact_window(const CtaKeys& K, uint32_t T, uint32_t take_eq,
+                                   uint64_t* wtot, uint32_t* misc2, int w0, int w1, F&& emit) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (w0 >= w1) return;                                         // block-uniform
+  const uint32_t* keys = K.keys;
+  const int n = K.n;
+  const int seg = (n + NT - 1) / NT;
+  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg), len = s1 - s0;
+  uint32_t gt = 0u, eq = 0u;
+  const int r = len > 0 ? tid % len : 0;
+  constexpr int kU = 8;
+  for (int c = 0; c < len; c += kU) {
+    uint32_t v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      int off = c + u + r;
+      if (off >= len) off -= len;
+      v[u] = c + u < len ? keys[s0 + off] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const bool in = c + u < len;
+      gt += in && v[u] > T;
+      eq += in && v[u] == T;
+    }
+  }
+  // exclusive scan of the packed counts over the block
+  const uint64_t mine = ((uint64_t)gt << 32) | eq;
+  uint64_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  if (tid == 0) misc2[0] = 0xffffffffu;                          // no segment holds w0 yet
+  __syncthreads();
+  const uint64_t wv = lane < NW ? wtot[lane] : 0ull;
+  const uint64_t before = incl - mine;
+  const uint32_t gt_before =
+      (uint32_t)(before >> 32) +
+      __reduce_add_sync(0xffffffffu, lane < warp ? (uint32_t)(wv >> 32) : 0u);
+  const uint32_t eq_before =
+      (uint32_t)before + __reduce_add_sync(0xffffffffu, lane < warp ? (uint32_t)wv : 0u);
+  const uint32_t first = gt_before + min(eq_before, take_eq);
+  const uint32_t last = gt_before + gt + min(eq_before + eq, take_eq);   // exclusive
+  if (len > 0 && first <= (uint32_t)w0 && (uint32_t)w0 < last) {        // exactly one thread
+    misc2[0] = (uint32_t)s0;
+    misc2[1] = gt_before;
+    misc2[2] = eq_before;
+  }
+  __syncthreads();
+  if (warp != 0 || misc2[0] == 0xffffffffu) return;            // the window is past the list
+  uint32_t g_run = misc2[1], e_run = misc2[2];
+  const uint32_t below = (1u << lane) - 1u;
+  for (int base = (int)misc2[0]; base < n; base += 32) {
+    const int i = base + lane;
+    const uint32_t v = i < n ? keys[i] : 0u;
+    const uint32_t bg = __ballot_sync(0xffffffffu, i < n && v > T);
+    const uint32_t be = __ballot_sync(0xffffffffu, i < n && v == T);
+    const uint32_t g_me = g_run + __popc(bg & below);
+    const uint32_t e_me = e_run + __popc(be & below);
+    int pos = -1;
+    if ((bg >> lane) & 1u) pos = (int)(g_me + min(e_me, take_eq));
+    else if (((be >> lane) & 1u) && e_me < take_eq) pos = (int)(g_me + e_me);
+    if (pos >= w0 && pos < w1) emit(i, pos);
+    g_run += __popc(bg);
+    e_run += __popc(be);
+    if (g_run + min(e_run, take_eq) >= (uint32_t)w1) break;       // past the window
   }
 }
 

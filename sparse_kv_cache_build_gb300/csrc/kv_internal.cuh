@@ -2,6 +2,7 @@
 // Not part of the public interface (include/sparsekv.h is).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -207,9 +208,10 @@ __device__ __forceinline__ int checked_len(const DevCtx& c, const kv_cache_desc&
 // Launchers (one per kernel family; each returns cudaGetLastError()).
 // ------------------------------------------------------------------------------------
 // stats_exp == NULL: statistics in the cache's dtype; otherwise FP8 bytes in stats and one
-// int8 exponent per (page, KV head) in stats_exp (fp8_stats.cuh).
+// int8 exponent per (page, KV head) in stats_exp (fp8_stats.cuh). subset != NULL: only the
+// mapped pages whose physical index is in subset[0, n_subset) (strictly ascending).
 cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, int8_t* stats_exp,
-                              DevCtx ctx, cudaStream_t s);
+                              const int32_t* subset, int n_subset, DevCtx ctx, cudaStream_t s);
 // Entmax decoding (entmax.cu). Moments: zb/cz/vz [B][Hq][stride]. Selection: one block per
 // group writes the kept pages ascending. Attention: logits [B][Hq][cap_slots] scratch, then
 // out [B][Hq][D] and tau [B][Hq] (in z = logit/2 units).
@@ -272,6 +274,11 @@ cudaError_t launch_fused_step(const kv_cache_desc& d, int G, int CL, const void*
                               const void* stats, float sm_scale, double keep_ratio, int budget,
                               int k_max, int dense, int32_t* sel_out, int32_t* cnt_out,
                               float* out, float* lse, DevCtx ctx, cudaStream_t s);
+
+// The 2-D TMA tensor map of a bf16 pool ([NP*Hkv*PS rows][D columns], boxes of 64 columns x
+// PS rows, 128-byte swizzle) for the current device, from a small cache of encoded maps
+// (thread-safe); false if it cannot be encoded.
+bool pool_tensor_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d);
 
 // Dynamic shared memory bytes of the attention kernel for this shape (0 = unsupported).
 size_t split_attn_smem_bytes(int dtype, int head_dim, int group_size);

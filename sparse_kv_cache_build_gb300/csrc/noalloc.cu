@@ -9,17 +9,21 @@
 // The scratch is one file-scope __device__ array of KV_STATIC_SCRATCH_BYTES (8 MiB). Every
 // GPU that loads the library holds it until the process exits. In host code the array's name
 // is only a host-side stand-in, never a device address, so the first call on each device
-// looks the address up with cudaGetSymbolAddress (with that device current) and keeps it;
-// that first call should therefore come before any stream capture. All calls share the one
-// array and it keeps the previous call's contents: calls that overlap on the GPU (other
-// streams, other host threads) race on it and must be serialised by the caller. Nothing in
-// it needs to start at zero -- every call writes each scratch byte before reading it.
+// looks the address up with cudaGetSymbolAddress (with that device current) and keeps it.
+// CUDA loads this file's module lazily, so that first lookup is also when the module is
+// loaded and the array reserved on the device (it can fail under memory pressure, or
+// synchronise): the first call belongs at start-up, before any stream capture. All calls
+// share the one array and it keeps the previous call's contents: calls that overlap on the
+// GPU (other streams, other host threads) race on it and must be serialised by the caller.
+// Nothing in it needs to start at zero -- every call writes each scratch byte before reading
+// it.
 //
 // The step runs the four public calls (score, select, split-K attention, merge) on
-// sub-buffers carved from the array like kv_decode_step's workspace. They keep no
-// per-group counters, so no value has to survive from one call to the next; the selection
-// matches kv_decode_step's bit for bit and the outputs match up to float32 rounding of the
-// merge (kv_decode_step merges inside its attention kernel for bf16 caches).
+// sub-buffers carved from the array like kv_decode_step's workspace, without its per-group
+// counters, so no value has to survive from one call to the next; the limit checked is this
+// layout's size. num_splits <= 0 takes kv_auto_num_splits' count. The selection matches
+// kv_decode_step's bit for bit and the outputs match up to float32 rounding of the merge
+// (kv_decode_step merges inside its attention kernel for bf16 caches).
 #include <stdint.h>
 #include <string.h>
 

@@ -6,6 +6,11 @@
 // The statistic kept here is the coordinate-wise [min, max] box of the page's keys, which
 // makes the page score an exact upper bound of q.k (see score.cu).
 //
+// Subset builds: given a strictly ascending list of physical pages, only mapped pages whose
+// physical index is in the list are (re)built (a binary search per page; the rest of the
+// table costs one int32 read per page). Block (0, 0) checks that the list is ascending and
+// inside the pool, and flags it otherwise.
+//
 // Layout: one warp per (physical page, KV head) chunk. The chunk is PS rows of D
 // contiguous elements; lane l owns D/32 consecutive columns, so every row read by the warp
 // is one coalesced 128- or 256-byte access. Values are compared as floats and written back
@@ -58,12 +63,32 @@ __device__ __forceinline__ void store_row(T* p, const float* f) {
   }
 }
 
+// Whether P is one of list[0, n) (strictly ascending): lower bound by bisection. Every lane of
+// a warp reads the same entries (broadcast loads).
+__device__ __forceinline__ bool in_sorted(const int32_t* __restrict__ list, int n, int P) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(list + mid) < P) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo < n && __ldg(list + lo) == P;
+}
+
 template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kStatsWarps * 32)
 page_stats_kernel(kv_cache_desc d, T* __restrict__ stats, uint8_t* __restrict__ codes,
-                  int8_t* __restrict__ exps, DevCtx ctx) {
+                  int8_t* __restrict__ exps, const int32_t* __restrict__ subset, int n_subset,
+                  DevCtx ctx) {
   constexpr int EPL = D / 32;
   const int b = blockIdx.y;
+  if (subset != nullptr && blockIdx.x == 0 && b == 0) {
+    for (int i = threadIdx.x; i < n_subset; i += blockDim.x) {
+      const int P = __ldg(subset + i);
+      if (P < 0 || P >= d.num_phys_pages || (i + 1 < n_subset && __ldg(subset + i + 1) <= P))
+        flag(ctx, KV_DEVERR_BAD_PAGE);
+    }
+  }
   const int len = checked_len(ctx, d, b);
   const int PS = d.page_size, Hkv = d.num_kv_heads;
   const int n_pages = ceil_div(len, PS);
@@ -82,6 +107,7 @@ page_stats_kernel(kv_cache_desc d, T* __restrict__ stats, uint8_t* __restrict__ 
       if (lane == 0) flag(ctx, KV_DEVERR_BAD_PAGE);
       continue;
     }
+    if (subset != nullptr && !in_sorted(subset, n_subset, P)) continue;
     const int valid = min(PS, len - p * PS);
     const T* src = kp + (((long)P * Hkv + g) * PS) * D + lane * EPL;
     float mn[EPL], mx[EPL], v[EPL];
@@ -127,27 +153,29 @@ page_stats_kernel(kv_cache_desc d, T* __restrict__ stats, uint8_t* __restrict__ 
 }
 
 template <typename T, int D>
-cudaError_t launch_t(const kv_cache_desc& d, void* stats, int8_t* exps, DevCtx ctx,
-                     cudaStream_t s) {
+cudaError_t launch_t(const kv_cache_desc& d, void* stats, int8_t* exps, const int32_t* subset,
+                     int n_subset, DevCtx ctx, cudaStream_t s) {
   dim3 grid(ceil_div(d.page_table_stride, kStatsPagesPerBlock), d.batch);
   if (exps != nullptr)
     page_stats_kernel<T, D, true><<<grid, kStatsWarps * 32, 0, s>>>(
-        d, nullptr, static_cast<uint8_t*>(stats), exps, ctx);
+        d, nullptr, static_cast<uint8_t*>(stats), exps, subset, n_subset, ctx);
   else
     page_stats_kernel<T, D, false><<<grid, kStatsWarps * 32, 0, s>>>(
-        d, static_cast<T*>(stats), nullptr, nullptr, ctx);
+        d, static_cast<T*>(stats), nullptr, nullptr, subset, n_subset, ctx);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, int8_t* stats_exp,
-                              DevCtx ctx, cudaStream_t s) {
+                              const int32_t* subset, int n_subset, DevCtx ctx,
+                              cudaStream_t s) {
   const bool bf = d.dtype == KV_BF16;
-  if (d.head_dim == 128) return bf ? launch_t<bf16_t, 128>(d, stats, stats_exp, ctx, s)
-                                   : launch_t<float, 128>(d, stats, stats_exp, ctx, s);
-  return bf ? launch_t<bf16_t, 64>(d, stats, stats_exp, ctx, s)
-            : launch_t<float, 64>(d, stats, stats_exp, ctx, s);
+  if (d.head_dim == 128)
+    return bf ? launch_t<bf16_t, 128>(d, stats, stats_exp, subset, n_subset, ctx, s)
+              : launch_t<float, 128>(d, stats, stats_exp, subset, n_subset, ctx, s);
+  return bf ? launch_t<bf16_t, 64>(d, stats, stats_exp, subset, n_subset, ctx, s)
+            : launch_t<float, 64>(d, stats, stats_exp, subset, n_subset, ctx, s);
 }
 
 }  // namespace skv

@@ -32,6 +32,8 @@
 // Every CTA of a cluster takes the same branches (they depend only on the group's length,
 // keep count and the summed histograms), so every cluster barrier is reached by all of them;
 // bounded copy waits that run out mark the CTA's share empty, never skip a barrier.
+#include <atomic>
+
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
@@ -217,7 +219,8 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
       np = kFusedMaxRun;
     }
-    cta_compact<kFusedThreads>(K, T, take_eq, s_misc64, pos0, pos0 + np, [&](int p, int pos) {
+    cta_compact_window<kFusedThreads>(K, T, take_eq, s_misc64, s_misc, pos0, pos0 + np,
+                                      [&](int p, int pos) {
       if (pos >= pos0 && pos < pos0 + np) {
         const int P = s_phys[p];
         s_runp[pos - pos0] = P;
@@ -321,33 +324,6 @@ fused_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 // ------------------------------------------------------------------------------------------
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 fused_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
-  }();
-  return fn;
-}
-
-bool fused_pool_map(CUtensorMap* map, const void* pool, const kv_cache_desc& d) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = fused_encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t rows = (cuuint64_t)d.num_phys_pages * d.num_kv_heads * d.page_size;
-  const cuuint64_t dims[2] = {(cuuint64_t)d.head_dim, rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)d.head_dim * 2};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)d.page_size};
-  const cuuint32_t elem_strides[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides,
-            box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 template <int D, int G>
 cudaError_t fused_launch_t(const kv_cache_desc& d, int CL, const void* q, const void* stats,
                            float sm_scale, double keep_ratio, int budget, int k_max, int dense,
@@ -355,16 +331,16 @@ cudaError_t fused_launch_t(const kv_cache_desc& d, int CL, const void* q, const 
                            DevCtx ctx, cudaStream_t s, bool query_only, int* max_clusters) {
   using C = FusedCfg<D, G>;
   auto kern = fused_step_kernel<D, G>;
-  static int attr_set_for_device[64] = {0};
+  static std::atomic<int> attr_set_for_device[64];   // see launch_mma in attn_bf16.cu
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set_for_device[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set_for_device[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    attr_set_for_device[dev] = 1;
+    attr_set_for_device[dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, d.num_kv_heads, d.batch);
@@ -385,7 +361,7 @@ cudaError_t fused_launch_t(const kv_cache_desc& d, int CL, const void* q, const 
     return cudaOccupancyMaxActiveClusters(max_clusters, kern, &cfg);
   }
   CUtensorMap mk, mv;
-  if (!fused_pool_map(&mk, d.k_pool, d) || !fused_pool_map(&mv, d.v_pool, d))
+  if (!pool_tensor_map(&mk, d.k_pool, d) || !pool_tensor_map(&mv, d.v_pool, d))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mk, mv, d, static_cast<const uint16_t*>(q),
                                      static_cast<const uint16_t*>(stats), sm_scale * kLog2e,

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_version() == 100
+    assert lib.kv_version() == 101
     for code in range(-7, 1):
         s = lib.kv_status_string(code).decode()
         assert s and s != "unknown status"
@@ -63,14 +63,19 @@ def desc(**kw):
 def test_invalid_arguments_are_rejected_on_the_host(lib):
     d = desc()
     null = None
-    assert lib.kv_build_page_stats(None, 256, null) == -1
-    assert lib.kv_build_page_stats(ctypes.byref(desc(k_pool=None)), 256, null) == -1
-    assert lib.kv_build_page_stats(ctypes.byref(desc(head_dim=96)), 256, null) == -2
-    assert lib.kv_build_page_stats(ctypes.byref(desc(page_size=8)), 256, null) == -2
-    assert lib.kv_build_page_stats(ctypes.byref(desc(dtype=7)), 256, null) == -2
-    assert lib.kv_build_page_stats(ctypes.byref(desc(k_pool=16 * 1000 + 2)), 256, null) == -7
-    assert lib.kv_build_page_stats(ctypes.byref(d), None, null) == -1
-    assert lib.kv_build_page_stats(ctypes.byref(d), 258, null) == -7
+    assert lib.kv_build_page_stats(None, 256, None, 0, null) == -1
+    assert lib.kv_build_page_stats(ctypes.byref(desc(k_pool=None)), 256, None, 0, null) == -1
+    assert lib.kv_build_page_stats(ctypes.byref(desc(head_dim=96)), 256, None, 0, null) == -2
+    assert lib.kv_build_page_stats(ctypes.byref(desc(page_size=8)), 256, None, 0, null) == -2
+    assert lib.kv_build_page_stats(ctypes.byref(desc(dtype=7)), 256, None, 0, null) == -2
+    assert lib.kv_build_page_stats(ctypes.byref(desc(k_pool=16 * 1000 + 2)), 256, None, 0, null) == -7
+    assert lib.kv_build_page_stats(ctypes.byref(d), None, None, 0, null) == -1
+    assert lib.kv_build_page_stats(ctypes.byref(d), 258, None, 0, null) == -7
+    # a physical-page subset: its length must lie in [0, num_phys_pages]; an empty list
+    # has nothing to rebuild and launches nothing
+    assert lib.kv_build_page_stats(ctypes.byref(d), 256, 4096, -1, null) == -1
+    assert lib.kv_build_page_stats(ctypes.byref(d), 256, 4096, 5, null) == -1
+    assert lib.kv_build_page_stats(ctypes.byref(d), 256, 4096, 0, null) == 0
     # group size 3 is outside {1, 2, 4, 8}; 7 heads do not divide into 2 KV heads
     assert lib.kv_score_pages(ctypes.byref(d), 512, 6, 256, 1024, 4, null) == -2
     assert lib.kv_score_pages(ctypes.byref(d), 512, 7, 256, 1024, 4, null) == -1
@@ -96,6 +101,20 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.kv_decode_step(ctypes.byref(d), 512, 8, 0.1, 256, 0.3, 0, 4, 1, 1024, None,
                               4096 + 16, 1 << 20, null) == -4
     assert lib.kv_set_wait_limit_ns(2_000_000_000) == 0
+
+
+def test_workspace_size_dispatches_to_each_calls_own_size(lib):
+    d = desc(batch=3, page_table_stride=40)
+    ref = ctypes.byref(d)
+    assert lib.kv_workspace_size(0, ref, 8, 12, 5) == lib.kv_decode_step_workspace_size(ref, 8, 12, 5)
+    assert lib.kv_workspace_size(0, ref, 8, 12, 5) > 0
+    assert lib.kv_workspace_size(1, ref, 8, 0, 0) == lib.kv_dropped_mass_workspace_size(ref, 8)
+    assert lib.kv_workspace_size(2, ref, 8, 12, 0) == lib.kv_entmax_attn_workspace_size(ref, 8, 12)
+    assert lib.kv_workspace_size(2, ref, 8, 0, 0) == lib.kv_entmax_attn_workspace_size(ref, 8, 0)
+    assert lib.kv_workspace_size(3, ref, 8, 12, 0) == \
+        lib.kv_entmax_decode_step_workspace_size(ref, 8, 12)
+    assert lib.kv_workspace_size(99, ref, 8, 12, 5) == 0
+    assert lib.kv_workspace_size(0, None, 8, 12, 5) == 0
 
 
 def test_dropped_mass_workspace_size_formula(lib):

@@ -60,6 +60,47 @@ def test_page_stats_bit_exact(dtype, D, G, PS):
     assert np.isnan(got[~mapped]).all()          # unmapped pages are never written
 
 
+@pytest.mark.parametrize("dtype,D,G,PS", SHAPES[:4])
+def test_page_stats_rebuild_of_a_physical_page_subset(dtype, D, G, PS):
+    """A strictly ascending list of physical pages: exactly the mapped ones among them are
+    rebuilt, bit-exact; every other row keeps what it held; listed unmapped pages stay
+    unwritten; an out-of-order list is flagged."""
+    c = make(dtype, D, G, PS)
+    kv = skv.PagedKV.from_cache(c)
+    NP = c.num_phys_pages
+    K, table, lens = f64(c.k_pool), c.page_table.cpu().numpy(), c.seq_lens.cpu().numpy()
+    mn, mx = oracle.page_stats(K, table, lens, PS)
+    mapped = ~np.isnan(mn[:, 0, 0])
+    rng = np.random.default_rng(11)
+    subset = np.sort(rng.choice(NP, size=NP // 3, replace=False))
+    unmapped = np.nonzero(~mapped)[0]
+    subset = np.unique(np.concatenate([subset, unmapped[:2]]))   # two listed unmapped pages
+    stats = torch.full((NP, 2, 2, D), float("nan"), dtype=c.k_pool.dtype, device="cuda")
+    skv.kv_build_page_stats(kv, stats,
+                            phys_pages=torch.tensor(subset, dtype=torch.int32, device="cuda"))
+    assert_no_device_error()
+    got = f64(stats)
+    want = np.zeros(NP, dtype=bool)
+    want[subset] = True
+    rebuilt = want & mapped
+    assert rebuilt.sum() > 0 and (mapped & ~want).sum() > 0
+    np.testing.assert_array_equal(got[rebuilt, :, 0, :], mn[rebuilt])
+    np.testing.assert_array_equal(got[rebuilt, :, 1, :], mx[rebuilt])
+    assert np.isnan(got[~rebuilt]).all()
+    # an empty list rebuilds nothing; the full build then matches the oracle everywhere
+    skv.kv_build_page_stats(kv, stats, phys_pages=torch.zeros((0,), dtype=torch.int32,
+                                                              device="cuda"))
+    assert np.isnan(f64(stats)[~rebuilt]).all()
+    skv.kv_build_page_stats(kv, stats)
+    got = f64(stats)
+    np.testing.assert_array_equal(got[mapped, :, 0, :], mn[mapped])
+    # a list out of order is flagged as a bad page
+    bad = torch.tensor([3, 1, 2], dtype=torch.int32, device="cuda")
+    skv.kv_build_page_stats(kv, stats, phys_pages=bad)
+    st, flags = skv.kv_check_device_errors()
+    assert flags & 1
+
+
 # ------------------------------------------------------------------------------ score
 
 @pytest.mark.parametrize("dtype,D,G,PS", SHAPES)

@@ -209,17 +209,22 @@ def test_one_workspace_serves_sparse_dense_and_other_k_max():
 def test_decode_step_plan_by_shape():
     """kv_decode_step's plan: bf16 groups of up to 16384 pages select inside the attention
     kernel, longer ones in the score launch, dense bf16 is the attention kernel alone, fp32
-    keeps four kernels;
-    the plan's kernels called one by one give kv_decode_step's output."""
+    keeps four kernels; with 8 splits or more the merge is a kernel of its own (plans 6, 7
+    and 4 in place of 1, 2 and 3). The plan's kernels called one by one give kv_decode_step's
+    output bit for bit."""
     cases = [("bf16", (1000, 4097, 37), 1), ("bf16", (8200 * 16,), 1), ("bf16", (16400 * 16,), 2),
-             ("fp32", (1000, 37), 0)]
+             ("fp32", (1000, 37), 0), ("bf16", (2000,), 1)]
+    seen = set()
     for dtype, lens, want in cases:
         w, c = _make(dtype, 128, 4, 16, lens)
         kv = skv.PagedKV.from_cache(c)
         plan, S = skv.kv_decode_step_plan(kv, w.num_q_heads, keep_ratio=0.3)
-        assert plan == want, (dtype, lens, plan)
-        dplan, _ = skv.kv_decode_step_plan(kv, w.num_q_heads, keep_ratio=1.0)
-        assert dplan == (3 if dtype == "bf16" else 4)
+        separate = dtype == "bf16" and S >= 8
+        assert plan == {1: 6, 2: 7}.get(want, want) if separate else plan == want, \
+            (dtype, lens, plan, S)
+        dplan, dS = skv.kv_decode_step_plan(kv, w.num_q_heads, keep_ratio=1.0)
+        assert dplan == (4 if dtype != "bf16" or dS >= 8 else 3), (dplan, dS)
+        seen.add(plan)
         if dtype != "bf16":
             continue
         stats = skv.kv_build_page_stats(kv)
@@ -229,8 +234,18 @@ def test_decode_step_plan_by_shape():
             scores = skv.kv_score_pages(kv, c.q, stats)
             out2, lse2 = skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, keep_ratio=0.3,
                                                    k_max=k_max, num_splits=S)
-        else:
+        elif plan == 2:
             _, sel, cnt = skv.kv_score_select(kv, c.q, stats, keep_ratio=0.3, k_max=k_max)
             out2, lse2 = skv.kv_decode_attn_merge(kv, c.q, w.sm_scale, sel, cnt, num_splits=S)
+        else:
+            # the same partials through the selected list, then the merge kernel
+            if plan == 6:
+                scores = skv.kv_score_pages(kv, c.q, stats)
+                sel, cnt = skv.kv_select_topk(scores, c.seq_lens, 16, keep_ratio=0.3, k_max=k_max)
+            else:
+                _, sel, cnt = skv.kv_score_select(kv, c.q, stats, keep_ratio=0.3, k_max=k_max)
+            acc, ml = skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, sel, cnt, num_splits=S)
+            out2, lse2 = skv.kv_merge_splits(acc, ml)
         assert_no_device_error()
-        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+        assert torch.equal(out, out2) and torch.equal(lse, lse2), plan
+    assert {0, 6, 7} <= seen or {0, 1, 2} <= seen, seen

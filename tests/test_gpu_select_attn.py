@@ -121,6 +121,16 @@ def _score_rows(kind, n, gen):
         return s
     if kind == "ramp":                         # distinct, ascending
         return torch.arange(n, dtype=torch.float32) * 0.5 - n / 4
+    if kind == "sampled_high":                 # the largest scores sit exactly on the pages
+        s = torch.randn(n, generator=gen)      # a strided 512-key sample of the row reads, so
+        st = (n // 512) | 1                    # the sample puts its bound L too high: fewer
+        idx = torch.tensor(sorted({(j * st) % n for j in range(512)}))   # than k keys >= L
+        s[idx] = 1000.0 + torch.arange(len(idx), dtype=torch.float32)
+        return s
+    if kind == "tied_low":                     # a few distinct high scores over a floor of
+        s = torch.full((n,), 1.0)              # ties: every key >= L, too many to gather
+        s[torch.randint(0, n, (20,), generator=gen)] = 5.0 + torch.rand(20, generator=gen)
+        return s
     return torch.randn(n, generator=gen)
 
 
@@ -144,12 +154,20 @@ def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
         k_max = skv.max_keep_pages(kv.stride, ratio if not budget else None, budget or None)
         sel = torch.full((w.batch, Hkv, k_max), -1, dtype=torch.int32, device="cuda")
         cnt = torch.full((w.batch, Hkv), -1, dtype=torch.int32, device="cuda")
-        S = min(8, skv.kv_auto_num_splits(kv, w.num_q_heads, k_max))
+        S_auto = skv.kv_auto_num_splits(kv, w.num_q_heads, k_max)
+        S = min(8, S_auto)
         out, _ = skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, keep_ratio=ratio,
                                            budget_pages=budget, k_max=k_max, num_splits=S,
                                            sel_idx=sel, sel_cnt=cnt)
         assert_no_device_error()
+        # the automatic split count: short runs per CTA (each CTA writes its run's part)
+        sel_a = torch.full_like(sel, -1)
+        skv.kv_select_decode_attn(kv, c.q, w.sm_scale, scores, keep_ratio=ratio,
+                                  budget_pages=budget, k_max=k_max, num_splits=S_auto,
+                                  sel_idx=sel_a, sel_cnt=torch.empty_like(cnt))
+        assert_no_device_error()
         sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+        np.testing.assert_array_equal(sel_a.cpu().numpy(), sel)
         for b in range(w.batch):
             nb = oracle.num_pages(int(c.seq_lens[b]), PS)
             k = (oracle.keep_count(nb, budget_tokens=budget * PS, page_size=PS) if budget
@@ -165,11 +183,14 @@ def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
 
 
 @pytest.mark.parametrize("n", [4096, 9001, 20000])
-@pytest.mark.parametrize("kind", ["coarse", "outliers", "ramp", "normal"])
+@pytest.mark.parametrize("kind", ["coarse", "outliers", "ramp", "normal", "sampled_high",
+                                  "tied_low"])
 def test_select_topk_long_groups_keeping_few(n, kind):
     """Groups of 4096 pages or more keeping at most a sixteenth, where the block top-k first
     filters the keys by a sample: the oracle's rule exactly (score descending, lower page
-    first on ties, ascending output), ties, outliers and ramps included."""
+    first on ties, ascending output), ties, outliers and ramps included. sampled_high and
+    tied_low defeat the sample (too few keys at or above its bound; too many to gather), so
+    the search takes its path over every key."""
     PS, Hkv, B = 16, 2, 2
     gen = torch.Generator().manual_seed(n + 31 * len(kind))
     scores = torch.stack([torch.stack([_score_rows(kind, n, gen) for _ in range(Hkv)])

@@ -1,7 +1,9 @@
 """Parity at the full sizes of the five named workloads, in the launch configuration the
-benchmark times (automatic split count, the fused decode step). Every group's selection is
-checked exactly against the oracle's rule on the GPU's scores; sampled groups are checked
-against the oracle end to end (statistics, scores, tie band, attention, dense, delta)."""
+benchmark times (automatic split count, the fused decode step). Every group's selection --
+the standalone top-k's and the one the benchmarked step itself made, read back from its
+workspace -- is checked exactly against the oracle's rule on the GPU's scores; sampled groups
+are checked against the oracle end to end (statistics, scores, tie band, attention over the
+step's own selection, dense, delta)."""
 
 import numpy as np
 import pytest
@@ -11,7 +13,8 @@ import oracle
 import sparse_kv_cache_build_gb300 as skv
 from sparse_kv_cache_build_gb300 import inputs
 
-from gpu_helpers import assert_no_device_error, f64, group_inputs, need_gpu, oracle_group, out_tol
+from gpu_helpers import (assert_no_device_error, f64, group_inputs, need_gpu, oracle_group,
+                         out_tol, round4, step_score_region, step_selection)
 
 pytestmark = pytest.mark.gpu
 
@@ -73,12 +76,21 @@ def test_workload_full_size(name):
         sel, cnt = skv.kv_select_topk(scores, c.seq_lens, PS, **sel_kw)
         acc, ml = skv.kv_sparse_decode_attn(kv, c.q, w.sm_scale, sel, cnt, num_splits=S)
         out, lse = skv.kv_merge_splits(acc, ml)
-        fused = None
+        fused = step_sel = step_cnt = step_sc = None
         if "keep" not in sel_kw:
-            # the step as the benchmark times it, and the one-launch step
+            # the step as the benchmark times it (its selection read back from the
+            # workspace), and the one-launch step
+            ws = torch.zeros((skv.kv_decode_step_workspace_size(kv, Hq, k_max),),
+                             dtype=torch.uint8, device="cuda")
             fused, _ = skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max,
                                           keep_ratio=lib_kw.get("keep_ratio", 1.0),
-                                          budget_pages=lib_kw.get("budget_pages", 0))
+                                          budget_pages=lib_kw.get("budget_pages", 0),
+                                          workspace=ws)
+            torch.cuda.synchronize()
+            step_sel, step_cnt = step_selection(ws, B, Hkv, kv.stride, k_max)
+            r4 = round4(kv.stride)
+            step_sc = f64(step_score_region(ws, B, Hkv, kv.stride).view(torch.float32)
+                          [: B * Hkv * r4].view(B, Hkv, r4))
             one, _ = skv.kv_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max,
                                         keep_ratio=lib_kw.get("keep_ratio", 1.0),
                                         budget_pages=lib_kw.get("budget_pages", 0),
@@ -99,6 +111,11 @@ def test_workload_full_size(name):
             for g in range(Hkv):
                 assert cnt[b, g] == k
                 np.testing.assert_array_equal(sel[b, g, :k], oracle.select_pages(sc[b, g, :n], k))
+                if step_sel is not None:
+                    assert step_cnt[b, g] == k
+                    np.testing.assert_array_equal(
+                        step_sel[b, g, :k], oracle.select_pages(step_sc[b, g, :n], k))
+                    np.testing.assert_array_equal(step_sel[b, g, :k], sel[b, g, :k])
 
         # sampled groups against the oracle end to end
         for b, g in groups:
@@ -115,8 +132,11 @@ def test_workload_full_size(name):
             err = np.abs(out[b, hs] - ref[0]).max()
             assert err < tol, f"{label} b={b} g={g}: max err {err}"
             if fused is not None:
-                err = np.abs(fused[b, hs] - ref[0]).max()
-                assert err < tol, f"{label} one-launch b={b} g={g}: max err {err}"
+                s_step = step_sel[b, g, : step_cnt[b, g]]
+                ref_step, _ = oracle.attend(o["q"], o["K"], o["V"], o["table"], o["lens"], PS,
+                                            w.sm_scale, selected=[[s_step]])
+                err = np.abs(fused[b, hs] - ref_step[0]).max()
+                assert err < tol, f"{label} step b={b} g={g}: max err {err}"
             d_ref = oracle.dropped_mass(o["q"], o["K"], o["table"], o["lens"], PS, w.sm_scale,
                                         [[s]])
             np.testing.assert_allclose(delta[b, hs], d_ref[0], rtol=1e-3, atol=1e-5)
