@@ -918,9 +918,9 @@ def run_ours(args):
 
     # ---- end to end through the public API, host buffers, copies inside the timing -------
     # (1) the captured step (kv_decode_step_graph_*), the call a serving loop makes per token:
-    #     the query copied from pinned host memory into the captured query buffer, one graph
-    #     launch, the output copied back to pinned host memory, then the host waits;
-    # (2) the same with a direct kv_decode_step call instead of the graph launch.
+    #     one launch copies the query in from pinned host memory, runs the step and copies
+    #     the output back to pinned host memory; then the host waits;
+    # (2) the same copies around a direct kv_decode_step call through the binding.
     q_host = c.q.detach().cpu().pin_memory()
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(c.q)
@@ -928,19 +928,19 @@ def run_ours(args):
     if step_kw is not None:
         ws_g = torch.zeros_like(ws)
         sg = skv.DecodeStepGraph(kv, q_dev, w.sm_scale, stats, k_max=k_max, workspace=ws_g,
-                                 **step_kw)
+                                 q_host=q_host, out_host=out_host, **step_kw)
         for graph_call, res in ((True, e2e_us), (False, e2e_direct_us)):
             for i in range(args.warmup + min(args.steps, 500)):
                 flush.zero_()
                 torch.cuda.synchronize()
                 h0 = time.perf_counter()
-                q_dev.copy_(q_host, non_blocking=True)
                 if graph_call:
-                    g_out, _ = sg.launch()
+                    sg.launch()
                 else:
+                    q_dev.copy_(q_host, non_blocking=True)
                     g_out, _ = skv.kv_decode_step(kv, q_dev, w.sm_scale, stats, k_max=k_max,
                                                   out=out, lse=lse, workspace=ws, **step_kw)
-                out_host.copy_(g_out, non_blocking=True)
+                    out_host.copy_(g_out, non_blocking=True)
                 torch.cuda.synchronize()
                 if i >= args.warmup:
                     res.append((time.perf_counter() - h0) * 1e6)
@@ -1067,8 +1067,8 @@ def run_ours(args):
                        "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
                        "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
                        "api": "kv_decode_step_graph_launch (the step captured once by "
-                              "kv_decode_step_graph_create; query copied in, output copied "
-                              "out, host waits)",
+                              "kv_decode_step_graph_create with the query's copy in from and "
+                              "the output's copy out to pinned host memory; host waits)",
                        "direct_call_us": round(statistics.median(e2e_direct_us), 3),
                        "direct_call_api": "kv_decode_step through the Python binding"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

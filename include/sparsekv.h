@@ -401,6 +401,10 @@ size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_h
  * workspace). destroy frees the graph (NULL is accepted). create returns kv_decode_step's
  * status for bad arguments, KV_ERR_CUDA if capture or instantiation fails; *graph is NULL
  * then. The graph holds host and driver resources only; no device buffer is allocated.
+ * q_host (host, page-locked, batch * num_q_heads * head_dim elements of the cache dtype)
+ * and out_host (host, page-locked, batch * num_q_heads * head_dim float32) may be NULL;
+ * when given, every launch first copies q_host into q and finally copies out into
+ * out_host, so one launch per token carries the query in and the output back.
  */
 typedef struct kv_step_graph kv_step_graph;
 kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
@@ -408,6 +412,7 @@ kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
                                       double keep_ratio, int32_t budget_pages, int32_t k_max,
                                       int32_t num_splits, float* out, float* lse,
                                       void* workspace, size_t workspace_bytes,
+                                      const void* q_host, float* out_host,
                                       kv_step_graph** graph);
 kv_status kv_decode_step_graph_launch(kv_step_graph* graph, cudaStream_t stream);
 kv_status kv_decode_step_graph_destroy(kv_step_graph* graph);

@@ -84,7 +84,7 @@ def _declare(lib):
         "kv_build_page_stats": (I32, [D, P, P, I32, P]),
         "kv_workspace_size": (SZ, [I32, D, I32, I32, I32]),
         "kv_decode_step_graph_create": (I32, [D, P, I32, F32, P, F64, I32, I32, I32, P, P, P, SZ,
-                                              ctypes.POINTER(P)]),
+                                              P, P, ctypes.POINTER(P)]),
         "kv_decode_step_graph_launch": (I32, [P, P]),
         "kv_decode_step_graph_destroy": (I32, [P]),
         "kv_score_pages": (I32, [D, P, I32, P, P, I32, P]),
@@ -585,8 +585,15 @@ class DecodeStepGraph:
 
     def __init__(self, kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: float = 1.0,
                  budget_pages: int = 0, k_max: int | None = None, num_splits: int = 0,
-                 out=None, lse=None, workspace=None):
+                 out=None, lse=None, workspace=None, q_host=None, out_host=None):
+        """q_host / out_host: optional page-locked CPU tensors; each launch then copies
+        q_host into q first and the output into out_host last."""
         _need(q, "q", kv.dtype)
+        for t, name in ((q_host, "q_host"), (out_host, "out_host")):
+            if t is not None and (t.is_cuda or not t.is_pinned() or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous page-locked CPU tensor")
+        if q_host is not None and (q_host.dtype != q.dtype or q_host.shape != q.shape):
+            raise ValueError("q_host must match q")
         B, Hq, D = q.shape
         if k_max is None:
             k_max = max_keep_pages(kv.stride, keep_ratio, budget_pages)
@@ -597,13 +604,17 @@ class DecodeStepGraph:
         if workspace is None:
             nbytes = kv_decode_step_workspace_size(kv, Hq, k_max, max(num_splits, 0))
             workspace = torch.zeros((nbytes,), dtype=torch.uint8, device=q.device)
+        if out_host is not None and (out_host.dtype != torch.float32 or
+                                     out_host.shape != self.out.shape):
+            raise ValueError("out_host must be float32 of the output's shape")
         # the buffers must outlive the graph: keep them referenced
-        self._keep = (kv, q, stats, workspace)
+        self._keep = (kv, q, stats, workspace, q_host, out_host)
         handle = ctypes.c_void_p()
         _check("kv_decode_step_graph_create", lib().kv_decode_step_graph_create(
             kv.ref(), _ptr(q), Hq, float(sm_scale), _ptr(stats), float(keep_ratio),
             int(budget_pages), int(k_max), int(num_splits), _ptr(self.out), _ptr(self.lse),
-            _ptr(workspace), workspace.numel(), ctypes.byref(handle)))
+            _ptr(workspace), workspace.numel(), _ptr(q_host), _ptr(out_host),
+            ctypes.byref(handle)))
         self._handle = handle
 
     def launch(self, stream=None):

@@ -779,9 +779,14 @@ kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
                                       double keep_ratio, int32_t budget_pages, int32_t k_max,
                                       int32_t num_splits, float* out, float* lse,
                                       void* workspace, size_t workspace_bytes,
+                                      const void* q_host, float* out_host,
                                       kv_step_graph** graph) {
   if (graph == nullptr) return KV_ERR_INVALID_ARG;
   *graph = nullptr;
+  if (cache == nullptr || cache->batch <= 0 || num_q_heads <= 0 || cache->head_dim <= 0)
+    return KV_ERR_INVALID_ARG;
+  const size_t elems = (size_t)cache->batch * num_q_heads * cache->head_dim;
+  const size_t q_bytes = elems * (cache->dtype == KV_BF16 ? 2 : 4);
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KV_ERR_CUDA;
   // one uncaptured call first: it checks the arguments and does every first-use set-up
@@ -794,8 +799,17 @@ kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
       r = KV_ERR_CUDA;
     } else {
-      r = kv_decode_step(cache, q, num_q_heads, sm_scale, stats, keep_ratio, budget_pages,
-                         k_max, num_splits, out, lse, workspace, workspace_bytes, s);
+      if (q_host != nullptr &&
+          cudaMemcpyAsync(const_cast<void*>(q), q_host, q_bytes, cudaMemcpyHostToDevice, s) !=
+              cudaSuccess)
+        r = KV_ERR_CUDA;
+      if (r == KV_OK)
+        r = kv_decode_step(cache, q, num_q_heads, sm_scale, stats, keep_ratio, budget_pages,
+                           k_max, num_splits, out, lse, workspace, workspace_bytes, s);
+      if (r == KV_OK && out_host != nullptr &&
+          cudaMemcpyAsync(out_host, out, elems * sizeof(float), cudaMemcpyDeviceToHost, s) !=
+              cudaSuccess)
+        r = KV_ERR_CUDA;
       const cudaError_t e = cudaStreamEndCapture(s, &g);
       if (r == KV_OK && e != cudaSuccess) r = KV_ERR_CUDA;
     }

@@ -60,3 +60,27 @@ def test_captured_step_rejects_bad_arguments_without_a_graph():
     kv = skv.PagedKV.from_cache(c)
     with pytest.raises(skv.binding.KVError):
         skv.DecodeStepGraph(kv, c.q, -1.0, keep_ratio=1.0)        # non-positive scale
+
+
+def test_captured_step_with_host_copies():
+    """q_host copied in and the output copied out by the same launch."""
+    w = workload(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, dtype="bf16",
+                 seed=8, seq_lens=(3000,), planted=4)
+    c = inputs.make_cache(w, "cuda")
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    q_dev = torch.empty_like(c.q)
+    q_host = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
+    out_host = torch.empty((1, 8, 128), dtype=torch.float32).pin_memory()
+    g = skv.DecodeStepGraph(kv, q_dev, w.sm_scale, stats, keep_ratio=0.3, q_host=q_host,
+                            out_host=out_host)
+    gen = torch.Generator().manual_seed(4)
+    for _ in range(2):
+        q_host.copy_(torch.randn(c.q.shape, generator=gen).to(c.q.dtype))
+        g.launch()
+        torch.cuda.synchronize()
+        ref, _ = skv.kv_decode_step(kv, q_host.cuda(), w.sm_scale, stats, keep_ratio=0.3)
+        assert_no_device_error()
+        np.testing.assert_allclose(out_host.numpy().astype(np.float64), f64(ref), rtol=0,
+                                   atol=1e-6)
+    g.close()
