@@ -445,6 +445,59 @@ def measure_config(name, keep_index, args, dev, flush, peak, peak_kind):
     return res
 
 
+def measure_entmax_pruning(args, dev, flush):
+    """The entmax step (page moments, Gaussian-aware selection, entmax over the kept pages)
+    against dense entmax over every page, on the workload whose page boxes are tight enough
+    for the selector to prune."""
+    import sparse_kv_cache_build_gb300 as skv
+    from sparse_kv_cache_build_gb300 import binding, inputs
+    w = inputs.workload("entmax_pruning_32k")
+    c = inputs.make_cache(w, dev)
+    kv = skv.PagedKV.from_cache(c)
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    stats = skv.kv_build_page_stats(kv)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    tau = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    ws = torch.zeros((skv.kv_entmax_decode_step_workspace_size(kv, Hq, kv.stride),),
+                     dtype=torch.uint8, device=dev)
+    wsd = torch.empty((int(binding.lib().kv_entmax_attn_workspace_size(kv.ref(), Hq, 0)),),
+                      dtype=torch.uint8, device=dev)
+
+    def step():
+        skv.kv_entmax_decode_step(kv, c.q, w.sm_scale, stats, k_max=kv.stride, out=out, tau=tau,
+                                  workspace=ws)
+
+    def dense():
+        skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, out=out, tau=tau, workspace=wsd)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+        dense()
+    torch.cuda.synchronize()
+    gs, gd = capture_graph(step), capture_graph(dense)
+    for _ in range(args.warmup):
+        time_replays(gs, 1, flush)
+        time_replays(gd, 1, flush)
+    step_us = time_replays(gs, args.steps, flush)
+    dense_us = time_replays(gd, args.steps, flush)
+    step()
+    torch.cuda.synchronize()
+    M = (B * Hq * kv.stride * 4 + 255) // 256 * 256
+    cb = 3 * M + (B * Hkv * kv.stride * 4 + 255) // 256 * 256
+    kept = int(ws[cb: cb + B * Hkv * 4].view(torch.int32).sum())
+    st, flags = skv.kv_check_device_errors()
+    if st != 0:
+        raise RuntimeError(f"entmax pruning: device error word {flags:#x}")
+    res = {"workload": w.name, "description": w.description, "step_us": spread(step_us),
+           "dense_us": spread(dense_us),
+           "speedup_vs_dense": round(statistics.median(dense_us) / statistics.median(step_us), 3),
+           "kept_pages": kept, "pages": int(B * Hkv * kv.stride),
+           "gpu_launches": args.steps * (5 + 3)}
+    del c, kv, stats, ws, wsd
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_block_child(args):
     """One fresh-process block: the headline sparse and dense steps, replayed alternately
     (L2 flushed before each), printed as one JSON line for the parent."""
@@ -1081,6 +1134,10 @@ def run_ours(args):
             r = measure_config(name, ki, args, dev, flush, peak, peak_kind)
             line["configs"][f"{name}:{r['keep']}"] = r
             line["gpu_launches"] += r.pop("gpu_launches")
+    if world == 1 and not args.no_configs:
+        r = measure_entmax_pruning(args, dev, flush)
+        line["gpu_launches"] += r.pop("gpu_launches")
+        line["entmax_pruning"] = r
     if world == 1 and args.blocks > 0:
         line["blocks"] = run_blocks(args, args.blocks)
     return line

@@ -15,10 +15,12 @@
 //                          group: upper bound zb, centre logit c and within-box variance v of
 //                          z. Eight lanes own a row and hold the same columns of its min and
 //                          max halves, so (max - min)^2 is formed element-wise.
-//   entmax_select_kernel   one block per (sequence, KV head): the token-weighted mean and
-//                          variance of each head's z (double), tau_hat by bisection on the
-//                          closed-form Gaussian tail, then the kept pages in ascending order by
-//                          one block scan per 256 pages.
+//   entmax_select_kernel   one block of 1024 threads per (sequence, KV head): one pass
+//                          loading every head's moments of a batch of pages at once into
+//                          token-weighted double sums, one block reduction, a warp per head
+//                          solving tau_hat on the closed-form Gaussian tail (32 points per
+//                          round, then Newton), then the kept pages in ascending order by one
+//                          ballot-and-scan pass per 1024 pages.
 //   entmax_logits_kernel   split over the selected list; each warp takes a page, each lane a
 //                          token (or half of one), and computes the G heads' logits from the
 //                          page's keys: K is read once per group.
@@ -32,7 +34,7 @@ namespace skv {
 namespace {
 
 constexpr int kMomWarps = 4;                 // moments: 4 warps x 4 rows = 16 pages per block
-constexpr int kESelThreads = 256;
+constexpr int kESelThreads = 512;
 constexpr int kLogitWarps = 4;
 constexpr int kOutThreads = 512;
 constexpr int kCandCap = 16384;              // candidate logits held in shared memory
@@ -148,19 +150,29 @@ __device__ __forceinline__ void gaussian_tail(float mu, float sigma, float tau, 
 }
 
 // tau_hat with count * E[max(Z - tau_hat, 0)^2] = 1: f(t) = count * E[...] - 1 is convex and
-// decreasing, so a bracketing bisection followed by Newton steps from its f >= 0 end.
-__device__ float gaussian_threshold(float mu, float var, float count) {
+// decreasing in t. Called by a whole warp with the same arguments: each round the 32 lanes
+// evaluate f at 32 interior points of the bracket and keep the sub-interval where f changes
+// sign (four rounds shrink it about a million-fold), then Newton steps from its f >= 0 end
+// converge to float precision. Every lane returns the same value.
+__device__ float gaussian_threshold_warp(float mu, float var, float count) {
+  const int lane = threadIdx.x & 31;
   const float sigma = sqrtf(fmaxf(var, 0.f));
   float lo = mu - 1.f - 40.f * sigma, hi = mu + 40.f * sigma + 1.f;
   float f2, f1;
   gaussian_tail(mu, sigma, lo, f2, f1);
   if (count * f2 < 1.f) return lo;
-  for (int i = 0; i < 30; ++i) {
-    const float mid = 0.5f * (lo + hi);
-    if (!(mid > lo && mid < hi)) break;
-    gaussian_tail(mu, sigma, mid, f2, f1);
-    if (count * f2 >= 1.f) lo = mid;
-    else hi = mid;
+  for (int round = 0; round < 4; ++round) {
+    const float t = lo + (hi - lo) * (float)(lane + 1) / 33.f;
+    gaussian_tail(mu, sigma, t, f2, f1);
+    const uint32_t pos = __ballot_sync(0xffffffffu, count * f2 >= 1.f);   // a prefix of lanes
+    const int j = __popc(pos) - 1;                   // last point with f >= 0 (-1: none)
+    const float tj = __shfl_sync(0xffffffffu, t, j < 0 ? 0 : j);
+    const float tn = __shfl_sync(0xffffffffu, t, j + 1 > 31 ? 31 : j + 1);
+    const float nlo = j < 0 ? lo : tj;
+    const float nhi = j >= 31 ? hi : tn;
+    if (!(nlo < nhi)) break;
+    lo = nlo;
+    hi = nhi;
   }
   float t = lo;
   for (int i = 0; i < 6; ++i) {
@@ -174,6 +186,15 @@ __device__ float gaussian_threshold(float mu, float var, float count) {
   return t;
 }
 
+// One block of 512 threads per (sequence, KV head). Thread t takes pages t, t + 512, ...;
+// one pass loads every head's (c, v, zb) of a batch of its pages at once and accumulates, per
+// head, the token-weighted sums of (c - c0), (c - c0)^2 and v in float, c0 being the head's
+// first-page centre (so the variance of c is sum (c - c0)^2 / N - (sum (c - c0) / N)^2 with
+// little cancellation: the centres spread over a few standard deviations), and the first
+// maximum of zb; one block reduction; a warp per head solves tau_hat; then the kept pages,
+// ascending, by one ballot-and-scan pass per 512 pages. G: the group's query heads (1 to 8).
+// (FP64 is scarce on this part: double sums here cost more than the rest of the kernel.)
+template <int G>
 __global__ void __launch_bounds__(kESelThreads)
 entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int Hkv,
                      int table_stride, const float* __restrict__ zb,
@@ -181,16 +202,18 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
                      int k_max, int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt,
                      float* __restrict__ tau_hat, DevCtx ctx) {
   constexpr int NW = kESelThreads / 32;
-  constexpr int U = 4;                           // pages per thread per batch
-  __shared__ float s_red[8][NW];
-  __shared__ int s_redi[8][NW];
-  __shared__ float s_mu[8], s_tau[8];
-  __shared__ int s_arg[8];
+  constexpr int U = G <= 4 ? 2 : 1;              // pages per thread per batch
+  static_assert(G >= 1 && G <= 8 && G <= NW, "group size");
+  __shared__ float s_sum[3][G][NW];
+  __shared__ float s_bv[G][NW];
+  __shared__ int s_bi[G][NW];
+  __shared__ float s_tau[G];
+  __shared__ int s_arg[G];
   __shared__ uint32_t s_wsum[NW];
   pdl_trigger();
   pdl_wait();
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
-  const int warp = tid >> 5, G = Hq / Hkv;
+  const int warp = tid >> 5;
   int len = seq_lens[b];
   if (len < 0 || len > table_stride * PS) {
     if (tid == 0) flag(ctx, KV_DEVERR_BAD_LEN);
@@ -205,141 +228,118 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
       tau_hat[(long)b * Hq + g * G + tid] = __int_as_float(0x7fc00000);
     return;
   }
-  const float N = (float)len;
-  // pass 1, every head at once: token-weighted sum of c, and the first maximum of zb
-  float sc[8], best[8];
-  int besti[8];
+  // one pass: every head's sums and first maximum
+  float s1[G], s2[G], sv[G], c0[G];
+  float best[G];
+  int besti[G];
 #pragma unroll
-  for (int h = 0; h < 8; ++h) { sc[h] = 0.f; best[h] = -INFINITY; besti[h] = 0x7fffffff; }
+  for (int h = 0; h < G; ++h) c0[h] = __ldg(cz + row0 + (long)h * stride);   // page 0
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    s1[h] = s2[h] = sv[h] = 0.f;
+    best[h] = -INFINITY;
+    besti[h] = 0x7fffffff;
+  }
   for (int base = 0; base < n; base += kESelThreads * U) {
+    float cv[G][U], vv[G][U], zv[G][U];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      if (h >= G) break;
-      float cv[U], zv[U];
+    for (int h = 0; h < G; ++h) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int p = base + u * kESelThreads + tid;
-        cv[u] = p < n ? cz[row0 + (long)h * stride + p] : 0.f;
-        zv[u] = p < n ? zb[row0 + (long)h * stride + p] : -INFINITY;
+        const bool in = p < n;
+        const long i = row0 + (long)h * stride + p;
+        cv[h][u] = in ? cz[i] : 0.f;
+        vv[h][u] = in ? vz[i] : 0.f;
+        zv[h][u] = in ? zb[i] : -INFINITY;
       }
+    }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int p = base + u * kESelThreads + tid;
-        if (p < n) {
-          sc[h] = fmaf((float)min(PS, len - p * PS), cv[u], sc[h]);
-          if (zv[u] > best[h]) { best[h] = zv[u]; besti[h] = p; }   // pages increase
+    for (int u = 0; u < U; ++u) {
+      const int p = base + u * kESelThreads + tid;
+      if (p < n) {
+        const float wt = (float)min(PS, len - p * PS);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float dc = cv[h][u] - c0[h];
+          s1[h] = fmaf(wt, dc, s1[h]);
+          s2[h] = fmaf(wt * dc, dc, s2[h]);
+          sv[h] = fmaf(wt, vv[h][u], sv[h]);
+          if (zv[h][u] > best[h]) { best[h] = zv[h][u]; besti[h] = p; }   // pages increase
         }
       }
     }
   }
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    if (h >= G) break;
+  for (int h = 0; h < G; ++h) {
+    {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s1[h] += __shfl_xor_sync(0xffffffffu, s1[h], o);
+        s2[h] += __shfl_xor_sync(0xffffffffu, s2[h], o);
+        sv[h] += __shfl_xor_sync(0xffffffffu, sv[h], o);
+        const float ov = __shfl_xor_sync(0xffffffffu, best[h], o);
+        const int oi = __shfl_xor_sync(0xffffffffu, besti[h], o);
+        if (ov > best[h] || (ov == best[h] && oi < besti[h])) { best[h] = ov; besti[h] = oi; }
+      }
+      if (lane == 0) {
+        s_sum[0][h][warp] = s1[h];
+        s_sum[1][h][warp] = s2[h];
+        s_sum[2][h][warp] = sv[h];
+        s_bv[h][warp] = best[h];
+        s_bi[h][warp] = besti[h];
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < G) {                                // warp h: head h's moments and tau_hat
+    const int h = warp;
+    const bool lv = lane < NW;
+    float a1 = lv ? s_sum[0][h][lane] : 0.f, a2 = lv ? s_sum[1][h][lane] : 0.f;
+    float av = lv ? s_sum[2][h][lane] : 0.f;
+    float bv = lv ? s_bv[h][lane] : -INFINITY;
+    int bi = lv ? s_bi[h][lane] : 0x7fffffff;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], o);
-      const float ov = __shfl_xor_sync(0xffffffffu, best[h], o);
-      const int oi = __shfl_xor_sync(0xffffffffu, besti[h], o);
-      if (ov > best[h] || (ov == best[h] && oi < besti[h])) { best[h] = ov; besti[h] = oi; }
+      a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+      a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+      av += __shfl_xor_sync(0xffffffffu, av, o);
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
     }
-    if (lane == 0) { s_red[h][warp] = sc[h]; }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < 8; ++h)
-      if (h < G) { s_redi[h][warp] = besti[h]; }
-  }
-  __shared__ float s_bv[8][NW];
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < 8; ++h)
-      if (h < G) s_bv[h][warp] = best[h];
-  }
-  __syncthreads();
-  if (tid < G) {
-    float tot = 0.f, bv = s_bv[tid][0];
-    int bi = s_redi[tid][0];
-    for (int w = 0; w < NW; ++w) {
-      tot += s_red[tid][w];
-      if (s_bv[tid][w] > bv || (s_bv[tid][w] == bv && s_redi[tid][w] < bi)) {
-        bv = s_bv[tid][w];
-        bi = s_redi[tid][w];
-      }
-    }
-    s_mu[tid] = tot / N;
-    s_arg[tid] = bi;
-  }
-  __syncthreads();
-  // pass 2: token-weighted spread of c around mu plus the within-page variances
-  float sv[8];
-#pragma unroll
-  for (int h = 0; h < 8; ++h) sv[h] = 0.f;
-  for (int base = 0; base < n; base += kESelThreads * U) {
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      if (h >= G) break;
-      float cv[U], vv[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int p = base + u * kESelThreads + tid;
-        cv[u] = p < n ? cz[row0 + (long)h * stride + p] : 0.f;
-        vv[u] = p < n ? vz[row0 + (long)h * stride + p] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int p = base + u * kESelThreads + tid;
-        if (p < n) {
-          const float dc = cv[u] - s_mu[h];
-          sv[h] = fmaf((float)min(PS, len - p * PS), fmaf(dc, dc, vv[u]), sv[h]);
-        }
-      }
+    const float N = (float)len;
+    const float m1 = a1 / N;                     // mean of c - c0
+    const float var = fmaxf(a2 / N - m1 * m1, 0.f) + av / N;
+    const float t = gaussian_threshold_warp(__ldg(cz + row0 + (long)h * stride) + m1, var, N);
+    if (lane == 0) {
+      s_tau[h] = t;
+      s_arg[h] = bi;
+      if (tau_hat != nullptr) tau_hat[(long)b * Hq + g * G + h] = t;
     }
   }
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    if (h >= G) break;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sv[h] += __shfl_xor_sync(0xffffffffu, sv[h], o);
-  }
-  __syncthreads();                               // s_red of pass 1 is consumed
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < 8; ++h)
-      if (h < G) s_red[h][warp] = sv[h];
-  }
   __syncthreads();
-  if (tid < G) {                                 // the heads' thresholds, one thread each
-    float tot = 0.f;
-    for (int w = 0; w < NW; ++w) tot += s_red[tid][w];
-    s_tau[tid] = gaussian_threshold(s_mu[tid], tot / N, N);
-    if (tau_hat != nullptr) tau_hat[(long)b * Hq + g * G + tid] = s_tau[tid];
-  }
-  __syncthreads();
-  // kept pages, ascending: one block scan per 256 pages
+  // kept pages, ascending: one ballot-and-scan pass per 1024 pages
   uint32_t carry = 0;
   int32_t* out = sel_idx + grp * k_max;
   for (int base = 0; base < n; base += kESelThreads) {
     const int p = base + tid;
     bool keep = false;
     if (p < n) {
-      float zv[8];
+      float zvv[G];
 #pragma unroll
-      for (int h = 0; h < 8; ++h)                // the group's heads' loads together
-        zv[h] = h < G ? zb[row0 + (long)h * stride + p] : -INFINITY;
+      for (int h = 0; h < G; ++h)                // the group's heads' loads together
+        zvv[h] = zb[row0 + (long)h * stride + p];
 #pragma unroll
-      for (int h = 0; h < 8; ++h)
-        if (h < G) keep |= zv[h] > s_tau[h] || p == s_arg[h];
+      for (int h = 0; h < G; ++h) keep |= zvv[h] > s_tau[h] || p == s_arg[h];
     }
     const uint32_t bal = __ballot_sync(0xffffffffu, keep);
     if (lane == 0) s_wsum[warp] = __popc(bal);
     __syncthreads();
-    uint32_t before = carry, all = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      before += w < warp ? s_wsum[w] : 0u;
-      all += s_wsum[w];
-    }
-    before += __popc(bal & ((1u << lane) - 1u));
+    const uint32_t wv = lane < NW ? s_wsum[lane] : 0u;
+    const uint32_t before = carry + __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) +
+                            __popc(bal & ((1u << lane) - 1u));
+    const uint32_t all = __reduce_add_sync(0xffffffffu, wv);
     if (keep && (int)before < k_max) out[before] = p;
     carry += all;
     __syncthreads();
@@ -939,9 +939,22 @@ cudaError_t launch_entmax_select(const int32_t* seq_lens, int page_size, int bat
                                  const float* vz, int stride, int k_max, int32_t* sel_idx,
                                  int32_t* sel_cnt, float* tau_hat, DevCtx ctx, cudaStream_t s) {
   dim3 grid(Hkv, batch);
-  return launch_pdl(entmax_select_kernel, grid, dim3(kESelThreads), 0, s, seq_lens, page_size,
-                    Hq, Hkv, table_stride, zb, cz, vz, stride, k_max, sel_idx, sel_cnt, tau_hat,
-                    ctx);
+#define SKV_ESEL(GG)                                                                          \
+  return launch_pdl(entmax_select_kernel<GG>, grid, dim3(kESelThreads), 0, s, seq_lens,        \
+                    page_size, Hq, Hkv, table_stride, zb, cz, vz, stride, k_max, sel_idx,       \
+                    sel_cnt, tau_hat, ctx)
+  switch (Hq / Hkv) {
+    case 1: SKV_ESEL(1);
+    case 2: SKV_ESEL(2);
+    case 3: SKV_ESEL(3);
+    case 4: SKV_ESEL(4);
+    case 5: SKV_ESEL(5);
+    case 6: SKV_ESEL(6);
+    case 7: SKV_ESEL(7);
+    case 8: SKV_ESEL(8);
+    default: return cudaErrorInvalidValue;
+  }
+#undef SKV_ESEL
 }
 
 int entmax_max_splits() { return kMaxEntSplits; }

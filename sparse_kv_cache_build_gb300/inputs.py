@@ -11,6 +11,8 @@ Recipe (one ``torch.Generator`` seeded per workload, draws made in the order bel
    ``sum_b ceil(len_b / PS)`` pages (or the identity for a contiguous table);
 3. queries ``q ~ N(0, 1)`` in float32, rounded to the storage dtype;
 4. keys and values ``~ N(0, 1)`` in float32, drawn page-chunk by page-chunk;
+   (or, with ``page_noise``, a mean ~ N(0, 1) per (page, KV head) and coordinate plus
+   ``page_noise`` times N(0, 1) per key);
 5. planted salient tokens: for each (sequence, KV head), ``planted`` distinct positions drawn
    uniformly over the whole context get the key ``4 * qbar / |qbar| + N(0, 0.5^2)``, where
    ``qbar`` is the mean of the group's (rounded) query heads, so attention mass
@@ -49,6 +51,9 @@ class Workload:
     seq_len_range: tuple[int, int] | None = None   # inclusive uniform range instead
     seq_lens: tuple[int, ...] | None = None         # explicit per-sequence lengths instead
     planted: int = 0                    # salient tokens per (sequence, KV head)
+    page_noise: float | None = None     # None: keys N(0, 1); else each (page, KV head) draws a
+                                        # mean ~ N(0, 1) per coordinate and its keys are that
+                                        # mean + N(0, page_noise^2) (tight page boxes)
     permute_pages: bool = True          # random physical placement of pages
     keep_ratios: tuple[float, ...] = ()  # sparse keep ratios r_KV to run
     keep_pages: int | None = None       # fixed pages kept per group (instead of a ratio)
@@ -85,6 +90,11 @@ WORKLOADS = {
         name="batched_serving", batch=32, num_q_heads=32, num_kv_heads=8, head_dim=128,
         page_size=16, dtype="bf16", seed=4, seq_len_range=(8192, 65536), budget_tokens=2048,
         description="32 sequences, lengths U[8192, 65536], shared pool, 2048-token budget"),
+    "entmax_pruning_32k": Workload(
+        name="entmax_pruning_32k", batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        page_size=16, dtype="bf16", seed=6, seq_len=32768, page_noise=0.05, keep_ratios=(0.3,),
+        description="8B-shaped decode, 32K tokens, PS 16, keys tight around per-page means "
+                    "(within-page std 0.05): the entmax selector's boxes are tight"),
     "llama70b_1m": Workload(
         name="llama70b_1m", batch=1, num_q_heads=64, num_kv_heads=8, head_dim=128,
         page_size=64, dtype="bf16", seed=5, seq_len=1048576, planted=256,
@@ -163,8 +173,12 @@ def make_cache(w: Workload, device="cpu", extra_phys_pages: int = 0) -> KVCache:
     for p0 in range(0, NP, chunk):
         p1 = min(NP, p0 + chunk)
         shape = (p1 - p0, Hkv, PS, D)
-        k_pool[p0:p1] = torch.randn(shape, generator=gen, device=device,
-                                    dtype=torch.float32).to(dt)
+        k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        if w.page_noise is not None:
+            mean = torch.randn((p1 - p0, Hkv, 1, D), generator=gen, device=device,
+                               dtype=torch.float32)
+            k = mean + float(w.page_noise) * k
+        k_pool[p0:p1] = k.to(dt)
         v_pool[p0:p1] = torch.randn(shape, generator=gen, device=device,
                                     dtype=torch.float32).to(dt)
 

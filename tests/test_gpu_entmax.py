@@ -206,3 +206,33 @@ def test_flat_logits_take_the_global_candidate_path():
         for h in range(g * w.group_size, (g + 1) * w.group_size):
             assert np.abs(f64(out)[0, h] - mean).max() < 1e-5
             assert f64(tau)[0, h] == pytest.approx(-1 / math.sqrt(n), abs=1e-6)
+
+
+def test_entmax_step_prunes_tight_boxes_and_matches_oracle():
+    """Keys tight around per-page means (the pruning workload's recipe at 4096 tokens): the
+    Gaussian-aware selector keeps few pages, and the step's output is the oracle's entmax
+    over exactly the pages it kept."""
+    w = inputs.workload("entmax_pruning_32k", seq_len=4096, num_q_heads=8, num_kv_heads=2)
+    c = inputs.make_cache(w, "cuda")
+    kv = skv.PagedKV.from_cache(c)
+    stats = skv.kv_build_page_stats(kv)
+    B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
+    ws = torch.zeros((skv.kv_entmax_decode_step_workspace_size(kv, Hq, kv.stride),),
+                     dtype=torch.uint8, device="cuda")
+    out, tau = skv.kv_entmax_decode_step(kv, c.q, w.sm_scale, stats, k_max=kv.stride,
+                                         workspace=ws)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    M = (B * Hq * kv.stride * 4 + 255) // 256 * 256
+    a = 3 * M
+    cb = a + (B * Hkv * kv.stride * 4 + 255) // 256 * 256
+    sel = ws[a: a + B * Hkv * kv.stride * 4].view(torch.int32).view(B, Hkv, kv.stride).cpu()
+    cnt = ws[cb: cb + B * Hkv * 4].view(torch.int32).view(B, Hkv).cpu().numpy()
+    n = kv.stride
+    assert 0 < cnt.max() and cnt.sum() < 0.5 * B * Hkv * n, cnt
+    chosen = [[sel[b, g, : cnt[b, g]].numpy() for g in range(Hkv)] for b in range(B)]
+    q, K, V, table, lens = host(c)
+    ref, ref_tau = E.entmax_attend(q, K, V, table, lens, w.page_size, w.sm_scale,
+                                   selected=chosen)
+    assert np.abs(f64(out) - ref).max() < out_tol(w)
+    assert np.abs(f64(tau) - ref_tau).max() < 1e-4
