@@ -506,8 +506,8 @@ kv_status kv_entmax_page_moments(const kv_cache_desc* cache, const void* q, int3
  * head, with n_p the valid tokens of page p and N = sum n_p,
  *   mu = sum n_p cz_p / N,  sigma^2 = sum n_p (cz_p - mu)^2 / N + sum n_p vz_p / N,
  *   tau_hat solving N * E[max(Z - tau_hat, 0)^2] = 1 for Z ~ N(mu, sigma^2)
- * (closed form s^2((u^2+1) Phi(u) + u phi(u)), u = (mu - tau)/s, solved by bisection in
- * double). A page is kept if zb > tau_hat for some head of the group, and each head's
+ * (closed form s^2((u^2+1) Phi(u) + u phi(u)), u = (mu - tau)/s, solved in float by Newton
+ * on its logarithm). A page is kept if zb > tau_hat for some head of the group, and each head's
  * highest-zb page (the lower index on ties) is always kept. Kept pages go to
  * sel_idx[b][g][...] ascending, their count to sel_cnt[b][g]; more than k_max is flagged
  * (KV_DEVERR_KEEP) and the first k_max are kept. tau_hat [batch][num_q_heads] may be NULL.
@@ -524,7 +524,10 @@ kv_status kv_entmax_select(const float* zb, const float* cz, const float* vz, in
  * out[b][h] = sum_t max(z_t - tau, 0)^2 v_t with tau solved exactly over those tokens
  * (tau[b][h] written if tau is not NULL; NaN and a zero output for a group with no token).
  * K is read for the attended pages, V only for tokens with a nonzero weight.
- * workspace: device, kv_entmax_attn_workspace_size() bytes (the logits), 16-byte aligned.
+ * workspace: device, kv_entmax_attn_workspace_size() bytes (the candidate lists: 8 bytes
+ * per attended token slot and query head, plus 8 bytes per split), 16-byte aligned.
+ * KV_ERR_UNSUPPORTED when the pools hold more than 2^32 - 1 rows (num_phys_pages *
+ * num_kv_heads * page_size): the candidate lists keep a token's row in 32 bits.
  */
 size_t kv_entmax_attn_workspace_size(const kv_cache_desc* cache, int32_t num_q_heads,
                                      int32_t sel_stride);

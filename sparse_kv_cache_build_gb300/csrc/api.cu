@@ -899,12 +899,17 @@ size_t kv_entmax_attn_workspace_size(const kv_cache_desc* cache, int32_t num_q_h
   const long long pages = sel_stride > 0 ? sel_stride : cache->page_table_stride;
   const size_t slots = (size_t)cache->batch * num_q_heads * pages * cache->page_size;
   const size_t splits = (size_t)cache->batch * num_q_heads * entmax_max_splits();
-  return 3 * round256(slots * 4) + 2 * round256(splits * 4);
+  return 2 * round256(slots * 4) + 2 * round256(splits * 4);
 }
 
 }  // extern "C"
 
 namespace {
+
+// The candidate lists hold a token's V-pool row as 32 bits.
+bool entmax_rows_fit(const kv_cache_desc* cache) {
+  return (long long)cache->num_phys_pages * cache->num_kv_heads * cache->page_size <= UINT32_MAX;
+}
 
 int entmax_splits(const kv_cache_desc* cache, int pages, const DeviceState* st) {
   const long groups = (long)cache->batch * cache->num_kv_heads;
@@ -921,11 +926,10 @@ EntmaxScratch entmax_scratch(void* base, const kv_cache_desc* cache, int Hq, int
   const size_t splits = (size_t)cache->batch * Hq * entmax_max_splits();
   char* p = static_cast<char*>(base);
   EntmaxScratch w;
-  w.logits = reinterpret_cast<float*>(p);
-  w.cand_z = reinterpret_cast<float*>(p + round256(slots * 4));
-  w.cand_slot = reinterpret_cast<int*>(p + 2 * round256(slots * 4));
-  w.split_max = reinterpret_cast<float*>(p + 3 * round256(slots * 4));
-  w.split_cnt = reinterpret_cast<int*>(p + 3 * round256(slots * 4) + round256(splits * 4));
+  w.cand_z = reinterpret_cast<float*>(p);
+  w.cand_row = reinterpret_cast<uint32_t*>(p + round256(slots * 4));
+  w.split_floor = reinterpret_cast<float*>(p + 2 * round256(slots * 4));
+  w.split_cnt = reinterpret_cast<int*>(p + 2 * round256(slots * 4) + round256(splits * 4));
   return w;
 }
 
@@ -940,6 +944,7 @@ kv_status kv_entmax_decode_attn(const kv_cache_desc* cache, const void* q, int32
   kv_status r = check_desc(cache);
   if (r != KV_OK) return r;
   if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (!entmax_rows_fit(cache)) return KV_ERR_UNSUPPORTED;
   if (out == nullptr || !(sm_scale > 0.f) || !isfinite(sm_scale)) return KV_ERR_INVALID_ARG;
   if (sel_idx != nullptr && (sel_cnt == nullptr || sel_stride <= 0)) return KV_ERR_INVALID_ARG;
   const int stride = sel_idx != nullptr ? sel_stride : cache->page_table_stride;
@@ -977,6 +982,7 @@ kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32
   kv_status r = check_desc(cache);
   if (r != KV_OK) return r;
   if ((r = check_heads(cache, q, num_q_heads)) != KV_OK) return r;
+  if (!entmax_rows_fit(cache)) return KV_ERR_UNSUPPORTED;
   if (stats == nullptr || out == nullptr || k_max <= 0 || !(sm_scale > 0.f) ||
       !isfinite(sm_scale))
     return KV_ERR_INVALID_ARG;
@@ -996,8 +1002,7 @@ kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32
   float* vz = reinterpret_cast<float*>(ws + 2 * mom);
   int32_t* sel = reinterpret_cast<int32_t*>(ws + 3 * mom);
   int32_t* cnt = reinterpret_cast<int32_t*>(ws + 3 * mom + round256(B * Hkv * k_max * 4));
-  float* logits = reinterpret_cast<float*>(ws + 3 * mom + round256(B * Hkv * k_max * 4) +
-                                           round256(B * Hkv * 4));
+  void* scratch = ws + 3 * mom + round256(B * Hkv * k_max * 4) + round256(B * Hkv * 4);
   const int G = num_q_heads / cache->num_kv_heads;
   cudaError_t e = launch_entmax_moments(*cache, G, q, stats, sm_scale, zb, cz, vz, stride, ctx,
                                         stream);
@@ -1008,7 +1013,7 @@ kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32
   if (e != cudaSuccess) return KV_ERR_CUDA;
   return from_cuda(launch_entmax_attn(*cache, G, q, sm_scale, sel, cnt, k_max,
                                       entmax_splits(cache, k_max, st),
-                                      entmax_scratch(logits, cache, num_q_heads, k_max),
+                                      entmax_scratch(scratch, cache, num_q_heads, k_max),
                                       k_max * cache->page_size, out, tau, ctx, stream));
 }
 

@@ -14,33 +14,44 @@
 //   entmax_moments_kernel  per (page, KV head) row of statistics, for each query head of the
 //                          group: upper bound zb, centre logit c and within-box variance v of
 //                          z. Eight lanes own a row and hold the same columns of its min and
-//                          max halves, so (max - min)^2 is formed element-wise.
-//   entmax_select_kernel   one block of 1024 threads per (sequence, KV head): one pass
-//                          loading every head's moments of a batch of pages at once into
-//                          token-weighted double sums, one block reduction, a warp per head
-//                          solving tau_hat on the closed-form Gaussian tail (32 points per
-//                          round, then Newton), then the kept pages in ascending order by one
-//                          ballot-and-scan pass per 1024 pages.
-//   entmax_logits_kernel   split over the selected list; each warp takes a page, each lane a
-//                          token (or half of one), and computes the G heads' logits from the
-//                          page's keys: K is read once per group.
-//   entmax_out_kernel      one block per (sequence, query head): the largest z, the
-//                          candidates within 1 of it (tau >= max z - 1), tau bracketed by
-//                          bisection and then solved exactly from the support's sums, and the
-//                          output sum over the support, reading V rows of support tokens only.
+//                          max halves (and of the query, in registers), so the box's width and
+//                          centre are formed element-wise.
+//   entmax_select_kernel   one block of 512 threads per (sequence, KV head): one pass loading
+//                          every head's moments of a batch of pages at once into float sums
+//                          shifted by the head's first-page centre, one block reduction, a warp
+//                          per head solving tau_hat on the closed-form Gaussian tail (Newton on
+//                          its logarithm), then the kept pages in ascending order:
+//                          each warp ballots its own run, one block scan, then writes it.
+//   entmax_logits_*kernel  split over the attended list, K read once per group for its G
+//                          heads (bf16: on the tensor cores); z of a chunk kept in shared
+//                          memory, and only the tokens above the chunk's own threshold written
+//                          out, as candidates.
+//   entmax_out_kernel      one block per (sequence, query head): the splits' candidates, tau
+//                          solved exactly over them (Newton from a floor, closed-form finish),
+//                          and the output sum over the support, reading V rows of support
+//                          tokens only.
+#include <type_traits>
+
 #include "kv_internal.cuh"
 
 namespace skv {
 namespace {
 
-constexpr int kMomWarps = 4;                 // moments: 4 warps x 4 rows = 16 pages per block
+constexpr int kMomWarps = 4;                 // moments: 4 warps x rounds x 4 rows per block
+// rounds of 4 rows per warp (the query's columns for all G heads stay in registers)
+constexpr int mom_rounds(int G) { return G >= 8 ? 1 : 2; }
 constexpr int kESelThreads = 512;
+constexpr int kSelSteps = 16;               // selector: 32-page ballot words per warp per pass
 constexpr int kLogitWarps = 4;
 constexpr int kOutThreads = 512;
 constexpr int kCandCap = 16384;              // candidate logits held in shared memory
 
 // ------------------------------------------------------------------------------ moments
 
+// A warp takes mom_rounds(G) rounds of 4 statistics rows, 8 lanes a row; lane j of a row holds
+// columns (j + 8u) * EPC .. + EPC of both halves, and the query's same columns for every head
+// in registers (no shared memory, no barrier). With s = mn + mx and w = mx - mn per column,
+// max(q mn, q mx) = (q s + |q| w) / 2, so one pass gives all three sums.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kMomWarps * 32)
 entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restrict__ stats,
@@ -49,80 +60,86 @@ entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restr
   constexpr int EPC = 16 / ElemTraits<T>::bytes;   // elements per 16-byte chunk
   constexpr int CH = D / EPC;                      // chunks per half row
   constexpr int NU = CH / 8;                       // chunks per lane per half row
-  __shared__ float s_q[G][D], s_pos[G][D], s_neg[G][D];
+  constexpr int R = mom_rounds(G);
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.z, g = blockIdx.y, tid = threadIdx.x;
   const int Hkv = d.num_kv_heads, Hq = Hkv * G;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
-  const int p_block = blockIdx.x * kMomWarps * 4;
+  const int p_block = blockIdx.x * kMomWarps * R * 4;
   if (p_block >= n_pages) return;
   const int warp = tid >> 5, lane = tid & 31, j = lane & 7;
-  const int p = p_block + warp * 4 + (lane >> 3);
-  uint4 rmn[NU], rmx[NU];
-  bool ok = false;
-  if (p < n_pages) {
-    const int P = d.page_table[(long)b * d.page_table_stride + p];
-    if (P >= 0 && P < d.num_phys_pages) {
-      ok = true;
-      const uint4* row = reinterpret_cast<const uint4*>(stats + ((long)P * Hkv + g) * 2 * D);
+  uint4 rmn[R][NU], rmx[R][NU];
+  bool ok[R];
 #pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        rmn[u] = __ldg(row + j + 8 * u);
-        rmx[u] = __ldg(row + CH + j + 8 * u);
+  for (int r = 0; r < R; ++r) {
+    const int p = p_block + (warp * R + r) * 4 + (lane >> 3);
+    ok[r] = false;
+    if (p < n_pages) {
+      const int P = d.page_table[(long)b * d.page_table_stride + p];
+      if (P >= 0 && P < d.num_phys_pages) {
+        ok[r] = true;
+        const uint4* row = reinterpret_cast<const uint4*>(stats + ((long)P * Hkv + g) * 2 * D);
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          rmn[r][u] = __ldg(row + j + 8 * u);
+          rmx[r][u] = __ldg(row + CH + j + 8 * u);
+        }
+      } else if (j == 0) {
+        flag(ctx, KV_DEVERR_BAD_PAGE);
       }
-    } else if (j == 0) {
-      flag(ctx, KV_DEVERR_BAD_PAGE);
     }
   }
-  for (int i = tid; i < G * D; i += kMomWarps * 32) {
-    const int h = i / D, t = i - h * D;
-    const float x = load_elem<T>(q, ((long)b * Hq + g * G + h) * D + t);
-    s_q[h][t] = x;
-    s_pos[h][t] = fmaxf(x, 0.f);
-    s_neg[h][t] = fminf(x, 0.f);
+  float qv[G][NU][EPC];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const uint4* qr = reinterpret_cast<const uint4*>(q + ((long)b * Hq + g * G + h) * D);
+#pragma unroll
+    for (int u = 0; u < NU; ++u) chunk_to_f32<T>(__ldg(qr + j + 8 * u), qv[h][u]);
   }
-  __syncthreads();
-  float bnd[G], cen[G], var[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) bnd[h] = cen[h] = var[h] = 0.f;
-  if (ok) {
+  for (int r = 0; r < R; ++r) {
+    float bnd[G], cen[G], var[G];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-      float lo[EPC], hi[EPC];
-      chunk_to_f32<T>(rmn[u], lo);
-      chunk_to_f32<T>(rmx[u], hi);
-      const int d0 = (j + 8 * u) * EPC;
+    for (int h = 0; h < G; ++h) bnd[h] = cen[h] = var[h] = 0.f;
+    if (ok[r]) {
 #pragma unroll
-      for (int e = 0; e < EPC; ++e) {
-        const float w = hi[e] - lo[e], s = lo[e] + hi[e];
+      for (int u = 0; u < NU; ++u) {
+        float lo[EPC], hi[EPC];
+        chunk_to_f32<T>(rmn[r][u], lo);
+        chunk_to_f32<T>(rmx[r][u], hi);
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float qd = s_q[h][d0 + e];
-          bnd[h] = fmaf(s_pos[h][d0 + e], hi[e], fmaf(s_neg[h][d0 + e], lo[e], bnd[h]));
-          cen[h] = fmaf(qd, s, cen[h]);
-          var[h] = fmaf(qd * qd, w * w, var[h]);
+        for (int e = 0; e < EPC; ++e) {
+          const float w = hi[e] - lo[e], sm = lo[e] + hi[e], w2 = w * w;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float qd = qv[h][u][e];
+            cen[h] = fmaf(qd, sm, cen[h]);
+            bnd[h] = fmaf(fabsf(qd), w, bnd[h]);
+            var[h] = fmaf(qd * qd, w2, var[h]);
+          }
         }
       }
     }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1) {
-      bnd[h] += __shfl_xor_sync(0xffffffffu, bnd[h], o);
-      cen[h] += __shfl_xor_sync(0xffffffffu, cen[h], o);
-      var[h] += __shfl_xor_sync(0xffffffffu, var[h], o);
-    }
-  }
-  if (j == 0 && ok) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const long i = ((long)b * Hq + g * G + h) * stride + p;
-      zb[i] = half_scale * bnd[h];
-      cz[i] = half_scale * 0.5f * cen[h];
-      vz[i] = half_scale * half_scale * var[h] / 12.f;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        bnd[h] += __shfl_xor_sync(0xffffffffu, bnd[h], o);
+        cen[h] += __shfl_xor_sync(0xffffffffu, cen[h], o);
+        var[h] += __shfl_xor_sync(0xffffffffu, var[h], o);
+      }
+    }
+    const int p = p_block + (warp * R + r) * 4 + (lane >> 3);
+    if (j == 0 && ok[r]) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const long i = ((long)b * Hq + g * G + h) * stride + p;
+        zb[i] = half_scale * 0.5f * (cen[h] + bnd[h]);
+        cz[i] = half_scale * 0.5f * cen[h];
+        vz[i] = half_scale * half_scale * var[h] / 12.f;
+      }
     }
   }
 }
@@ -132,58 +149,46 @@ entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restr
 // Everything here is float: FP64 is scarce on this part (a double erfc costs microseconds),
 // and the threshold is an estimate, so float accuracy (a relative 1e-6 or so) is ample.
 
-// E[max(Z - tau, 0)^2] for Z ~ N(mu, sigma^2) and its derivative in tau,
-// -2 E[max(Z - tau, 0)] = -2 sigma (u Phi(u) + phi(u)), u = (mu - tau) / sigma.
-__device__ __forceinline__ void gaussian_tail(float mu, float sigma, float tau, float& f2,
-                                              float& f1) {
-  if (!(sigma > 0.f)) {
-    const float x = fmaxf(mu - tau, 0.f);
-    f2 = x * x;
-    f1 = x;
-    return;
-  }
-  const float u = (mu - tau) / sigma;
+// psi(u) = E[max(X + u, 0)^2] for X ~ N(0, 1), = (u^2 + 1) Phi(u) + u phi(u), and its
+// derivative psi'(u) = 2 (u Phi(u) + phi(u)).
+__device__ __forceinline__ void gaussian_psi(float u, float& p, float& dp) {
   const float Phi = 0.5f * erfcf(-u * 0.70710678f);      // 1/sqrt(2)
-  const float phi = expf(-0.5f * u * u) * 0.39894228f;    // 1/sqrt(2 pi)
-  f2 = sigma * sigma * ((u * u + 1.f) * Phi + u * phi);
-  f1 = sigma * (u * Phi + phi);
+  const float phi = __expf(-0.5f * u * u) * 0.39894228f;  // 1/sqrt(2 pi)
+  p = (u * u + 1.f) * Phi + u * phi;
+  dp = 2.f * (u * Phi + phi);
 }
 
-// tau_hat with count * E[max(Z - tau_hat, 0)^2] = 1: f(t) = count * E[...] - 1 is convex and
-// decreasing in t. Called by a whole warp with the same arguments: each round the 32 lanes
-// evaluate f at 32 interior points of the bracket and keep the sub-interval where f changes
-// sign (four rounds shrink it about a million-fold), then Newton steps from its f >= 0 end
-// converge to float precision. Every lane returns the same value.
-__device__ float gaussian_threshold_warp(float mu, float var, float count) {
-  const int lane = threadIdx.x & 31;
+// tau_hat with count * E[max(Z - tau_hat, 0)^2] = 1 for Z ~ N(mu, var). With sigma > 0 and
+// u = (mu - tau_hat) / sigma this reads psi(u) = c, c = 1 / (count var). psi is positive,
+// increasing and log-concave, so Newton on ln psi(u) - ln c converges from any start: a step
+// from the right of the root lands on its left, and from there the iterates rise to it. The
+// start: u = sqrt(c - 1) when c >= 1 (psi(u) ~ u^2 + 1 above zero), 0 down to c = 0.05, else
+// the tail asymptote psi(u) ~ 2 phi(u) / |u|^3. sigma = 0 gives tau_hat = mu - 1/sqrt(count).
+__device__ float gaussian_threshold(float mu, float var, float count) {
   const float sigma = sqrtf(fmaxf(var, 0.f));
-  float lo = mu - 1.f - 40.f * sigma, hi = mu + 40.f * sigma + 1.f;
-  float f2, f1;
-  gaussian_tail(mu, sigma, lo, f2, f1);
-  if (count * f2 < 1.f) return lo;
-  for (int round = 0; round < 4; ++round) {
-    const float t = lo + (hi - lo) * (float)(lane + 1) / 33.f;
-    gaussian_tail(mu, sigma, t, f2, f1);
-    const uint32_t pos = __ballot_sync(0xffffffffu, count * f2 >= 1.f);   // a prefix of lanes
-    const int j = __popc(pos) - 1;                   // last point with f >= 0 (-1: none)
-    const float tj = __shfl_sync(0xffffffffu, t, j < 0 ? 0 : j);
-    const float tn = __shfl_sync(0xffffffffu, t, j + 1 > 31 ? 31 : j + 1);
-    const float nlo = j < 0 ? lo : tj;
-    const float nhi = j >= 31 ? hi : tn;
-    if (!(nlo < nhi)) break;
-    lo = nlo;
-    hi = nhi;
+  if (!(sigma > 0.f)) return mu - rsqrtf(count);
+  const float c = 1.f / (count * sigma * sigma), lnc = logf(c);
+  float u;
+  if (c >= 1.f) {
+    u = sqrtf(c - 1.f);
+  } else if (c >= 0.05f) {
+    u = 0.f;
+  } else {
+    const float L2 = 2.f * logf(0.79788456f / c);        // 2 ln(2 / (sqrt(2 pi) c))
+    u = -sqrtf(fmaxf(L2 - 3.f * logf(L2), 0.25f));
   }
-  float t = lo;
-  for (int i = 0; i < 6; ++i) {
-    gaussian_tail(mu, sigma, t, f2, f1);
-    const float step = (count * f2 - 1.f) / (2.f * count * f1);
-    if (!(step > 0.f) || !(f1 > 0.f)) break;
-    const float tn = t + step;
-    if (!(tn > t) || !(tn < hi)) break;
-    t = tn;
+  for (int it = 0; it < 16; ++it) {
+    float p, dp;
+    gaussian_psi(u, p, dp);
+    if (!(p > 0.f) || !(dp > 0.f)) {                     // underflow far left: move right
+      u += 1.f;
+      continue;
+    }
+    const float du = __fdividef((lnc - __logf(p)) * p, dp);
+    u += du;
+    if (!(fabsf(du) > 2e-6f * (1.f + fabsf(u)))) break;
   }
-  return t;
+  return mu - sigma * u;
 }
 
 // One block of 512 threads per (sequence, KV head). Thread t takes pages t, t + 512, ...;
@@ -192,7 +197,8 @@ __device__ float gaussian_threshold_warp(float mu, float var, float count) {
 // first-page centre (so the variance of c is sum (c - c0)^2 / N - (sum (c - c0) / N)^2 with
 // little cancellation: the centres spread over a few standard deviations), and the first
 // maximum of zb; one block reduction; a warp per head solves tau_hat; then the kept pages,
-// ascending, by one ballot-and-scan pass per 512 pages. G: the group's query heads (1 to 8).
+// ascending: each warp ballots its own run of pages, one block scan of the warps' counts, then
+// each writes its run's. G: the group's query heads (1 to 8).
 // (FP64 is scarce on this part: double sums here cost more than the rest of the kernel.)
 template <int G>
 __global__ void __launch_bounds__(kESelThreads)
@@ -208,8 +214,10 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
   __shared__ float s_bv[G][NW];
   __shared__ int s_bi[G][NW];
   __shared__ float s_tau[G];
+  __shared__ float s_c0[G];
   __shared__ int s_arg[G];
   __shared__ uint32_t s_wsum[NW];
+  __shared__ uint32_t s_bal[NW][kSelSteps];
   pdl_trigger();
   pdl_wait();
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
@@ -234,6 +242,7 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
   int besti[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) c0[h] = __ldg(cz + row0 + (long)h * stride);   // page 0
+  if (tid < G) s_c0[tid] = __ldg(cz + row0 + (long)tid * stride);
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     s1[h] = s2[h] = sv[h] = 0.f;
@@ -311,7 +320,7 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
     const float N = (float)len;
     const float m1 = a1 / N;                     // mean of c - c0
     const float var = fmaxf(a2 / N - m1 * m1, 0.f) + av / N;
-    const float t = gaussian_threshold_warp(__ldg(cz + row0 + (long)h * stride) + m1, var, N);
+    const float t = gaussian_threshold(s_c0[h] + m1, var, N);
     if (lane == 0) {
       s_tau[h] = t;
       s_arg[h] = bi;
@@ -319,54 +328,350 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
     }
   }
   __syncthreads();
-  // kept pages, ascending: one ballot-and-scan pass per 1024 pages
-  uint32_t carry = 0;
+  // kept pages, ascending. Warp w owns a contiguous run of each super-chunk of pages (32 pages
+  // a step, coalesced loads, several steps' loads in flight); its ballots go to shared memory
+  // and its count to one block scan, and then it writes its kept pages from its offset.
+  constexpr int SB = G <= 4 ? 8 : 4;            // steps whose loads are in flight together
+  int carry = 0;
   int32_t* out = sel_idx + grp * k_max;
-  for (int base = 0; base < n; base += kESelThreads) {
-    const int p = base + tid;
-    bool keep = false;
-    if (p < n) {
-      float zvv[G];
+  for (int c0p = 0; c0p < n; c0p += NW * 32 * kSelSteps) {
+    const int c1p = min(n, c0p + NW * 32 * kSelSteps);
+    const int PW = ceil_div(c1p - c0p, NW * 32) * 32;     // pages per warp
+    const int w0 = c0p + warp * PW, w1 = min(c1p, w0 + PW);
+    const int steps = PW / 32;
+    int wcount = 0;
+    for (int st = 0; st < steps; st += SB) {
+      float zv[SB][G];
 #pragma unroll
-      for (int h = 0; h < G; ++h)                // the group's heads' loads together
-        zvv[h] = zb[row0 + (long)h * stride + p];
+      for (int k = 0; k < SB; ++k) {
+        const int p = w0 + (st + k) * 32 + lane;
 #pragma unroll
-      for (int h = 0; h < G; ++h) keep |= zvv[h] > s_tau[h] || p == s_arg[h];
+        for (int h = 0; h < G; ++h)
+          zv[k][h] = st + k < steps && p < w1 ? zb[row0 + (long)h * stride + p] : -INFINITY;
+      }
+#pragma unroll
+      for (int k = 0; k < SB; ++k) {
+        const int p = w0 + (st + k) * 32 + lane;
+        bool keep = false;
+#pragma unroll
+        for (int h = 0; h < G; ++h) keep |= zv[k][h] > s_tau[h] || p == s_arg[h];
+        keep = keep && st + k < steps && p < w1;
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        if (st + k < steps && lane == 0) s_bal[warp][st + k] = bal;
+        wcount += __popc(bal);
+      }
     }
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    if (lane == 0) s_wsum[warp] = __popc(bal);
+    if (lane == 0) s_wsum[warp] = (uint32_t)wcount;
     __syncthreads();
-    const uint32_t wv = lane < NW ? s_wsum[lane] : 0u;
-    const uint32_t before = carry + __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) +
-                            __popc(bal & ((1u << lane) - 1u));
-    const uint32_t all = __reduce_add_sync(0xffffffffu, wv);
-    if (keep && (int)before < k_max) out[before] = p;
-    carry += all;
-    __syncthreads();
+    int at = carry, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      at += w < warp ? (int)s_wsum[w] : 0;
+      total += (int)s_wsum[w];
+    }
+    for (int st = 0; st < steps; ++st) {
+      const uint32_t bal = s_bal[warp][st];
+      if ((bal >> lane) & 1u) {
+        const int pos = at + __popc(bal & ((1u << lane) - 1u));
+        if (pos < k_max) out[pos] = w0 + st * 32 + lane;
+      }
+      at += __popc(bal);
+    }
+    carry += total;
+    __syncthreads();                             // s_bal and s_wsum are reused
   }
   if (tid == 0) {
-    if ((int)carry > k_max) flag(ctx, KV_DEVERR_KEEP);
-    sel_cnt[grp] = min((int)carry, k_max);
+    if (carry > k_max) flag(ctx, KV_DEVERR_KEEP);
+    sel_cnt[grp] = min(carry, k_max);
   }
 }
 
+// ------------------------------------------------------------------------------ threshold
+//
+// The entmax threshold of a set of z values solves f(t) = sum max(z - t, 0)^2 = 1. f is
+// convex and decreasing, so Newton from a point where f >= 0 (any t <= max z - 1) rises to the
+// root; once every member of {z > t} lies above the closed-form root of that set, the root is
+// the threshold. The closed form is taken about a pivot p near the top (the maximum):
+// with y = z - p over the K members, tau = p + mean(y) - sqrt((1 - Q) / K), Q = sum (y -
+// mean)^2, so flat sets (all z equal) are exact and no large sums cancel. Float throughout:
+// FP64 is scarce on this part, and the logits themselves carry float rounding.
+
+struct TauSums {
+  float k, y1, y2, e1, e2, zmin;               // count, sums of y, y^2, e = z - t, e^2; min z
+};
+
+__device__ __forceinline__ TauSums tau_zero() { return {0.f, 0.f, 0.f, 0.f, 0.f, INFINITY}; }
+
+__device__ __forceinline__ void tau_add(TauSums& s, float z, float t, float pivot) {
+  if (z > t) {
+    const float y = z - pivot, e = z - t;
+    s.k += 1.f;
+    s.y1 += y;
+    s.y2 = fmaf(y, y, s.y2);
+    s.e1 += e;
+    s.e2 = fmaf(e, e, s.e2);
+    s.zmin = fminf(s.zmin, z);
+  }
+}
+
+// Butterfly: every lane ends with bitwise the same sums.
+__device__ __forceinline__ void tau_warp_reduce(TauSums& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s.k += __shfl_xor_sync(0xffffffffu, s.k, o);
+    s.y1 += __shfl_xor_sync(0xffffffffu, s.y1, o);
+    s.y2 += __shfl_xor_sync(0xffffffffu, s.y2, o);
+    s.e1 += __shfl_xor_sync(0xffffffffu, s.e1, o);
+    s.e2 += __shfl_xor_sync(0xffffffffu, s.e2, o);
+    s.zmin = fminf(s.zmin, __shfl_xor_sync(0xffffffffu, s.zmin, o));
+  }
+}
+
+// One step from the sums over {z > t}: true when t is final (the closed form holds, or Newton
+// cannot advance any further), else t has taken a Newton step.
+__device__ __forceinline__ bool tau_step(const TauSums& s, float pivot, float& t) {
+  if (s.k == 0.f) return true;
+  const float mean = s.y1 / s.k;
+  const float r = 1.f - fmaxf(s.y2 - s.y1 * mean, 0.f);
+  if (r >= 0.f) {
+    const float root = pivot + mean - sqrtf(r / s.k);
+    if (s.zmin >= root) {
+      t = root;
+      return true;
+    }
+  }
+  const float step = (s.e2 - 1.f) / (2.f * s.e1);
+  if (!(step > 0.f)) return true;
+  t += step;
+  return false;
+}
+
+// The threshold of zat(0 .. n-1) by one warp, from t (f(t) >= 0); all lanes return it.
+template <class ZAt>
+__device__ float warp_entmax_tau(ZAt zat, int n, float t, float pivot, int lane) {
+  for (int it = 0; it < 64; ++it) {
+    TauSums s = tau_zero();
+    for (int i = lane; i < n; i += 32) tau_add(s, zat(i), t, pivot);
+    tau_warp_reduce(s);
+    if (tau_step(s, pivot, t)) break;
+  }
+  return t;
+}
+
+// The same by a block of NT threads (two barriers a step; warp 0 takes the step).
+template <int NT, class ZAt>
+__device__ float block_entmax_tau(ZAt zat, int n, float t, float pivot, TauSums* s_red,
+                                  float* s_bc) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int it = 0; it < 64; ++it) {
+    TauSums s = tau_zero();
+    for (int i = tid; i < n; i += NT) tau_add(s, zat(i), t, pivot);
+    tau_warp_reduce(s);
+    if (lane == 0) s_red[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+      TauSums w = lane < NW ? s_red[lane] : tau_zero();
+      tau_warp_reduce(w);
+      float tn = t;
+      const bool done = tau_step(w, pivot, tn);
+      if (lane == 0) {
+        s_bc[0] = tn;
+        s_bc[1] = done ? 1.f : 0.f;
+      }
+    }
+    __syncthreads();
+    t = s_bc[0];
+    if (s_bc[1] != 0.f) break;
+  }
+  return t;
+}
+
+// The exact threshold of the 32 values v held one per lane (-inf: no value), by the sorting
+// form: with the values descending, the support is the longest prefix whose k-th value lies
+// above the closed-form root of the first k. A lower bound on the threshold of any set that
+// holds these values; every lane returns it (-inf when every value is -inf).
+__device__ float warp32_tau(float v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {          // bitonic sort, descending across the lanes
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, j);
+      v = (((lane & k) == 0) == ((lane & j) == 0)) ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  const float v0 = __shfl_sync(0xffffffffu, v, 0);
+  if (v0 == -INFINITY) return v0;
+  const float y = v - v0;
+  float s1 = y, s2 = y * y;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float a = __shfl_up_sync(0xffffffffu, s1, o), b = __shfl_up_sync(0xffffffffu, s2, o);
+    if (lane >= o) {
+      s1 += a;
+      s2 += b;
+    }
+  }
+  const float k = (float)(lane + 1), mean = s1 / k;
+  const float r = 1.f - fmaxf(s2 - s1 * mean, 0.f);
+  const float root = v0 + mean - sqrtf(r / k);
+  const uint32_t ok = __ballot_sync(0xffffffffu, r >= 0.f && v > root);   // a prefix of lanes
+  return __shfl_sync(0xffffffffu, root, 31 - __clz(ok | 1u));
+}
+
+// A start for the Newton passes: the threshold of the lanes' largest values, less a rounding
+// margin (f >= 0 there), and never below max - 1.
+__device__ __forceinline__ float tau_start(float lane_max, float zmax, int lane) {
+  const float t = warp32_tau(lane_max, lane);
+  return fmaxf(zmax - 1.f, t - 1e-6f * (fabsf(t) + 1.f));
+}
+
 // ------------------------------------------------------------------------------ logits
+//
+// One CTA per (split, KV head, sequence) over its run of the attended pages, in chunks of
+// kChunkFloats / G tokens whose z values (all G heads) stay in shared memory. After each
+// chunk, a warp per head finds the chunk's own entmax threshold: the threshold of any subset of
+// a head's tokens is at most the full one (adding tokens only raises it), so a token at or
+// below it has weight zero. The tokens above it (less a rounding margin) are appended in list
+// order to the head's candidate list of this split, as (z, row of the token in the V pool);
+// the split's floor (its chunks' largest threshold, a lower bound on tau) and candidate count
+// are written at the end. No logit goes to memory.
 
-constexpr int kLogitRun = 1024;              // run entries resolved per pass
-constexpr int kMaxEntSplits = 1024;          // splits of the logits pass (their maxima kept)
+constexpr int kMaxEntSplits = 1024;          // splits of the logits pass
+constexpr int kChunkFloats = 8192;           // z values of one chunk (all heads): 32 KB
 
+template <int G, int NW>
+struct ChunkLists {                          // a warp's heads: warp, warp + NW, ...
+  static constexpr int HPW = (G + NW - 1) / NW;
+  int count[HPW];
+  float floor[HPW];
+  __device__ void init() {
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) {
+      count[j] = 0;
+      floor[j] = -INFINITY;
+    }
+  }
+};
+
+// The chunk's candidates. s_z + h * zs: head h's n values (-inf for tokens past the sequence);
+// token i of the chunk sits in physical page s_P[i / PS] (PS = 1 << ps_log2), KV head g;
+// cz/cs: the split's candidate region of head 0 of the group (head h at + h * cap_slots).
+template <int G, int NW>
+__device__ void chunk_candidates(const float* s_z, int zs, int n, const int* s_P, int ps_log2,
+                                 int Hkv, int g, int warp, int lane, float* cz, uint32_t* cs,
+                                 long cap_slots, ChunkLists<G, NW>& L) {
+#pragma unroll
+  for (int j = 0; j < ChunkLists<G, NW>::HPW; ++j) {
+    const int h = warp + j * NW;
+    if (h >= G) break;
+    const float* z = s_z + h * zs;
+    float lm = -INFINITY;
+    for (int i = lane; i < n; i += 32) lm = fmaxf(lm, z[i]);
+    float m = lm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (m == -INFINITY) continue;
+    const float tc = warp_entmax_tau([&](int i) { return z[i]; }, n, tau_start(lm, m, lane), m,
+                                     lane);
+    const float thr = tc - 1e-5f * (fabsf(tc) + 1.f);
+    L.floor[j] = fmaxf(L.floor[j], thr);
+    float* oz = cz + (long)h * cap_slots;
+    uint32_t* os = cs + (long)h * cap_slots;
+    int c = L.count[j];
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const float v = i < n ? z[i] : -INFINITY;
+      const bool keep = v > thr;
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
+        const int at = c + __popc(bal & ((1u << lane) - 1u));
+        const int pg = i >> ps_log2;
+        oz[at] = v;
+        os[at] = ((uint32_t)s_P[pg] * (uint32_t)Hkv + (uint32_t)g) * (1u << ps_log2) +
+                 (uint32_t)(i - (pg << ps_log2));
+      }
+      c += __popc(bal);
+    }
+    L.count[j] = c;
+  }
+}
+
+// Resolves the chunk's pages (list positions r0 .. r0 + rn) to physical pages and valid
+// token counts; flags bad entries (their tokens count as past the sequence).
+__device__ __forceinline__ void resolve_chunk(const kv_cache_desc& d, int b, long grp,
+                                              const int32_t* sel_idx, int sel_stride, int r0,
+                                              int rn, int n_pages, int len, int* s_P,
+                                              int* s_valid, DevCtx ctx) {
+  for (int i = threadIdx.x; i < rn; i += blockDim.x) {
+    const int pos = r0 + i;
+    const int page = sel_idx != nullptr ? sel_idx[grp * sel_stride + pos] : pos;
+    int P = -1, valid = 0;
+    if (page < 0 || page >= n_pages) {
+      flag(ctx, KV_DEVERR_BAD_SEL);
+    } else {
+      P = d.page_table[(long)b * d.page_table_stride + page];
+      if (P < 0 || P >= d.num_phys_pages) {
+        flag(ctx, KV_DEVERR_BAD_PAGE);
+        P = -1;
+      } else {
+        valid = min(d.page_size, len - page * d.page_size);
+      }
+    }
+    s_P[i] = P;
+    s_valid[i] = valid;
+  }
+}
+
+// The group's attended page count (clamped and flagged when out of range) and this split's
+// run [pos0, pos1) of it.
+__device__ __forceinline__ int split_run(const int32_t* sel_idx, const int32_t* sel_cnt,
+                                         int sel_stride, long grp, int n_pages, int s, int S,
+                                         int& pos0, int& pos1, DevCtx ctx) {
+  int cnt = n_pages;
+  if (sel_idx != nullptr) {
+    cnt = sel_cnt[grp];
+    if (cnt < 0 || cnt > sel_stride) {
+      if (threadIdx.x == 0) flag(ctx, KV_DEVERR_BAD_SEL);
+      cnt = cnt < 0 ? 0 : sel_stride;
+    }
+  }
+  const int cps = ceil_div(cnt, S);
+  pos0 = min(cnt, s * cps);
+  pos1 = min(cnt, pos0 + cps);
+  return cnt;
+}
+
+template <int G, int NW>
+__device__ __forceinline__ void write_split(const ChunkLists<G, NW>& L, int warp, int lane,
+                                            float* split_floor, int* split_cnt, long row0,
+                                            int S, int s) {
+#pragma unroll
+  for (int j = 0; j < ChunkLists<G, NW>::HPW; ++j) {
+    const int h = warp + j * NW;
+    if (h < G && lane == 0) {
+      split_floor[(row0 + h) * S + s] = L.floor[j];
+      split_cnt[(row0 + h) * S + s] = L.count[j];
+    }
+  }
+}
+
+// CUDA-core form (float caches): a warp takes a page, a lane a token (or half of one).
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kLogitWarps * 32)
 entmax_logits_kernel(kv_cache_desc d, const T* __restrict__ q, float scale,
                      const int32_t* __restrict__ sel_idx, const int32_t* __restrict__ sel_cnt,
-                     int sel_stride, float* __restrict__ logits, int cap_slots,
-                     float* __restrict__ split_max, DevCtx ctx) {
+                     int sel_stride, int cap_slots, float* __restrict__ split_floor,
+                     float* __restrict__ cand_z, uint32_t* __restrict__ cand_row,
+                     int* __restrict__ split_cnt, DevCtx ctx) {
   constexpr int EPC = 16 / ElemTraits<T>::bytes;
   constexpr int MAXC = D / EPC;                // chunks per lane at most (one lane per token)
+  constexpr int CT = kChunkFloats / G;         // tokens per chunk
+  constexpr int ZS = CT + 4;
   __shared__ float s_q[G][D];
-  __shared__ float s_wmax[kLogitWarps][G];
-  __shared__ int s_P[kLogitRun];
-  __shared__ int s_valid[kLogitRun];
+  __shared__ __align__(16) float s_z[G * ZS];
+  __shared__ int s_P[CT / 16];
+  __shared__ int s_valid[CT / 16];
   pdl_trigger();
   pdl_wait();
   const int s = blockIdx.x, S = gridDim.x, g = blockIdx.y, b = blockIdx.z;
@@ -374,60 +679,35 @@ entmax_logits_kernel(kv_cache_desc d, const T* __restrict__ q, float scale,
   const int Hkv = d.num_kv_heads, Hq = Hkv * G, PS = d.page_size;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, PS);
-  const long grp = (long)b * Hkv + g;
-  int cnt = n_pages;
-  if (sel_idx != nullptr) {
-    cnt = sel_cnt[grp];
-    if (cnt < 0 || cnt > sel_stride) {
-      if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
-      cnt = cnt < 0 ? 0 : sel_stride;
-    }
-  }
-  const int c = ceil_div(cnt, S);
-  const int pos0 = min(cnt, s * c), pos1 = min(cnt, pos0 + c);
-  float* smax = split_max + ((long)b * Hq + g * G) * S + s;     // head h: smax[h * S]
+  const long grp = (long)b * Hkv + g, row0 = (long)b * Hq + g * G;
+  int pos0, pos1;
+  split_run(sel_idx, sel_cnt, sel_stride, grp, n_pages, s, S, pos0, pos1, ctx);
+  ChunkLists<G, kLogitWarps> L;
+  L.init();
   if (pos0 >= pos1) {
-    if (tid < G) smax[(long)tid * S] = -INFINITY;
+    write_split(L, warp, lane, split_floor, split_cnt, row0, S, s);
     return;
   }
   for (int i = tid; i < G * D; i += kLogitWarps * 32) {
     const int h = i / D, t = i - h * D;
-    s_q[h][t] = load_elem<T>(q, ((long)b * Hq + g * G + h) * D + t);
+    s_q[h][t] = load_elem<T>(q, (row0 + h) * D + t);
   }
-  float lmax[G];                               // this lane's largest logit per head
-#pragma unroll
-  for (int h = 0; h < G; ++h) lmax[h] = -INFINITY;
   const int TPW = PS < 32 ? PS : 32;           // tokens per item
   const int SPT = 32 / TPW;                    // lanes per token (1 or 2)
   const int DS = D / SPT;                      // columns per lane
   const int NCH = DS / EPC;                    // 16-byte chunks per lane
   const int IPP = PS / TPW;                    // items per page
   const int sl = lane / TPW, tl = lane % TPW;
+  const int CP = CT / PS;                      // pages per chunk
+  const int ps_log2 = __ffs(PS) - 1;
   const T* __restrict__ kp = static_cast<const T*>(d.k_pool);
-  for (int r0 = pos0; r0 < pos1; r0 += kLogitRun) {
-    const int rn = min(kLogitRun, pos1 - r0);
-    __syncthreads();                           // the previous pass is done with s_P
-    for (int i = tid; i < rn; i += kLogitWarps * 32) {
-      const int pos = r0 + i;
-      const int page = sel_idx != nullptr ? sel_idx[grp * sel_stride + pos] : pos;
-      int P = -1, valid = 0;
-      if (page < 0 || page >= n_pages) {
-        flag(ctx, KV_DEVERR_BAD_SEL);
-      } else {
-        P = d.page_table[(long)b * d.page_table_stride + page];
-        if (P < 0 || P >= d.num_phys_pages) {
-          flag(ctx, KV_DEVERR_BAD_PAGE);
-          P = -1;
-        } else {
-          valid = min(PS, len - page * PS);
-        }
-      }
-      s_P[i] = P;
-      s_valid[i] = valid;
-    }
+  float* cz = cand_z + row0 * cap_slots + (long)pos0 * PS;
+  uint32_t* cs = cand_row + row0 * cap_slots + (long)pos0 * PS;
+  for (int r0 = pos0; r0 < pos1; r0 += CP) {
+    const int rn = min(CP, pos1 - r0);
+    __syncthreads();                           // the previous chunk is done with s_z, s_P
+    resolve_chunk(d, b, grp, sel_idx, sel_stride, r0, rn, n_pages, len, s_P, s_valid, ctx);
     __syncthreads();
-    // items (page, token group) of this warp: two buffers alternate, so the next item's keys
-    // are in flight while the current one is computed (no register copy waits for them)
     uint4 bufA[MAXC], bufB[MAXC];
     auto load = [&](int item, uint4* buf) {
       const int i = item / IPP, t = (item - i * IPP) * TPW + tl;
@@ -463,13 +743,8 @@ entmax_logits_kernel(kv_cache_desc d, const T* __restrict__ q, float scale,
         for (int h = 0; h < G; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 16);
       }
       if (sl == 0) {
-        const long slot = (long)(r0 + i) * PS + t;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float x = live ? scale * acc[h] : -INFINITY;
-          logits[((long)b * Hq + g * G + h) * cap_slots + slot] = x;
-          lmax[h] = fmaxf(lmax[h], x);
-        }
+        for (int h = 0; h < G; ++h) s_z[h * ZS + i * PS + t] = live ? 0.5f * scale * acc[h] : -INFINITY;
       }
     };
     int item = warp;
@@ -482,165 +757,163 @@ entmax_logits_kernel(kv_cache_desc d, const T* __restrict__ q, float scale,
       if (i2 + kLogitWarps < items) load(i2 + kLogitWarps, bufA);
       compute(i2, bufB);
     }
+    __syncthreads();
+    chunk_candidates(s_z, ZS, rn * PS, s_P, ps_log2, Hkv, g, warp, lane, cz, cs, cap_slots,
+                     L);
   }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lmax[h] = fmaxf(lmax[h], __shfl_xor_sync(0xffffffffu, lmax[h], o));
+  write_split(L, warp, lane, split_floor, split_cnt, row0, S, s);
+}
+
+// Tensor-core form (bf16 caches). A warp takes 16-token tiles of the chunk's pages: one
+// mma.sync m16n8k16 per 16 key columns, the tile's tokens as the m rows and the group's G
+// query heads as the n columns (zero-padded to 8). A dot product does not depend on the order
+// of the head dimension, so each lane loads whole 16-byte pieces of its two rows straight into
+// A fragments and takes the query's words at the same positions for its B fragment: lane
+// (r = lane / 4, c = lane % 4) holds words 16u + 4c + e (e < 4) of rows r and r + 8, and
+// k-step k uses words e = 2 (k % 2) and e + 1 of piece u = k / 2. Four lanes read 64
+// contiguous bytes of a row per load; the next tile's loads are in flight while the current
+// one is multiplied. bf16 products are exact in f32, as in the CUDA-core form.
+constexpr int kLogitMmaWarps = 4;
+
+template <int D, int G>
+__global__ void __launch_bounds__(kLogitMmaWarps * 32, 4)
+entmax_logits_mma_kernel(kv_cache_desc d, const bf16_t* __restrict__ q, float scale,
+                         const int32_t* __restrict__ sel_idx, const int32_t* __restrict__ sel_cnt,
+                         int sel_stride, int cap_slots, float* __restrict__ split_floor,
+                         float* __restrict__ cand_z, uint32_t* __restrict__ cand_row,
+                         int* __restrict__ split_cnt, DevCtx ctx) {
+  static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head");
+  constexpr int U = D / 32;                    // 16-byte pieces per lane per row
+  constexpr int ROW4 = D / 8;                  // 16-byte pieces per row
+  constexpr int CT = kChunkFloats / G;         // tokens per chunk
+  constexpr int ZS = CT + 4;                   // head stride: the 4 lanes of a row hit 4 banks
+  __shared__ __align__(16) float s_z[G * ZS];
+  __shared__ int s_P[CT / 16];
+  __shared__ int s_valid[CT / 16];
+  pdl_trigger();
+  pdl_wait();
+  const int s = blockIdx.x, S = gridDim.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = lane >> 2, c = lane & 3;
+  const int Hkv = d.num_kv_heads, Hq = Hkv * G, PS = d.page_size, TPP = PS / 16;
+  const int len = checked_len(ctx, d, b);
+  const int n_pages = ceil_div(len, PS);
+  const long grp = (long)b * Hkv + g, row0 = (long)b * Hq + g * G;
+  int pos0, pos1;
+  split_run(sel_idx, sel_cnt, sel_stride, grp, n_pages, s, S, pos0, pos1, ctx);
+  ChunkLists<G, kLogitMmaWarps> L;
+  L.init();
+  if (pos0 >= pos1) {
+    write_split(L, warp, lane, split_floor, split_cnt, row0, S, s);
+    return;
   }
-  if (lane == 0) {
+  // B fragment: head r of the group (zero for r >= G), the words this lane's A pieces cover
+  uint32_t bq[U][4];
+  {
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(q) + (row0 + r) * D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) s_wmax[warp][h] = lmax[h];
-  }
-  __syncthreads();
-  if (tid < G) {
-    float m = -INFINITY;
+    for (int u = 0; u < U; ++u) {
 #pragma unroll
-    for (int w = 0; w < kLogitWarps; ++w) m = fmaxf(m, s_wmax[w][tid]);
-    smax[(long)tid * S] = m;
+      for (int e = 0; e < 4; ++e) {
+        const int w = 16 * u + 4 * c + e;
+        bq[u][e] = r < G ? (uint32_t)qh[2 * w] | ((uint32_t)qh[2 * w + 1] << 16) : 0u;
+      }
+    }
   }
+  const float zscale = 0.5f * scale;
+  const uint4* __restrict__ kp = static_cast<const uint4*>(d.k_pool);
+  const int CP = CT / PS;                      // pages per chunk
+  const int ps_log2 = __ffs(PS) - 1;
+  float* cz = cand_z + row0 * cap_slots + (long)pos0 * PS;
+  uint32_t* cs = cand_row + row0 * cap_slots + (long)pos0 * PS;
+  for (int r0 = pos0; r0 < pos1; r0 += CP) {
+    const int rn = min(CP, pos1 - r0);
+    __syncthreads();                           // the previous chunk is done with s_z, s_P
+    resolve_chunk(d, b, grp, sel_idx, sel_stride, r0, rn, n_pages, len, s_P, s_valid, ctx);
+    __syncthreads();
+    const int tiles = rn * TPP;
+    auto load = [&](int it, uint4 (&a)[2][U]) {
+      const int i = it / TPP, t0 = (it - i * TPP) * 16;
+      const int P = s_P[i], valid = s_valid[i];
+      const bool la = P >= 0 && t0 + r < valid, lb = P >= 0 && t0 + r + 8 < valid;
+      const uint4* rowa = kp + (((long)(P >= 0 ? P : 0) * Hkv + g) * PS + t0 + r) * ROW4 + c;
+      const uint4* rowb = rowa + 8 * ROW4;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        a[0][u] = la ? __ldg(rowa + 4 * u) : make_uint4(0, 0, 0, 0);
+        a[1][u] = lb ? __ldg(rowb + 4 * u) : make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto compute = [&](int it, const uint4 (&a)[2][U]) {
+      const int i = it / TPP, t0 = (it - i * TPP) * 16;
+      const int P = s_P[i], valid = s_valid[i];
+      const bool la = P >= 0 && t0 + r < valid, lb = P >= 0 && t0 + r + 8 < valid;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        mma_bf16(acc, a[0][u].x, a[1][u].x, a[0][u].y, a[1][u].y, bq[u][0], bq[u][1]);
+        mma_bf16(acc, a[0][u].z, a[1][u].z, a[0][u].w, a[1][u].w, bq[u][2], bq[u][3]);
+      }
+      const int tok = it * 16 + r;             // = i * PS + t0 + r
+      if (2 * c < G) {
+        s_z[(2 * c) * ZS + tok] = la ? zscale * acc[0] : -INFINITY;
+        s_z[(2 * c) * ZS + tok + 8] = lb ? zscale * acc[2] : -INFINITY;
+      }
+      if (2 * c + 1 < G) {
+        s_z[(2 * c + 1) * ZS + tok] = la ? zscale * acc[1] : -INFINITY;
+        s_z[(2 * c + 1) * ZS + tok + 8] = lb ? zscale * acc[3] : -INFINITY;
+      }
+    };
+    uint4 bufA[2][U], bufB[2][U];
+    int it = warp;
+    if (it < tiles) load(it, bufA);
+    for (; it < tiles; it += 2 * kLogitMmaWarps) {
+      const int i2 = it + kLogitMmaWarps;
+      if (i2 < tiles) load(i2, bufB);
+      compute(it, bufA);
+      if (i2 >= tiles) break;
+      if (i2 + kLogitMmaWarps < tiles) load(i2 + kLogitMmaWarps, bufA);
+      compute(i2, bufB);
+    }
+    __syncthreads();
+    chunk_candidates(s_z, ZS, rn * PS, s_P, ps_log2, Hkv, g, warp, lane, cz, cs, cap_slots,
+                     L);
+  }
+  write_split(L, warp, lane, split_floor, split_cnt, row0, S, s);
 }
 
 // ------------------------------------------------------------------------------ output
 
-// Warp-level: from the splits' maxima z_s = sm[s]/2 (one token each), a floor below tau. The
-// entmax threshold of a subset of the tokens is at most the full one (adding tokens only
-// raises it); Newton on f(t) = sum max(z_s - t, 0)^2 - 1 (convex, decreasing) from
-// t = max z - 1, where f >= 0, stays at f >= 0 and rises to the subset's threshold. Every
-// lane returns the same value (the gather and the output kernels call this on the same data).
-// sm: the S maxima in shared memory (the Newton passes re-read them).
-__device__ float entmax_floor(const float* sm, int S, int lane) {
-  float zmax = -INFINITY;
-  for (int s = lane; s < S; s += 32) zmax = fmaxf(zmax, 0.5f * sm[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
-  if (zmax == -INFINITY) return zmax;
-  float t = zmax - 1.f;
-  for (int it = 0; it < 32; ++it) {
-    float s1 = 0.f, s2 = 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float e = 0.5f * sm[s] - t;
-      if (e > 0.f) { s1 += e; s2 = fmaf(e, e, s2); }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
-      s2 += __shfl_xor_sync(0xffffffffu, s2, off);
-    }
-    const float step = (s2 - 1.f) / (2.f * s1);
-    if (!(step > 1e-6f * (fabsf(t) + 1.f))) break;
-    t += 0.999f * step;                        // stay on the f >= 0 side despite rounding
-  }
-  return t - 1e-5f * (fabsf(t) + 1.f);         // margin: the floor must not pass tau
+// Group (b, g)'s attended page count (out-of-range counts were flagged by the logits pass).
+__device__ __forceinline__ int entmax_count(bool selected, const int32_t* sel_cnt, int sel_stride,
+                                            long grp, int n_pages) {
+  if (!selected) return n_pages;
+  const int cnt = sel_cnt[grp];
+  return cnt < 0 ? 0 : (cnt > sel_stride ? sel_stride : cnt);
 }
 
-// Group (b, g)'s attended page count.
-__device__ __forceinline__ int entmax_count(const kv_cache_desc& d, int b, long grp, int n_pages,
-                                            const int32_t* sel_idx, const int32_t* sel_cnt,
-                                            int sel_stride) {
-  int cnt = n_pages;
-  if (sel_idx != nullptr) {
-    cnt = sel_cnt[grp];
-    cnt = cnt < 0 ? 0 : (cnt > sel_stride ? sel_stride : cnt);   // flagged by the logits pass
-  }
-  return cnt;
-}
-
-// One CTA per (split, query head): the split's candidates (z > floor), in slot order, to
-// cand_z / cand_slot at the split's first slot; their count to split_cnt.
-constexpr int kGatherThreads = 256;
-
-__global__ void __launch_bounds__(kGatherThreads)
-entmax_gather_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
-                     const int32_t* __restrict__ sel_cnt, int sel_stride,
-                     const float* __restrict__ logits, int cap_slots,
-                     const float* __restrict__ split_max, float* __restrict__ cand_z,
-                     int* __restrict__ cand_slot, int* __restrict__ split_cnt, DevCtx ctx) {
-  constexpr int NW = kGatherThreads / 32;
-  constexpr int U = 4;
-  __shared__ float s_floor;
-  __shared__ int s_cnt[U][NW];
-  __shared__ float s_sm[kMaxEntSplits];
-  pdl_trigger();
-  pdl_wait();
-  const int s = blockIdx.x, S = gridDim.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int Hkv = d.num_kv_heads, Hq = Hkv * G, g = h / G, PS = d.page_size;
-  const int len = checked_len(ctx, d, b);
-  const long grp = (long)b * Hkv + g;
-  const int cnt = entmax_count(d, b, grp, ceil_div(len, PS), sel_idx, sel_cnt, sel_stride);
-  const int cps = ceil_div(cnt, S);
-  const int a0 = min(cnt, s * cps) * PS, a1 = min(cnt, (s + 1) * cps) * PS;
-  const long row = (long)b * Hq + h;
-  for (int i = tid; i < S; i += kGatherThreads) s_sm[i] = __ldcg(split_max + row * S + i);
-  __syncthreads();
-  if (warp == 0) {
-    const float f = entmax_floor(s_sm, S, lane);
-    if (lane == 0) s_floor = f;
-  }
-  __syncthreads();
-  const float zfloor = s_floor;
-  int carry = 0;
-  if (a0 < a1 && 0.5f * s_sm[s] > zfloor) {
-    const float* x = logits + row * cap_slots;
-    float* cz = cand_z + row * cap_slots;
-    int* cs = cand_slot + row * cap_slots;
-    for (int base = a0; base < a1; base += kGatherThreads * U) {
-      float z[U];
-      uint32_t bal[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = base + u * kGatherThreads + tid;
-        z[u] = i < a1 ? 0.5f * __ldcg(x + i) : -INFINITY;
-        bal[u] = __ballot_sync(0xffffffffu, z[u] > zfloor);
-      }
-      __syncthreads();
-      if (lane == 0) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) s_cnt[u][warp] = __popc(bal[u]);
-      }
-      __syncthreads();
-      int pre = carry;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int in_chunk_before = 0, chunk_total = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          in_chunk_before += w < warp ? s_cnt[u][w] : 0;
-          chunk_total += s_cnt[u][w];
-        }
-        if (z[u] > zfloor) {
-          const int at = a0 + pre + in_chunk_before + __popc(bal[u] & ((1u << lane) - 1u));
-          cz[at] = z[u];
-          cs[at] = base + u * kGatherThreads + tid;
-        }
-        pre += chunk_total;
-      }
-      carry = pre;
-    }
-  }
-  if (tid == 0) split_cnt[row * S + s] = carry;
-}
-
+// One block per (sequence, query head): the splits' candidate lists joined in split order (in
+// shared memory when they fit), tau solved over them from the largest split floor, then the
+// output sum over the support, reading V rows of support tokens only.
 template <typename T, int D>
 __global__ void __launch_bounds__(kOutThreads)
-entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
-                  const int32_t* __restrict__ sel_cnt, int sel_stride,
-                  const float* __restrict__ logits, int cap_slots,
-                  const float* __restrict__ split_max, const float* __restrict__ cand_z,
-                  const int* __restrict__ cand_slot, const int* __restrict__ split_cnt, int S,
-                  float* __restrict__ out, float* __restrict__ tau_out, DevCtx ctx) {
+entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, int sel_stride,
+                  bool selected, int cap_slots, const float* __restrict__ split_floor,
+                  const float* __restrict__ cand_z, const uint32_t* __restrict__ cand_row,
+                  const int* __restrict__ split_cnt, int S, float* __restrict__ out,
+                  float* __restrict__ tau_out, DevCtx ctx) {
   constexpr int NW = kOutThreads / 32;
   constexpr int EPL = D / 32;
   extern __shared__ __align__(16) unsigned char dyn[];
   float* s_z = reinterpret_cast<float*>(dyn);                     // [kCandCap]
-  int* s_slot = reinterpret_cast<int*>(s_z + kCandCap);           // [kCandCap]
-  __shared__ double s_redd[5 * NW];
+  uint32_t* s_row = reinterpret_cast<uint32_t*>(s_z + kCandCap);  // [kCandCap]
+  __shared__ TauSums s_red[NW];
   __shared__ int s_redi[NW];
   __shared__ float s_acc[NW][D];
   __shared__ int s_off[kMaxEntSplits + 1];
-  __shared__ float s_sm[kMaxEntSplits];
-  __shared__ float s_floor;
+  __shared__ float s_fl[kMaxEntSplits];
+  __shared__ float s_bc[4];
+  __shared__ float s_wt[NW];
   pdl_trigger();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -648,26 +921,28 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, PS);
   const long grp = (long)b * Hkv + g;
-  const int cnt = entmax_count(d, b, grp, n_pages, sel_idx, sel_cnt, sel_stride);
-  const int n_slots = cnt * PS;
+  const int cnt = entmax_count(selected, sel_cnt, sel_stride, grp, n_pages);
   const long row = (long)b * Hq + h;
-  const float* x = logits + row * cap_slots;
   float* o = out + row * D;
-  if (n_slots == 0) {
+  if (cnt * PS == 0) {
     for (int i = tid; i < D; i += kOutThreads) o[i] = 0.f;
     if (tid == 0 && tau_out != nullptr) tau_out[row] = __int_as_float(0x7fc00000);
     return;
   }
   const int cps = ceil_div(cnt, S);
-  for (int i = tid; i < S; i += kOutThreads) s_sm[i] = __ldcg(split_max + row * S + i);
+  for (int i = tid; i < S; i += kOutThreads) {
+    s_fl[i] = __ldcg(split_floor + row * S + i);
+    s_off[i] = __ldcg(split_cnt + row * S + i);
+  }
   __syncthreads();
-  // warp 0: the floor (as the gather kernel found it) and the splits' candidate offsets
+  // warp 0: the largest floor and the splits' candidate offsets (exclusive scan in place)
   if (warp == 0) {
-    const float f = entmax_floor(s_sm, S, lane);
+    float f = -INFINITY;
     int run = 0;
     for (int s0 = 0; s0 < S; s0 += 32) {
       const int sp = s0 + lane;
-      const int c_ = sp < S ? split_cnt[row * S + sp] : 0;
+      const int c_ = sp < S ? s_off[sp] : 0;
+      if (sp < S) f = fmaxf(f, s_fl[sp]);
       int incl = c_;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -677,109 +952,87 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
       if (sp < S) s_off[sp] = run + incl - c_;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) { s_off[S] = run; s_floor = f; }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
+    if (lane == 0) {
+      s_off[S] = run;
+      s_bc[2] = f;
+    }
   }
   __syncthreads();
-  const float zfloor = s_floor;
-  const int total = s_off[S];
-  const bool in_smem = total <= kCandCap;
+  const float floor_t = s_bc[2];
+  const int nc = s_off[S];
+  const bool in_smem = nc <= kCandCap;
+  // candidate i -> its place in memory: it belongs to the last split with s_off <= i
+  auto cand_src = [&](int i) -> long {
+    int lo = 0, hi = S;                        // s_off[lo] <= i < s_off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= i) lo = mid;
+      else hi = mid;
+    }
+    return row * cap_slots + (long)min(cnt, lo * cps) * PS + (i - s_off[lo]);
+  };
   if (in_smem) {
-    // the candidates in order: candidate i belongs to the last split with s_off <= i (binary
-    // search), so every load is independent of the others
-    for (int i = tid; i < total; i += kOutThreads) {
-      int lo = 0, hi = S;                      // s_off[lo] <= i < s_off[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_off[mid] <= i) lo = mid;
-        else hi = mid;
+    for (int i0 = tid; i0 < nc; i0 += 4 * kOutThreads) {   // four candidates' loads in flight
+      float zv[4];
+      uint32_t rv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kOutThreads;
+        const long src = i < nc ? cand_src(i) : 0;
+        zv[u] = i < nc ? __ldcg(cand_z + src) : 0.f;
+        rv[u] = i < nc ? __ldcg(cand_row + src) : 0u;
       }
-      const long src = row * cap_slots + (long)min(cnt, lo * cps) * PS + (i - s_off[lo]);
-      s_z[i] = __ldcg(cand_z + src);
-      s_slot[i] = __ldcg(cand_slot + src);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kOutThreads;
+        if (i < nc) {
+          s_z[i] = zv[u];
+          s_row[i] = rv[u];
+        }
+      }
     }
   }
   __syncthreads();
-  const int nc = in_smem ? total : n_slots;
-  auto cand_z_at = [&](int i) -> float { return in_smem ? s_z[i] : 0.5f * __ldcg(x + i); };
-  // tau: from zfloor (f >= 0), each pass sums over S = {z > tau}; the exact root of
-  // sum_S (z - t)^2 = 1, t* = (Z1 - sqrt(Z1^2 - k (Z2 - 1))) / k, is tau when every z of S
-  // lies above it (S is then the support); otherwise a Newton step (f = A2 - 1, f' = -2 A1),
-  // which from the f >= 0 side stays there and rises to the root, and another pass. Small
-  // candidate sets are solved by warp 0 alone (no block barrier per pass).
-  double tau = (double)zfloor;
-  const bool one_warp = in_smem && nc <= 1024;
-  if (!one_warp || warp == 0) {
-    for (int it = 0; it < 64; ++it) {
-      double a1 = 0.0, a2 = 0.0, z1 = 0.0, z2 = 0.0, zmin = INFINITY;
-      int k = 0;
-      const int step_i = one_warp ? 32 : kOutThreads;
-      for (int i = one_warp ? lane : tid; i < nc; i += step_i) {
-        const double z = (double)cand_z_at(i);
-        if (z > tau) {
-          const double e = z - tau;
-          a1 += e; a2 += e * e; z1 += z; z2 += z * z; ++k;
-          zmin = z < zmin ? z : zmin;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        a1 += __shfl_xor_sync(0xffffffffu, a1, off);
-        a2 += __shfl_xor_sync(0xffffffffu, a2, off);
-        z1 += __shfl_xor_sync(0xffffffffu, z1, off);
-        z2 += __shfl_xor_sync(0xffffffffu, z2, off);
-        zmin = fmin(zmin, __shfl_xor_sync(0xffffffffu, zmin, off));
-        k += __shfl_xor_sync(0xffffffffu, k, off);
-      }
-      double A1 = a1, A2 = a2, Z1 = z1, Z2 = z2, ZMIN = zmin;
-      int K = k;
-      if (!one_warp) {
-        __syncthreads();
-        if (lane == 0) {
-          s_redd[warp] = a1; s_redd[NW + warp] = a2; s_redd[2 * NW + warp] = z1;
-          s_redd[3 * NW + warp] = z2; s_redd[4 * NW + warp] = zmin; s_redi[warp] = k;
-        }
-        __syncthreads();
-        A1 = A2 = Z1 = Z2 = 0.0;
-        ZMIN = INFINITY;
-        K = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          A1 += s_redd[w]; A2 += s_redd[NW + w]; Z1 += s_redd[2 * NW + w];
-          Z2 += s_redd[3 * NW + w]; ZMIN = fmin(ZMIN, s_redd[4 * NW + w]); K += s_redi[w];
-        }
-      }
-      if (K == 0) break;
-      const double disc = Z1 * Z1 - (double)K * (Z2 - 1.0);
-      const double t_star = (Z1 - sqrt(disc > 0.0 ? disc : 0.0)) / (double)K;
-      if (disc >= 0.0 && ZMIN > t_star) {
-        tau = t_star;
-        break;
-      }
-      const double t_new = tau + (A2 - 1.0) / (2.0 * A1);
-      if (!(t_new > tau)) break;
-      tau = t_new;
+  // tau from the larger of the floor and the threshold of the lanes' largest candidates (both
+  // lower bounds, f >= 0 there); pivot the floor: the candidates lie within about 1 of it
+  float tau;
+  if (in_smem && nc <= 1024) {
+    if (warp == 0) {
+      float lm = -INFINITY;
+      for (int i = lane; i < nc; i += 32) lm = fmaxf(lm, s_z[i]);
+      const float t0 = fmaxf(floor_t, warp32_tau(lm, lane) - 1e-6f * (fabsf(floor_t) + 1.f));
+      const float t = warp_entmax_tau([&](int i) { return s_z[i]; }, nc, t0, floor_t, lane);
+      if (lane == 0) s_bc[0] = t;
     }
-  }
-  if (one_warp) {
-    if (tid == 0) s_redd[0] = tau;
     __syncthreads();
-    tau = s_redd[0];
+    tau = s_bc[0];
+  } else {
+    float lm = -INFINITY;
+    for (int i = tid; i < nc; i += kOutThreads)
+      lm = fmaxf(lm, in_smem ? s_z[i] : __ldcg(cand_z + cand_src(i)));
+    const float tw = warp32_tau(lm, lane);
+    if (lane == 0) s_wt[warp] = tw;
+    __syncthreads();
+    float t0 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) t0 = fmaxf(t0, s_wt[w]);
+    t0 = fmaxf(floor_t, t0 - 1e-6f * (fabsf(floor_t) + 1.f));
+    if (in_smem)
+      tau = block_entmax_tau<kOutThreads>([&](int i) { return s_z[i]; }, nc, t0, floor_t, s_red,
+                                          s_bc);
+    else
+      tau = block_entmax_tau<kOutThreads>([&](int i) { return __ldcg(cand_z + cand_src(i)); },
+                                          nc, t0, floor_t, s_red, s_bc);
   }
-  // out = sum over the support of (z - tau)^2 v. The support (in candidate order) is
-  // compacted into the candidate buffer's front as (weight, slot) when the candidates are in
-  // shared memory; warps then take four support tokens at a time, loads in flight together.
+  // out = sum over the support of (z - tau)^2 v. In shared memory the support (in candidate
+  // order) is first compacted to the buffer's front as (weight, row); warps then take four
+  // support tokens at a time, loads in flight together.
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  const T* __restrict__ vp = static_cast<const T*>(d.v_pool);
-  auto v_row = [&](int slot) -> const T* {
-    const int pos = slot / PS, t = slot - pos * PS;
-    const int page = sel_idx != nullptr ? sel_idx[grp * sel_stride + pos] : pos;
-    if (page < 0 || page >= n_pages) return nullptr;
-    const int P = d.page_table[(long)b * d.page_table_stride + page];
-    if (P < 0 || P >= d.num_phys_pages) return nullptr;
-    return vp + (((long)P * Hkv + g) * PS + t) * D + lane * EPL;
-  };
+  const T* __restrict__ vp = static_cast<const T*>(d.v_pool) + lane * EPL;
   if (in_smem) {
     // in place, round by round: every thread reads its candidate before any write of the
     // round, and a support token lands at an index no larger than its own
@@ -787,12 +1040,12 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
     for (int base = 0; base < nc; base += kOutThreads) {
       const int i = base + tid;
       float zi = 0.f;
-      int si = 0;
+      uint32_t ri = 0;
       bool keep = false;
       if (i < nc) {
         zi = s_z[i];
-        si = s_slot[i];
-        keep = (double)zi > tau;
+        ri = s_row[i];
+        keep = zi > tau;
       }
       const uint32_t bal = __ballot_sync(0xffffffffu, keep);
       __syncthreads();                         // the round's reads are done; s_redi is free
@@ -806,22 +1059,22 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
       }
       if (keep) {
         const int at = before + __popc(bal & ((1u << lane) - 1u));
-        const double dz = (double)zi - tau;
-        s_z[at] = (float)(dz * dz);
-        s_slot[at] = si;
+        const float dz = zi - tau;
+        s_z[at] = dz * dz;
+        s_row[at] = ri;
       }
       ns += round_total;
     }
     __syncthreads();
     for (int i0 = warp * 4; i0 < ns; i0 += NW * 4) {
-      const T* rows[4];
       float pw[4], vals[4][EPL];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        rows[u] = i0 + u < ns ? v_row(s_slot[i0 + u]) : nullptr;
-        pw[u] = i0 + u < ns ? s_z[i0 + u] : 0.f;
+        const bool live = i0 + u < ns;
+        pw[u] = live ? s_z[i0 + u] : 0.f;
+        const T* rw = vp + (long)(live ? s_row[i0 + u] : 0u) * D;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) vals[u][e] = rows[u] ? load_elem<T>(rows[u], e) : 0.f;
+        for (int e = 0; e < EPL; ++e) vals[u][e] = live ? load_elem<T>(rw, e) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -831,13 +1084,13 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
     }
   } else {
     for (int i = warp; i < nc; i += NW) {
-      const double z = (double)cand_z_at(i);
+      const long src = cand_src(i);
+      const float z = __ldcg(cand_z + src);
       if (!(z > tau)) continue;
-      const T* row = v_row(i);
-      if (row == nullptr) continue;
-      const float pw = (float)((z - tau) * (z - tau));
+      const T* rw = vp + (long)__ldcg(cand_row + src) * D;
+      const float pw = (z - tau) * (z - tau);
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, load_elem<T>(row, e), acc[e]);
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, load_elem<T>(rw, e), acc[e]);
     }
   }
 #pragma unroll
@@ -849,7 +1102,7 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
     for (int w = 0; w < NW; ++w) s += s_acc[w][i];
     o[i] = s;
   }
-  if (tid == 0 && tau_out != nullptr) tau_out[(long)b * Hq + h] = (float)tau;
+  if (tid == 0 && tau_out != nullptr) tau_out[row] = tau;
 }
 
 // ------------------------------------------------------------------------------ launchers
@@ -857,7 +1110,8 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_idx,
 template <typename T, int D, int G>
 cudaError_t moments_t(const kv_cache_desc& d, const void* q, const void* stats, float scale,
                       float* zb, float* cz, float* vz, int stride, DevCtx ctx, cudaStream_t s) {
-  dim3 grid(ceil_div(d.page_table_stride, kMomWarps * 4), d.num_kv_heads, d.batch);
+  dim3 grid(ceil_div(d.page_table_stride, kMomWarps * mom_rounds(G) * 4), d.num_kv_heads,
+            d.batch);
   return launch_pdl(entmax_moments_kernel<T, D, G>, grid, dim3(kMomWarps * 32), 0, s, d,
                     static_cast<const T*>(q), static_cast<const T*>(stats), 0.5f * scale, zb,
                     cz, vz, stride, ctx);
@@ -865,31 +1119,32 @@ cudaError_t moments_t(const kv_cache_desc& d, const void* q, const void* stats, 
 
 template <typename T, int D, int G>
 cudaError_t logits_t(const kv_cache_desc& d, const void* q, float scale, const int32_t* sel,
-                     const int32_t* cnt, int sel_stride, int S, float* logits, int cap_slots,
-                     float* split_max, DevCtx ctx, cudaStream_t s) {
+                     const int32_t* cnt, int sel_stride, int S, const EntmaxScratch& w,
+                     int cap_slots, DevCtx ctx, cudaStream_t s) {
   dim3 grid(S, d.num_kv_heads, d.batch);
-  return launch_pdl(entmax_logits_kernel<T, D, G>, grid, dim3(kLogitWarps * 32), 0, s, d,
-                    static_cast<const T*>(q), scale, sel, cnt, sel_stride, logits, cap_slots,
-                    split_max, ctx);
+  if constexpr (std::is_same<T, bf16_t>::value)
+    return launch_pdl(entmax_logits_mma_kernel<D, G>, grid, dim3(kLogitMmaWarps * 32), 0, s, d,
+                      static_cast<const T*>(q), scale, sel, cnt, sel_stride, cap_slots,
+                      w.split_floor, w.cand_z, w.cand_row, w.split_cnt, ctx);
+  else
+    return launch_pdl(entmax_logits_kernel<T, D, G>, grid, dim3(kLogitWarps * 32), 0, s, d,
+                      static_cast<const T*>(q), scale, sel, cnt, sel_stride, cap_slots,
+                      w.split_floor, w.cand_z, w.cand_row, w.split_cnt, ctx);
 }
 
 template <typename T, int D>
 cudaError_t out_t(const kv_cache_desc& d, int G, const int32_t* sel, const int32_t* cnt,
-                  int sel_stride, const float* logits, int cap_slots, const float* split_max,
-                  float* cand_z, int* cand_slot, int* split_cnt, int S, float* out, float* tau,
-                  DevCtx ctx, cudaStream_t s) {
-  cudaError_t e0 = launch_pdl(entmax_gather_kernel, dim3(S, d.num_kv_heads * G, d.batch),
-                              dim3(kGatherThreads), 0, s, d, G, sel, cnt, sel_stride, logits,
-                              cap_slots, split_max, cand_z, cand_slot, split_cnt, ctx);
-  if (e0 != cudaSuccess) return e0;
-  const size_t smem = (size_t)kCandCap * (sizeof(float) + sizeof(int));
+                  int sel_stride, const EntmaxScratch& w, int cap_slots, int S, float* out,
+                  float* tau, DevCtx ctx, cudaStream_t s) {
+  const size_t smem = (size_t)kCandCap * (sizeof(float) + sizeof(uint32_t));
   auto kern = entmax_out_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.num_kv_heads * G, d.batch);
-  return launch_pdl(kern, grid, dim3(kOutThreads), smem, s, d, G, sel, cnt, sel_stride, logits,
-                    cap_slots, split_max, cand_z, cand_slot, split_cnt, S, out, tau, ctx);
+  return launch_pdl(kern, grid, dim3(kOutThreads), smem, s, d, G, cnt, sel_stride,
+                    sel != nullptr, cap_slots, w.split_floor, w.cand_z, w.cand_row, w.split_cnt,
+                    S, out, tau, ctx);
 }
 
 #define SKV_G_SWITCH(CALL_T_D)                                                   \
@@ -913,12 +1168,21 @@ cudaError_t moments_d(const kv_cache_desc& d, int G, const void* q, const void* 
 template <typename T, int D>
 cudaError_t logits_d(const kv_cache_desc& d, int G, const void* q, float scale,
                      const int32_t* sel, const int32_t* cnt, int sel_stride, int S,
-                     float* logits, int cap_slots, float* split_max, DevCtx ctx,
-                     cudaStream_t s) {
+                     const EntmaxScratch& w, int cap_slots, DevCtx ctx, cudaStream_t s) {
 #define SKV_CALL(GG) \
-  logits_t<T, D, GG>(d, q, scale, sel, cnt, sel_stride, S, logits, cap_slots, split_max, ctx, s)
+  logits_t<T, D, GG>(d, q, scale, sel, cnt, sel_stride, S, w, cap_slots, ctx, s)
   SKV_G_SWITCH(SKV_CALL)
 #undef SKV_CALL
+}
+
+template <typename T, int D>
+cudaError_t attn_d(const kv_cache_desc& d, int G, const void* q, float scale, const int32_t* sel,
+                   const int32_t* cnt, int sel_stride, int S, const EntmaxScratch& w,
+                   int cap_slots, float* out, float* tau, DevCtx ctx, cudaStream_t s) {
+  const cudaError_t e = logits_d<T, D>(d, G, q, scale, sel, cnt, sel_stride, S, w, cap_slots,
+                                       ctx, s);
+  if (e != cudaSuccess) return e;
+  return out_t<T, D>(d, G, sel, cnt, sel_stride, w, cap_slots, S, out, tau, ctx, s);
 }
 
 }  // namespace
@@ -965,28 +1229,15 @@ cudaError_t launch_entmax_attn(const kv_cache_desc& d, int G, const void* q, flo
                                DevCtx ctx, cudaStream_t s) {
   if (S < 1 || S > kMaxEntSplits) return cudaErrorInvalidValue;
   const bool bf = d.dtype == KV_BF16;
-  cudaError_t e;
   if (d.head_dim == 128)
-    e = bf ? logits_d<bf16_t, 128>(d, G, q, scale, sel, cnt, sel_stride, S, w.logits, cap_slots,
-                                   w.split_max, ctx, s)
-           : logits_d<float, 128>(d, G, q, scale, sel, cnt, sel_stride, S, w.logits, cap_slots,
-                                  w.split_max, ctx, s);
-  else
-    e = bf ? logits_d<bf16_t, 64>(d, G, q, scale, sel, cnt, sel_stride, S, w.logits, cap_slots,
-                                  w.split_max, ctx, s)
-           : logits_d<float, 64>(d, G, q, scale, sel, cnt, sel_stride, S, w.logits, cap_slots,
-                                 w.split_max, ctx, s);
-  if (e != cudaSuccess) return e;
-#define SKV_OUT(TT, DD)                                                                    \
-  return out_t<TT, DD>(d, G, sel, cnt, sel_stride, w.logits, cap_slots, w.split_max,       \
-                       w.cand_z, w.cand_slot, w.split_cnt, S, out, tau, ctx, s)
-  if (d.head_dim == 128) {
-    if (bf) SKV_OUT(bf16_t, 128);
-    SKV_OUT(float, 128);
-  }
-  if (bf) SKV_OUT(bf16_t, 64);
-  SKV_OUT(float, 64);
-#undef SKV_OUT
+    return bf ? attn_d<bf16_t, 128>(d, G, q, scale, sel, cnt, sel_stride, S, w, cap_slots, out,
+                                    tau, ctx, s)
+              : attn_d<float, 128>(d, G, q, scale, sel, cnt, sel_stride, S, w, cap_slots, out,
+                                   tau, ctx, s);
+  return bf ? attn_d<bf16_t, 64>(d, G, q, scale, sel, cnt, sel_stride, S, w, cap_slots, out, tau,
+                                 ctx, s)
+            : attn_d<float, 64>(d, G, q, scale, sel, cnt, sel_stride, S, w, cap_slots, out, tau,
+                                ctx, s);
 }
 
 }  // namespace skv

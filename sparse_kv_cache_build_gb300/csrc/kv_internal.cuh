@@ -51,6 +51,16 @@ template <> __device__ __forceinline__ void chunk_to_f32<float>(uint4 v, float* 
 }
 
 // Load `n` consecutive elements (n * bytes a multiple of 4) from shared or global memory.
+// D += A * B, m16n8k16, bf16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 template <typename T> __device__ __forceinline__ float load_elem(const void* base, long i);
 template <> __device__ __forceinline__ float load_elem<bf16_t>(const void* base, long i) {
   const uint16_t v = reinterpret_cast<const uint16_t*>(base)[i];
@@ -225,11 +235,10 @@ cudaError_t launch_entmax_select(const int32_t* seq_lens, int page_size, int bat
 // Entmax attention scratch: logits, candidate z and slot ([B][Hq][cap_slots] each), and per
 // split the largest logit and the candidate count ([B][Hq][entmax_max_splits()] each).
 struct EntmaxScratch {
-  float* logits;
-  float* cand_z;
-  int* cand_slot;
-  float* split_max;
-  int* split_cnt;
+  float* cand_z;        // [batch * Hq][slots]: candidates' z, per split from its first slot
+  uint32_t* cand_row;   // same layout: the candidate's row in the V pool
+  float* split_floor;   // [batch * Hq][kMaxEntSplits]: lower bounds on tau
+  int* split_cnt;       // same layout: candidates per split
 };
 int entmax_max_splits();
 cudaError_t launch_entmax_attn(const kv_cache_desc& d, int G, const void* q, float scale,
