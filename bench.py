@@ -1241,6 +1241,23 @@ def run_only_step(args):
     c = inputs.make_cache(w, "cuda")
     kv = skv.PagedKV.from_cache(c)
     stats = skv.kv_build_page_stats(kv)
+    if args.only_step.startswith("entmax"):
+        flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device="cuda")
+        ews = torch.empty((skv.kv_entmax_decode_step_workspace_size(kv, w.num_q_heads, kv.stride),),
+                          dtype=torch.uint8, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            flush.zero_()
+            if args.only_step == "entmax_step":
+                skv.kv_entmax_decode_step(kv, c.q, w.sm_scale, stats, k_max=kv.stride,
+                                          workspace=ews)
+            else:
+                skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale)
+        torch.cuda.synchronize()
+        st, flags = skv.kv_check_device_errors()
+        if st != 0:
+            raise RuntimeError(f"device error word {flags:#x}")
+        print(f"{w.name} {args.only_step}: {args.warmup + args.steps} calls", flush=True)
+        return
     if args.only_step == "dense" or "keep_pages" in keep:
         kw = dict(keep_ratio=1.0)
         k_max = 1
@@ -1282,9 +1299,10 @@ def main():
                     help="fresh-process blocks of the headline sparse/dense pair (0: none)")
     ap.add_argument("--block-steps", type=int, default=50)
     ap.add_argument("--block-child", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--only-step", choices=["sparse", "dense"],
-                    help="profiling aid: run warm-up + steps plain kv_decode_step calls "
-                         "(L2 flushed before each) and print no benchmark line")
+    ap.add_argument("--only-step", choices=["sparse", "dense", "entmax_step", "entmax_dense"],
+                    help="profiling aid: run warm-up + steps plain kv_decode_step (or entmax "
+                         "step / dense entmax) calls, L2 flushed before each, and print no "
+                         "benchmark line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.block_child:

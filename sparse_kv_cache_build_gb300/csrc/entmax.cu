@@ -390,11 +390,13 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
 //
 // The entmax threshold of a set of z values solves f(t) = sum max(z - t, 0)^2 = 1. f is
 // convex and decreasing, so Newton from a point where f >= 0 (any t <= max z - 1) rises to the
-// root; once every member of {z > t} lies above the closed-form root of that set, the root is
-// the threshold. The closed form is taken about a pivot p near the top (the maximum):
-// with y = z - p over the K members, tau = p + mean(y) - sqrt((1 - Q) / K), Q = sum (y -
-// mean)^2, so flat sets (all z equal) are exact and no large sums cancel. Float throughout:
-// FP64 is scarce on this part, and the logits themselves carry float rounding.
+// root; once every member of {z > t} lies above the closed-form root of that set (and the root
+// is not below t, where the non-members lie), the root is the threshold. The closed form is
+// taken about a pivot p: with y = z - p over the K members, tau = p + mean(y) - sqrt((1 - Q)
+// / K), Q = sum (y - mean)^2 = sum y^2 - K mean^2. That difference keeps its digits only while
+// the pivot lies within about a standard deviation of the members' mean, so a root is taken
+// only then; otherwise the pass is repeated about the mean. Float throughout: FP64 is scarce
+// on this part, and the logits themselves carry float rounding.
 
 struct TauSums {
   float k, y1, y2, e1, e2, zmin;               // count, sums of y, y^2, e = z - t, e^2; min z
@@ -427,22 +429,46 @@ __device__ __forceinline__ void tau_warp_reduce(TauSums& s) {
   }
 }
 
-// One step from the sums over {z > t}: true when t is final (the closed form holds, or Newton
-// cannot advance any further), else t has taken a Newton step.
-__device__ __forceinline__ bool tau_step(const TauSums& s, float pivot, float& t) {
-  if (s.k == 0.f) return true;
-  const float mean = s.y1 / s.k;
-  const float r = 1.f - fmaxf(s.y2 - s.y1 * mean, 0.f);
+// The closed form over the members {z > t} from their sums about pivot.
+struct TauClosed {
+  float root, mean_z;
+  bool valid;                                  // members at or above root, root >= t
+  bool pivot_ok;                               // pivot within a standard deviation of mean_z
+};
+
+__device__ __forceinline__ TauClosed tau_closed(const TauSums& s, float pivot, float t) {
+  TauClosed c{-INFINITY, pivot, false, true};
+  if (s.k == 0.f) return c;
+  const float m = s.y1 / s.k;
+  const float q = fmaxf(s.y2 - s.y1 * m, 0.f);
+  c.mean_z = pivot + m;
+  c.pivot_ok = m * m <= q / s.k + 1e-6f;
+  const float r = 1.f - q;
   if (r >= 0.f) {
-    const float root = pivot + mean - sqrtf(r / s.k);
-    if (s.zmin >= root) {
-      t = root;
+    c.root = c.mean_z - sqrtf(r / s.k);
+    c.valid = s.zmin >= c.root && c.root >= t;
+  }
+  return c;
+}
+
+// One step from the sums over {z > t}: true when t is final (the closed form holds about a
+// good pivot, or Newton cannot advance any further); else t has taken a Newton step, or the
+// pivot has moved to the members' mean for another pass at the same t.
+__device__ __forceinline__ bool tau_step(const TauSums& s, float& pivot, float& t) {
+  if (s.k == 0.f) return true;
+  const TauClosed c = tau_closed(s, pivot, t);
+  if (c.valid) {
+    if (c.pivot_ok) {
+      t = c.root;
       return true;
     }
+    pivot = c.mean_z;
+    return false;
   }
   const float step = (s.e2 - 1.f) / (2.f * s.e1);
   if (!(step > 0.f)) return true;
   t += step;
+  pivot = c.mean_z;
   return false;
 }
 
@@ -473,25 +499,55 @@ __device__ float block_entmax_tau(ZAt zat, int n, float t, float pivot, TauSums*
     if (warp == 0) {
       TauSums w = lane < NW ? s_red[lane] : tau_zero();
       tau_warp_reduce(w);
-      float tn = t;
-      const bool done = tau_step(w, pivot, tn);
+      float tn = t, pn = pivot;
+      const bool done = tau_step(w, pn, tn);
       if (lane == 0) {
         s_bc[0] = tn;
         s_bc[1] = done ? 1.f : 0.f;
+        s_bc[2] = pn;
       }
     }
     __syncthreads();
     t = s_bc[0];
+    pivot = s_bc[2];
     if (s_bc[1] != 0.f) break;
   }
   return t;
 }
 
+// A block's first pass: warp w takes the point lo + (hi - lo) w / NW of a bracket [lo, hi]
+// with f(lo) >= 0 and sums over all n values there (no barrier inside the pass). A point
+// whose closed form holds about a good pivot gives tau; otherwise the Newton passes start
+// from the highest point with f >= 0, within 1/NW of the bracket from the root.
+template <int NT, class ZAt>
+__device__ float block_entmax_tau_bracket(ZAt zat, int n, float lo, float hi, float pivot,
+                                          TauSums* s_red, float* s_pts, float* s_bc) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float tw = lo + (hi - lo) * (float)warp / (float)NW;
+  TauSums s = tau_zero();
+  for (int i = lane; i < n; i += 32) tau_add(s, zat(i), tw, pivot);
+  tau_warp_reduce(s);
+  if (lane == 0) {
+    const TauClosed c = tau_closed(s, pivot, tw);
+    s_pts[warp] = s.e2 - 1.f;                    // f(tw)
+    s_pts[NW + warp] = c.valid && c.pivot_ok ? c.root : -INFINITY;
+  }
+  __syncthreads();
+  float start = lo;
+  for (int w = 0; w < NW; ++w) {
+    if (s_pts[NW + w] != -INFINITY) return s_pts[NW + w];
+    if (s_pts[w] >= 0.f) start = lo + (hi - lo) * (float)w / (float)NW;
+  }
+  return block_entmax_tau<NT>(zat, n, start, pivot, s_red, s_bc);
+}
+
 // The exact threshold of the 32 values v held one per lane (-inf: no value), by the sorting
 // form: with the values descending, the support is the longest prefix whose k-th value lies
 // above the closed-form root of the first k. A lower bound on the threshold of any set that
-// holds these values; every lane returns it (-inf when every value is -inf).
-__device__ float warp32_tau(float v, int lane) {
+// holds these values; .x the threshold, .y the mean of that support (-inf, -inf when every
+// value is -inf). Every lane returns the same.
+__device__ float2 warp32_tau(float v, int lane) {
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {          // bitonic sort, descending across the lanes
 #pragma unroll
@@ -501,7 +557,7 @@ __device__ float warp32_tau(float v, int lane) {
     }
   }
   const float v0 = __shfl_sync(0xffffffffu, v, 0);
-  if (v0 == -INFINITY) return v0;
+  if (v0 == -INFINITY) return make_float2(v0, v0);
   const float y = v - v0;
   float s1 = y, s2 = y * y;
 #pragma unroll
@@ -516,14 +572,16 @@ __device__ float warp32_tau(float v, int lane) {
   const float r = 1.f - fmaxf(s2 - s1 * mean, 0.f);
   const float root = v0 + mean - sqrtf(r / k);
   const uint32_t ok = __ballot_sync(0xffffffffu, r >= 0.f && v > root);   // a prefix of lanes
-  return __shfl_sync(0xffffffffu, root, 31 - __clz(ok | 1u));
+  const int K = 31 - __clz(ok | 1u);
+  return make_float2(__shfl_sync(0xffffffffu, root, K), v0 + __shfl_sync(0xffffffffu, mean, K));
 }
 
-// A start for the Newton passes: the threshold of the lanes' largest values, less a rounding
-// margin (f >= 0 there), and never below max - 1.
-__device__ __forceinline__ float tau_start(float lane_max, float zmax, int lane) {
-  const float t = warp32_tau(lane_max, lane);
-  return fmaxf(zmax - 1.f, t - 1e-6f * (fabsf(t) + 1.f));
+// A start for the Newton passes from the lanes' largest values: .x the threshold of those
+// values less a rounding margin (f >= 0 there), never below max - 1; .y a pivot, the mean of
+// their support.
+__device__ __forceinline__ float2 tau_start(float lane_max, float zmax, int lane) {
+  const float2 w = warp32_tau(lane_max, lane);
+  return make_float2(fmaxf(zmax - 1.f, w.x - 1e-6f * (fabsf(w.x) + 1.f)), w.y);
 }
 
 // ------------------------------------------------------------------------------ logits
@@ -572,8 +630,8 @@ __device__ void chunk_candidates(const float* s_z, int zs, int n, const int* s_P
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (m == -INFINITY) continue;
-    const float tc = warp_entmax_tau([&](int i) { return z[i]; }, n, tau_start(lm, m, lane), m,
-                                     lane);
+    const float2 st = tau_start(lm, m, lane);
+    const float tc = warp_entmax_tau([&](int i) { return z[i]; }, n, st.x, st.y, lane);
     const float thr = tc - 1e-5f * (fabsf(tc) + 1.f);
     L.floor[j] = fmaxf(L.floor[j], thr);
     float* oz = cz + (long)h * cap_slots;
@@ -913,7 +971,8 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
   __shared__ int s_off[kMaxEntSplits + 1];
   __shared__ float s_fl[kMaxEntSplits];
   __shared__ float s_bc[4];
-  __shared__ float s_wt[NW];
+  __shared__ float s_wt[3 * NW];
+  __shared__ float s_pts[2 * NW];
   pdl_trigger();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -996,35 +1055,54 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
   }
   __syncthreads();
   // tau from the larger of the floor and the threshold of the lanes' largest candidates (both
-  // lower bounds, f >= 0 there); pivot the floor: the candidates lie within about 1 of it
+  // lower bounds, f >= 0 there), about the mean of that threshold's support
   float tau;
   if (in_smem && nc <= 1024) {
     if (warp == 0) {
       float lm = -INFINITY;
       for (int i = lane; i < nc; i += 32) lm = fmaxf(lm, s_z[i]);
-      const float t0 = fmaxf(floor_t, warp32_tau(lm, lane) - 1e-6f * (fabsf(floor_t) + 1.f));
-      const float t = warp_entmax_tau([&](int i) { return s_z[i]; }, nc, t0, floor_t, lane);
+      const float2 w32 = warp32_tau(lm, lane);
+      const float t0 = fmaxf(floor_t, w32.x - 1e-6f * (fabsf(w32.x) + 1.f));
+      const float t = warp_entmax_tau([&](int i) { return s_z[i]; }, nc, t0, w32.y, lane);
       if (lane == 0) s_bc[0] = t;
     }
     __syncthreads();
     tau = s_bc[0];
   } else {
+    // lower end: the larger of the floor and the threshold of a warp's lanes' largest
+    // candidates; upper end: max z - 1/sqrt(nc) (the support, at most nc tokens, carries
+    // weights summing to 1, each at most (max z - tau)^2)
     float lm = -INFINITY;
     for (int i = tid; i < nc; i += kOutThreads)
       lm = fmaxf(lm, in_smem ? s_z[i] : __ldcg(cand_z + cand_src(i)));
-    const float tw = warp32_tau(lm, lane);
-    if (lane == 0) s_wt[warp] = tw;
-    __syncthreads();
-    float t0 = -INFINITY;
+    const float2 w32 = warp32_tau(lm, lane);
+    float wm = lm;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) t0 = fmaxf(t0, s_wt[w]);
-    t0 = fmaxf(floor_t, t0 - 1e-6f * (fabsf(floor_t) + 1.f));
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+    if (lane == 0) {
+      s_wt[warp] = w32.x;
+      s_wt[NW + warp] = wm;
+      s_wt[2 * NW + warp] = w32.y;
+    }
+    __syncthreads();
+    float t0 = -INFINITY, zm = -INFINITY, pivot = floor_t;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      if (s_wt[w] > t0) {                        // the pivot: the highest warp's support mean
+        t0 = s_wt[w];
+        pivot = s_wt[2 * NW + w];
+      }
+      zm = fmaxf(zm, s_wt[NW + w]);
+    }
+    t0 = fmaxf(floor_t, t0 - 1e-6f * (fabsf(t0) + 1.f));
+    const float hi = fmaxf(t0, zm - rsqrtf((float)nc));
     if (in_smem)
-      tau = block_entmax_tau<kOutThreads>([&](int i) { return s_z[i]; }, nc, t0, floor_t, s_red,
-                                          s_bc);
+      tau = block_entmax_tau_bracket<kOutThreads>([&](int i) { return s_z[i]; }, nc, t0, hi,
+                                                  pivot, s_red, s_pts, s_bc);
     else
-      tau = block_entmax_tau<kOutThreads>([&](int i) { return __ldcg(cand_z + cand_src(i)); },
-                                          nc, t0, floor_t, s_red, s_bc);
+      tau = block_entmax_tau_bracket<kOutThreads>(
+          [&](int i) { return __ldcg(cand_z + cand_src(i)); }, nc, t0, hi, pivot, s_red, s_pts,
+          s_bc);
   }
   // out = sum over the support of (z - tau)^2 v. In shared memory the support (in candidate
   // order) is first compacted to the buffer's front as (weight, row); warps then take four
