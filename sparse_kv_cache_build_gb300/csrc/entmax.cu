@@ -1032,38 +1032,60 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
     }
     return row * cap_slots + (long)min(cnt, lo * cps) * PS + (i - s_off[lo]);
   };
+  // in shared memory: only the candidates above the largest floor (every other one has weight
+  // zero), compacted in candidate order; four per thread per round, loads in flight together
+  int nk = nc;                                  // candidates held (block-uniform)
   if (in_smem) {
-    for (int i0 = tid; i0 < nc; i0 += 4 * kOutThreads) {   // four candidates' loads in flight
+    nk = 0;
+    for (int base = 0; base < nc; base += 4 * kOutThreads) {
       float zv[4];
       uint32_t rv[4];
+      int mine = 0;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kOutThreads;
+        const int i = base + 4 * tid + u;
         const long src = i < nc ? cand_src(i) : 0;
-        zv[u] = i < nc ? __ldcg(cand_z + src) : 0.f;
+        zv[u] = i < nc ? __ldcg(cand_z + src) : -INFINITY;
         rv[u] = i < nc ? __ldcg(cand_row + src) : 0u;
       }
 #pragma unroll
+      for (int u = 0; u < 4; ++u) mine += zv[u] > floor_t ? 1 : 0;
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) s_redi[warp] = incl;
+      __syncthreads();
+      int at = nk + incl - mine, round_total = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        at += w < warp ? s_redi[w] : 0;
+        round_total += s_redi[w];
+      }
+#pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kOutThreads;
-        if (i < nc) {
-          s_z[i] = zv[u];
-          s_row[i] = rv[u];
+        if (zv[u] > floor_t) {
+          s_z[at] = zv[u];
+          s_row[at] = rv[u];
+          ++at;
         }
       }
+      nk += round_total;
+      __syncthreads();                           // s_redi is reused
     }
   }
-  __syncthreads();
   // tau from the larger of the floor and the threshold of the lanes' largest candidates (both
   // lower bounds, f >= 0 there), about the mean of that threshold's support
   float tau;
-  if (in_smem && nc <= 1024) {
+  if (in_smem && nk <= 1024) {
     if (warp == 0) {
       float lm = -INFINITY;
-      for (int i = lane; i < nc; i += 32) lm = fmaxf(lm, s_z[i]);
+      for (int i = lane; i < nk; i += 32) lm = fmaxf(lm, s_z[i]);
       const float2 w32 = warp32_tau(lm, lane);
       const float t0 = fmaxf(floor_t, w32.x - 1e-6f * (fabsf(w32.x) + 1.f));
-      const float t = warp_entmax_tau([&](int i) { return s_z[i]; }, nc, t0, w32.y, lane);
+      const float t = warp_entmax_tau([&](int i) { return s_z[i]; }, nk, t0, w32.y, lane);
       if (lane == 0) s_bc[0] = t;
     }
     __syncthreads();
@@ -1073,7 +1095,7 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
     // candidates; upper end: max z - 1/sqrt(nc) (the support, at most nc tokens, carries
     // weights summing to 1, each at most (max z - tau)^2)
     float lm = -INFINITY;
-    for (int i = tid; i < nc; i += kOutThreads)
+    for (int i = tid; i < nk; i += kOutThreads)
       lm = fmaxf(lm, in_smem ? s_z[i] : __ldcg(cand_z + cand_src(i)));
     const float2 w32 = warp32_tau(lm, lane);
     float wm = lm;
@@ -1095,9 +1117,9 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
       zm = fmaxf(zm, s_wt[NW + w]);
     }
     t0 = fmaxf(floor_t, t0 - 1e-6f * (fabsf(t0) + 1.f));
-    const float hi = fmaxf(t0, zm - rsqrtf((float)nc));
+    const float hi = fmaxf(t0, zm - rsqrtf((float)nk));
     if (in_smem)
-      tau = block_entmax_tau_bracket<kOutThreads>([&](int i) { return s_z[i]; }, nc, t0, hi,
+      tau = block_entmax_tau_bracket<kOutThreads>([&](int i) { return s_z[i]; }, nk, t0, hi,
                                                   pivot, s_red, s_pts, s_bc);
     else
       tau = block_entmax_tau_bracket<kOutThreads>(
@@ -1115,12 +1137,12 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
     // in place, round by round: every thread reads its candidate before any write of the
     // round, and a support token lands at an index no larger than its own
     int ns = 0;
-    for (int base = 0; base < nc; base += kOutThreads) {
+    for (int base = 0; base < nk; base += kOutThreads) {
       const int i = base + tid;
       float zi = 0.f;
       uint32_t ri = 0;
       bool keep = false;
-      if (i < nc) {
+      if (i < nk) {
         zi = s_z[i];
         ri = s_row[i];
         keep = zi > tau;

@@ -236,3 +236,26 @@ def test_entmax_step_prunes_tight_boxes_and_matches_oracle():
                                    selected=chosen)
     assert np.abs(f64(out) - ref).max() < out_tol(w)
     assert np.abs(f64(tau) - ref_tau).max() < 1e-4
+
+
+def test_one_outlier_over_flat_logits():
+    """One token well above thousands of tied logits: the threshold's closed form is taken about
+    a pivot near the members' mean, not the outlier, so tau and the output keep float accuracy
+    (sum y^2 - K mean^2 would otherwise cancel)."""
+    w, c = make("bf16", 128, 4, 16, lens=(6000,), seed=45, planted=0)
+    kv = skv.PagedKV.from_cache(c)
+    n = 6000
+    # q along the first coordinate only; every key zero there except one token's
+    q0 = torch.zeros_like(c.q)
+    q0[..., 0] = 1.0
+    table = c.page_table[0].cpu().numpy()
+    c.k_pool[:, :, :, 0] = 0
+    j = 4321
+    big = 2 * 0.9 / w.sm_scale                    # z_j = sm_scale * q . k_j / 2 = 0.9
+    c.k_pool[table[j // 16], :, j % 16, 0] = big
+    out, tau = skv.kv_entmax_decode_attn(kv, q0, w.sm_scale)
+    assert_no_device_error()
+    q, K, V, tab, lens = host(c)
+    ref, ref_tau = E.entmax_attend(f64(q0), K, V, tab, lens, 16, w.sm_scale)
+    assert np.abs(f64(tau) - ref_tau).max() < 2e-6
+    assert np.abs(f64(out) - ref).max() < out_tol(w)
