@@ -48,6 +48,56 @@ constexpr int kCandCap = 16384;              // candidate logits held in shared 
 
 // ------------------------------------------------------------------------------ moments
 
+// One statistics row's three sums for every head (this lane's columns): with s = mn + mx and
+// w = mx - mn per column, max(q mn, q mx) = (q s + |q| w) / 2. Then summed over the row's 8
+// lanes (xor 1, 2, 4), so every lane of the row holds the row's totals.
+template <typename T, int G, int NU, int EPC>
+__device__ __forceinline__ void mom_row(const uint4 (&rmn)[NU], const uint4 (&rmx)[NU],
+                                        const float (&qv)[G][NU][EPC], bool ok, float (&bnd)[G],
+                                        float (&cen)[G], float (&var)[G]) {
+#pragma unroll
+  for (int h = 0; h < G; ++h) bnd[h] = cen[h] = var[h] = 0.f;
+  if (ok) {
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      float lo[EPC], hi[EPC];
+      chunk_to_f32<T>(rmn[u], lo);
+      chunk_to_f32<T>(rmx[u], hi);
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) {
+        const float w = hi[e] - lo[e], sm = lo[e] + hi[e], w2 = w * w;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float qd = qv[h][u][e];
+          cen[h] = fmaf(qd, sm, cen[h]);
+          bnd[h] = fmaf(fabsf(qd), w, bnd[h]);
+          var[h] = fmaf(qd * qd, w2, var[h]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      bnd[h] += __shfl_xor_sync(0xffffffffu, bnd[h], o);
+      cen[h] += __shfl_xor_sync(0xffffffffu, cen[h], o);
+      var[h] += __shfl_xor_sync(0xffffffffu, var[h], o);
+    }
+  }
+}
+
+// This lane's query columns (j + 8u) * EPC .. + EPC of every head of group (b, g).
+template <typename T, int D, int G, int NU, int EPC>
+__device__ __forceinline__ void mom_query(const T* q, long row0, int j, float (&qv)[G][NU][EPC]) {
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const uint4* qr = reinterpret_cast<const uint4*>(q + (row0 + h) * D);
+#pragma unroll
+    for (int u = 0; u < NU; ++u) chunk_to_f32<T>(__ldg(qr + j + 8 * u), qv[h][u]);
+  }
+}
+
 // A warp takes mom_rounds(G) rounds of 4 statistics rows, 8 lanes a row; lane j of a row holds
 // columns (j + 8u) * EPC .. + EPC of both halves, and the query's same columns for every head
 // in registers (no shared memory, no barrier). With s = mn + mx and w = mx - mn per column,
@@ -92,45 +142,11 @@ entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restr
     }
   }
   float qv[G][NU][EPC];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint4* qr = reinterpret_cast<const uint4*>(q + ((long)b * Hq + g * G + h) * D);
-#pragma unroll
-    for (int u = 0; u < NU; ++u) chunk_to_f32<T>(__ldg(qr + j + 8 * u), qv[h][u]);
-  }
+  mom_query<T, D, G, NU, EPC>(q, (long)b * Hq + g * G, j, qv);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     float bnd[G], cen[G], var[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) bnd[h] = cen[h] = var[h] = 0.f;
-    if (ok[r]) {
-#pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        float lo[EPC], hi[EPC];
-        chunk_to_f32<T>(rmn[r][u], lo);
-        chunk_to_f32<T>(rmx[r][u], hi);
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) {
-          const float w = hi[e] - lo[e], sm = lo[e] + hi[e], w2 = w * w;
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float qd = qv[h][u][e];
-            cen[h] = fmaf(qd, sm, cen[h]);
-            bnd[h] = fmaf(fabsf(qd), w, bnd[h]);
-            var[h] = fmaf(qd * qd, w2, var[h]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) {
-        bnd[h] += __shfl_xor_sync(0xffffffffu, bnd[h], o);
-        cen[h] += __shfl_xor_sync(0xffffffffu, cen[h], o);
-        var[h] += __shfl_xor_sync(0xffffffffu, var[h], o);
-      }
-    }
+    mom_row<T, G, NU, EPC>(rmn[r], rmx[r], qv, ok[r], bnd, cen, var);
     const int p = p_block + (warp * R + r) * 4 + (lane >> 3);
     if (j == 0 && ok[r]) {
 #pragma unroll

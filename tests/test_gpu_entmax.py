@@ -38,6 +38,22 @@ def host(c):
             c.seq_lens.cpu().numpy())
 
 
+def G_(w):
+    return w.num_q_heads // w.num_kv_heads
+
+
+def step_workspace_selection(ws, B, Hq, Hkv, stride, k_max):
+    """The entmax step's selection and bounds, read back from its workspace (layout of
+    kv_entmax_decode_step_workspace_size: zb, cz, vz, then sel_idx, then sel_cnt)."""
+    M = (B * Hq * stride * 4 + 255) // 256 * 256
+    a = 3 * M
+    cb = a + (B * Hkv * k_max * 4 + 255) // 256 * 256
+    sel = ws[a: a + B * Hkv * k_max * 4].view(torch.int32).view(B, Hkv, k_max).cpu()
+    cnt = ws[cb: cb + B * Hkv * 4].view(torch.int32).view(B, Hkv).cpu()
+    zb = ws[: B * Hq * stride * 4].view(torch.float32).view(B, Hq, stride).cpu()
+    return sel, cnt, zb
+
+
 @pytest.mark.parametrize("dtype,D,G,PS", SHAPES)
 def test_page_moments_match_oracle(dtype, D, G, PS):
     w, c = make(dtype, D, G, PS)
@@ -170,12 +186,30 @@ def test_selector_adapts_to_gaussian_scores():
     ws = torch.empty((skv.kv_entmax_decode_step_workspace_size(kv, w.num_q_heads, k_max),),
                      dtype=torch.uint8, device="cuda")
     out, tau = skv.kv_entmax_decode_step(kv, c.q, w.sm_scale, stats, k_max=k_max, workspace=ws)
-    zb, cz, vz = skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale)
-    sel, cnt, _ = skv.kv_entmax_select(zb, cz, vz, c.seq_lens, 16, Hkv, k_max=k_max)
-    out2, tau2 = skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, sel, cnt)
-    assert_no_device_error()
-    assert torch.equal(out, out2) and torch.equal(tau, tau2)
+    torch.cuda.synchronize()
     B, Hq = w.batch, w.num_q_heads
+    step_sel, step_cnt, step_zb = step_workspace_selection(ws, B, Hq, Hkv, kv.stride, k_max)
+    zb, cz, vz = skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale)
+    sel, cnt, tau_hat = skv.kv_entmax_select(zb, cz, vz, c.seq_lens, 16, Hkv, k_max=k_max)
+    out2, tau2 = skv.kv_entmax_decode_attn(kv, c.q, w.sm_scale, step_sel.cuda(), step_cnt.cuda())
+    assert_no_device_error()
+    # the step's own moments are the public kernel's, bit for bit; its kept pages are the public
+    # selector's up to pages whose bound sits at tau_hat (a different summation order)
+    for b in range(B):
+        n_b = oracle.num_pages(int(c.seq_lens[b]), 16)
+        assert torch.equal(step_zb[b, :, :n_b], zb.cpu()[b, :, :n_b])
+    th = tau_hat.cpu().numpy()
+    zbh = zb.cpu().numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            got = set(step_sel[b, g, : step_cnt[b, g]].tolist())
+            want = set(sel[b, g, : cnt[b, g]].tolist())
+            for p_ in got ^ want:
+                near = np.abs(zbh[b, g * G_(w): (g + 1) * G_(w), p_] - th[b, g * G_(w): (g + 1) * G_(w)])
+                assert near.min() <= 1e-5 * (np.abs(th[b]).max() + 1), (b, g, p_)
+    # and its output is the attention over exactly the pages it kept
+    assert torch.equal(out, out2) and torch.equal(tau, tau2)
+    sel, cnt = step_sel.cuda(), step_cnt.cuda()
     cnt_h = cnt.cpu().numpy()
     for b in range(B):
         n = oracle.num_pages(int(c.seq_lens[b]), 16)
