@@ -866,9 +866,10 @@ kv_status kv_entmax_page_moments(const kv_cache_desc* cache, const void* q, int3
     return KV_ERR_INVALID_ARG;
   if (!aligned16(stats)) return KV_ERR_MISALIGNED;
   DevCtx ctx;
-  if ((r = ctx_for_call(&ctx)) != KV_OK) return r;
+  DeviceState* st = nullptr;
+  if ((r = ctx_for_call(&ctx, &st)) != KV_OK) return r;
   return from_cuda(launch_entmax_moments(*cache, num_q_heads / cache->num_kv_heads, q, stats,
-                                         sm_scale, zb, cz, vz, stride, ctx, stream));
+                                         sm_scale, zb, cz, vz, stride, st->sms, ctx, stream));
 }
 
 kv_status kv_entmax_select(const float* zb, const float* cz, const float* vz, int32_t stride,
@@ -1004,8 +1005,8 @@ kv_status kv_entmax_decode_step(const kv_cache_desc* cache, const void* q, int32
   int32_t* cnt = reinterpret_cast<int32_t*>(ws + 3 * mom + round256(B * Hkv * k_max * 4));
   void* scratch = ws + 3 * mom + round256(B * Hkv * k_max * 4) + round256(B * Hkv * 4);
   const int G = num_q_heads / cache->num_kv_heads;
-  cudaError_t e = launch_entmax_moments(*cache, G, q, stats, sm_scale, zb, cz, vz, stride, ctx,
-                                        stream);
+  cudaError_t e = launch_entmax_moments(*cache, G, q, stats, sm_scale, zb, cz, vz, stride,
+                                        st->sms, ctx, stream);
   if (e != cudaSuccess) return KV_ERR_CUDA;
   e = launch_entmax_select(cache->seq_lens, cache->page_size, cache->batch, num_q_heads,
                            cache->num_kv_heads, stride, zb, cz, vz, stride, k_max, sel, cnt,

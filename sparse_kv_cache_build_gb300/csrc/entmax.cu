@@ -30,6 +30,8 @@
 //                          solved exactly over them (Newton from a floor, closed-form finish),
 //                          and the output sum over the support, reading V rows of support
 //                          tokens only.
+#include <algorithm>
+#include <cooperative_groups.h>
 #include <type_traits>
 
 #include "kv_internal.cuh"
@@ -37,11 +39,12 @@
 namespace skv {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kMomWarps = 4;                 // moments: 4 warps x rounds x 4 rows per block
-// rounds of 4 rows per warp (the query's columns for all G heads stay in registers)
-constexpr int mom_rounds(int G) { return G >= 8 ? 1 : 2; }
-constexpr int kESelThreads = 512;
-constexpr int kSelSteps = 16;               // selector: 32-page ballot words per warp per pass
+constexpr int kSelThreads = 256;             // selector: threads per CTA
+constexpr int kSelCluster = 8;               // selector: CTAs per group (one portable cluster)
+constexpr int kSelSteps = 32;               // selector: 32-page ballot words per warp per pass
 constexpr int kLogitWarps = 4;
 constexpr int kOutThreads = 512;
 constexpr int kCandCap = 16384;              // candidate logits held in shared memory
@@ -49,7 +52,7 @@ constexpr int kCandCap = 16384;              // candidate logits held in shared 
 // ------------------------------------------------------------------------------ moments
 
 // One statistics row's three sums for every head (this lane's columns): with s = mn + mx and
-// w = mx - mn per column, max(q mn, q mx) = (q s + |q| w) / 2. Then summed over the row's 8
+// w = mx - mn per column, max(q mn, q mx) = (q s + |q| w) / 2, and q^2 w^2 = (q w)^2. Then summed over the row's 8
 // lanes (xor 1, 2, 4), so every lane of the row holds the row's totals.
 template <typename T, int G, int NU, int EPC>
 __device__ __forceinline__ void mom_row(const uint4 (&rmn)[NU], const uint4 (&rmx)[NU],
@@ -65,13 +68,13 @@ __device__ __forceinline__ void mom_row(const uint4 (&rmn)[NU], const uint4 (&rm
       chunk_to_f32<T>(rmx[u], hi);
 #pragma unroll
       for (int e = 0; e < EPC; ++e) {
-        const float w = hi[e] - lo[e], sm = lo[e] + hi[e], w2 = w * w;
+        const float w = hi[e] - lo[e], sm = lo[e] + hi[e];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float qd = qv[h][u][e];
+          const float qd = qv[h][u][e], qw = qd * w;
           cen[h] = fmaf(qd, sm, cen[h]);
           bnd[h] = fmaf(fabsf(qd), w, bnd[h]);
-          var[h] = fmaf(qd * qd, w2, var[h]);
+          var[h] = fmaf(qw, qw, var[h]);
         }
       }
     }
@@ -98,57 +101,59 @@ __device__ __forceinline__ void mom_query(const T* q, long row0, int j, float (&
   }
 }
 
-// A warp takes mom_rounds(G) rounds of 4 statistics rows, 8 lanes a row; lane j of a row holds
-// columns (j + 8u) * EPC .. + EPC of both halves, and the query's same columns for every head
-// in registers (no shared memory, no barrier). With s = mn + mx and w = mx - mn per column,
-// max(q mn, q mx) = (q s + |q| w) / 2, so one pass gives all three sums.
+// A warp takes rpw rounds of 4 statistics rows (the next round's loads in flight while a round
+// is summed), 8 lanes a row; lane j of a row holds columns (j + 8u) * EPC .. + EPC of both
+// halves, and the query's same columns for every head in registers (no shared memory, no
+// barrier). rpw is chosen so that the grid is about one wave.
+// blocks per SM the moments kernel is sized for (the query's columns of all G heads live in
+// registers: 64 floats a lane for 4 bf16 heads)
+template <typename T, int G>
+constexpr int mom_blocks() { return (ElemTraits<T>::bytes == 4 || G >= 8) ? 2 : 4; }
+
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kMomWarps * 32)
+__global__ void __launch_bounds__(kMomWarps * 32, mom_blocks<T, G>())
 entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restrict__ stats,
                       float half_scale, float* __restrict__ zb, float* __restrict__ cz,
-                      float* __restrict__ vz, int stride, DevCtx ctx) {
+                      float* __restrict__ vz, int stride, int rpw, DevCtx ctx) {
   constexpr int EPC = 16 / ElemTraits<T>::bytes;   // elements per 16-byte chunk
   constexpr int CH = D / EPC;                      // chunks per half row
   constexpr int NU = CH / 8;                       // chunks per lane per half row
-  constexpr int R = mom_rounds(G);
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.z, g = blockIdx.y, tid = threadIdx.x;
   const int Hkv = d.num_kv_heads, Hq = Hkv * G;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
-  const int p_block = blockIdx.x * kMomWarps * R * 4;
+  const int p_block = blockIdx.x * kMomWarps * rpw * 4;
   if (p_block >= n_pages) return;
   const int warp = tid >> 5, lane = tid & 31, j = lane & 7;
-  uint4 rmn[R][NU], rmx[R][NU];
-  bool ok[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int p = p_block + (warp * R + r) * 4 + (lane >> 3);
-    ok[r] = false;
-    if (p < n_pages) {
-      const int P = d.page_table[(long)b * d.page_table_stride + p];
-      if (P >= 0 && P < d.num_phys_pages) {
-        ok[r] = true;
-        const uint4* row = reinterpret_cast<const uint4*>(stats + ((long)P * Hkv + g) * 2 * D);
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-          rmn[r][u] = __ldg(row + j + 8 * u);
-          rmx[r][u] = __ldg(row + CH + j + 8 * u);
-        }
-      } else if (j == 0) {
-        flag(ctx, KV_DEVERR_BAD_PAGE);
-      }
+  const int p0 = p_block + warp * rpw * 4 + (lane >> 3);
+  auto load = [&](int r, uint4 (&rmn)[NU], uint4 (&rmx)[NU]) -> bool {
+    const int p = p0 + 4 * r;
+    if (r >= rpw || p >= n_pages) return false;
+    const int P = d.page_table[(long)b * d.page_table_stride + p];
+    if (P < 0 || P >= d.num_phys_pages) {
+      if (j == 0) flag(ctx, KV_DEVERR_BAD_PAGE);
+      return false;
     }
-  }
+    const uint4* row = reinterpret_cast<const uint4*>(stats + ((long)P * Hkv + g) * 2 * D);
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      rmn[u] = __ldg(row + j + 8 * u);
+      rmx[u] = __ldg(row + CH + j + 8 * u);
+    }
+    return true;
+  };
+  uint4 amn[NU], amx[NU], bmn[NU], bmx[NU];
+  bool aok = load(0, amn, amx);
   float qv[G][NU][EPC];
   mom_query<T, D, G, NU, EPC>(q, (long)b * Hq + g * G, j, qv);
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
+  for (int r = 0; r < rpw && p0 + 4 * r < n_pages; ++r) {
+    const bool bok = load(r + 1, bmn, bmx);
     float bnd[G], cen[G], var[G];
-    mom_row<T, G, NU, EPC>(rmn[r], rmx[r], qv, ok[r], bnd, cen, var);
-    const int p = p_block + (warp * R + r) * 4 + (lane >> 3);
-    if (j == 0 && ok[r]) {
+    mom_row<T, G, NU, EPC>(amn, amx, qv, aok, bnd, cen, var);
+    if (j == 0 && aok) {
+      const int p = p0 + 4 * r;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const long i = ((long)b * Hq + g * G + h) * stride + p;
@@ -157,6 +162,12 @@ entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restr
         vz[i] = half_scale * half_scale * var[h] / 12.f;
       }
     }
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      amn[u] = bmn[u];
+      amx[u] = bmx[u];
+    }
+    aok = bok;
   }
 }
 
@@ -207,72 +218,85 @@ __device__ float gaussian_threshold(float mu, float var, float count) {
   return mu - sigma * u;
 }
 
-// One block of 512 threads per (sequence, KV head). Thread t takes pages t, t + 512, ...;
-// one pass loads every head's (c, v, zb) of a batch of its pages at once and accumulates, per
-// head, the token-weighted sums of (c - c0), (c - c0)^2 and v in float, c0 being the head's
-// first-page centre (so the variance of c is sum (c - c0)^2 / N - (sum (c - c0) / N)^2 with
-// little cancellation: the centres spread over a few standard deviations), and the first
-// maximum of zb; one block reduction; a warp per head solves tau_hat; then the kept pages,
-// ascending: each warp ballots its own run of pages, one block scan of the warps' counts, then
-// each writes its run's. G: the group's query heads (1 to 8).
-// (FP64 is scarce on this part: double sums here cost more than the rest of the kernel.)
+// A cluster of kSelCluster CTAs per (sequence, KV head) group, each over its own range of the
+// group's pages. Each CTA loads every head's (c, v, zb) of its pages (a batch of pages per
+// thread at once) and accumulates, per head, the token-weighted sums of (c - c0), (c - c0)^2
+// and v in float, c0 being the head's first-page centre (so the variance of c is
+// sum (c - c0)^2 / N - (sum (c - c0) / N)^2 with little cancellation: the centres spread over
+// a few standard deviations), and the first maximum of zb. The CTAs' sums are added in rank
+// order through distributed shared memory, so every CTA holds the same totals and a warp per
+// head solves the same tau_hat in each. Each CTA then counts its kept pages; the counts of the
+// lower ranks (again through distributed shared memory) give its offset, and it writes its
+// kept pages, ascending, by warp ballots over contiguous runs. G: the group's query heads (1
+// to 8). (FP64 is scarce on this part: double sums here cost more than the rest.)
 template <int G>
-__global__ void __launch_bounds__(kESelThreads)
+__global__ void __launch_bounds__(kSelThreads)
 entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int Hkv,
                      int table_stride, const float* __restrict__ zb,
                      const float* __restrict__ cz, const float* __restrict__ vz, int stride,
                      int k_max, int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt,
                      float* __restrict__ tau_hat, DevCtx ctx) {
-  constexpr int NW = kESelThreads / 32;
-  constexpr int U = G <= 4 ? 2 : 1;              // pages per thread per batch
+  constexpr int NW = kSelThreads / 32;
+  constexpr int U = G <= 4 ? 4 : 2;              // pages per thread per batch
   static_assert(G >= 1 && G <= 8 && G <= NW, "group size");
-  __shared__ float s_sum[3][G][NW];
-  __shared__ float s_bv[G][NW];
-  __shared__ int s_bi[G][NW];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  __shared__ float s_wsum[3][G][NW];
+  __shared__ float s_wbest[G][NW];
+  __shared__ int s_wbi[G][NW];
+  __shared__ float s_part[3 * G];                // this CTA's sums (read by the cluster)
+  __shared__ float s_best[G];
+  __shared__ int s_bidx[G];
   __shared__ float s_tau[G];
-  __shared__ float s_c0[G];
   __shared__ int s_arg[G];
-  __shared__ uint32_t s_wsum[NW];
+  __shared__ float s_c0[G];
   __shared__ uint32_t s_bal[NW][kSelSteps];
+  __shared__ int s_wcnt[NW];
+  __shared__ int s_cnt;                          // this CTA's kept pages (read by the cluster)
   pdl_trigger();
   pdl_wait();
-  const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  const int g = blockIdx.y, b = blockIdx.z, tid = threadIdx.x, lane = tid & 31;
   const int warp = tid >> 5;
   int len = seq_lens[b];
   if (len < 0 || len > table_stride * PS) {
-    if (tid == 0) flag(ctx, KV_DEVERR_BAD_LEN);
+    if (tid == 0 && rank == 0) flag(ctx, KV_DEVERR_BAD_LEN);
     len = len < 0 ? 0 : table_stride * PS;
   }
   const int n = ceil_div(len, PS);
   const long grp = (long)b * Hkv + g;
   const long row0 = ((long)b * Hq + g * G) * stride;     // head h of the group: row0 + h*stride
-  if (n == 0) {
-    if (tid == 0) sel_cnt[grp] = 0;
-    if (tid < G && tau_hat != nullptr)
-      tau_hat[(long)b * Hq + g * G + tid] = __int_as_float(0x7fc00000);
+  if (n == 0) {                                  // every CTA of the cluster returns here
+    if (rank == 0) {
+      if (tid == 0) sel_cnt[grp] = 0;
+      if (tid < G && tau_hat != nullptr)
+        tau_hat[(long)b * Hq + g * G + tid] = __int_as_float(0x7fc00000);
+    }
     return;
   }
-  // one pass: every head's sums and first maximum
-  float s1[G], s2[G], sv[G], c0[G];
-  float best[G];
-  int besti[G];
+  const int PC = ceil_div(n, CL);
+  const int p_begin = min(n, rank * PC), p_end = min(n, p_begin + PC);
+  if (tid < G) s_c0[tid] = __ldg(cz + row0 + (long)tid * stride);   // page 0
+  __syncthreads();
+  float c0[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) c0[h] = __ldg(cz + row0 + (long)h * stride);   // page 0
-  if (tid < G) s_c0[tid] = __ldg(cz + row0 + (long)tid * stride);
+  for (int h = 0; h < G; ++h) c0[h] = s_c0[h];
+  // one pass over this CTA's pages: every head's sums and first maximum
+  float s1[G], s2[G], sv[G], best[G];
+  int besti[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     s1[h] = s2[h] = sv[h] = 0.f;
     best[h] = -INFINITY;
     besti[h] = 0x7fffffff;
   }
-  for (int base = 0; base < n; base += kESelThreads * U) {
+  for (int base = p_begin; base < p_end; base += kSelThreads * U) {
     float cv[G][U], vv[G][U], zv[G][U];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int p = base + u * kESelThreads + tid;
-        const bool in = p < n;
+        const int p = base + u * kSelThreads + tid;
+        const bool in = p < p_end;
         const long i = row0 + (long)h * stride + p;
         cv[h][u] = in ? cz[i] : 0.f;
         vv[h][u] = in ? vz[i] : 0.f;
@@ -281,8 +305,8 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int p = base + u * kESelThreads + tid;
-      if (p < n) {
+      const int p = base + u * kSelThreads + tid;
+      if (p < p_end) {
         const float wt = (float)min(PS, len - p * PS);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -297,33 +321,31 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
   }
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        s1[h] += __shfl_xor_sync(0xffffffffu, s1[h], o);
-        s2[h] += __shfl_xor_sync(0xffffffffu, s2[h], o);
-        sv[h] += __shfl_xor_sync(0xffffffffu, sv[h], o);
-        const float ov = __shfl_xor_sync(0xffffffffu, best[h], o);
-        const int oi = __shfl_xor_sync(0xffffffffu, besti[h], o);
-        if (ov > best[h] || (ov == best[h] && oi < besti[h])) { best[h] = ov; besti[h] = oi; }
-      }
-      if (lane == 0) {
-        s_sum[0][h][warp] = s1[h];
-        s_sum[1][h][warp] = s2[h];
-        s_sum[2][h][warp] = sv[h];
-        s_bv[h][warp] = best[h];
-        s_bi[h][warp] = besti[h];
-      }
+    for (int o = 16; o > 0; o >>= 1) {
+      s1[h] += __shfl_xor_sync(0xffffffffu, s1[h], o);
+      s2[h] += __shfl_xor_sync(0xffffffffu, s2[h], o);
+      sv[h] += __shfl_xor_sync(0xffffffffu, sv[h], o);
+      const float ov = __shfl_xor_sync(0xffffffffu, best[h], o);
+      const int oi = __shfl_xor_sync(0xffffffffu, besti[h], o);
+      if (ov > best[h] || (ov == best[h] && oi < besti[h])) { best[h] = ov; besti[h] = oi; }
+    }
+    if (lane == 0) {
+      s_wsum[0][h][warp] = s1[h];
+      s_wsum[1][h][warp] = s2[h];
+      s_wsum[2][h][warp] = sv[h];
+      s_wbest[h][warp] = best[h];
+      s_wbi[h][warp] = besti[h];
     }
   }
   __syncthreads();
-  if (warp < G) {                                // warp h: head h's moments and tau_hat
+  if (warp < G) {                                // warp h: this CTA's sums for head h
     const int h = warp;
     const bool lv = lane < NW;
-    float a1 = lv ? s_sum[0][h][lane] : 0.f, a2 = lv ? s_sum[1][h][lane] : 0.f;
-    float av = lv ? s_sum[2][h][lane] : 0.f;
-    float bv = lv ? s_bv[h][lane] : -INFINITY;
-    int bi = lv ? s_bi[h][lane] : 0x7fffffff;
+    float a1 = lv ? s_wsum[0][h][lane] : 0.f, a2 = lv ? s_wsum[1][h][lane] : 0.f;
+    float av = lv ? s_wsum[2][h][lane] : 0.f;
+    float bv = lv ? s_wbest[h][lane] : -INFINITY;
+    int bi = lv ? s_wbi[h][lane] : 0x7fffffff;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       a1 += __shfl_xor_sync(0xffffffffu, a1, o);
@@ -333,59 +355,86 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
     }
+    if (lane == 0) {
+      s_part[3 * h] = a1;
+      s_part[3 * h + 1] = a2;
+      s_part[3 * h + 2] = av;
+      s_best[h] = bv;
+      s_bidx[h] = bi;
+    }
+  }
+  cluster.sync();                                // every CTA's sums are final
+  if (warp < G) {                                // warp h: the group's totals, rank order
+    const int h = warp;
+    float a1 = 0.f, a2 = 0.f, av = 0.f, bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int rk = 0; rk < CL; ++rk) {
+      const float* part = cluster.map_shared_rank(s_part, rk);
+      a1 += part[3 * h];
+      a2 += part[3 * h + 1];
+      av += part[3 * h + 2];
+      const float ob = cluster.map_shared_rank(s_best, rk)[h];
+      const int oi = cluster.map_shared_rank(s_bidx, rk)[h];
+      if (ob > bv || (ob == bv && oi < bi)) { bv = ob; bi = oi; }
+    }
     const float N = (float)len;
     const float m1 = a1 / N;                     // mean of c - c0
     const float var = fmaxf(a2 / N - m1 * m1, 0.f) + av / N;
-    const float t = gaussian_threshold(s_c0[h] + m1, var, N);
+    const float t = gaussian_threshold(c0[h] + m1, var, N);
     if (lane == 0) {
       s_tau[h] = t;
       s_arg[h] = bi;
-      if (tau_hat != nullptr) tau_hat[(long)b * Hq + g * G + h] = t;
+      if (tau_hat != nullptr && rank == 0) tau_hat[(long)b * Hq + g * G + h] = t;
     }
   }
   __syncthreads();
-  // kept pages, ascending. Warp w owns a contiguous run of each super-chunk of pages (32 pages
-  // a step, coalesced loads, several steps' loads in flight); its ballots go to shared memory
-  // and its count to one block scan, and then it writes its kept pages from its offset.
-  constexpr int SB = G <= 4 ? 8 : 4;            // steps whose loads are in flight together
-  int carry = 0;
+  auto kept_page = [&](int p) -> bool {
+    bool keep = false;
+#pragma unroll
+    for (int h = 0; h < G; ++h) keep |= zb[row0 + (long)h * stride + p] > s_tau[h] || p == s_arg[h];
+    return keep;
+  };
+  int mine = 0;
+  for (int p = p_begin + tid; p < p_end; p += kSelThreads) mine += kept_page(p) ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) s_wcnt[warp] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    int c = 0;
+    for (int w = 0; w < NW; ++w) c += s_wcnt[w];
+    s_cnt = c;
+  }
+  cluster.sync();                                // every CTA's count is final
+  int carry = 0, total_all = 0;
+  for (int rk = 0; rk < CL; ++rk) {
+    const int c = *cluster.map_shared_rank(&s_cnt, rk);
+    carry += rk < rank ? c : 0;
+    total_all += c;
+  }
+  // this CTA's kept pages from its offset: warp-contiguous runs, 32 pages a ballot
   int32_t* out = sel_idx + grp * k_max;
-  for (int c0p = 0; c0p < n; c0p += NW * 32 * kSelSteps) {
-    const int c1p = min(n, c0p + NW * 32 * kSelSteps);
-    const int PW = ceil_div(c1p - c0p, NW * 32) * 32;     // pages per warp
-    const int w0 = c0p + warp * PW, w1 = min(c1p, w0 + PW);
-    const int steps = PW / 32;
+  for (int c0p = p_begin; c0p < p_end; c0p += NW * 32 * kSelSteps) {
+    const int c1p = min(p_end, c0p + NW * 32 * kSelSteps);
+    const int pw = ceil_div(c1p - c0p, NW * 32) * 32;     // pages per warp
+    const int w0 = c0p + warp * pw, w1 = min(c1p, w0 + pw);
+    const int st_n = pw / 32;
     int wcount = 0;
-    for (int st = 0; st < steps; st += SB) {
-      float zv[SB][G];
-#pragma unroll
-      for (int k = 0; k < SB; ++k) {
-        const int p = w0 + (st + k) * 32 + lane;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          zv[k][h] = st + k < steps && p < w1 ? zb[row0 + (long)h * stride + p] : -INFINITY;
-      }
-#pragma unroll
-      for (int k = 0; k < SB; ++k) {
-        const int p = w0 + (st + k) * 32 + lane;
-        bool keep = false;
-#pragma unroll
-        for (int h = 0; h < G; ++h) keep |= zv[k][h] > s_tau[h] || p == s_arg[h];
-        keep = keep && st + k < steps && p < w1;
-        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-        if (st + k < steps && lane == 0) s_bal[warp][st + k] = bal;
-        wcount += __popc(bal);
-      }
+    for (int st = 0; st < st_n; ++st) {
+      const int p = w0 + st * 32 + lane;
+      const uint32_t bal = __ballot_sync(0xffffffffu, p < w1 && kept_page(p));
+      if (lane == 0) s_bal[warp][st] = bal;
+      wcount += __popc(bal);
     }
-    if (lane == 0) s_wsum[warp] = (uint32_t)wcount;
+    __syncthreads();                             // earlier readers of s_wcnt are done
+    if (lane == 0) s_wcnt[warp] = wcount;
     __syncthreads();
     int at = carry, total = 0;
-#pragma unroll
     for (int w = 0; w < NW; ++w) {
-      at += w < warp ? (int)s_wsum[w] : 0;
-      total += (int)s_wsum[w];
+      at += w < warp ? s_wcnt[w] : 0;
+      total += s_wcnt[w];
     }
-    for (int st = 0; st < steps; ++st) {
+    for (int st = 0; st < st_n; ++st) {
       const uint32_t bal = s_bal[warp][st];
       if ((bal >> lane) & 1u) {
         const int pos = at + __popc(bal & ((1u << lane) - 1u));
@@ -394,12 +443,12 @@ entmax_select_kernel(const int32_t* __restrict__ seq_lens, int PS, int Hq, int H
       at += __popc(bal);
     }
     carry += total;
-    __syncthreads();                             // s_bal and s_wsum are reused
   }
-  if (tid == 0) {
-    if (carry > k_max) flag(ctx, KV_DEVERR_KEEP);
-    sel_cnt[grp] = min(carry, k_max);
+  if (rank == 0 && tid == 0) {
+    if (total_all > k_max) flag(ctx, KV_DEVERR_KEEP);
+    sel_cnt[grp] = min(total_all, k_max);
   }
+  cluster.sync();                                // no CTA leaves while another reads its memory
 }
 
 // ------------------------------------------------------------------------------ threshold
@@ -1225,12 +1274,16 @@ entmax_out_kernel(kv_cache_desc d, int G, const int32_t* __restrict__ sel_cnt, i
 
 template <typename T, int D, int G>
 cudaError_t moments_t(const kv_cache_desc& d, const void* q, const void* stats, float scale,
-                      float* zb, float* cz, float* vz, int stride, DevCtx ctx, cudaStream_t s) {
-  dim3 grid(ceil_div(d.page_table_stride, kMomWarps * mom_rounds(G) * 4), d.num_kv_heads,
-            d.batch);
+                      float* zb, float* cz, float* vz, int stride, int sms, DevCtx ctx,
+                      cudaStream_t s) {
+  // rounds per warp: at least 2, and enough that the grid is about one wave
+  const long rows = (long)d.page_table_stride * d.num_kv_heads * d.batch;
+  const long slots = (long)mom_blocks<T, G>() * (sms > 0 ? sms : 1) * kMomWarps * 4;
+  const int rpw = (int)std::max(2L, (rows + slots - 1) / slots);
+  dim3 grid(ceil_div(d.page_table_stride, kMomWarps * rpw * 4), d.num_kv_heads, d.batch);
   return launch_pdl(entmax_moments_kernel<T, D, G>, grid, dim3(kMomWarps * 32), 0, s, d,
                     static_cast<const T*>(q), static_cast<const T*>(stats), 0.5f * scale, zb,
-                    cz, vz, stride, ctx);
+                    cz, vz, stride, rpw, ctx);
 }
 
 template <typename T, int D, int G>
@@ -1274,9 +1327,9 @@ cudaError_t out_t(const kv_cache_desc& d, int G, const int32_t* sel, const int32
 
 template <typename T, int D>
 cudaError_t moments_d(const kv_cache_desc& d, int G, const void* q, const void* stats,
-                      float scale, float* zb, float* cz, float* vz, int stride, DevCtx ctx,
-                      cudaStream_t s) {
-#define SKV_CALL(GG) moments_t<T, D, GG>(d, q, stats, scale, zb, cz, vz, stride, ctx, s)
+                      float scale, float* zb, float* cz, float* vz, int stride, int sms,
+                      DevCtx ctx, cudaStream_t s) {
+#define SKV_CALL(GG) moments_t<T, D, GG>(d, q, stats, scale, zb, cz, vz, stride, sms, ctx, s)
   SKV_G_SWITCH(SKV_CALL)
 #undef SKV_CALL
 }
@@ -1305,24 +1358,38 @@ cudaError_t attn_d(const kv_cache_desc& d, int G, const void* q, float scale, co
 
 cudaError_t launch_entmax_moments(const kv_cache_desc& d, int G, const void* q,
                                   const void* stats, float scale, float* zb, float* cz,
-                                  float* vz, int stride, DevCtx ctx, cudaStream_t s) {
+                                  float* vz, int stride, int sms, DevCtx ctx, cudaStream_t s) {
   const bool bf = d.dtype == KV_BF16;
   if (d.head_dim == 128)
-    return bf ? moments_d<bf16_t, 128>(d, G, q, stats, scale, zb, cz, vz, stride, ctx, s)
-              : moments_d<float, 128>(d, G, q, stats, scale, zb, cz, vz, stride, ctx, s);
-  return bf ? moments_d<bf16_t, 64>(d, G, q, stats, scale, zb, cz, vz, stride, ctx, s)
-            : moments_d<float, 64>(d, G, q, stats, scale, zb, cz, vz, stride, ctx, s);
+    return bf ? moments_d<bf16_t, 128>(d, G, q, stats, scale, zb, cz, vz, stride, sms, ctx, s)
+              : moments_d<float, 128>(d, G, q, stats, scale, zb, cz, vz, stride, sms, ctx, s);
+  return bf ? moments_d<bf16_t, 64>(d, G, q, stats, scale, zb, cz, vz, stride, sms, ctx, s)
+            : moments_d<float, 64>(d, G, q, stats, scale, zb, cz, vz, stride, sms, ctx, s);
 }
 
 cudaError_t launch_entmax_select(const int32_t* seq_lens, int page_size, int batch, int Hq,
                                  int Hkv, int table_stride, const float* zb, const float* cz,
                                  const float* vz, int stride, int k_max, int32_t* sel_idx,
                                  int32_t* sel_cnt, float* tau_hat, DevCtx ctx, cudaStream_t s) {
-  dim3 grid(Hkv, batch);
-#define SKV_ESEL(GG)                                                                          \
-  return launch_pdl(entmax_select_kernel<GG>, grid, dim3(kESelThreads), 0, s, seq_lens,        \
-                    page_size, Hq, Hkv, table_stride, zb, cz, vz, stride, k_max, sel_idx,       \
-                    sel_cnt, tau_hat, ctx)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSelCluster, Hkv, batch);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSelCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e;
+#define SKV_ESEL(GG)                                                                           \
+  e = cudaLaunchKernelEx(&cfg, entmax_select_kernel<GG>, seq_lens, page_size, Hq, Hkv,         \
+                         table_stride, zb, cz, vz, stride, k_max, sel_idx, sel_cnt, tau_hat,    \
+                         ctx);                                                                 \
+  break
   switch (Hq / Hkv) {
     case 1: SKV_ESEL(1);
     case 2: SKV_ESEL(2);
@@ -1335,6 +1402,7 @@ cudaError_t launch_entmax_select(const int32_t* seq_lens, int page_size, int bat
     default: return cudaErrorInvalidValue;
   }
 #undef SKV_ESEL
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int entmax_max_splits() { return kMaxEntSplits; }

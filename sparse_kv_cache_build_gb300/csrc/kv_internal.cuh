@@ -227,7 +227,7 @@ cudaError_t launch_page_stats(const kv_cache_desc& d, void* stats, int8_t* stats
 // out [B][Hq][D] and tau [B][Hq] (in z = logit/2 units).
 cudaError_t launch_entmax_moments(const kv_cache_desc& d, int G, const void* q,
                                   const void* stats, float scale, float* zb, float* cz,
-                                  float* vz, int stride, DevCtx ctx, cudaStream_t s);
+                                  float* vz, int stride, int sms, DevCtx ctx, cudaStream_t s);
 cudaError_t launch_entmax_select(const int32_t* seq_lens, int page_size, int batch, int Hq,
                                  int Hkv, int table_stride, const float* zb, const float* cz,
                                  const float* vz, int stride, int k_max, int32_t* sel_idx,

@@ -74,7 +74,20 @@ def test_page_moments_match_oracle(dtype, D, G, PS):
 
 @pytest.mark.parametrize("dtype,D,G,PS", SHAPES)
 def test_select_is_the_oracle_rule_on_gpu_moments(dtype, D, G, PS):
-    w, c = make(dtype, D, G, PS, lens=(1000, 2049, 37, 0, 5))
+    check_select_rule(*make(dtype, D, G, PS, lens=(1000, 2049, 37, 0, 5)), G, PS)
+
+
+@pytest.mark.parametrize("lens", [(70003, 33000, 5, 0), (16 * 4096 * 4 + 9,)],
+                         ids=["4376_pages", "16385_pages"])
+def test_select_over_a_cluster_of_ctas_is_the_oracle_rule(lens):
+    """Long tables: every CTA of a group's cluster holds hundreds to thousands of pages (sums
+    added in rank order, kept pages placed by the lower ranks' counts, several ballot passes
+    in a CTA)."""
+    w, c = make("bf16", 128, 4, 16, lens=lens, seed=46, Hkv=2, planted=8)
+    check_select_rule(w, c, 4, 16)
+
+
+def check_select_rule(w, c, G, PS):
     kv = skv.PagedKV.from_cache(c)
     stats = skv.kv_build_page_stats(kv)
     zb, cz, vz = skv.kv_entmax_page_moments(kv, c.q, stats, w.sm_scale)
