@@ -122,16 +122,20 @@ entmax_moments_kernel(kv_cache_desc d, const T* __restrict__ q, const T* __restr
   pdl_wait();
   const int b = blockIdx.z, g = blockIdx.y, tid = threadIdx.x;
   const int Hkv = d.num_kv_heads, Hq = Hkv * G;
+  const int warp = tid >> 5, lane = tid & 31, j = lane & 7;
+  const int p_block = blockIdx.x * kMomWarps * rpw * 4;
+  const int p0 = p_block + warp * rpw * 4 + (lane >> 3);
+  const int32_t* trow = d.page_table + (long)b * d.page_table_stride;
+  // the first round's page-table entry before the length (it lies in the table's row either
+  // way and is used only below the length), so the two loads are in flight together
+  const int P0 = p0 < d.page_table_stride ? __ldg(trow + p0) : -1;
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
-  const int p_block = blockIdx.x * kMomWarps * rpw * 4;
   if (p_block >= n_pages) return;
-  const int warp = tid >> 5, lane = tid & 31, j = lane & 7;
-  const int p0 = p_block + warp * rpw * 4 + (lane >> 3);
   auto load = [&](int r, uint4 (&rmn)[NU], uint4 (&rmx)[NU]) -> bool {
     const int p = p0 + 4 * r;
     if (r >= rpw || p >= n_pages) return false;
-    const int P = d.page_table[(long)b * d.page_table_stride + p];
+    const int P = r == 0 ? P0 : trow[p];
     if (P < 0 || P >= d.num_phys_pages) {
       if (j == 0) flag(ctx, KV_DEVERR_BAD_PAGE);
       return false;

@@ -67,15 +67,32 @@ constexpr int kSelWarps = 16;                          // score + select blocks:
 constexpr int kSelThreads = kSelWarps * 32;
 constexpr int kSelCandWords = 4096;                    // gathered keys of the threshold bin
 
+// This lane's page of block `chunk` (its row of the page table, whatever the length).
+template <int WARPS, bool F8>
+__device__ __forceinline__ int score_page(int chunk) {
+  constexpr int RPW = rows_per_warp<F8>();
+  return chunk * WARPS * RPW + (threadIdx.x >> 5) * RPW + (threadIdx.x & 31) / (32 / RPW);
+}
+
+// The page-table entry of this lane's page, loaded before the sequence length is known (the
+// entry lies in the table's row whatever the length; it is used only below the length), so
+// the two loads are in flight together.
+template <int WARPS, bool F8>
+__device__ __forceinline__ int score_table_entry(const kv_cache_desc& d, int b, int chunk) {
+  const int p = score_page<WARPS, F8>(chunk);
+  return p < d.page_table_stride ? __ldg(d.page_table + (long)b * d.page_table_stride + p) : -1;
+}
+
 // Scores of the WARPS*4 pages of this block for group (b, g) into scores; returns false
-// (block-uniform) if the block has no page of the sequence. F8: stats are E4M3 bytes with
-// one exponent per row in stats_exp; otherwise stats are of the query's type T.
+// (block-uniform) if the block has no page of the sequence. P_lane: this lane's page-table
+// entry (score_table_entry). F8: stats are E4M3 bytes with one exponent per row in
+// stats_exp; otherwise stats are of the query's type T.
 template <typename T, int D, int WARPS, bool F8>
 __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __restrict__ q,
                                             int G, const void* __restrict__ stats,
                                             const int8_t* __restrict__ stats_exp, float* w,
                                             float* __restrict__ scores, int scores_stride,
-                                            int b, int g, int chunk, int n_pages,
+                                            int b, int g, int chunk, int n_pages, int P_lane,
                                             const DevCtx& ctx) {
   constexpr int EB = F8 ? 1 : ElemTraits<T>::bytes;   // bytes per statistic
   constexpr int EPC = 16 / EB;                // elements per 16-byte chunk
@@ -93,7 +110,7 @@ __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __r
   bool ok = false;
   int row_exp = 0;
   if (p < n_pages) {
-    const int P = d.page_table[(long)b * d.page_table_stride + p];
+    const int P = P_lane;
     if (P >= 0 && P < d.num_phys_pages) {
       ok = true;
       const uint4* row = reinterpret_cast<const uint4*>(
@@ -147,10 +164,11 @@ score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const void* __rest
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.z, g = blockIdx.y, chunk = blockIdx.x;
+  const int P_lane = score_table_entry<kScoreWarps, F8>(d, b, chunk);
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
   score_block<T, D, kScoreWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b, g,
-                                     chunk, n_pages, ctx);
+                                     chunk, n_pages, P_lane, ctx);
 }
 
 // Shared words for the keys of a group of up to max_pages pages (cta_topk.cuh).
@@ -178,6 +196,7 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   pdl_wait();
   const int b = blockIdx.z, tid = threadIdx.x;
   const int g = blockIdx.y, chunk = blockIdx.x;
+  const int P_lane = score_table_entry<kSelWarps, F8>(d, b, chunk);
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
   const long grp = (long)b * d.num_kv_heads + g;
@@ -186,7 +205,7 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
     return;
   }
   if (!score_block<T, D, kSelWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b,
-                                        g, chunk, n_pages, ctx))
+                                        g, chunk, n_pages, P_lane, ctx))
     return;
 
   // ---- the group's last block selects -----------------------------------------------------
