@@ -16,11 +16,12 @@
 // its contiguous stats row with that vector.
 //
 // The pass streams the stats array (2*D elements per page and KV head) once: it is
-// HBM-bound, and short, so it is built to put every load in flight in one wave. Eight lanes
-// own one page (16-byte chunks j, j+8, ... of the row), a 128-thread block covers 16 pages,
-// and the grid covers every page of every group. Each block issues its page-table and
-// statistics loads first and only then builds Pos/Neg from q, so the two latency chains
-// overlap.
+// HBM-bound, and short, so it is built to put every load in flight in about one wave. Eight
+// lanes own one page (16-byte chunks j, j+8, ... of the row), a 128-thread block covers runs
+// of 16 pages (one run, or as many as keep the grid to about 8 blocks per SM, the next run's
+// loads in flight while a run is summed), and the grid covers every page of every group.
+// Each block issues its first page-table load before the sequence length, then its
+// statistics loads, and only then builds Pos/Neg from q, so the latency chains overlap.
 //
 // score_select_kernel is the same pass followed by the group's top-k (the rule of
 // select.cu): 512-thread blocks of 64 pages each; the block of a group that finishes last
@@ -35,6 +36,9 @@
 // scaling commutes with the fp32 rounding of the sum, so this equals summing the decoded
 // values times 2^e).
 #include <cuda_fp8.h>
+
+#include <algorithm>
+#include <atomic>
 
 #include "cta_topk.cuh"
 #include "fp8_stats.cuh"
@@ -67,61 +71,68 @@ constexpr int kSelWarps = 16;                          // score + select blocks:
 constexpr int kSelThreads = kSelWarps * 32;
 constexpr int kSelCandWords = 4096;                    // gathered keys of the threshold bin
 
-// This lane's page of block `chunk` (its row of the page table, whatever the length).
+// This lane's first page of block `chunk` (a block takes `rounds` runs of WARPS * RPW pages;
+// the page lies in the table's row whatever the length).
 template <int WARPS, bool F8>
-__device__ __forceinline__ int score_page(int chunk) {
+__device__ __forceinline__ int score_page(int chunk, int rounds) {
   constexpr int RPW = rows_per_warp<F8>();
-  return chunk * WARPS * RPW + (threadIdx.x >> 5) * RPW + (threadIdx.x & 31) / (32 / RPW);
+  return chunk * WARPS * RPW * rounds + (threadIdx.x >> 5) * RPW + (threadIdx.x & 31) / (32 / RPW);
 }
 
-// The page-table entry of this lane's page, loaded before the sequence length is known (the
-// entry lies in the table's row whatever the length; it is used only below the length), so
-// the two loads are in flight together.
+// The page-table entry of this lane's first page, loaded before the sequence length is known
+// (the entry lies in the table's row whatever the length; it is used only below the length),
+// so the two loads are in flight together.
 template <int WARPS, bool F8>
-__device__ __forceinline__ int score_table_entry(const kv_cache_desc& d, int b, int chunk) {
-  const int p = score_page<WARPS, F8>(chunk);
+__device__ __forceinline__ int score_table_entry(const kv_cache_desc& d, int b, int chunk,
+                                                 int rounds) {
+  const int p = score_page<WARPS, F8>(chunk, rounds);
   return p < d.page_table_stride ? __ldg(d.page_table + (long)b * d.page_table_stride + p) : -1;
 }
 
-// Scores of the WARPS*4 pages of this block for group (b, g) into scores; returns false
-// (block-uniform) if the block has no page of the sequence. P_lane: this lane's page-table
-// entry (score_table_entry). F8: stats are E4M3 bytes with one exponent per row in
-// stats_exp; otherwise stats are of the query's type T.
+// Scores of this block's pages for group (b, g) into scores: `rounds` runs of WARPS * RPW
+// pages, the next run's loads in flight while a run is summed. Returns false (block-uniform)
+// if the block has no page of the sequence. P_lane: this lane's first page-table entry
+// (score_table_entry). F8: stats are E4M3 bytes with one exponent per row in stats_exp;
+// otherwise stats are of the query's type T.
 template <typename T, int D, int WARPS, bool F8>
 __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __restrict__ q,
                                             int G, const void* __restrict__ stats,
                                             const int8_t* __restrict__ stats_exp, float* w,
                                             float* __restrict__ scores, int scores_stride,
-                                            int b, int g, int chunk, int n_pages, int P_lane,
-                                            const DevCtx& ctx) {
+                                            int b, int g, int chunk, int rounds, int n_pages,
+                                            int P_lane, const DevCtx& ctx) {
   constexpr int EB = F8 ? 1 : ElemTraits<T>::bytes;   // bytes per statistic
   constexpr int EPC = 16 / EB;                // elements per 16-byte chunk
   constexpr int RPW = rows_per_warp<F8>();
   constexpr int LPR = 32 / RPW;               // lanes per row
   constexpr int CPL = (2 * D * EB / 16) / LPR;  // chunks per lane per stats row
-  const int p_block = chunk * WARPS * RPW;
+  constexpr int SPAN = WARPS * RPW;           // pages of one run
+  const int p_block = chunk * SPAN * rounds;
   if (p_block >= n_pages) return false;
 
   const int Hkv = d.num_kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, j = lane % LPR;
-  const int p = p_block + warp * RPW + grp;
-  uint4 raw[CPL];
-  bool ok = false;
-  int row_exp = 0;
-  if (p < n_pages) {
-    const int P = P_lane;
-    if (P >= 0 && P < d.num_phys_pages) {
-      ok = true;
-      const uint4* row = reinterpret_cast<const uint4*>(
-          reinterpret_cast<const char*>(stats) + (((long)P * Hkv + g) * 2 * D) * EB);
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) raw[u] = __ldg(row + j + LPR * u);
-      if constexpr (F8) row_exp = __ldg(stats_exp + (long)P * Hkv + g);
-    } else if (j == 0) {
-      flag(ctx, KV_DEVERR_BAD_PAGE);
+  const int p0 = p_block + warp * RPW + grp;
+  const int32_t* trow = d.page_table + (long)b * d.page_table_stride;
+  auto load = [&](int r, uint4 (&raw)[CPL], int& row_exp) -> bool {
+    const int p = p0 + r * SPAN;
+    if (r >= rounds || p >= n_pages) return false;
+    const int P = r == 0 ? P_lane : trow[p];
+    if (P < 0 || P >= d.num_phys_pages) {
+      if (j == 0) flag(ctx, KV_DEVERR_BAD_PAGE);
+      return false;
     }
-  }
+    const uint4* row = reinterpret_cast<const uint4*>(
+        reinterpret_cast<const char*>(stats) + (((long)P * Hkv + g) * 2 * D) * EB);
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) raw[u] = __ldg(row + j + LPR * u);
+    if constexpr (F8) row_exp = __ldg(stats_exp + (long)P * Hkv + g);
+    return true;
+  };
+  uint4 raw[CPL], nraw[CPL];
+  int row_exp = 0, nrow_exp = 0;
+  bool ok = load(0, raw, row_exp);
 
   const int Hq = Hkv * G;
   for (int t = threadIdx.x; t < D; t += WARPS * 32) {
@@ -136,22 +147,29 @@ __device__ __forceinline__ bool score_block(const kv_cache_desc& d, const T* __r
   }
   __syncthreads();
 
-  float acc = 0.f;
-  if (ok) {
+  for (int r = 0; r < rounds && p_block + r * SPAN < n_pages; ++r) {   // block-uniform
+    const bool nok = load(r + 1, nraw, nrow_exp);
+    float acc = 0.f;
+    if (ok) {
 #pragma unroll
-    for (int u = 0; u < CPL; ++u) {
-      float f[EPC];
-      if constexpr (F8) fp8_chunk_to_f32(raw[u], f);
-      else chunk_to_f32<T>(raw[u], f);
-      const float* wc = w + (j + LPR * u) * EPC;
+      for (int u = 0; u < CPL; ++u) {
+        float f[EPC];
+        if constexpr (F8) fp8_chunk_to_f32(raw[u], f);
+        else chunk_to_f32<T>(raw[u], f);
+        const float* wc = w + (j + LPR * u) * EPC;
 #pragma unroll
-      for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
+        for (int e = 0; e < EPC; ++e) acc = fmaf(wc[e], f[e], acc);
+      }
     }
-  }
 #pragma unroll
-  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if constexpr (F8) acc *= fp8::pow2(row_exp);
-  if (j == 0 && ok) scores[((long)b * Hkv + g) * scores_stride + p] = acc;
+    for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if constexpr (F8) acc *= fp8::pow2(row_exp);
+    if (j == 0 && ok) scores[((long)b * Hkv + g) * scores_stride + p0 + r * SPAN] = acc;
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) raw[u] = nraw[u];
+    row_exp = nrow_exp;
+    ok = nok;
+  }
   return true;
 }
 
@@ -159,16 +177,16 @@ template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kScoreWarps * 32)
 score_kernel(kv_cache_desc d, const T* __restrict__ q, int G, const void* __restrict__ stats,
              const int8_t* __restrict__ stats_exp, float* __restrict__ scores,
-             int scores_stride, DevCtx ctx) {
+             int scores_stride, int rounds, DevCtx ctx) {
   __shared__ __align__(16) float w[2 * D];    // [Neg | Pos], matching a row's [mn | mx]
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.z, g = blockIdx.y, chunk = blockIdx.x;
-  const int P_lane = score_table_entry<kScoreWarps, F8>(d, b, chunk);
+  const int P_lane = score_table_entry<kScoreWarps, F8>(d, b, chunk, rounds);
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
   score_block<T, D, kScoreWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b, g,
-                                     chunk, n_pages, P_lane, ctx);
+                                     chunk, rounds, n_pages, P_lane, ctx);
 }
 
 // Shared words for the keys of a group of up to max_pages pages (cta_topk.cuh).
@@ -196,7 +214,7 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   pdl_wait();
   const int b = blockIdx.z, tid = threadIdx.x;
   const int g = blockIdx.y, chunk = blockIdx.x;
-  const int P_lane = score_table_entry<kSelWarps, F8>(d, b, chunk);
+  const int P_lane = score_table_entry<kSelWarps, F8>(d, b, chunk, 1);
   const int len = checked_len(ctx, d, b);
   const int n_pages = ceil_div(len, d.page_size);
   const long grp = (long)b * d.num_kv_heads + g;
@@ -205,7 +223,7 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
     return;
   }
   if (!score_block<T, D, kSelWarps, F8>(d, q, G, stats, stats_exp, w, scores, scores_stride, b,
-                                        g, chunk, n_pages, P_lane, ctx))
+                                        g, chunk, 1, n_pages, P_lane, ctx))
     return;
 
   // ---- the group's last block selects -----------------------------------------------------
@@ -253,15 +271,33 @@ score_select_kernel(kv_cache_desc d, const T* __restrict__ q, int G,
   cta_compact<kSelThreads>(K, thr, take_eq, wtot, 0, k, [&](int p, int pos) { out[pos] = p; });
 }
 
+// Multiprocessors of the current device (cached per device).
+int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 template <typename T, int D, bool F8>
 cudaError_t launch_t(const kv_cache_desc& d, const void* q, int Hq, const void* stats,
                      const int8_t* stats_exp, float* scores, int scores_stride, DevCtx ctx,
                      cudaStream_t s) {
-  dim3 grid(ceil_div(d.page_table_stride, kScoreWarps * rows_per_warp<F8>()), d.num_kv_heads,
-            d.batch);
+  // runs per block: one, or enough that the grid is about one wave of 8 blocks per SM
+  constexpr int SPAN = kScoreWarps * rows_per_warp<F8>();
+  const long rows = (long)d.page_table_stride * d.num_kv_heads * d.batch;
+  const long per_run = 8L * device_sms() * SPAN;
+  const int rounds = (int)std::max(1L, (rows + per_run - 1) / per_run);
+  dim3 grid(ceil_div(d.page_table_stride, SPAN * rounds), d.num_kv_heads, d.batch);
   return launch_pdl(score_kernel<T, D, F8>, grid, dim3(kScoreWarps * 32), 0, s, d,
                     static_cast<const T*>(q), Hq / d.num_kv_heads, stats, stats_exp, scores,
-                    scores_stride, ctx);
+                    scores_stride, rounds, ctx);
 }
 
 template <typename T, int D, bool F8>
