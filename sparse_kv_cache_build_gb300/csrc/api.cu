@@ -22,9 +22,9 @@ __device__ int32_t g_kv_error_word = 0;
 constexpr int kMaxDevices = 64;
 constexpr int kDroppedSplits = 64;          // page ranges per group in the dropped-mass probe
 // Longest group (pages) whose selection kv_decode_step leaves to the attention kernel's CTAs;
-// longer groups select once, in the score launch. Measured with the bulk-copied rows and
-// 11-bit digits: 70.8 against 81.0 us a step at 8192 pages (128K context), 81.1 against
-// 85.1 us at 16384 pages (1M context, page size 64).
+// longer groups select once, in the score launch. Measured with the bulk-copied rows, 11-bit
+// digits and the one-wave score pass: 70.8 against 88.3 us a step at 8192 pages (128K
+// context), 66.7 against 97.4 us at 16384 pages (1M context, page size 64).
 constexpr int kInAttnSelectPages = 16384;
 // Split count from which the step merges in a separate kernel (chained by programmatic
 // dependent launch) rather than in the attention kernel's last CTA per group. Measured on
