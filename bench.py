@@ -12,7 +12,7 @@ with its sparse and dense steps, FP8-statistics step, KV-window step, attention-
 roofline, byte bound, dropped mass and a bounded oracle baseline; and ``blocks``: the
 headline sparse/dense pair timed in fresh processes, with paired ratios and resampled
 intervals. ``e2e`` goes through the captured step (``kv_decode_step_graph_*``) with the
-query and output copied between pinned host memory and the device inside the timing.
+query taken from and the output returned to pinned host memory inside the timing.
 
 Prints one JSON line. ``--impl reference`` times the float64 CPU oracle on the same
 workload instead (the reference arm of this comparison).
@@ -971,8 +971,8 @@ def run_ours(args):
 
     # ---- end to end through the public API, host buffers, copies inside the timing -------
     # (1) the captured step (kv_decode_step_graph_*), the call a serving loop makes per token:
-    #     one launch copies the query in from pinned host memory, runs the step and copies
-    #     the output back to pinned host memory; then the host waits;
+    #     one launch runs the step, its kernels reading the query from and writing the output
+    #     to pinned host memory in place (the device addresses it); then the host waits;
     # (2) the same copies around a direct kv_decode_step call through the binding.
     q_host = c.q.detach().cpu().pin_memory()
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
@@ -1120,8 +1120,9 @@ def run_ours(args):
                        "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
                        "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
                        "api": "kv_decode_step_graph_launch (the step captured once by "
-                              "kv_decode_step_graph_create with the query's copy in from and "
-                              "the output's copy out to pinned host memory; host waits)",
+                              "kv_decode_step_graph_create with q_host and out_host, pinned "
+                              "host memory that the step's kernels read and write in place "
+                              "over the host link; host waits)",
                        "direct_call_us": round(statistics.median(e2e_direct_us), 3),
                        "direct_call_api": "kv_decode_step through the Python binding"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -403,8 +403,11 @@ size_t kv_decode_step_workspace_size(const kv_cache_desc* cache, int32_t num_q_h
  * then. The graph holds host and driver resources only; no device buffer is allocated.
  * q_host (host, page-locked, batch * num_q_heads * head_dim elements of the cache dtype)
  * and out_host (host, page-locked, batch * num_q_heads * head_dim float32) may be NULL;
- * when given, every launch first copies q_host into q and finally copies out into
- * out_host, so one launch per token carries the query in and the output back.
+ * when given, one launch per token carries the query in and the output back. A buffer the
+ * device addresses in place (page-locked memory under unified addressing, as
+ * cudaPointerGetAttributes reports) is read (q_host) or written (out_host) by the step's
+ * kernels themselves over the host link, and q (or out) is then not used; any other is
+ * copied: q_host into q before the step, out into out_host after it.
  */
 typedef struct kv_step_graph kv_step_graph;
 kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,

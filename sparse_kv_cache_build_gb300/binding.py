@@ -586,8 +586,9 @@ class DecodeStepGraph:
     def __init__(self, kv: PagedKV, q, sm_scale: float, stats=None, keep_ratio: float = 1.0,
                  budget_pages: int = 0, k_max: int | None = None, num_splits: int = 0,
                  out=None, lse=None, workspace=None, q_host=None, out_host=None):
-        """q_host / out_host: optional page-locked CPU tensors; each launch then copies
-        q_host into q first and the output into out_host last."""
+        """q_host / out_host: optional page-locked CPU tensors; each launch then takes the
+        query from q_host and leaves the output in out_host (read and written in place by the
+        kernels when the device addresses them, else copied through q and out)."""
         _need(q, "q", kv.dtype)
         for t, name in ((q_host, "q_host"), (out_host, "out_host")):
             if t is not None and (t.is_cuda or not t.is_pinned() or not t.is_contiguous()):
@@ -618,9 +619,11 @@ class DecodeStepGraph:
         self._handle = handle
 
     def launch(self, stream=None):
+        """Runs the step; returns (output, lse), the output being out_host when given."""
         _check("kv_decode_step_graph_launch",
                lib().kv_decode_step_graph_launch(self._handle, _stream(stream)))
-        return self.out, self.lse
+        out_host = self._keep[5]
+        return (out_host if out_host is not None else self.out), self.lse
 
     def close(self):
         if getattr(self, "_handle", None) is not None and self._handle.value is not None:

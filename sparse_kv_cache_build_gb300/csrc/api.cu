@@ -774,6 +774,25 @@ struct kv_step_graph {
   cudaGraphExec_t exec = nullptr;
 };
 
+}  // extern "C"
+
+namespace {
+
+// The device's address of a page-locked host buffer it can read and write in place (unified
+// addressing), or nullptr (then the buffer is reached by copies).
+void* mapped_device_ptr(const void* host) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();                          // not a CUDA pointer: clear the error
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
 kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
                                       int32_t num_q_heads, float sm_scale, const void* stats,
                                       double keep_ratio, int32_t budget_pages, int32_t k_max,
@@ -787,26 +806,34 @@ kv_status kv_decode_step_graph_create(const kv_cache_desc* cache, const void* q,
     return KV_ERR_INVALID_ARG;
   const size_t elems = (size_t)cache->batch * num_q_heads * cache->head_dim;
   const size_t q_bytes = elems * (cache->dtype == KV_BF16 ? 2 : 4);
+  // host buffers the device addresses in place are read and written by the kernels over the
+  // host link (no copy node); others are copied in and out around the step
+  const void* q_in = q_host != nullptr ? mapped_device_ptr(q_host) : nullptr;
+  float* out_to = out_host != nullptr ? static_cast<float*>(mapped_device_ptr(out_host)) : nullptr;
+  const void* q_step = q_in != nullptr ? q_in : q;
+  float* out_step = out_to != nullptr ? out_to : out;
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KV_ERR_CUDA;
   // one uncaptured call first: it checks the arguments and does every first-use set-up
   // (device state, kernel attributes, tensor maps) outside the capture
-  kv_status r = kv_decode_step(cache, q, num_q_heads, sm_scale, stats, keep_ratio, budget_pages, k_max,
-                     num_splits, out, lse, workspace, workspace_bytes, s);
+  kv_status r = kv_decode_step(cache, q_step, num_q_heads, sm_scale, stats, keep_ratio,
+                               budget_pages, k_max, num_splits, out_step, lse, workspace,
+                               workspace_bytes, s);
   if (r == KV_OK && cudaStreamSynchronize(s) != cudaSuccess) r = KV_ERR_CUDA;
   cudaGraph_t g = nullptr;
   if (r == KV_OK) {
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
       r = KV_ERR_CUDA;
     } else {
-      if (q_host != nullptr &&
+      if (q_host != nullptr && q_in == nullptr &&
           cudaMemcpyAsync(const_cast<void*>(q), q_host, q_bytes, cudaMemcpyHostToDevice, s) !=
               cudaSuccess)
         r = KV_ERR_CUDA;
       if (r == KV_OK)
-        r = kv_decode_step(cache, q, num_q_heads, sm_scale, stats, keep_ratio, budget_pages,
-                           k_max, num_splits, out, lse, workspace, workspace_bytes, s);
-      if (r == KV_OK && out_host != nullptr &&
+        r = kv_decode_step(cache, q_step, num_q_heads, sm_scale, stats, keep_ratio,
+                           budget_pages, k_max, num_splits, out_step, lse, workspace,
+                           workspace_bytes, s);
+      if (r == KV_OK && out_host != nullptr && out_to == nullptr &&
           cudaMemcpyAsync(out_host, out, elems * sizeof(float), cudaMemcpyDeviceToHost, s) !=
               cudaSuccess)
         r = KV_ERR_CUDA;

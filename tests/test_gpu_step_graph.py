@@ -62,8 +62,9 @@ def test_captured_step_rejects_bad_arguments_without_a_graph():
         skv.DecodeStepGraph(kv, c.q, -1.0, keep_ratio=1.0)        # non-positive scale
 
 
-def test_captured_step_with_host_copies():
-    """q_host copied in and the output copied out by the same launch."""
+def test_captured_step_with_host_buffers():
+    """The query taken from q_host and the output left in out_host by the same launch (page-
+    locked buffers: the kernels read and write them in place under unified addressing)."""
     w = workload(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, dtype="bf16",
                  seed=8, seq_lens=(3000,), planted=4)
     c = inputs.make_cache(w, "cuda")
