@@ -87,6 +87,66 @@ merge_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_
   }
 }
 
+// Up to 64 splits (the automatic split counts): every load is issued at once (each thread
+// its column of a quarter of the splits, each warp every split's (m, l)), each warp finds M
+// and L itself from its (m, l) with warp instructions, and one barrier joins the four
+// partial sums: one dependent memory round trip and one barrier.
+constexpr int kMergeShortSplits = 64;
+
+template <int D>
+__global__ void __launch_bounds__(D * kMergeParts)
+merge_kernel_short(const float* __restrict__ part_acc, const float* __restrict__ part_ml,
+                   int S, float* __restrict__ out, float* __restrict__ lse) {
+  constexpr int PER = kMergeShortSplits / kMergeParts;   // splits per thread at most
+  __shared__ float partial[kMergeParts][D];
+  pdl_trigger();
+  pdl_wait();
+  const long bh = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int d = tid % D, part = tid / D;
+  const float* ml = part_ml + bh * S * 2;
+  const float* a = part_acc + bh * S * D + d;
+  float av[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int sp = part + k * kMergeParts;
+    av[k] = sp < S ? __ldcg(a + (long)sp * D) : 0.f;
+  }
+  const float m0 = lane < S ? __ldcg(ml + 2 * lane) : -INFINITY;
+  const float m1 = lane + 32 < S ? __ldcg(ml + 2 * (lane + 32)) : -INFINITY;
+  const float l0 = lane < S ? __ldcg(ml + 2 * lane + 1) : 0.f;
+  const float l1 = lane + 32 < S ? __ldcg(ml + 2 * (lane + 32) + 1) : 0.f;
+  float M = fmaxf(m0, m1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (M == -INFINITY) {                          // every split empty (block-uniform)
+    if (part == 0) out[bh * D + d] = 0.f;
+    if (tid == 0 && lse != nullptr) lse[bh] = -INFINITY;
+    return;
+  }
+  const float w0 = m0 == -INFINITY ? 0.f : expf(m0 - M);
+  const float w1 = m1 == -INFINITY ? 0.f : expf(m1 - M);
+  float L = fmaf(l0, w0, l1 * w1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int sp = part + k * kMergeParts;                // block-uniform per k
+    const float ws = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+    if (sp < S) acc = fmaf(av[k], ws, acc);
+  }
+  partial[part][d] = acc;
+  __syncthreads();
+  if (part == 0) {
+    float A = 0.f;
+#pragma unroll
+    for (int p = 0; p < kMergeParts; ++p) A += partial[p][d];
+    out[bh * D + d] = A / L;
+    if (d == 0 && lse != nullptr) lse[bh] = M + logf(L);
+  }
+}
+
 // Fallback for more splits than the shared weight table holds: one thread per column.
 __global__ void merge_kernel_many(const float* __restrict__ part_acc,
                                   const float* __restrict__ part_ml, int S, int D,
@@ -122,6 +182,13 @@ cudaError_t launch_merge(const float* part_acc, const float* part_ml, int batch,
   if (num_splits > kMergeMaxSplits)
     return launch_pdl(merge_kernel_many, dim3(blocks), dim3(D), 0, s, part_acc, part_ml,
                       num_splits, D, out, lse);
+  if (num_splits <= kMergeShortSplits) {
+    if (D == 128)
+      return launch_pdl(merge_kernel_short<128>, dim3(blocks), dim3(128 * kMergeParts), 0, s,
+                        part_acc, part_ml, num_splits, out, lse);
+    return launch_pdl(merge_kernel_short<64>, dim3(blocks), dim3(64 * kMergeParts), 0, s,
+                      part_acc, part_ml, num_splits, out, lse);
+  }
   if (D == 128)
     return launch_pdl(merge_kernel<128>, dim3(blocks), dim3(128 * kMergeParts), 0, s,
                       part_acc, part_ml, num_splits, out, lse);
