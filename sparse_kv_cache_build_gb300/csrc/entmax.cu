@@ -657,11 +657,11 @@ __device__ __forceinline__ float2 tau_start(float lane_max, float zmax, int lane
 //
 // One CTA per (split, KV head, sequence) over its run of the attended pages, in chunks of
 // kChunkFloats / G tokens whose z values (all G heads) stay in shared memory. After each
-// chunk, a warp per head finds the chunk's own entmax threshold: the threshold of any subset of
-// a head's tokens is at most the full one (adding tokens only raises it), so a token at or
-// below it has weight zero. The tokens above it (less a rounding margin) are appended in list
+// chunk, a warp per head bounds the chunk's entmax threshold from below by the exact threshold
+// of its lanes' largest values: the threshold of any subset of a head's tokens is at most the
+// full one (adding tokens only raises it), so a token at or below it has weight zero. The tokens above it (less a rounding margin) are appended in list
 // order to the head's candidate list of this split, as (z, row of the token in the V pool);
-// the split's floor (its chunks' largest threshold, a lower bound on tau) and candidate count
+// the split's floor (its chunks' largest bound, a lower bound on tau) and candidate count
 // are written at the end. No logit goes to memory.
 
 constexpr int kMaxEntSplits = 1024;          // splits of the logits pass
@@ -681,7 +681,8 @@ struct ChunkLists {                          // a warp's heads: warp, warp + NW,
   }
 };
 
-// The chunk's candidates. s_z + h * zs: head h's n values (-inf for tokens past the sequence);
+// The chunk's candidates (tokens above the bound). s_z + h * zs: head h's n values (-inf for
+// tokens past the sequence);
 // token i of the chunk sits in physical page s_P[i / PS] (PS = 1 << ps_log2), KV head g;
 // cz/cs: the split's candidate region of head 0 of the group (head h at + h * cap_slots).
 template <int G, int NW>
@@ -699,9 +700,9 @@ __device__ void chunk_candidates(const float* s_z, int zs, int n, const int* s_P
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (m == -INFINITY) continue;
-    const float2 st = tau_start(lm, m, lane);
-    const float tc = warp_entmax_tau([&](int i) { return z[i]; }, n, st.x, st.y, lane);
-    const float thr = tc - 1e-5f * (fabsf(tc) + 1.f);
+    // the threshold of the lanes' largest values bounds the chunk's own from below (a subset
+    // of its tokens), and measured closer to it than the Newton passes are worth here
+    const float thr = tau_start(lm, m, lane).x;
     L.floor[j] = fmaxf(L.floor[j], thr);
     float* oz = cz + (long)h * cap_slots;
     uint32_t* os = cs + (long)h * cap_slots;
