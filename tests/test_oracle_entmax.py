@@ -196,6 +196,10 @@ def _one_page(q, mn, mx):
 
 
 def test_page_moments_golden():
+    check_page_moments_golden(E)
+
+
+def check_page_moments_golden(E):
     for case in json.load(open(GOLDEN))["moments"]:
         q, mn, mx, table, lens, PS = _one_page(case["q"], case["mn"], case["mx"])
         zb, c, v, nt = E.page_moments(q, mn, mx, table, lens, PS, case["scale"])
@@ -211,6 +215,10 @@ def test_page_moments_match_monte_carlo_uniform_keys(seed):
     variance of z = (scale/2) q.k land within six standard errors of c and v. The query's
     coordinates span 0.1 to 3 in magnitude with both signs and the box widths 0 to 3, so
     weighting by |q_d| or q_d, another divisor than 12, or (scale/2) unsquared all miss."""
+    check_page_moments_monte_carlo(E, seed)
+
+
+def check_page_moments_monte_carlo(E, seed):
     rng = np.random.default_rng(100 + seed)
     D = 12
     q = rng.choice([-1.0, 1.0], D) * rng.uniform(0.1, 3.0, D)
@@ -248,6 +256,10 @@ def _tau_by_quadrature(mu, sigma2, count):
 
 
 def test_entmax_select_golden_token_weighted_threshold():
+    check_select_golden(E)
+
+
+def check_select_golden(E):
     for case in json.load(open(GOLDEN))["select"]:
         G = case["G"]
         zb, c, v = (np.asarray(case[k], dtype=np.float64) for k in ("zb", "c", "v"))
@@ -264,6 +276,10 @@ def test_entmax_select_golden_token_weighted_threshold():
 def test_entmax_select_weights_pages_by_their_tokens():
     """Splitting a page into two half pages with the same box (same c and v, half the
     tokens each) changes nothing under token weighting; under page weighting it would."""
+    check_token_weighting(E)
+
+
+def check_token_weighting(E):
     rng = np.random.default_rng(9)
     n = 12
     c = rng.normal(0.0, 1.0, (1, n))
