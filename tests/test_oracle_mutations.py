@@ -62,3 +62,83 @@ def test_the_unmutated_oracle_passes_every_pin():
 @pytest.mark.parametrize("name,old,new", SLIPS, ids=[s[0] for s in SLIPS])
 def test_every_planted_slip_fails_a_pin(name, old, new):
     assert pins_fail(mutated_module(old, new)) >= 1, name
+
+
+# ---- the attention oracle (oracle/kvattn.py) against test_oracle_pins.py -----------------
+
+import inspect
+
+import test_oracle_pins as attn_pins
+
+KV_SRC = os.path.join(os.path.dirname(oracle.__file__), "kvattn.py")
+
+KV_SLIPS = [
+    ("mean in place of the minimum", "mn[P] = keys.min(axis=1)", "mn[P] = keys.mean(axis=1)"),
+    ("the min side of the bound dropped",
+     "total += np.maximum(qh * lo, qh * hi).sum(axis=1)", "total += (qh * hi).sum(axis=1)"),
+    ("ties to the higher page index", "order = np.lexsort((np.arange(n), -s))",
+     "order = np.lexsort((-np.arange(n), -s))"),
+    ("keep count rounded down", "return min(n, max(1, math.ceil(ratio * n - 1e-9)))",
+     "return min(n, max(1, int(ratio * n)))"),
+    ("softmax scale dropped", "x = scale * (K @ qh)", "x = K @ qh"),
+    ("lse without the max", "lse[b, h] = M + np.log(L)", "lse[b, h] = np.log(L)"),
+    ("merge weights with the wrong sign", "w = np.exp(m[live] - M)", "w = np.exp(M - m[live])"),
+    ("dropped mass of the kept tokens", "delta[b, h] = w[~tok_keep].sum() / w.sum()",
+     "delta[b, h] = w[tok_keep].sum() / w.sum()"),
+    ("last page one token long",
+     "return max(0, min(int(page_size), int(seq_len) - int(p) * int(page_size)))",
+     "return max(0, min(int(page_size), int(seq_len) - int(p) * int(page_size) + 1))"),
+    ("page count rounded down", "return -(-int(seq_len) // int(page_size))",
+     "return int(seq_len) // int(page_size)"),
+]
+
+
+def attn_pin_calls():
+    """Every pin of test_oracle_pins.py callable with its first parametrisation."""
+    calls = []
+    for name, fn in inspect.getmembers(attn_pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        kwargs = {}
+        for mark in getattr(fn, "pytestmark", []):
+            if mark.name != "parametrize":
+                continue
+            names = mark.args[0]
+            names = [a.strip() for a in names.split(",")] if isinstance(names, str) else list(names)
+            first = mark.args[1][0]
+            kwargs.update({names[0]: first} if len(names) == 1 else dict(zip(names, first)))
+        if set(inspect.signature(fn).parameters) <= set(kwargs):
+            calls.append((name, fn, kwargs))
+    return calls
+
+
+def attn_pins_fail(monkeypatch, old, new):
+    text = open(KV_SRC).read()
+    assert text.count(old) == 1, f"the oracle no longer holds {old!r}"
+    name = "oracle._kvattn_slip"
+    spec = importlib.util.spec_from_loader(name, loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    exec(compile(text.replace(old, new), KV_SRC + " (planted slip)", "exec"), mod.__dict__)
+    for attr, val in vars(mod).items():
+        if inspect.isfunction(val) and val.__module__ == name:
+            for target in (oracle, oracle.kvattn):
+                if hasattr(target, attr):
+                    monkeypatch.setattr(target, attr, val)
+    failed = []
+    for pin, fn, kwargs in attn_pin_calls():
+        try:
+            fn(**kwargs)
+        except Exception:                       # an assertion, or a crash on bad shapes
+            failed.append(pin)
+    return failed
+
+
+def test_the_unmutated_attention_oracle_passes_every_pin(monkeypatch):
+    assert len(attn_pin_calls()) >= 20
+    assert attn_pins_fail(monkeypatch, "import math", "import math") == []
+
+
+@pytest.mark.parametrize("name,old,new", KV_SLIPS, ids=[s[0] for s in KV_SLIPS])
+def test_every_planted_attention_slip_fails_a_pin(monkeypatch, name, old, new):
+    assert attn_pins_fail(monkeypatch, old, new), name
