@@ -93,10 +93,10 @@ KV_SLIPS = [
 ]
 
 
-def attn_pin_calls():
-    """Every pin of test_oracle_pins.py callable with its first parametrisation."""
+def pin_calls(pins):
+    """Every pin of a pin module callable with its first parametrisation."""
     calls = []
-    for name, fn in inspect.getmembers(attn_pins, inspect.isfunction):
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
         if not name.startswith("test_"):
             continue
         kwargs = {}
@@ -126,7 +126,7 @@ def attn_pins_fail(monkeypatch, old, new):
                 if hasattr(target, attr):
                     monkeypatch.setattr(target, attr, val)
     failed = []
-    for pin, fn, kwargs in attn_pin_calls():
+    for pin, fn, kwargs in pin_calls(attn_pins):
         try:
             fn(**kwargs)
         except Exception:                       # an assertion, or a crash on bad shapes
@@ -135,10 +135,62 @@ def attn_pins_fail(monkeypatch, old, new):
 
 
 def test_the_unmutated_attention_oracle_passes_every_pin(monkeypatch):
-    assert len(attn_pin_calls()) >= 20
+    assert len(pin_calls(attn_pins)) >= 20
     assert attn_pins_fail(monkeypatch, "import math", "import math") == []
 
 
 @pytest.mark.parametrize("name,old,new", KV_SLIPS, ids=[s[0] for s in KV_SLIPS])
 def test_every_planted_attention_slip_fails_a_pin(monkeypatch, name, old, new):
     assert attn_pins_fail(monkeypatch, old, new), name
+
+
+# ---- the FP8 statistics oracle (oracle/fp8stats.py) against test_oracle_fp8.py -----------
+
+import test_oracle_fp8 as fp8_pins
+
+FP8_SRC = os.path.join(os.path.dirname(oracle.__file__), "fp8stats.py")
+
+FP8_SLIPS = [
+    ("the minimum rounded up", "code_mn[rows] = quantize_down(lo, e[:, :, None])",
+     "code_mn[rows] = quantize_up(lo, e[:, :, None])"),
+    ("row exponent one too large", "e = np.maximum(e, MIN_EXPONENT)",
+     "e = np.maximum(e, MIN_EXPONENT) + 1"),
+    ("subnormal scale 2^-7", "return sign * (mant / 8.0) * 2.0 ** -6",
+     "return sign * (mant / 8.0) * 2.0 ** -7"),
+    ("an on-grid value rounded down a step", 'idx = np.searchsorted(vals, a, side="right") - 1',
+     'idx = np.searchsorted(vals, a, side="left") - 1'),
+]
+
+
+def fp8_pins_fail(monkeypatch, old, new):
+    text = open(FP8_SRC).read()
+    assert text.count(old) == 1, f"the oracle no longer holds {old!r}"
+    name = "oracle._fp8stats_slip"
+    spec = importlib.util.spec_from_loader(name, loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    exec(compile(text.replace(old, new), FP8_SRC + " (planted slip)", "exec"), mod.__dict__)
+    for attr, val in vars(mod).items():
+        if inspect.isfunction(val) and val.__module__ == name:
+            for target in (oracle, oracle.fp8stats):
+                if hasattr(target, attr):
+                    monkeypatch.setattr(target, attr, val)
+            if hasattr(fp8_pins, attr):
+                monkeypatch.setattr(fp8_pins, attr, val)
+    failed = []
+    for pin, fn, kwargs in pin_calls(fp8_pins):
+        try:
+            fn(**kwargs)
+        except Exception:
+            failed.append(pin)
+    return failed
+
+
+def test_the_unmutated_fp8_oracle_passes_every_pin(monkeypatch):
+    assert len(pin_calls(fp8_pins)) >= 5
+    assert fp8_pins_fail(monkeypatch, "import numpy as np", "import numpy as np") == []
+
+
+@pytest.mark.parametrize("name,old,new", FP8_SLIPS, ids=[s[0] for s in FP8_SLIPS])
+def test_every_planted_fp8_slip_fails_a_pin(monkeypatch, name, old, new):
+    assert fp8_pins_fail(monkeypatch, old, new), name
