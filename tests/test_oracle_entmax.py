@@ -51,6 +51,41 @@ def test_entmax15_uniform_and_translation():
     np.testing.assert_allclose(E.entmax15(z + 12.5)[0], E.entmax15(z)[0], atol=1e-12)
 
 
+def check_entmax15(E):
+    """Bisection on tau and the two-value closed form (the pins above, for a planted slip)."""
+    for n, scale in ((7, 1.0), (100, 0.2)):
+        z = np.random.default_rng(n).normal(0, scale, n)
+        p, tau = E.entmax15(z)
+        assert tau == pytest.approx(bisect_tau(z), abs=1e-12)
+        np.testing.assert_allclose(p, np.maximum(z - tau, 0) ** 2, atol=1e-12)
+    p, tau = E.entmax15(np.array([0.3, 0.0]))
+    t = (0.3 - math.sqrt(2.0 - 0.09)) / 2.0
+    np.testing.assert_allclose(p, [(0.3 - t) ** 2, t * t], atol=1e-14)
+
+
+def test_entmax_attend_two_tokens_closed_form():
+    """One page of two tokens, q.k = a and b, V the unit rows: with z = scale * q.k / 2 the
+    output is ((z1 - t)^2, (z2 - t)^2), t the two-value root (or (1, 0) when z1 - z2 >= 1)."""
+    check_entmax_attend_golden(E)
+
+
+def check_entmax_attend_golden(E):
+    PS, D = 2, 2
+    for a, b, scale in ((1.0, 0.2, 0.9), (0.5, -0.5, 0.7), (3.0, 0.0, 1.0)):
+        q = np.array([[[1.0, 0.0]]])
+        k = np.array([[[[a, 0.0], [b, 0.0]]]])            # [NP][Hkv][PS][D]
+        v = np.array([[[[1.0, 0.0], [0.0, 1.0]]]])
+        out, tau = E.entmax_attend(q, k, v, np.array([[0]]), np.array([2]), PS, scale)
+        z1, z2 = scale * a / 2.0, scale * b / 2.0
+        if z1 - z2 >= 1.0:
+            want = [1.0, 0.0]
+        else:
+            t = ((z1 + z2) - math.sqrt(2.0 - (z1 - z2) ** 2)) / 2.0
+            want = [(z1 - t) ** 2, (z2 - t) ** 2]
+            assert tau[0, 0] == pytest.approx(t, abs=1e-14)
+        np.testing.assert_allclose(out[0, 0], want, atol=1e-14)
+
+
 def _cache(seed=0, NP=24, Hkv=2, PS=16, D=32, G=2, B=2):
     rng = np.random.default_rng(seed)
     k = rng.normal(0, 1, (NP, Hkv, PS, D))

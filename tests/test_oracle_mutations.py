@@ -18,6 +18,11 @@ SLIPS = [
     ("divisor 12 -> 4", "((hi - lo) ** 2 / 12.0)", "((hi - lo) ** 2 / 4.0)"),
     ("q_d^2 -> |q_d|", "@ (qh * qh)", "@ np.abs(qh)"),
     ("(scale/2) unsquared", "v_b[h] = half * half *", "v_b[h] = half *"),
+    ("2-entmax weights (no square)", "p = np.maximum(z - tau, 0.0) ** 2",
+     "p = np.maximum(z - tau, 0.0)"),
+    ("support not checked against its root", "support = np.nonzero(ok & (tau_k < zs))[0]",
+     "support = np.nonzero(ok)[0]"),
+    ("z = x, not x / 2, in the attention", "p, t = entmax15(x / 2.0)", "p, t = entmax15(x)"),
     ("page-weighted mu and sigma^2",
      "        mu = (n_tok * c[h]).sum() / N\n"
      "        var = (n_tok * (c[h] - mu) ** 2).sum() / N + (n_tok * v[h]).sum() / N\n",
@@ -45,7 +50,9 @@ def pins_fail(E):
     checks = [lambda: pins.check_page_moments_golden(E),
               lambda: [pins.check_page_moments_monte_carlo(E, s) for s in (0, 1, 2)],
               lambda: pins.check_select_golden(E),
-              lambda: pins.check_token_weighting(E)]
+              lambda: pins.check_token_weighting(E),
+              lambda: pins.check_entmax15(E),
+              lambda: pins.check_entmax_attend_golden(E)]
     failed = 0
     for check in checks:
         try:
