@@ -97,6 +97,8 @@ KV_SLIPS = [
      "return max(0, min(int(page_size), int(seq_len) - int(p) * int(page_size) + 1))"),
     ("page count rounded down", "return -(-int(seq_len) // int(page_size))",
      "return int(seq_len) // int(page_size)"),
+    ("local window one page too long", "forced[max(0, n - int(local)):] = True",
+     "forced[max(0, n - int(local) - 1):] = True"),
 ]
 
 
