@@ -48,6 +48,7 @@ namespace skv {
 namespace {
 
 constexpr int kScoreWarps = 4;
+constexpr int kScoreMaxRuns = 8;              // 16-page runs per score block at most
 // rows (pages) per warp: eight lanes per row, four for FP8 rows
 template <bool F8>
 constexpr int rows_per_warp() { return F8 ? 8 : 4; }
@@ -289,11 +290,14 @@ template <typename T, int D, bool F8>
 cudaError_t launch_t(const kv_cache_desc& d, const void* q, int Hq, const void* stats,
                      const int8_t* stats_exp, float* scores, int scores_stride, DevCtx ctx,
                      cudaStream_t s) {
-  // runs per block: one, or enough that the grid is about one wave of 8 blocks per SM
+  // runs per block: one, or enough that the grid is about one wave of 8 blocks per SM, but
+  // at most kScoreMaxRuns: the grid is sized by the longest sequence, so with sequences of
+  // mixed lengths longer blocks would leave the short sequences' SMs idle; several waves of
+  // short blocks balance instead
   constexpr int SPAN = kScoreWarps * rows_per_warp<F8>();
   const long rows = (long)d.page_table_stride * d.num_kv_heads * d.batch;
   const long per_run = 8L * device_sms() * SPAN;
-  const int rounds = (int)std::max(1L, (rows + per_run - 1) / per_run);
+  const int rounds = (int)std::min((long)kScoreMaxRuns, std::max(1L, (rows + per_run - 1) / per_run));
   dim3 grid(ceil_div(d.page_table_stride, SPAN * rounds), d.num_kv_heads, d.batch);
   return launch_pdl(score_kernel<T, D, F8>, grid, dim3(kScoreWarps * 32), 0, s, d,
                     static_cast<const T*>(q), Hq / d.num_kv_heads, stats, stats_exp, scores,
