@@ -469,19 +469,22 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     const CtaKeys K = cta_keys_finish<C::THREADS>(ring, n_pages, misc + 8);
     uint32_t T, take_eq;
+    CtaCand list;
     cta_threshold<C::THREADS, LONG>(K, cnt, ring + used, misc, ring + used + kHistWords,
-                                    C::RING_WORDS - used - kHistWords, T, take_eq);
-    // this CTA's run only; each CTA also writes its run's part of the selection output. A
-    // short run (many splits): per-thread counts and one warp walking from the run's start;
-    // a long one (few splits, where that walk would cover most of the list): every warp
-    // walking its own segment
+                                    C::RING_WORDS - used - kHistWords, T, take_eq, &list);
+    // this CTA's run only; each CTA also writes its run's part of the selection output.
+    // After a prefilter, from its page-ordered candidates; else a short run (many splits):
+    // per-thread counts and one warp walking from the run's start; a long one (few splits,
+    // where that walk would cover most of the list): every warp walking its own segment
     int32_t* sel_out = sa.sel_out;
     auto emit = [&](int p, int pos) {
       if (sel_out != nullptr) sel_out[grp * sa.k_max + pos] = p;
       s_phys[pos - pos0] = p;
     };
     uint64_t* wtot = reinterpret_cast<uint64_t*>(smem + C::OFF_WTOT);
-    if (4 * np < cnt)
+    if (LONG && list.n >= 0)
+      cta_compact_list<C::THREADS>(list, T, take_eq, wtot, pos0, pos0 + np, emit);
+    else if (4 * np < cnt)
       cta_compact_window<C::THREADS>(K, T, take_eq, wtot, misc, pos0, pos0 + np, emit);
     else
       cta_compact<C::THREADS>(K, T, take_eq, wtot, pos0, pos0 + np, emit);
