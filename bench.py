@@ -75,18 +75,28 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def file_hash(path):
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+def file_hash(*paths):
+    """First 16 hex digits of the sha256 of the files' bytes, concatenated in order."""
+    h = hashlib.sha256()
+    for path in paths:
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def kernel_sources(source):
+    """The files whose code the timed kernel compiles from: the attention kernel's header and
+    the in-block top-k it selects with."""
+    return (source, os.path.join(os.path.dirname(source), "cta_topk.cuh"))
 
 
 def committed_traffic(workload, keep_label, source):
     """Per-launch DRAM bytes of the timed kernel from a committed ncu summary, if the
-    kernel source has not changed since the counters were taken."""
+    kernel's sources have not changed since the counters were taken."""
     p = os.path.join(PROFILE_DIR, f"{os.path.basename(source).split('.')[0]}_{workload}.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("source_hash") != file_hash(source):
+    if d.get("source_hash") != file_hash(*kernel_sources(source)):
         return None
     return d.get("traffic_bytes_per_launch", {}).get(keep_label)
 
