@@ -227,8 +227,11 @@ def time_replays(graph, steps, flush):
 
 
 def spread(xs):
+    """Median, p10, p90 and mean. Event-timed steps on this part come in steps of about
+    1.02 us, so a median can sit on either of two adjacent steps; the mean dithers between
+    them."""
     return {"median": round(statistics.median(xs), 3), "p10": round(pct(xs, 10), 3),
-            "p90": round(pct(xs, 90), 3)}
+            "p90": round(pct(xs, 90), 3), "mean": round(statistics.mean(xs), 3)}
 
 
 def window_byte_account(w, k_total, n_total):
