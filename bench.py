@@ -442,6 +442,7 @@ def measure_config(name, keep_index, args, dev, flush, peak, peak_kind):
                                                  7: " (attend)"}[plan],
             "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "peak_kind": peak_kind,
             "unit": "GB/s", "frac": round(ach / peak, 4),
+            "traffic": committed_traffic(w.name, label, ATTN_KERNEL[w.dtype][1]),
             "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_us": round(a_us, 3),
             "dense_same_kernel": {
                 "achieved": round(acct["dense_step"] / (dense_mean * 1e-6) / 1e9, 1),
