@@ -19,24 +19,28 @@
 //     starts at the highest of them; digits are 11 bits wide, so that after the first pass
 //     the threshold's bin usually holds fewer keys than the block has threads (a pass
 //     costs several block-wide steps; more bins cost only a wider histogram);
-//   * after one digit pass the keys of the threshold's bin are gathered through one
-//     shared counter (order does not matter for the threshold, and the bin holds few keys,
-//     so this costs one pass and no block scan), and if they are at most one per thread
-//     each finds its exact rank among them directly; larger bins take further radix passes
-//     over the gathered keys only;
+//   * after one digit pass the keys of the threshold's bin are gathered in any order (the
+//     threshold does not need it), each warp reserving its slots with one atomic, so this
+//     costs one pass and no block scan; if they are at most one per thread each finds its
+//     exact rank among them directly; larger bins take further radix passes over the
+//     gathered keys only;
+//   * a pass over whole 16-byte groups carries no per-key bound test; the partial last
+//     group goes to one thread (a bound test on every key made a count loop ~6x slower);
 //   * histograms take plain shared-memory atomics into a bank-padded array (warp-wide
 //     match instructions cost hundreds of cycles when a warp holds many distinct digits);
 //     their throughput (~1.6 keys per clock per SM) is what a pass over many keys costs, so
 //     long groups keeping few pages histogram only the keys at or above a bound taken from
-//     a sample (cta_threshold);
+//     a sample (cta_threshold), gathered with their pages in page order;
 //   * block reductions read the per-warp words one per lane and reduce with warp
 //     instructions, rather than every thread reading every warp's word;
 //   * the ordered compaction of the whole list gives each warp a contiguous segment of
 //     pages, walked 32 at a time with ballots, after one scan of the per-warp counts; the
 //     compaction of a short window of positions (one attention CTA's run) gives each thread
-//     a contiguous segment instead, counted with a rotated start (no bank conflicts) and
-//     one block scan, and only the few threads whose segments overlap the window walk
-//     theirs, so its cost does not depend on where the window lies.
+//     a contiguous segment of 16-byte groups instead, counted with a rotated start (no
+//     bank conflicts) and one block scan, and one warp walks from the segment holding the
+//     window's first position, four rows a step, so its cost does not depend on where the
+//     window lies; after the sample filter, a window is compacted from the page-ordered
+//     candidates alone (cta_compact_list).
 #pragma once
 
 #include "kv_internal.cuh"
