@@ -135,10 +135,14 @@ def _score_rows(kind, n, gen):
 
 
 @pytest.mark.parametrize("n", [5, 300, 2048, 8192, 21440])
-@pytest.mark.parametrize("kind", ["coarse", "tied", "outliers", "ramp", "normal"])
+@pytest.mark.parametrize("kind", ["coarse", "tied", "outliers", "ramp", "normal",
+                                  "sampled_high", "tied_low"])
 def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
     """Arbitrary score rows through the in-kernel selection: the oracle's rule exactly
-    (score descending, lower page first on ties, ascending output)."""
+    (score descending, lower page first on ties, ascending output). At 8192 and 21440 pages
+    with keep ratio 0.02 the attention kernel's sample filter runs and its runs come from the
+    page-ordered candidates; sampled_high and tied_low defeat the filter, so those runs come
+    from the search over every key instead."""
     PS, D, G, Hkv = 16, 128, 4, 2
     w = workload(num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, page_size=PS, dtype="bf16",
                  seed=n, seq_lens=(n * PS, n * PS - 5))
