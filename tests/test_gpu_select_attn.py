@@ -134,7 +134,7 @@ def _score_rows(kind, n, gen):
     return torch.randn(n, generator=gen)
 
 
-@pytest.mark.parametrize("n", [5, 300, 2048, 8192, 21440])
+@pytest.mark.parametrize("n", [5, 300, 2047, 2048, 8192, 9003, 21440])
 @pytest.mark.parametrize("kind", ["coarse", "tied", "outliers", "ramp", "normal",
                                   "sampled_high", "tied_low"])
 def test_in_kernel_selection_is_exact_on_given_scores(n, kind):
