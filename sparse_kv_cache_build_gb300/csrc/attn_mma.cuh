@@ -219,7 +219,10 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
       const uint32_t kbase = smem_addr(stages + (size_t)st * C::STAGE_BYTES);
       const uint32_t vbase = kbase + C::TILE_BYTES;
       // ---- S = Q K^T for 16 tokens (two n-tiles of 8) ------------------------------------
+      // even and odd k-steps accumulate apart (two dependent chains of KSTEPS/2 MMAs each
+      // instead of one of KSTEPS), summed once at the end
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int ks = 0; ks < C::KSTEPS; ++ks) {
         const int row = tok_base + (lm >> 1) * 8 + lr;
@@ -227,8 +230,14 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
         const uint32_t addr = kbase + (col >> 6) * C::HALF_BYTES + swz(row, (col & 63) >> 3);
         uint32_t b00, b01, b10, b11;
         ldsm_x4(addr, b00, b01, b10, b11);
-        mma_bf16(sc[0], qa0[ks], 0u, qa2[ks], 0u, b00, b01);
-        mma_bf16(sc[1], qa0[ks], 0u, qa2[ks], 0u, b10, b11);
+        float (&a)[2][4] = (ks & 1) ? so : sc;
+        mma_bf16(a[0], qa0[ks], 0u, qa2[ks], 0u, b00, b01);
+        mma_bf16(a[1], qa0[ks], 0u, qa2[ks], 0u, b10, b11);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sc[0][i] += so[0][i];
+        sc[1][i] += so[1][i];
       }
       // ---- online softmax (base 2) for row gid; tokens nt*8 + 2*tig + {0,1} ---------------
       float x[4];
