@@ -160,7 +160,7 @@ __device__ __forceinline__ void load_q_frags(const uint16_t* q, long row0, uint3
 // The group running it is 4 warps (128 threads): by default the whole CTA synchronised with
 // __syncthreads; a CTA may run two independent groups, each with its own stages, barriers,
 // run and named barrier bar_id (gtid = thread index within the group).
-template <int D, int G, int NST>
+template <int D, int G, int NST, bool WARP_ISSUE = true>
 __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char* stages,
                           uint64_t* bars, uint32_t ring_base, const int32_t* s_phys,
                           const int16_t* s_valid, int np, int g, int Hkv, int PS,
@@ -176,29 +176,54 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
   const int n_tiles = ceil_div(np, PPT);
   const uint32_t page_half_bytes = (uint32_t)PS * 128;
 
+  // warp 0 issues a stage. Several pages a stage (PS < 64): lane l copies one 64-column half
+  // of K or V of one page (at most 4 pages x 2 halves x 2 tensors = 16 copies), so the issue
+  // costs the warp one pass instead of a loop of copies in one thread between its tiles
+  // (dense 128K: 115.6 -> 97.6 us a step). With WARP_ISSUE false (the instantiation for long
+  // tables, whose larger selection code measured 1.3 us slower at 1M with the warp-wide form
+  // compiled in) or one page a stage, lane 0 copies the stage's halves in a loop.
   auto issue = [&](int t) {
     const uint32_t u = ring_base + (uint32_t)t;
     const int st = (int)(u % NST);
     char* kdst = stages + (size_t)st * C::STAGE_BYTES;
     char* vdst = kdst + C::TILE_BYTES;
     const int i0 = t * PPT, i1 = min(np, i0 + PPT);
-    uint32_t bytes = 0;
-    for (int i = i0; i < i1; ++i)
-      bytes += s_valid[i] > 0 ? 2u * C::HALVES * page_half_bytes : 0u;
-    mbar_arrive_expect_tx(&bars[st], bytes);
     const uint64_t pol = l2_evict_first_policy();
-    for (int i = i0; i < i1; ++i) {
-      if (s_valid[i] <= 0) continue;
-      const int y = (s_phys[i] * Hkv + g) * PS;
-      const uint32_t off = (uint32_t)(i - i0) * page_half_bytes;
+    if (!WARP_ISSUE || PPT == 1) {
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int i = i0; i < i1; ++i)
+          bytes += s_valid[i] > 0 ? 2u * C::HALVES * page_half_bytes : 0u;
+        mbar_arrive_expect_tx(&bars[st], bytes);
+        for (int i = i0; i < i1; ++i) {
+          if (s_valid[i] <= 0) continue;
+          const int y = (s_phys[i] * Hkv + g) * PS;
+          const uint32_t off = (uint32_t)(i - i0) * page_half_bytes;
 #pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_2d(kdst + h * C::HALF_BYTES + off, tmK, 64 * h, y, &bars[st], pol);
-        tma_load_2d(vdst + h * C::HALF_BYTES + off, tmV, 64 * h, y, &bars[st], pol);
+          for (int h = 0; h < C::HALVES; ++h) {
+            tma_load_2d(kdst + h * C::HALF_BYTES + off, tmK, 64 * h, y, &bars[st], pol);
+            tma_load_2d(vdst + h * C::HALF_BYTES + off, tmV, 64 * h, y, &bars[st], pol);
+          }
+        }
       }
+      return;
+    }
+    constexpr int PER_PAGE = 2 * C::HALVES;
+    const int i = i0 + lane / PER_PAGE;
+    const bool mine = lane < PPT * PER_PAGE && i < i1 && s_valid[i] > 0;
+    const uint32_t copies = __popc(__ballot_sync(0xffffffffu, mine));
+    if (lane == 0) mbar_arrive_expect_tx(&bars[st], copies * page_half_bytes);
+    __syncwarp();
+    if (mine) {
+      const int h = (lane >> 1) % C::HALVES;
+      const int y = (s_phys[i] * Hkv + g) * PS;
+      const uint32_t off = (uint32_t)h * C::HALF_BYTES + (uint32_t)(i - i0) * page_half_bytes;
+      if (lane & 1) tma_load_2d(vdst + off, tmV, 64 * h, y, &bars[st], pol);
+      else tma_load_2d(kdst + off, tmK, 64 * h, y, &bars[st], pol);
     }
   };
-  if (tid == 0) {
+  const bool issuer = WARP_ISSUE ? warp == 0 : tid == 0;
+  if (issuer) {
     for (int t = 0; t < NST && t < n_tiles; ++t) issue(t);
   }
 
@@ -285,7 +310,7 @@ __device__ bool attend_run(const CUtensorMap* tmK, const CUtensorMap* tmV, char*
       }
     }
     group_sync(bar_id, 128);                               // the stage is free again
-    if (tid == 0 && t + NST < n_tiles) issue(t + NST);
+    if (issuer && t + NST < n_tiles) issue(t + NST);
   }
   if (aborted && tid == 0) {
     // let every copy this CTA issued land before its shared memory is reused or freed
@@ -518,7 +543,7 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
 
   WarpAcc<D> acc;
   acc.init();
-  const bool ok = attend_run<D, G, C::NSTAGE>(&tmK, &tmV, smem + C::OFF_STAGES, bars, 0u,
+  const bool ok = attend_run<D, G, C::NSTAGE, !LONG>(&tmK, &tmV, smem + C::OFF_STAGES, bars, 0u,
                                               s_phys, s_valid, np, g, Hkv, PS, qa0, qa2,
                                               qk_scale_log2, acc, ctx.wait_ns);
   const long out_row = ((long)b * Hq + g * G) * S + s;
