@@ -188,23 +188,25 @@ split_attn_kernel(kv_cache_desc d, const T* __restrict__ q, float qk_scale_log2,
   const char* kbase = static_cast<const char*>(d.k_pool);
   const char* vbase = static_cast<const char*>(d.v_pool);
 
+  // warp 0 issues a stage, lane l copying K (l even) or V (l odd) of page l / 2, so the copies
+  // cost the warp one pass between its tiles instead of a loop in one thread
   auto issue = [&](int t) {
     const int st = t % C::NSTAGE;
     char* kdst = smem + C::OFF_STAGES + (size_t)st * C::STAGE_BYTES;
     const int i0 = t * PPT, i1 = min(np, i0 + PPT);
-    uint32_t bytes = 0;
-    for (int i = i0; i < i1; ++i) bytes += s_valid[i] > 0 ? 2 * page_bytes : 0;
-    mbar_arrive_expect_tx(&bars[st], bytes);
-    const uint64_t pol = l2_evict_first_policy();
-    for (int i = i0; i < i1; ++i) {
-      if (s_valid[i] <= 0) continue;
+    const int i = i0 + (lane >> 1);
+    const bool mine = lane < 2 * PPT && i < i1 && s_valid[i] > 0;
+    const uint32_t copies = __popc(__ballot_sync(0xffffffffu, mine));
+    if (lane == 0) mbar_arrive_expect_tx(&bars[st], copies * page_bytes);
+    __syncwarp();
+    if (mine) {
       const size_t src = ((size_t)s_phys[i] * Hkv + g) * page_bytes;
-      const uint32_t dst = (uint32_t)(i - i0) * page_bytes;
-      bulk_g2s(kdst + dst, kbase + src, page_bytes, &bars[st], pol);
-      bulk_g2s(kdst + C::TILE_BYTES + dst, vbase + src, page_bytes, &bars[st], pol);
+      const uint32_t dst = (uint32_t)(i - i0) * page_bytes + ((lane & 1) ? C::TILE_BYTES : 0u);
+      bulk_g2s(kdst + dst, ((lane & 1) ? vbase : kbase) + src, page_bytes, &bars[st],
+               l2_evict_first_policy());
     }
   };
-  if (tid == 0) {
+  if (warp == 0) {
     for (int t = 0; t < C::NSTAGE && t < n_tiles; ++t) issue(t);
   }
 
@@ -340,7 +342,7 @@ split_attn_kernel(kv_cache_desc d, const T* __restrict__ q, float qk_scale_log2,
       }
     }
     __syncthreads();                                       // stage st is free again
-    if (tid == 0 && t + C::NSTAGE < n_tiles) issue(t + C::NSTAGE);
+    if (warp == 0 && t + C::NSTAGE < n_tiles) issue(t + C::NSTAGE);
   }
 
   const long out_row = ((long)b * Hq + g * G) * S + s;     // (b, first head of group, s)
