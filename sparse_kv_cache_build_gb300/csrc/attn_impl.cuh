@@ -12,8 +12,8 @@
 // group's selected-page list.
 //
 // Data movement: the CTA first resolves its pages (selected index -> page table ->
-// physical page, each checked against its bounds) into shared memory. Thread 0 then keeps
-// NSTAGE tiles of 64 tokens in flight: every page of a tile is one contiguous
+// physical page, each checked against its bounds) into shared memory. Warp 0 then keeps
+// NSTAGE tiles of 64 tokens in flight, one copy per lane: every page of a tile is one contiguous
 // PS*D-element chunk of the pool per KV head, moved with one bulk asynchronous copy for K
 // and one for V into the stage buffer, counted on the stage's mbarrier (bounded waits).
 // K/V are streamed with an L2 evict-first policy.

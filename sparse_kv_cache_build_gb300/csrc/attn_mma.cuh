@@ -19,8 +19,9 @@
 // Data movement: pages arrive by TMA tensor copies (cp.async.bulk.tensor.2d) from a 2-D view
 // of the pool, [NP*Hkv*PS rows][D columns], in boxes of 64 columns x PS rows with the
 // 128-byte swizzle, so ldmatrix reads eight consecutive rows at one 16-byte column chunk
-// without bank conflicts. Each stage holds 64 tokens of K and of V; thread 0 keeps NSTAGE
-// stages in flight, completion counted on one mbarrier per stage (bounded waits).
+// without bank conflicts. Each stage holds 64 tokens of K and of V; warp 0 keeps NSTAGE
+// stages in flight, one copy per lane, completion counted on one mbarrier per stage (bounded
+// waits).
 #pragma once
 
 #include <cuda.h>
@@ -151,7 +152,7 @@ __device__ __forceinline__ void load_q_frags(const uint16_t* q, long row0, uint3
 
 // Stream a run of np pages (physical ids and valid-token counts in shared memory) through a
 // ring of NST stages of 64 tokens, accumulating attention of the group's query heads into
-// the four warps' WarpAcc. All 128 threads call it; thread 0 issues the TMA copies. Ring use
+// the four warps' WarpAcc. All 128 threads call it; warp 0 issues the TMA copies. Ring use
 // number ring_base + t goes to stage (ring_base + t) % NST with phase parity
 // ((ring_base + t) / NST) & 1, so one ring can serve several runs or phases of a kernel.
 // It consumes ceil(np / (64 / PS)) ring uses. Returns false if a wait ran out (the copies
