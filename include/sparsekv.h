@@ -240,8 +240,11 @@ kv_status kv_select_structured(const float* scores, int32_t scores_stride,
  * kv_sparse_decode_attn -- [BYTEX] split-K decode attention over selected pages.
  * For each (b, g) the selected list (sel_idx[b][g][0..sel_cnt[b][g]), or every page
  * 0..n_b-1 when sel_idx is NULL: the dense baseline through the same kernel) is cut into
- * num_splits consecutive runs: split s takes list positions [s*c, min(cnt, (s+1)*c)) with
- * c = ceil(cnt / num_splits). For each query head h of the group and split s, over the
+ * num_splits consecutive runs of whole 64-token tiles: with p = 64 / page_size pages a tile
+ * and T = ceil(cnt / p) tiles, split s takes list positions
+ * [min(cnt, floor(s*T/num_splits)*p), min(cnt, floor((s+1)*T/num_splits)*p)), so the runs
+ * differ by at most one tile and only the list's last tile is partial. For each query head h
+ * of the group and split s, over the
  * valid tokens t of the run's pages (tokens at or past len_b are masked):
  *   x_t = sm_scale * q[b][h] . k_t,  m = max x_t,  l = sum exp(x_t - m),
  *   acc = sum exp(x_t - m) v_t

@@ -240,16 +240,19 @@ def attend(q, k_pool, v_pool, page_table, seq_lens, page_size, scale, selected=N
     return out, lse
 
 
-def split_ranges(count: int, num_splits: int):
+def split_ranges(count: int, num_splits: int, page_size: int):
     """Positions of the selected-page list handled by each split.
 
-    Split ``s`` takes positions ``[s*c, min(count, (s+1)*c))`` with ``c = ceil(count/S)``;
-    trailing splits may be empty. This partition is part of the documented interface of
-    the split-K call, so the partials can be compared split by split.
+    The list is cut into T = ceil(count / p) tiles of p = 64 / page_size pages (64 tokens);
+    split ``s`` takes the whole tiles ``[floor(s*T/S), floor((s+1)*T/S))``, i.e. positions
+    ``[min(count, floor(s*T/S)*p), min(count, floor((s+1)*T/S)*p))``. Runs differ by at most
+    one tile; splits may be empty. This partition is part of the documented interface of the
+    split-K call, so the partials can be compared split by split.
     """
-    S = int(num_splits)
-    c = -(-int(count) // S) if count > 0 else 0
-    return [(min(count, s * c), min(count, (s + 1) * c)) for s in range(S)]
+    S, n = int(num_splits), int(count)
+    p = 64 // int(page_size)
+    T = -(-n // p) if n > 0 else 0
+    return [(min(n, (s * T // S) * p), min(n, ((s + 1) * T // S) * p)) for s in range(S)]
 
 
 def split_partials(q_bh, K, V, scale, token_splits):

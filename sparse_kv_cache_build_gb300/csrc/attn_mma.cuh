@@ -477,9 +477,12 @@ split_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
       cnt = cnt < 0 ? 0 : sel_stride;
     }
   }
-  const int c = cnt > 0 ? ceil_div(cnt, S) : 0;
-  const int pos0 = min(cnt, s * c);
-  int np = min(cnt, pos0 + c) - pos0;
+  // split s takes whole 64-token tiles [s T / S, (s + 1) T / S) of the list's T tiles, so
+  // the splits differ by at most one tile and only the last tile of the list is partial
+  const int ppt = kTileTokens / PS;
+  const long n_tl = ceil_div(cnt, ppt);
+  const int pos0 = min(cnt, (int)((long)s * n_tl / S) * ppt);
+  int np = min(cnt, (int)((long)(s + 1) * n_tl / S) * ppt) - pos0;
   if (np > kMaxSplitPages) {
     if (tid == 0) flag(ctx, KV_DEVERR_BAD_SEL);
     np = kMaxSplitPages;

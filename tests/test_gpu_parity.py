@@ -233,7 +233,8 @@ def test_sparse_step_matches_oracle(dtype, D, G, PS, S):
                                                    for p in got_sel])]).astype(int)
             Kt = oracle.gather_tokens(o["K"], o["table"], o["lens"][0], w.page_size, 0, 0, got_sel)
             Vt = oracle.gather_tokens(o["V"], o["table"], o["lens"][0], w.page_size, 0, 0, got_sel)
-            tsplits = [(toks[a], toks[e]) for a, e in oracle.split_ranges(len(got_sel), r["S"])]
+            tsplits = [(toks[a], toks[e])
+                       for a, e in oracle.split_ranges(len(got_sel), r["S"], w.page_size)]
             acc, ml = f64(r["acc"][b, hs]), f64(r["ml"][b, hs])
             for hi in range(w.group_size):
                 m, l, a = oracle.split_partials(o["q"][0, hi], Kt, Vt, w.sm_scale, tsplits)

@@ -320,15 +320,26 @@ def test_attention_ignores_tokens_past_the_end_and_empty_sequences():
 # ----------------------------------------------------------------------------- merge
 
 def test_split_ranges_partition():
-    for count in (0, 1, 5, 33, 615):
-        for S in (1, 2, 3, 7, 19, 40):
-            r = oracle.split_ranges(count, S)
-            assert len(r) == S
-            assert r[0][0] == 0 and r[-1][1] == count
-            for (a0, a1), (b0, b1) in zip(r, r[1:]):
-                assert a1 == b0 and a0 <= a1
-            sizes = [b - a for a, b in r]
-            assert max(sizes) == (-(-count // S) if count else 0)
+    """Consecutive runs covering the list exactly; every boundary on a 64-token tile; run
+    lengths in whole tiles differing by at most one (the last tile may be partial)."""
+    for PS in (16, 32, 64):
+        p = 64 // PS
+        for count in (0, 1, 5, 33, 615, 2048):
+            for S in (1, 2, 3, 7, 19, 38, 40):
+                r = oracle.split_ranges(count, S, PS)
+                assert len(r) == S
+                assert r[0][0] == 0 and r[-1][1] == count
+                for (a0, a1), (b0, b1) in zip(r, r[1:]):
+                    assert a1 == b0 and a0 <= a1
+                assert all(a % p == 0 for a, _ in r)
+                tiles = [-(-(b - a) // p) for a, b in r]
+                T = -(-count // p)
+                assert sum(tiles) == T and max(tiles) - min(tiles) <= 1
+    # 615 pages of 16 tokens over 38 splits: 154 tiles; floor(s*154/38) gives splits 18 and 37
+    # five tiles each (pages 288-307, and 596-614 whose last tile holds 3 pages), 16 pages else
+    r = oracle.split_ranges(615, 38, 16)
+    assert r[18] == (288, 308) and r[-1] == (596, 615)
+    assert [b - a for a, b in r].count(16) == 36
 
 
 def test_merge_golden_cases():
